@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Bench: batch-1 VBQ decode step on the 9B-shaped stack (one JSON line on stdout).
+
+value    whole-job effective HBM GB/s of the decode step:
+         algorithmic bytes of all projections per step / device time per step.
+         The device is timed with CUDA events on the launching stream over
+         exactly --steps steps. A barrier and a synchronize bracket the timed
+         region on both sides, and the max over ranks is taken.
+extra    decode-step microseconds at the 9B and 1B shapes, the dominant kernel's
+         roofline, a dense bf16 GEMV on the same shapes, the CPU oracle timed on
+         host cores, and an end-to-end number through host buffers.
+
+--impl reference times the CPU oracle (the only reference implementation)
+on a bounded sample of the same workload, with the same metric.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torchrun, each rank runs an independent replica (the path has no data-path
+exchange), and value sums the ranks' bytes over the max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "mixed-bit dequant-GEMV HBM GB/s (% of peak); decode-step µs at 1B/9B shapes"
+GROUP_META_BYTES = 2.25  # fp16 scale + 2-bit class per group
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["vbq", "reference"], default="vbq")
+    p.add_argument("--no-1b", action="store_true", help="skip the 1B-shaped step")
+    p.add_argument("--no-dense", action="store_true", help="skip the dense bf16 baseline")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "vbq" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- workload
+
+def algorithmic_bytes(n: int, k: int, code_bytes: int) -> float:
+    """Codes + 2.25 B per group (fp16 scale + 2-bit class) + bf16 x + fp32 y."""
+    groups = n * (k // 64)
+    return code_bytes + GROUP_META_BYTES * groups + 2.0 * k + 4.0 * n
+
+
+class PackedModel:
+    def __init__(self, V, shape, seed=0):
+        from synth import gen_model_matrix, model_matrix_list
+        self.shape = shape
+        self.handles = []
+        self.alg_bytes = 0.0
+        self.code_bytes = 0
+        self.total_bytes = 0
+        self.weights = 0
+        self.per_matrix = []  # (layer, proj, N, K, algorithmic bytes, handle)
+        for (layer, proj) in model_matrix_list(shape):
+            m = gen_model_matrix(shape, layer, proj, seed=seed)
+            h = V.Matrix(m.codes, m.bits, m.scales)
+            info = h.info()
+            ab = algorithmic_bytes(m.N, m.K, info["code_bytes"])
+            self.alg_bytes += ab
+            self.code_bytes += info["code_bytes"]
+            self.total_bytes += info["total_bytes"]
+            self.weights += m.N * m.K
+            self.per_matrix.append((layer, proj, m.N, m.K, ab, h))
+            self.handles.append(h)
+            del m
+        desc = V.make_model_desc(shape.n_layers, shape.d, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                                 shape.d_ff, shape.vocab, 1e-5)
+        self.model = V.Model(desc, self.handles)
+
+    def close(self):
+        self.model.close()
+        for h in self.handles:
+            h.close()
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU timings
+
+def time_steps(fn, steps, warmup, stream, ws):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = start.elapsed_time(end) / steps
+    return ms
+
+
+def dominant_kernel_roofline(V, pm, stream, peak_gbs, reps=3):
+    """Each projection as its own vbq_gemv launch, bracketed by events on the launching stream."""
+    import torch
+    from synth import gen_x
+    xs = {}
+    ys = {}
+    for (_, proj, n, k, ab, h) in pm.per_matrix:
+        if k not in xs:
+            xs[k] = torch.from_numpy(gen_x(k, seed=9).view(np.int16)).cuda()
+        if n not in ys:
+            ys[n] = torch.empty(n, dtype=torch.float32, device="cuda")
+    ev = []
+    with torch.cuda.stream(stream):
+        for (_, _, n, k, ab, h) in pm.per_matrix:  # warm
+            V.vbq_gemv(h.handle, xs[k], ys[n], stream)
+        for _ in range(reps):
+            for (_, _, n, k, ab, h) in pm.per_matrix:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                V.vbq_gemv(h.handle, xs[k], ys[n], stream)
+                b.record(stream)
+                ev.append((a, b, ab))
+    torch.cuda.synchronize()
+    tot_ms = sum(a.elapsed_time(b) for a, b, _ in ev)
+    tot_b = sum(ab for _, _, ab in ev)
+    launches = len(ev)
+    achieved = tot_b / (tot_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(achieved / peak_gbs, 4), "traffic": None,
+            "kernel": "vbq_gemv_kernel<1,8>", "launches": launches,
+            "avg_launch_us": round(tot_ms * 1e3 / launches, 2),
+            "alg_bytes_per_launch": round(tot_b / launches),
+            "note": "each projection of the 9B stack launched alone; algorithmic bytes = codes + 2.25 B/group + 2K + 4N"}
+
+
+def dense_baseline(V, shape, stream, steps=3):
+    """Dense bf16 GEMV (same codebase) over one layer's projections x n_layers + the head."""
+    import torch
+    from synth import PROJS, model_matrix_shape
+    torch.manual_seed(0)
+    mats = []
+    for p in PROJS:
+        n, k = model_matrix_shape(shape, p)
+        mats.append((torch.randn(n, k, device="cuda", dtype=torch.bfloat16), n, k))
+    n, k = model_matrix_shape(shape, "head")
+    head = (torch.randn(n, k, device="cuda", dtype=torch.bfloat16), n, k)
+    xs = {k: torch.randn(k, device="cuda", dtype=torch.bfloat16) for (_, _, k) in mats + [head]}
+    ys = {n: torch.empty(n, device="cuda") for (_, n, _) in mats + [head]}
+
+    def step():
+        for _ in range(shape.n_layers):
+            for (W, n, k) in mats:
+                V.vbq_dense_gemv_bf16(W, xs[k], ys[n], n, k, stream)
+        W, n, k = head
+        V.vbq_dense_gemv_bf16(W, xs[k], ys[n], n, k, stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_steps(step, steps, 1, stream, 1)
+    nbytes = shape.n_layers * sum(2.0 * n * k for (_, n, k) in mats) + 2.0 * head[1] * head[2]
+    del mats, head
+    torch.cuda.empty_cache()
+    return {"us_per_step": round(ms * 1e3, 1), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "weight_bytes": nbytes}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(shape, budget_s: float):
+    """The oracle's GEMV over the first layers' projections, until the time budget is spent."""
+    from oracle import vbq_oracle as O
+    from synth import gen_model_matrix, gen_x, model_matrix_list, model_matrix_shape
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        threads = 1
+    done_bytes = 0.0
+    spent = 0.0
+    n_mats = 0
+    for (layer, proj) in model_matrix_list(shape):
+        m = gen_model_matrix(shape, layer, proj, seed=0)
+        x = gen_x(m.K, seed=9)
+        code_bytes = O.storage_bytes(m.bits)["code_bytes"]
+        t0 = time.perf_counter()
+        O.gemv(m.codes, m.bits, m.scales, x)
+        spent += time.perf_counter() - t0
+        done_bytes += algorithmic_bytes(m.N, m.K, code_bytes)
+        n_mats += 1
+        if spent >= budget_s:
+            break
+    gbs = done_bytes / spent / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"oracle gemv (fp32 dequant, fp64 dot) over the first {n_mats} projections of the "
+                      f"{shape.name} stack ({done_bytes / 1e6:.0f} MB algorithmic, {spent:.1f} s)",
+            "seconds": round(spent, 2)}
+
+
+# --------------------------------------------------------------------------- main arms
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from synth import model_9b
+    shape = model_9b()
+    vals = []
+    last = None
+    for _ in range(args.warmup):
+        cpu_oracle_sample(shape, budget_s=min(2.0, args.cpu_seconds))
+    for _ in range(args.steps):
+        last = cpu_oracle_sample(shape, budget_s=max(1.0, args.cpu_seconds / max(1, args.steps)))
+        vals.append(last["value"])
+    v = float(np.median(vals))
+    line = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "9B-shaped decode step, batch 1 (32 layers, d=4096, GQA 32/8x128, SwiGLU "
+                                   "14336, vocab 128256), per-group {1,2,4,8}-bit weights, seed 0"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_vbq(args, ws, rank, local):
+    import torch
+    import mixed_precision_weight_bit_b300 as V
+    from synth import gen_x, model_1b, model_9b
+
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    peak, peak_kind = peaks()
+
+    shape = model_9b()
+    t0 = time.perf_counter()
+    pm = PackedModel(V, shape, seed=0)
+    pack_s = time.perf_counter() - t0
+    x = torch.from_numpy(gen_x(shape.d, seed=7).view(np.int16)).cuda()
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+
+    def step():
+        V.vbq_decode_step(pm.model.handle, x, logits, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        launches0 = V.vbq_launch_count()
+        ms = time_steps(step, args.steps, 0, stream, ws)
+        launches = V.vbq_launch_count() - launches0
+        clk = clocks.stop()
+    assert V.vbq_device_check() == 0
+    ms_max = max_over_ranks(ms, ws)
+    value = ws * pm.alg_bytes / (ms_max * 1e-3) / 1e9
+
+    # end to end through host buffers (pinned): H2D of x, D2H of logits, every step
+    xh = torch.from_numpy(gen_x(shape.d, seed=7).view(np.int16)).pin_memory()
+    lh = torch.empty(shape.vocab, dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        V.vbq_decode_step_host(pm.model.handle, xh, lh, stream)
+    barrier(ws)
+    t1 = time.perf_counter()
+    for _ in range(args.steps):
+        V.vbq_decode_step_host(pm.model.handle, xh, lh, stream)
+    e2e_s = (time.perf_counter() - t1) / args.steps
+    e2e_s = max_over_ranks(e2e_s, ws)
+
+    roof = dominant_kernel_roofline(V, pm, stream, peak)
+    roof["peak_kind"] = peak_kind
+    extra = {"decode_step_us_9b": round(ms * 1e3, 1), "pack_seconds_9b": round(pack_s, 1),
+             "weights_9b": pm.weights, "alg_bytes_per_step_9b": round(pm.alg_bytes),
+             "device_bytes_9b": pm.total_bytes, "code_bytes_9b": pm.code_bytes}
+    pm.close()
+    torch.cuda.empty_cache()
+
+    if not args.no_1b:
+        s1 = model_1b()
+        pm1 = PackedModel(V, s1, seed=0)
+        x1 = torch.from_numpy(gen_x(s1.d, seed=7).view(np.int16)).cuda()
+        l1 = torch.empty(s1.vocab, dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            ms1 = time_steps(lambda: V.vbq_decode_step(pm1.model.handle, x1, l1, stream), args.steps,
+                             max(args.warmup, 3), stream, 1)
+        extra["decode_step_us_1b"] = round(ms1 * 1e3, 1)
+        extra["alg_bytes_per_step_1b"] = round(pm1.alg_bytes)
+        extra["GB/s_1b"] = round(pm1.alg_bytes / (ms1 * 1e-3) / 1e9, 1)
+        pm1.close()
+        torch.cuda.empty_cache()
+    if not args.no_dense:
+        extra["dense_bf16_9b"] = dense_baseline(V, shape, stream)
+        extra["dense_bf16_9b"]["speedup_vbq"] = round(extra["dense_bf16_9b"]["us_per_step"] / (ms * 1e3), 2)
+
+    cpu = None
+    if rank == 0:
+        cpu = cpu_oracle_sample(shape, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32 accumulate (bf16 x, packed 1/2/4/8-bit codes, fp16 scales)", "data": "synthetic",
+                "config": {"workload": "9B-shaped decode step, batch 1 (32 layers, d=4096, GQA 32/8x128, "
+                                       "SwiGLU 14336, vocab 128256), per-group {1,2,4,8}-bit weights, seed 0",
+                           "l2": "inputs larger than L2: 1.9 GB of packed weights streamed per step",
+                           "parallelism": f"replicas x{ws}"},
+                "frac_of_peak": round(value / ws / peak, 4), "peak_gbs": peak,
+                "roofline": roof,
+                "cpu_baseline": cpu,
+                "e2e": {"value": round(ws * pm_bytes(extra) / e2e_s / 1e9, 1), "unit": "GB/s",
+                        "h2d_bytes_per_step": 2 * shape.d, "d2h_bytes_per_step": 4 * shape.vocab,
+                        "us_per_step": round(e2e_s * 1e6, 1)},
+                "gpu_launches": int(launches),
+                "clocks": clk,
+                **extra}
+        print(json.dumps(line), flush=True)
+
+
+def pm_bytes(extra):
+    return extra["alg_bytes_per_step_9b"]
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_vbq(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

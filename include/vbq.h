@@ -1,0 +1,221 @@
+/*
+ * vbq.h: C ABI of the VBQ mixed-bit decode library (sm_103a).
+ *
+ * VBQ (Variable Bit-width Quantization) stores a linear layer's weights packed.
+ * Each contiguous group of 64 weights along the input dimension has its own
+ * bit-width b_g from {1,2,4,8}. Source: "Variable Bit-width Quantization:
+ * Learning Per-Group Precision for 'Bigger-but-Smaller' Language Models",
+ * abstract. The abstract says the learned recipe "maps directly to packed
+ * low-bit storage" and that fused dequantize-and-multiply kernels speed up
+ * memory-bandwidth-bound autoregressive decode. The pages fix no code grid;
+ * this library uses
+ *
+ *     w = s_g * (q - (2^b_g - 1) / 2),   s_g fp16,   q unsigned in [0, 2^b_g - 1],
+ *
+ * where group g of row r covers input columns [64g, 64g + 63].
+ *
+ * Conventions for every call:
+ *  - "host" pointers are ordinary CPU memory, and "device" pointers are CUDA
+ *    device memory of the current device (for example a torch tensor's
+ *    data_ptr()). bf16 and fp16 values are passed as uint16_t bit patterns.
+ *  - stream is a cudaStream_t cast to void*. NULL means the legacy default
+ *    stream. Device work is enqueued on the stream asynchronously unless the
+ *    call says otherwise. Output buffers are written when the stream reaches
+ *    the work.
+ *  - Arguments are validated on the host before any device work is enqueued.
+ *    On a validation error nothing is enqueued and nothing is written.
+ *  - A launch failure returns VBQ_ERR_CUDA, read with cudaGetLastError and
+ *    without an implicit synchronization. vbq_last_error() gives the text.
+ *  - Calls that share one vbq_matrix or vbq_model must not overlap on the GPU
+ *    if the object holds per-call state (vbq_model does). Calls on different
+ *    objects may run concurrently.
+ */
+#ifndef VBQ_H
+#define VBQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VBQ_API __attribute__((visibility("default")))
+#else
+#define VBQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct vbq_matrix vbq_matrix; /* packed matrix, owned by the library */
+typedef struct vbq_model vbq_model;   /* decode-step stack, owned by the library */
+
+typedef enum {
+  VBQ_OK = 0,
+  VBQ_ERR_INVALID_ARG = 1,  /* null pointer, bad count, mismatched objects */
+  VBQ_ERR_SHAPE = 2,        /* K not a multiple of 64, sizes out of range */
+  VBQ_ERR_CODE_RANGE = 3,   /* a code q >= 2^b of its group */
+  VBQ_ERR_BITS = 4,         /* a bit-width outside {1,2,4,8} */
+  VBQ_ERR_CUDA = 5,         /* a CUDA runtime call or a launch failed */
+  VBQ_ERR_OOM = 6,          /* device or host allocation failed */
+  VBQ_ERR_DEVICE_CHECK = 7, /* a kernel reported a failed internal check (bounded wait ran out) */
+  VBQ_ERR_UNSUPPORTED = 8   /* valid request this build does not serve */
+} vbq_status;
+
+/* Sizes and storage accounting of a packed matrix. */
+typedef struct {
+  int64_t N, K;          /* rows (outputs) and columns (inputs) */
+  int64_t code_bytes;    /* sum over groups of 64*b/8: the packed code bits */
+  int64_t meta_bytes;    /* scales, row indices, step descriptors and offsets, tile table */
+  int64_t total_bytes;   /* device bytes of the packed matrix */
+  double mean_bits;      /* 8*code_bytes/(N*K): mean code bits per weight */
+  int32_t n_tiles;       /* row tiles of the layout */
+  int32_t n_steps;       /* 256-byte code steps of the layout */
+  int64_t groups_by_bits[4]; /* groups at 1, 2, 4 and 8 bits */
+} vbq_info;
+
+/* Shapes of a decoder-only stack whose projections are VBQ matrices. */
+typedef struct {
+  int32_t n_layers;
+  int32_t d;           /* model width */
+  int32_t n_heads;     /* query heads */
+  int32_t n_kv_heads;  /* key/value heads (n_heads % n_kv_heads == 0) */
+  int32_t head_dim;
+  int32_t d_ff;        /* SwiGLU hidden width */
+  int32_t vocab;
+  float rms_eps;       /* RMSNorm epsilon (unit gain) */
+} vbq_model_desc;
+
+/* Text for a status code. Static storage. */
+VBQ_API const char* vbq_status_str(vbq_status s);
+
+/* Detail of the last error raised on the calling host thread ("" if none). */
+VBQ_API const char* vbq_last_error(void);
+
+/*
+ * vbq_pack: logical codes + per-group bit map + scales -> device layout.
+ * Source: the VBQ abstract ("maps directly to packed low-bit storage"). The
+ * layout is this library's own design.
+ *
+ *  codes      host, uint8 [N][K] row-major; codes[r][k] < 2^bits[r][k/64]
+ *  bits       host, uint8 [N][K/64]; each value in {1,2,4,8}
+ *  scales_f16 host, uint16 [N][K/64]; the fp16 bit pattern of s_g
+ *  N, K       N >= 0, K >= 0, K % 64 == 0, K/64 <= 65535, N < 2^31
+ *  stream     the upload is enqueued on it. The call returns after the upload
+ *             has finished, so the host arrays may be freed on return.
+ *  out        receives the new handle. Release it with vbq_matrix_free.
+ *
+ * The host arrays stay owned by the caller. The handle owns its device memory,
+ * allocated here with cudaMalloc on the current device.
+ * Errors: VBQ_ERR_INVALID_ARG (null pointers), VBQ_ERR_SHAPE, VBQ_ERR_BITS,
+ * VBQ_ERR_CODE_RANGE (nothing allocated), VBQ_ERR_OOM, VBQ_ERR_CUDA.
+ */
+VBQ_API vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const uint16_t* scales_f16,
+                    int64_t N, int64_t K, void* stream, vbq_matrix** out);
+
+/* Frees the handle and its device memory. It synchronizes the device first. NULL is a no-op. */
+VBQ_API void vbq_matrix_free(vbq_matrix* m);
+
+/* Fills *info from the handle. Host only, no device work. */
+VBQ_API vbq_status vbq_matrix_info(const vbq_matrix* m, vbq_info* info);
+
+/*
+ * vbq_dequant: packed -> fp32 W (for checking). W[r][k] = s * (q - c_b),
+ * computed exactly in fp32.
+ *  W_dev  device, float [N][K] row-major, caller-owned; every element is written.
+ */
+VBQ_API vbq_status vbq_dequant(const vbq_matrix* m, float* W_dev, void* stream);
+
+/*
+ * vbq_gemv: y = W x for one bf16 activation vector, fp32 accumulation.
+ * Source: the VBQ abstract ("custom fused dequantize-and-multiply kernels",
+ * batch-1 autoregressive decode).
+ *  x_dev  device, bf16 [K] (uint16 bit patterns)
+ *  y_dev  device, float [N]; every element is written (zeros when K == 0)
+ */
+VBQ_API vbq_status vbq_gemv(const vbq_matrix* m, const uint16_t* x_dev, float* y_dev, void* stream);
+
+/*
+ * vbq_gemm_smallbatch: Y[j] = W X[j] for a batch of 1..64 bf16 vectors, fp32 accumulation.
+ *  X_dev  device, bf16 [B][K] row-major
+ *  B      1 <= B <= 64
+ *  Y_dev  device, float [B][N] row-major; every element is written
+ * Batches up to 8 use the CUDA-core decode (each code is decoded once and
+ * reused across the batch). Larger batches use the tensor-core dequant-MMA
+ * path when this build has it.
+ */
+VBQ_API vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X_dev, int32_t B, float* Y_dev,
+                               void* stream);
+
+/*
+ * vbq_model_create: bind the packed projections of a decoder stack for vbq_decode_step.
+ *  desc  host; the shapes. Each matrix must match its projection's (N, K).
+ *  mats  host array of n_layers*7 + 1 handles: per layer q, k, v, o, gate, up,
+ *        down (in that order), then the LM head. The handles must stay alive
+ *        while the model exists. The model does not own them.
+ *  out   receives the model. It owns a device workspace for the activations
+ *        and a CUDA graph built on the first step.
+ */
+VBQ_API vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_matrix* const* mats, vbq_model** out);
+
+VBQ_API void vbq_model_free(vbq_model* model);
+
+/*
+ * vbq_decode_step: one batch-1 decode step (position 0) through the stack.
+ * Source: the VBQ abstract ("memory-bandwidth-bound autoregressive decode").
+ * The glue between projections is this library's reading, since the pages
+ * give no architecture:
+ *   h = x;  per layer:  u = bf16(rmsnorm(h)); q,k,v = Wq u, Wk u, Wv u;
+ *                       a = bf16(v of each head's kv group)   (softmax over one key = 1)
+ *                       h += Wo a;  u = bf16(rmsnorm(h));
+ *                       h += Wdown bf16(silu(Wgate u) * Wup u)
+ *   logits = Whead bf16(rmsnorm(h))
+ * The residual h is fp32. Every projection accumulates in fp32.
+ *  x_dev       device, bf16 [d]
+ *  logits_dev  device, float [vocab]
+ */
+VBQ_API vbq_status vbq_decode_step(vbq_model* model, const uint16_t* x_dev, float* logits_dev, void* stream);
+
+/*
+ * Same step through host buffers: copies x_host (bf16 [d]) in, runs the step,
+ * copies logits (float [vocab]) out and synchronizes the stream before
+ * returning. Pinned host memory makes the copies asynchronous DMA.
+ */
+VBQ_API vbq_status vbq_decode_step_host(vbq_model* model, const uint16_t* x_host, float* logits_host, void* stream);
+
+/*
+ * Teacher-forcing trace. When enabled, each step also records, for every
+ * projection p (layer-major, q..down per layer, then the head), the bf16
+ * input it consumed and its fp32 output. vbq_model_trace_info gives the
+ * offsets. The buffers live in the model, so nothing is recorded unless
+ * enabled. Enabling rebuilds the step's graph.
+ */
+VBQ_API vbq_status vbq_model_set_trace(vbq_model* model, int32_t enable);
+/* in_off/out_off: host int64 [n_layers*7+1]; element offsets into the buffers below. */
+VBQ_API vbq_status vbq_model_trace_info(const vbq_model* model, int64_t* in_off, int64_t* out_off,
+                                int64_t* in_total, int64_t* out_total);
+/* Copies the trace to host arrays (uint16 [in_total], float [out_total]). Synchronizes the device. */
+VBQ_API vbq_status vbq_model_read_trace(const vbq_model* model, uint16_t* in_host, float* out_host);
+
+/*
+ * Dense bf16 GEMV baseline on the same shapes: y = W x, W bf16 [N][K]
+ * row-major (device), x bf16 [K] (device), y float [N] (device). fp32
+ * accumulation. K % 8 == 0.
+ */
+VBQ_API vbq_status vbq_dense_gemv_bf16(const uint16_t* W_dev, const uint16_t* x_dev, float* y_dev, int64_t N,
+                               int64_t K, void* stream);
+
+/*
+ * Reads and clears the device-side check word of the current device. Kernels
+ * set it when a bounded wait runs out. Synchronizes the device. Returns
+ * VBQ_OK, or VBQ_ERR_DEVICE_CHECK with *code set (code may be NULL).
+ */
+VBQ_API vbq_status vbq_device_check(int32_t* code);
+
+/* Number of this library's kernel launches enqueued since the last reset (host counter). */
+VBQ_API int64_t vbq_launch_count(int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VBQ_H */

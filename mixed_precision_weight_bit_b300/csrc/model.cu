@@ -1,0 +1,361 @@
+// vbq_decode_step: one batch-1 decode step through a stack of VBQ projections.
+//
+// VBQ abstract ("Variable Bit-width Quantization ..."): the packed recipe makes
+// memory-bandwidth-bound autoregressive decode faster. The pages give no
+// architecture, so the glue below is this library's reading: unit-gamma
+// RMSNorm, attention at position 0 (a softmax over one key is 1, so each query
+// head returns its kv group's v), SwiGLU, fp32 residual, and bf16 at every
+// projection input.
+//
+// Each step is 1 + 4*n_layers + 1 kernels: h = x; per layer the fused
+// [q;k;v] GEMV (RMSNorm in its prologue), the o GEMV (GQA gather in its
+// prologue, residual add in its epilogue), the fused [gate;up] GEMV (RMSNorm
+// prologue), and the down GEMV (SwiGLU prologue, residual epilogue); then the
+// head GEMV. The sequence is captured once into a CUDA graph. Its edges are
+// programmatic: each GEMV starts streaming its weights while the previous one
+// finishes, and waits (griddepcontrol.wait) only before touching activations.
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "internal.h"
+#include "launch.h"
+
+using namespace vbq;
+
+namespace {
+
+enum { P_Q = 0, P_K, P_V, P_O, P_GATE, P_UP, P_DOWN, P_PER_LAYER };
+
+__global__ void init_h_kernel(const uint16_t* __restrict__ x, float* __restrict__ h, int32_t d) {
+  grid_dep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x)
+    h[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+}
+
+}  // namespace
+
+struct vbq_model {
+  vbq_model_desc desc{};
+  std::vector<const vbq_matrix*> mats;
+  int device = 0;
+  void* ws = nullptr;
+  float* h = nullptr;
+  float* qkv = nullptr;
+  float* gu = nullptr;
+  uint16_t* x_stage = nullptr;
+  float* logits_stage = nullptr;
+  bool trace = false;
+  uint16_t* tr_in = nullptr;
+  float* tr_out = nullptr;
+  std::vector<int64_t> in_off, out_off;
+  int64_t in_total = 0, out_total = 0;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  const uint16_t* g_x = nullptr;
+  float* g_logits = nullptr;
+  int64_t kernels_per_step = 0;
+};
+
+namespace {
+
+int64_t proj_n(const vbq_model_desc& d, int p) {
+  switch (p) {
+    case P_Q: return int64_t(d.n_heads) * d.head_dim;
+    case P_K:
+    case P_V: return int64_t(d.n_kv_heads) * d.head_dim;
+    case P_O:
+    case P_DOWN: return d.d;
+    default: return d.d_ff;
+  }
+}
+int64_t proj_k(const vbq_model_desc& d, int p) {
+  switch (p) {
+    case P_O: return int64_t(d.n_heads) * d.head_dim;
+    case P_DOWN: return d.d_ff;
+    default: return d.d;
+  }
+}
+
+void free_graph(vbq_model* m) {
+  if (m->exec) cudaGraphExecDestroy(m->exec);
+  m->exec = nullptr;
+}
+
+GemvArgs base_args(int* err) {
+  GemvArgs a{};
+  a.err = err;
+  a.ep = EP_STORE;
+  return a;
+}
+
+void add_seg(GemvArgs& a, int& tiles, const vbq_matrix* m, float* y, float* trace_y) {
+  a.seg[a.nseg] = view_of(m, y, static_cast<int32_t>(m->N), trace_y);
+  a.tile_base[a.nseg] = tiles;
+  tiles += m->n_tiles;
+  a.nseg += 1;
+  for (int s = a.nseg; s <= MAX_SEG; ++s) a.tile_base[s] = tiles;
+}
+
+// Enqueues one step; every kernel after the first may launch programmatically.
+cudaError_t enqueue_step(vbq_model* m, const uint16_t* x, float* logits, cudaStream_t st, int* err) {
+  const vbq_model_desc& d = m->desc;
+  const int L = d.n_layers;
+  const int64_t nq = proj_n(d, P_Q), nkv = proj_n(d, P_K);
+  float* q_out = m->qkv;
+  float* k_out = m->qkv + nq;
+  float* v_out = m->qkv + nq + nkv;
+  auto tin = [&](int p) -> uint16_t* { return m->trace ? m->tr_in + m->in_off[p] : nullptr; };
+  auto tout = [&](int p) -> float* { return m->trace ? m->tr_out + m->out_off[p] : nullptr; };
+
+  note_launches(1);
+  init_h_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x, m->h, d.d);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  for (int l = 0; l < L; ++l) {
+    const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
+    const int p0 = l * P_PER_LAYER;
+    {  // [q; k; v] = W u, u = bf16(rmsnorm(h))
+      GemvArgs a = base_args(err);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_Q], q_out, tout(p0 + P_Q));
+      add_seg(a, tiles, W[P_K], k_out, tout(p0 + P_K));
+      add_seg(a, tiles, W[P_V], v_out, tout(p0 + P_V));
+      a.xs.mode = X_RMSNORM;
+      a.xs.K = d.d;
+      a.xs.h = m->h;
+      a.xs.eps = d.rms_eps;
+      a.xs.trace_x = tin(p0 + P_Q);
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+    {  // h += Wo a, a = bf16(v of each head's kv group)
+      GemvArgs a = base_args(err);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_O], m->h, tout(p0 + P_O));
+      a.xs.mode = X_GQA;
+      a.xs.K = static_cast<int32_t>(nq);
+      a.xs.v = v_out;
+      a.xs.head_dim = d.head_dim;
+      a.xs.group = d.n_heads / d.n_kv_heads;
+      a.xs.trace_x = tin(p0 + P_O);
+      a.ep = EP_RESID;
+      a.resid = m->h;
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+    {  // [gate; up] = W u, u = bf16(rmsnorm(h))
+      GemvArgs a = base_args(err);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_GATE], m->gu, tout(p0 + P_GATE));
+      add_seg(a, tiles, W[P_UP], m->gu + d.d_ff, tout(p0 + P_UP));
+      a.xs.mode = X_RMSNORM;
+      a.xs.K = d.d;
+      a.xs.h = m->h;
+      a.xs.eps = d.rms_eps;
+      a.xs.trace_x = tin(p0 + P_GATE);
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+    {  // h += Wdown bf16(silu(gate) * up)
+      GemvArgs a = base_args(err);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_DOWN], m->h, tout(p0 + P_DOWN));
+      a.xs.mode = X_SWIGLU;
+      a.xs.K = d.d_ff;
+      a.xs.gate = m->gu;
+      a.xs.up = m->gu + d.d_ff;
+      a.xs.trace_x = tin(p0 + P_DOWN);
+      a.ep = EP_RESID;
+      a.resid = m->h;
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+  }
+  {  // logits = Whead bf16(rmsnorm(h))
+    GemvArgs a = base_args(err);
+    int tiles = 0;
+    const int ph = L * P_PER_LAYER;
+    add_seg(a, tiles, m->mats[ph], logits, tout(ph));
+    a.xs.mode = X_RMSNORM;
+    a.xs.K = d.d;
+    a.xs.h = m->h;
+    a.xs.eps = d.rms_eps;
+    a.xs.trace_x = tin(ph);
+    if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+vbq_status build_graph(vbq_model* m, const uint16_t* x, float* logits) {
+  free_graph(m);
+  int* err = device_check_word();
+  if (!err) return fail(VBQ_ERR_CUDA, "device check word");
+  warm_gemv(1);
+  const int64_t before = vbq_launch_count(0);
+  VBQ_CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+  cudaError_t e = enqueue_step(m, x, logits, m->cap_stream, err);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &graph);
+  // Capturing enqueues nothing: the counter tracks launches that actually run.
+  m->kernels_per_step = vbq_launch_count(0) - before;
+  note_launches(-m->kernels_per_step);
+  if (e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return cuda_fail(e, "decode step capture");
+  }
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamEndCapture");
+  e = cudaGraphInstantiate(&m->exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) {
+    m->exec = nullptr;
+    return cuda_fail(e, "cudaGraphInstantiate");
+  }
+  m->g_x = x;
+  m->g_logits = logits;
+  return VBQ_OK;
+}
+
+}  // namespace
+
+extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_matrix* const* mats, vbq_model** out) {
+  if (!out) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_create: out is NULL");
+  *out = nullptr;
+  if (!desc || !mats) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_create: NULL desc or mats");
+  const vbq_model_desc d = *desc;
+  if (d.n_layers < 0 || d.d <= 0 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.head_dim <= 0 || d.d_ff <= 0 ||
+      d.vocab <= 0 || d.n_heads % d.n_kv_heads || d.head_dim % 2 || !(d.rms_eps >= 0.0f))
+    return fail(VBQ_ERR_SHAPE, "vbq_model_create: invalid shapes");
+  const int nm = d.n_layers * P_PER_LAYER + 1;
+  int dev = 0;
+  VBQ_CUDA_TRY(cudaGetDevice(&dev));
+  for (int i = 0; i < nm; ++i) {
+    const vbq_matrix* w = mats[i];
+    if (!w) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_create: NULL matrix " + std::to_string(i));
+    const int p = i < nm - 1 ? i % P_PER_LAYER : -1;
+    const int64_t n = p >= 0 ? proj_n(d, p) : d.vocab;
+    const int64_t k = p >= 0 ? proj_k(d, p) : d.d;
+    if (w->N != n || w->K != k)
+      return fail(VBQ_ERR_SHAPE, "vbq_model_create: matrix " + std::to_string(i) + " is " + std::to_string(w->N) +
+                                     "x" + std::to_string(w->K) + ", expected " + std::to_string(n) + "x" +
+                                     std::to_string(k));
+    if (w->device != dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_create: matrices on another device");
+  }
+  auto* m = new (std::nothrow) vbq_model();
+  if (!m) return fail(VBQ_ERR_OOM, "vbq_model_create");
+  m->desc = d;
+  m->device = dev;
+  m->mats.assign(mats, mats + nm);
+  const int64_t nqkv = proj_n(d, P_Q) + 2 * proj_n(d, P_K);
+  auto al = [](int64_t b) { return (b + 255) & ~int64_t(255); };
+  const int64_t b_h = al(4 * d.d), b_qkv = al(4 * nqkv), b_gu = al(8 * int64_t(d.d_ff));
+  const int64_t b_x = al(2 * d.d), b_lg = al(4 * int64_t(d.vocab));
+  cudaError_t e = cudaMalloc(&m->ws, b_h + b_qkv + b_gu + b_x + b_lg);
+  if (e != cudaSuccess) {
+    delete m;
+    return cuda_fail(e, "vbq_model_create: workspace");
+  }
+  char* p = static_cast<char*>(m->ws);
+  m->h = reinterpret_cast<float*>(p);
+  m->qkv = reinterpret_cast<float*>(p + b_h);
+  m->gu = reinterpret_cast<float*>(p + b_h + b_qkv);
+  m->x_stage = reinterpret_cast<uint16_t*>(p + b_h + b_qkv + b_gu);
+  m->logits_stage = reinterpret_cast<float*>(p + b_h + b_qkv + b_gu + b_x);
+  e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    cudaFree(m->ws);
+    delete m;
+    return cuda_fail(e, "vbq_model_create: stream");
+  }
+  // Trace offsets: inputs shared by q/k/v and by gate/up.
+  m->in_off.assign(nm, 0);
+  m->out_off.assign(nm, 0);
+  int64_t io = 0, oo = 0;
+  for (int i = 0; i < nm; ++i) {
+    const int pp = i < nm - 1 ? i % P_PER_LAYER : -1;
+    if (pp == P_K || pp == P_V) {
+      m->in_off[i] = m->in_off[i - (pp - P_Q)];
+    } else if (pp == P_UP) {
+      m->in_off[i] = m->in_off[i - 1];
+    } else {
+      m->in_off[i] = io;
+      io += pp >= 0 ? proj_k(d, pp) : d.d;
+    }
+    m->out_off[i] = oo;
+    oo += pp >= 0 ? proj_n(d, pp) : d.vocab;
+  }
+  m->in_total = io;
+  m->out_total = oo;
+  *out = m;
+  return VBQ_OK;
+}
+
+extern "C" void vbq_model_free(vbq_model* m) {
+  if (!m) return;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  cudaSetDevice(m->device);
+  cudaDeviceSynchronize();
+  free_graph(m);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  cudaFree(m->ws);
+  cudaFree(m->tr_in);
+  cudaFree(m->tr_out);
+  cudaSetDevice(cur);
+  delete m;
+}
+
+extern "C" vbq_status vbq_decode_step(vbq_model* m, const uint16_t* x_dev, float* logits_dev, void* stream) {
+  if (!m || !x_dev || !logits_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: NULL argument");
+  if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 2)
+    return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: misaligned buffer");
+  if (!m->exec || m->g_x != x_dev || m->g_logits != logits_dev) {
+    vbq_status s = build_graph(m, x_dev, logits_dev);
+    if (s != VBQ_OK) return s;
+  }
+  VBQ_CUDA_TRY(cudaGraphLaunch(m->exec, static_cast<cudaStream_t>(stream)));
+  note_launches(m->kernels_per_step);
+  return VBQ_OK;
+}
+
+extern "C" vbq_status vbq_decode_step_host(vbq_model* m, const uint16_t* x_host, float* logits_host, void* stream) {
+  if (!m || !x_host || !logits_host) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_host: NULL argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  VBQ_CUDA_TRY(cudaMemcpyAsync(m->x_stage, x_host, 2 * static_cast<size_t>(m->desc.d), cudaMemcpyHostToDevice, st));
+  vbq_status s = vbq_decode_step(m, m->x_stage, m->logits_stage, stream);
+  if (s != VBQ_OK) return s;
+  VBQ_CUDA_TRY(cudaMemcpyAsync(logits_host, m->logits_stage, 4 * static_cast<size_t>(m->desc.vocab),
+                               cudaMemcpyDeviceToHost, st));
+  VBQ_CUDA_TRY(cudaStreamSynchronize(st));
+  return VBQ_OK;
+}
+
+extern "C" vbq_status vbq_model_set_trace(vbq_model* m, int32_t enable) {
+  if (!m) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_set_trace: NULL model");
+  if (enable && !m->tr_in) {
+    VBQ_CUDA_TRY(cudaMalloc(&m->tr_in, 2 * static_cast<size_t>(m->in_total)));
+    VBQ_CUDA_TRY(cudaMalloc(&m->tr_out, 4 * static_cast<size_t>(m->out_total)));
+  }
+  m->trace = enable != 0;
+  free_graph(m);
+  return VBQ_OK;
+}
+
+extern "C" vbq_status vbq_model_trace_info(const vbq_model* m, int64_t* in_off, int64_t* out_off, int64_t* in_total,
+                                           int64_t* out_total) {
+  if (!m) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_trace_info: NULL model");
+  const size_t nm = m->in_off.size();
+  if (in_off)
+    for (size_t i = 0; i < nm; ++i) in_off[i] = m->in_off[i];
+  if (out_off)
+    for (size_t i = 0; i < nm; ++i) out_off[i] = m->out_off[i];
+  if (in_total) *in_total = m->in_total;
+  if (out_total) *out_total = m->out_total;
+  return VBQ_OK;
+}
+
+extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host, float* out_host) {
+  if (!m || !in_host || !out_host) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_read_trace: NULL argument");
+  if (!m->tr_in) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_read_trace: trace was never enabled");
+  VBQ_CUDA_TRY(cudaDeviceSynchronize());
+  VBQ_CUDA_TRY(cudaMemcpy(in_host, m->tr_in, 2 * static_cast<size_t>(m->in_total), cudaMemcpyDeviceToHost));
+  VBQ_CUDA_TRY(cudaMemcpy(out_host, m->tr_out, 4 * static_cast<size_t>(m->out_total), cudaMemcpyDeviceToHost));
+  return VBQ_OK;
+}

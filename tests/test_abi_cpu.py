@@ -1,0 +1,87 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side validation (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixed_precision_weight_bit_b300 import build as b
+    path = b.build()
+    from mixed_precision_weight_bit_b300 import vbq as V
+    return V.load_library(path)
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "vbq.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"VBQ_API\s+[\w\s\*]*?\b(vbq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for must in ("vbq_pack", "vbq_dequant", "vbq_gemv", "vbq_gemm_smallbatch", "vbq_decode_step",
+                 "vbq_model_create", "vbq_matrix_info", "vbq_status_str"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_symbol(lib):
+    from mixed_precision_weight_bit_b300 import vbq as V
+    for name in declared_functions():
+        assert name in V._SIGNATURES, name
+        assert callable(getattr(V, name)), name
+
+
+def test_status_strings(lib):
+    from mixed_precision_weight_bit_b300 import vbq as V
+    for code, name in V.STATUS_NAMES.items():
+        assert V.vbq_status_str(code) == name
+
+
+def test_pack_validation_errors_without_gpu(lib):
+    """Every check below fails before any CUDA call, so it runs on a CPU-only host."""
+    from mixed_precision_weight_bit_b300 import vbq as V
+    rng = np.random.default_rng(0)
+    codes = rng.integers(0, 2, size=(4, 128)).astype(np.uint8)
+    bits = np.ones((4, 2), np.uint8)
+    scales = np.full((4, 2), 0x3C00, np.uint16)
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_pack(codes[:, :100], np.ones((4, 2), np.uint8), scales)
+    assert e.value.status == 2  # K % 64
+    bad = bits.copy()
+    bad[1, 1] = 3
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_pack(codes, bad, scales)
+    assert e.value.status == 4 and "group index 3" in e.value.detail
+    badc = codes.copy()
+    badc[2, 70] = 2  # 1-bit group holding code 2
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_pack(badc, bits, scales)
+    assert e.value.status == 3
+    out = ctypes.c_void_p()
+    st = lib.vbq_pack(None, None, None, 4, 128, None, ctypes.byref(out))
+    assert st == 1 and out.value is None
+    assert lib.vbq_pack(None, None, None, -1, 64, None, ctypes.byref(out)) == 2
+    assert lib.vbq_pack(None, None, None, 1, 64 * 65536, None, ctypes.byref(out)) == 2
+
+
+def test_null_handles_rejected(lib):
+    from mixed_precision_weight_bit_b300 import vbq as V
+    for fn, args in (("vbq_gemv", (None, None, None, None)), ("vbq_dequant", (None, None, None)),
+                     ("vbq_gemm_smallbatch", (None, None, 1, None, None)),
+                     ("vbq_decode_step", (None, None, None, None))):
+        assert getattr(lib, fn)(*args) == 1, fn
+    assert lib.vbq_model_create(None, None, None) == 1
+    info = V.VbqInfo()
+    assert lib.vbq_matrix_info(None, ctypes.byref(info)) == 1

@@ -1,0 +1,172 @@
+"""GPU decode step against the oracle: every projection under teacher forcing, the glue, and the logits."""
+
+import numpy as np
+import pytest
+
+from oracle import vbq_oracle as O
+from synth import PROJS, gen_model_matrix, gen_x, model_1b, model_matrix_list, model_matrix_shape, model_tiny
+from tests.gpu_util import TOL, bf16_ulp_diff, dev_u16, lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def V(cuda_device):
+    return lib()
+
+
+class Built:
+    def __init__(self, V, shape, seed=0, keep_inputs=True):
+        self.shape = shape
+        self.mats = {}
+        self.handles = []
+        for (layer, proj) in model_matrix_list(shape):
+            m = gen_model_matrix(shape, layer, proj, seed=seed)
+            if keep_inputs:
+                self.mats[(layer, proj)] = m
+            self.handles.append(V.Matrix(m.codes, m.bits, m.scales))
+        self.desc = V.make_model_desc(shape.n_layers, shape.d, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                                      shape.d_ff, shape.vocab, O.RMS_EPS)
+        self.model = V.Model(self.desc, self.handles)
+        self.order = model_matrix_list(shape)
+
+    def get(self, layer, proj):
+        m = self.mats[(layer, proj)]
+        return m.codes, m.bits, m.scales
+
+    def close(self):
+        self.model.close()
+        for h in self.handles:
+            h.close()
+
+
+def run_step(V, b, x, trace=False):
+    import torch
+    V.vbq_model_set_trace(b.model.handle, trace)
+    logits = torch.full((b.shape.vocab,), float("nan"), device="cuda")
+    V.vbq_decode_step(b.model.handle, dev_u16(x), logits)
+    torch.cuda.synchronize()
+    out = logits.cpu().numpy()
+    if not trace:
+        return out, None
+    n = len(b.order)
+    in_off, out_off, it, ot = V.vbq_model_trace_info(b.model.handle, n)
+    tin, tout = V.vbq_model_read_trace(b.model.handle, it, ot)
+    per = {}
+    for i, (layer, proj) in enumerate(b.order):
+        N, K = model_matrix_shape(b.shape, proj)
+        per[(layer, proj)] = (tin[in_off[i]:in_off[i] + K], tout[out_off[i]:out_off[i] + N])
+    return out, per
+
+
+def check_projections(b, per, rows_per_proj=None, seed=0):
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for key, (xin, yout) in per.items():
+        codes, bits, scales = b.get(*key)
+        rows = None
+        if rows_per_proj is not None and codes.shape[0] > rows_per_proj:
+            rows = np.unique(np.r_[0, codes.shape[0] - 1, rng.integers(0, codes.shape[0], rows_per_proj)])
+            codes, bits, scales, yout = codes[rows], bits[rows], scales[rows], yout[rows]
+        ref = O.gemv(codes, bits, scales, xin)
+        err = O.normalized_error(yout, ref, O.row_norms(codes, bits, scales), xin)
+        assert err <= TOL, (key, err)
+        worst = max(worst, err)
+    return worst
+
+
+def check_glue(b, per, x):
+    """Each projection input is the oracle's glue applied to the GPU's own earlier outputs."""
+    s = b.shape
+    h = O.bf16_bits_to_f64(x)
+    near = 0
+    total = 0
+    for layer in range(s.n_layers):
+        u = O.f64_to_bf16_bits(O.rmsnorm(h))
+        d = bf16_ulp_diff(per[(layer, "q")][0], u)
+        near += int((d > 0).sum())
+        total += d.size
+        assert d.max() <= 1
+        v = per[(layer, "v")][1].astype(np.float64)
+        a = O.f64_to_bf16_bits(O.attention_pos0(v, s.n_heads, s.n_kv_heads, s.head_dim))
+        assert np.array_equal(per[(layer, "o")][0], a)  # same fp32 v, same rounding
+        h = h + per[(layer, "o")][1].astype(np.float64)
+        u = O.f64_to_bf16_bits(O.rmsnorm(h))
+        d = bf16_ulp_diff(per[(layer, "gate")][0], u)
+        assert d.max() <= 1
+        near += int((d > 0).sum())
+        total += d.size
+        g = per[(layer, "gate")][1].astype(np.float64)
+        up = per[(layer, "up")][1].astype(np.float64)
+        mm = O.f64_to_bf16_bits(O.silu(g) * up)
+        d = bf16_ulp_diff(per[(layer, "down")][0], mm)
+        assert d.max() <= 1
+        near += int((d > 0).sum())
+        total += d.size
+        h = h + per[(layer, "down")][1].astype(np.float64)
+    u = O.f64_to_bf16_bits(O.rmsnorm(h))
+    d = bf16_ulp_diff(per[(s.n_layers, "head")][0], u)
+    assert d.max() <= 1
+    near += int((d > 0).sum())
+    total += d.size
+    # 1-ulp differences come only from fp32-vs-fp64 values that sit near a bf16 rounding tie
+    assert near <= max(8, total // 200), (near, total)
+
+
+def test_tiny_decode_step_teacher_forced(V):
+    b = Built(V, model_tiny())
+    x = gen_x(b.shape.d, seed=3)
+    logits, per = run_step(V, b, x, trace=True)
+    assert np.isfinite(logits).all()
+    assert np.array_equal(per[(b.shape.n_layers, "head")][1], logits)
+    check_projections(b, per)
+    check_glue(b, per, x)
+    # end to end (information): the fp64 chain from the same x
+    ref = O.decode_step(b.get, b.shape.n_layers, b.shape.n_heads, b.shape.n_kv_heads, b.shape.head_dim, x)
+    hm = b.get(b.shape.n_layers, "head")
+    drift = np.max(np.abs(logits - ref)) / (np.max(O.row_norms(*hm)) * np.sqrt(b.shape.d))
+    assert drift < 2e-2
+    b.close()
+
+
+def test_decode_step_repeatable_and_host_path(V):
+    import torch
+    b = Built(V, model_tiny(), seed=1)
+    x = gen_x(b.shape.d, seed=4)
+    l1, _ = run_step(V, b, x)
+    l2, _ = run_step(V, b, x)          # new device buffers: the graph is rebuilt
+    assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32))
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    lh = torch.empty(b.shape.vocab, dtype=torch.float32).pin_memory()
+    V.vbq_decode_step_host(b.model.handle, xh, lh)
+    assert np.array_equal(lh.numpy().view(np.uint32), l1.view(np.uint32))
+    # trace off and on give the same logits
+    l3, _ = run_step(V, b, x, trace=True)
+    assert np.array_equal(l3.view(np.uint32), l1.view(np.uint32))
+    b.close()
+
+
+def test_model_shape_mismatch_rejected(V):
+    t = model_tiny()
+    mats = []
+    for (layer, proj) in model_matrix_list(t):
+        m = gen_model_matrix(t, layer, proj, seed=0)
+        mats.append(V.Matrix(m.codes, m.bits, m.scales))
+    mats[3], mats[4] = mats[4], mats[3]   # o and gate swapped
+    desc = V.make_model_desc(t.n_layers, t.d, t.n_heads, t.n_kv_heads, t.head_dim, t.d_ff, t.vocab)
+    with pytest.raises(V.VbqError) as e:
+        V.Model(desc, mats)
+    assert e.value.status == 2
+    for m in mats:
+        m.close()
+
+
+def test_1b_decode_step_sampled(V):
+    b = Built(V, model_1b())
+    x = gen_x(b.shape.d, seed=5)
+    logits, per = run_step(V, b, x, trace=True)
+    assert np.isfinite(logits).all()
+    check_projections(b, per, rows_per_proj=24)
+    check_glue(b, per, x)
+    b.close()
+    assert V.vbq_device_check() == 0

@@ -1,0 +1,169 @@
+"""GPU parity of dequant / GEMV / small-batch GEMM against the CPU oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+
+from oracle import vbq_oracle as O
+from synth import (CONFIG0_PROBS, gen_matrix, gen_matrix_with_bits, gen_stress, gen_x, stress_bits)
+from tests.gpu_util import TOL, dev_u16, gemv_err, gpu_dequant, gpu_gemm, gpu_gemv, lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def V(cuda_device):
+    return lib()
+
+
+def _one_class(n, k, b, seed):
+    return gen_matrix_with_bits(np.full((n, k // 64), b, np.uint8), seed, (8, b))
+
+
+CASES = {
+    "config0_768": lambda: gen_matrix(768, 768, CONFIG0_PROBS, seed=0),
+    "ragged_1x64": lambda: gen_matrix(1, 64, CONFIG0_PROBS, seed=1),
+    "ragged_3x128": lambda: gen_matrix(3, 128, CONFIG0_PROBS, seed=2),
+    "ragged_300x1024": lambda: gen_matrix(300, 1024, CONFIG0_PROBS, seed=3),
+    "ragged_257x640": lambda: gen_matrix(257, 640, CONFIG0_PROBS, seed=4),
+    "ragged_511x192": lambda: gen_matrix(511, 192, CONFIG0_PROBS, seed=5),
+    "tall_4099x128": lambda: gen_matrix(4099, 128, CONFIG0_PROBS, seed=6),
+    "all1_200x512": lambda: _one_class(200, 512, 1, 7),
+    "all2_200x512": lambda: _one_class(200, 512, 2, 8),
+    "all4_200x512": lambda: _one_class(200, 512, 4, 9),
+    "all8_200x512": lambda: _one_class(200, 512, 8, 10),
+    "stress_a_1024": lambda: gen_stress("a", 1024, 1024),
+    "stress_b_1024": lambda: gen_stress("b", 1024, 1024),
+    "stress_c_1024": lambda: gen_stress("c", 1024, 1024),
+    "stress_d_1024": lambda: gen_stress("d", 1024, 1024),
+    "stress_e_1024": lambda: gen_stress("e", 1024, 1024),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_dequant_bit_exact(V, name):
+    m = CASES[name]()
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    W = gpu_dequant(V, mat)
+    ref = O.dequant(m.codes, m.bits, m.scales)
+    assert np.array_equal(W.view(np.uint32), ref.view(np.uint32))
+    mat.close()
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_gemv_parity(V, name):
+    m = CASES[name]()
+    x = gen_x(m.K, seed=11)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    y = gpu_gemv(V, mat, x)
+    assert np.isfinite(y).all()
+    assert gemv_err(m, x, y) <= TOL
+    mat.close()
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 5, 7, 8, 9, 13, 16])
+def test_smallbatch_parity(V, B):
+    m = gen_matrix(300, 1024, CONFIG0_PROBS, seed=12)
+    X = gen_x(m.K, seed=13, batch=B)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    Y = gpu_gemm(V, mat, X)
+    assert np.isfinite(Y).all()
+    assert gemv_err(m, X, Y) <= TOL
+    # column j equals the batch-1 result on x_j up to summation order
+    y0 = gpu_gemv(V, mat, X[0])
+    assert gemv_err(m, X[0], y0) <= TOL
+    mat.close()
+
+
+def test_smallbatch_full_width(V):
+    m = gen_matrix(1024, 4096, CONFIG0_PROBS, seed=14)
+    X = gen_x(m.K, seed=15, batch=64)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    Y = gpu_gemm(V, mat, X)
+    rows = np.r_[0:16, 1000:1024]
+    assert gemv_err(m, X, Y, rows) <= TOL
+    mat.close()
+
+
+def test_deterministic(V):
+    m = gen_matrix(2048, 2048, CONFIG0_PROBS, seed=16)
+    x = gen_x(m.K, seed=17)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    a = gpu_gemv(V, mat, x)
+    b = gpu_gemv(V, mat, x)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    mat.close()
+
+
+def test_empty_shapes(V):
+    import torch
+    m0 = gen_matrix(0, 128, CONFIG0_PROBS, seed=18)
+    mat = V.Matrix(m0.codes, m0.bits, m0.scales)
+    assert mat.info()["n_tiles"] == 0
+    V.vbq_gemv(mat.handle, dev_u16(gen_x(128, seed=1)), torch.empty(1, device="cuda"))
+    mat.close()
+    codes = np.zeros((5, 0), np.uint8)
+    mat = V.Matrix(codes, np.zeros((5, 0), np.uint8), np.zeros((5, 0), np.uint16))
+    y = torch.full((5,), 7.0, device="cuda")
+    V.vbq_gemv(mat.handle, dev_u16(np.zeros(2, np.uint16)), y)
+    torch.cuda.synchronize()
+    assert (y.cpu().numpy() == 0).all()
+    mat.close()
+
+
+def test_misaligned_x_rejected(V):
+    import torch
+    m = gen_matrix(8, 128, CONFIG0_PROBS, seed=19)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    xb = torch.zeros(130, dtype=torch.int16, device="cuda")
+    y = torch.zeros(8, device="cuda")
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_gemv(mat.handle, xb.data_ptr() + 2, y)
+    assert e.value.status == 1
+    mat.close()
+
+
+def test_info_accounting(V):
+    m = gen_matrix(777, 1280, CONFIG0_PROBS, seed=20)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    info = mat.info()
+    st = O.storage_bytes(m.bits)
+    assert info["code_bytes"] == st["code_bytes"]
+    assert info["mean_bits"] == pytest.approx(st["mean_bits"])
+    assert info["total_bytes"] == info["code_bytes"] + info["meta_bytes"]
+    for b in (1, 2, 4, 8):
+        assert info["groups_by_bits"][b] == int((m.bits == b).sum())
+    mat.close()
+
+
+# ---- full sizes: sampled rows against the oracle ----
+
+def _sample_rows(n, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.r_[0, 1, n - 2, n - 1, rng.integers(0, n, 60)])
+
+
+def test_full_14336x4096_batch_sweep(V):
+    m = gen_matrix(14336, 4096, CONFIG0_PROBS, seed=0)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    rows = _sample_rows(m.N, 1)
+    for B in (1, 2, 4, 8, 16, 32, 64):
+        X = gen_x(m.K, seed=100 + B, batch=B)
+        Y = gpu_gemm(V, mat, X)
+        assert np.isfinite(Y).all()
+        assert gemv_err(m, X, Y, rows) <= TOL, B
+    mat.close()
+
+
+@pytest.mark.parametrize("case", ["a", "b", "c", "d", "e"])
+def test_full_stress_8192(V, case):
+    m = gen_stress(case, 8192, 8192)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    x = gen_x(m.K, seed=21)
+    y = gpu_gemv(V, mat, x)
+    assert np.isfinite(y).all()
+    assert gemv_err(m, x, y, _sample_rows(m.N, 2)) <= TOL
+    mat.close()
+
+
+def test_device_check_clean(V):
+    assert V.vbq_device_check() == 0
