@@ -9,9 +9,24 @@ from oracle import vbq_oracle as O
 TOL = 2e-3  # max |y - y_ref| / (||W_r|| ||x||), the parity bar for every GEMV/GEMM
 
 
+def build_lib() -> str:
+    """Builds libvbq.so in-tree (no-op when up to date) and returns its path.
+
+    The build script is loaded by path, since importing the package loads the
+    library and fails while it is missing.
+    """
+    import importlib.util
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location(
+        "_vbq_build", os.path.join(root, "mixed_precision_weight_bit_b300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
 def lib():
-    from mixed_precision_weight_bit_b300 import build as b
-    b.build()
+    build_lib()
     import mixed_precision_weight_bit_b300 as V
     return V
 

@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from mixed_precision_weight_bit_b300 import build as b
-    path = b.build()
+    from tests.gpu_util import build_lib
+    path = build_lib()
     from mixed_precision_weight_bit_b300 import vbq as V
     return V.load_library(path)
 

@@ -75,6 +75,23 @@ def check_projections(b, per, rows_per_proj=None, seed=0):
     return worst
 
 
+UNDERFLOW = 2.0 ** -100
+
+
+def glue_ulps(gpu_bits, ref_bits):
+    """bf16 ulp distance, with both-negligible pairs counted as equal.
+
+    silu(g) = g / (1 + exp(-g)) in fp32 returns 0 once exp(-g) overflows
+    (g < -88.7), where the exact fp64 value is below |g| e^g |up| < 1e-30 and
+    still lands on some bf16 subnormal or tiny normal. Pairs whose magnitudes
+    are both below 2^-100 are therefore not compared in ulps.
+    """
+    d = bf16_ulp_diff(gpu_bits, ref_bits)
+    a = np.abs(O.bf16_bits_to_f64(gpu_bits))
+    r = np.abs(O.bf16_bits_to_f64(ref_bits))
+    return np.where((a <= UNDERFLOW) & (r <= UNDERFLOW), 0, d)
+
+
 def check_glue(b, per, x):
     """Each projection input is the oracle's glue applied to the GPU's own earlier outputs."""
     s = b.shape
@@ -99,7 +116,7 @@ def check_glue(b, per, x):
         g = per[(layer, "gate")][1].astype(np.float64)
         up = per[(layer, "up")][1].astype(np.float64)
         mm = O.f64_to_bf16_bits(O.silu(g) * up)
-        d = bf16_ulp_diff(per[(layer, "down")][0], mm)
+        d = glue_ulps(per[(layer, "down")][0], mm)
         assert d.max() <= 1
         near += int((d > 0).sum())
         total += d.size
