@@ -214,6 +214,46 @@ VBQ_API vbq_status vbq_device_check(int32_t* code);
 /* Number of this library's kernel launches enqueued since the last reset (host counter). */
 VBQ_API int64_t vbq_launch_count(int32_t reset);
 
+/*
+ * vbq_decode_step_noalloc: the step of vbq_decode_step for callers that may not
+ * allocate device memory while stepping. Examples are code running while
+ * another component captures the stream into its own CUDA graph (cudaMalloc
+ * is illegal during capture, and vbq_decode_step instantiates a graph of its
+ * own), loops whose device memory is fixed before they start, and hosts that
+ * hand out device memory only from their own pool. The pages have no
+ * counterpart: this is an interface of this library.
+ *
+ * It launches the same kernels in the same order as vbq_decode_step, directly
+ * on `stream` (no graph, no trace), and gives the same logits. The activations
+ * (h, [q;k;v], [gate;up]) live in one static device array of 65,600 floats
+ * (256.25 KiB) that every GPU loading this library holds until the process
+ * exits. The call allocates nothing: no cudaMalloc, no cudaFree, no graph.
+ *
+ *  model       from vbq_model_create, on the current device
+ *  x_dev       device, bf16 [d]
+ *  logits_dev  device, float [vocab]
+ *
+ * Size limit: 64 + r(d) + r(n_heads*head_dim + 2*n_kv_heads*head_dim) +
+ * r(2*d_ff) <= 65,600 floats, where r() rounds up to a multiple of 64 (the
+ * 9B-shaped stack needs 38,976). Larger models get VBQ_ERR_SHAPE and nothing
+ * is enqueued.
+ * Set-up: the first call on each device looks up the array's device address
+ * with cudaGetSymbolAddress and sets the GEMV kernel attributes, with that
+ * device current. Make that first call before any stream capture begins.
+ * Sharing: every call on a device uses the same array, and the array keeps
+ * the last call's contents. Each call writes h, q/k/v and gate/up before it
+ * reads them, so stale contents do no harm. Calls that overlap on the GPU
+ * (two streams, or two host threads) race on the array and give undefined
+ * results; serialize them.
+ * Errors: VBQ_ERR_INVALID_ARG (NULL or misaligned pointers, model on another
+ * device), VBQ_ERR_SHAPE (over the limit), VBQ_ERR_CUDA (a launch failed). A
+ * kernel's bounded wait that runs out is recorded in the array's status word,
+ * which each call clears first. This call does not read it back, because that
+ * would need a synchronization.
+ */
+VBQ_API vbq_status vbq_decode_step_noalloc(vbq_model* model, const uint16_t* x_dev, float* logits_dev,
+                                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,6 +16,9 @@
 // finishes, and waits (griddepcontrol.wait) only before touching activations.
 #include <cuda_runtime.h>
 
+#include <map>
+#include <mutex>
+#include <string>
 #include <vector>
 
 #include "internal.h"
@@ -357,5 +360,158 @@ extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host
   VBQ_CUDA_TRY(cudaDeviceSynchronize());
   VBQ_CUDA_TRY(cudaMemcpy(in_host, m->tr_in, 2 * static_cast<size_t>(m->in_total), cudaMemcpyDeviceToHost));
   VBQ_CUDA_TRY(cudaMemcpy(out_host, m->tr_out, 4 * static_cast<size_t>(m->out_total), cudaMemcpyDeviceToHost));
+  return VBQ_OK;
+}
+
+// ---------------------------------------------------------------- allocation-free decode step
+//
+// vbq_decode_step keeps its activations in a workspace that vbq_model_create
+// allocates, and it builds a CUDA graph on its first call and whenever the x or
+// logits pointers change; instantiating that graph allocates too. Some callers
+// cannot allow any allocation at step time: code that runs while another
+// component is capturing the stream into its own graph (cudaMalloc is illegal
+// during capture), real-time loops whose device memory is fixed before the loop
+// starts, or hosts that hand out device memory only from their own pool.
+// vbq_decode_step_noalloc serves them. It launches the same kernels in the same
+// order, directly on the caller's stream, and keeps the activations in the
+// file-scope array below.
+
+namespace {
+
+// Floats of g_step_scratch: a 64-float status block, then h [d], [q;k;v] and
+// [gate;up], each rounded up to 64 floats. 65536 + 64 floats = 256.25 KiB on
+// every device that loads this library, held until the process exits.
+constexpr int64_t kStepScratchFloats = 65536 + 64;
+static __device__ __align__(256) float g_step_scratch[kStepScratchFloats];
+
+std::mutex g_step_scratch_mu;
+std::map<int, float*> g_step_scratch_addr;  // device ordinal -> device address of g_step_scratch
+
+// Device address of g_step_scratch on the current device. The first call on a
+// device looks it up (and sets the GEMV kernel attributes); later calls only
+// read the cached address.
+vbq_status step_scratch_address(int dev, float** out) {
+  std::lock_guard<std::mutex> lock(g_step_scratch_mu);
+  auto it = g_step_scratch_addr.find(dev);
+  if (it != g_step_scratch_addr.end()) {
+    *out = it->second;
+    return VBQ_OK;
+  }
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: cudaGetSymbolAddress(g_step_scratch)");
+  warm_gemv(1);
+  g_step_scratch_addr[dev] = static_cast<float*>(p);
+  *out = static_cast<float*>(p);
+  return VBQ_OK;
+}
+
+__global__ void init_h_status_kernel(const uint16_t* __restrict__ x, float* __restrict__ h, int32_t d,
+                                     int* __restrict__ status) {
+  grid_dep_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x)
+    h[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+}
+
+int64_t round64(int64_t n) { return (n + 63) & ~int64_t(63); }
+
+// The launch sequence of enqueue_step with the activations at explicit addresses and no trace.
+cudaError_t enqueue_step_at(const vbq_model* m, const uint16_t* x, float* logits, float* h, float* qkv, float* gu,
+                            int* status, cudaStream_t st) {
+  const vbq_model_desc& d = m->desc;
+  const int64_t nq = proj_n(d, P_Q), nkv = proj_n(d, P_K);
+  note_launches(1);
+  init_h_status_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x, h, d.d, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  for (int l = 0; l < d.n_layers; ++l) {
+    const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
+    {
+      GemvArgs a = base_args(status);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_Q], qkv, nullptr);
+      add_seg(a, tiles, W[P_K], qkv + nq, nullptr);
+      add_seg(a, tiles, W[P_V], qkv + nq + nkv, nullptr);
+      a.xs.mode = X_RMSNORM;
+      a.xs.K = d.d;
+      a.xs.h = h;
+      a.xs.eps = d.rms_eps;
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+    {
+      GemvArgs a = base_args(status);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_O], h, nullptr);
+      a.xs.mode = X_GQA;
+      a.xs.K = static_cast<int32_t>(nq);
+      a.xs.v = qkv + nq + nkv;
+      a.xs.head_dim = d.head_dim;
+      a.xs.group = d.n_heads / d.n_kv_heads;
+      a.ep = EP_RESID;
+      a.resid = h;
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+    {
+      GemvArgs a = base_args(status);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_GATE], gu, nullptr);
+      add_seg(a, tiles, W[P_UP], gu + d.d_ff, nullptr);
+      a.xs.mode = X_RMSNORM;
+      a.xs.K = d.d;
+      a.xs.h = h;
+      a.xs.eps = d.rms_eps;
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+    {
+      GemvArgs a = base_args(status);
+      int tiles = 0;
+      add_seg(a, tiles, W[P_DOWN], h, nullptr);
+      a.xs.mode = X_SWIGLU;
+      a.xs.K = d.d_ff;
+      a.xs.gate = gu;
+      a.xs.up = gu + d.d_ff;
+      a.ep = EP_RESID;
+      a.resid = h;
+      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    }
+  }
+  GemvArgs a = base_args(status);
+  int tiles = 0;
+  add_seg(a, tiles, m->mats[static_cast<size_t>(d.n_layers) * P_PER_LAYER], logits, nullptr);
+  a.xs.mode = X_RMSNORM;
+  a.xs.K = d.d;
+  a.xs.h = h;
+  a.xs.eps = d.rms_eps;
+  return launch_gemv(1, a, tiles, st, true, 0);
+}
+
+}  // namespace
+
+extern "C" vbq_status vbq_decode_step_noalloc(vbq_model* m, const uint16_t* x_dev, float* logits_dev, void* stream) {
+  if (!m || !x_dev || !logits_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: NULL argument");
+  if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 2)
+    return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: misaligned buffer");
+  const vbq_model_desc& d = m->desc;
+  const int64_t n_h = round64(d.d);
+  const int64_t n_qkv = round64(proj_n(d, P_Q) + 2 * proj_n(d, P_K));
+  const int64_t n_gu = round64(2 * int64_t(d.d_ff));
+  const int64_t need = 64 + n_h + n_qkv + n_gu;
+  if (need > kStepScratchFloats)
+    return fail(VBQ_ERR_SHAPE, "vbq_decode_step_noalloc: the step needs " + std::to_string(need) +
+                                   " scratch floats (d + q,k,v + 2*d_ff, each rounded up to 64, plus 64); the "
+                                   "static scratch holds " + std::to_string(kStepScratchFloats));
+  int dev = 0;
+  VBQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: model is on another device");
+  float* base = nullptr;
+  vbq_status s = step_scratch_address(dev, &base);
+  if (s != VBQ_OK) return s;
+  float* h = base + 64;
+  float* qkv = h + n_h;
+  float* gu = qkv + n_qkv;
+  cudaError_t e = enqueue_step_at(m, x_dev, logits_dev, h, qkv, gu, reinterpret_cast<int*>(base),
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: launch");
   return VBQ_OK;
 }

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "vbq_model_free": (None, [_P]),
     "vbq_decode_step": (_ST, [_P, _P, _P, _P]),
     "vbq_decode_step_host": (_ST, [_P, _P, _P, _P]),
+    "vbq_decode_step_noalloc": (_ST, [_P, _P, _P, _P]),
     "vbq_model_set_trace": (_ST, [_P, _I32]),
     "vbq_model_trace_info": (_ST, [_P, _P, _P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "vbq_model_read_trace": (_ST, [_P, _P, _P]),
@@ -185,6 +186,11 @@ def vbq_model_free(model: int) -> None:
 
 def vbq_decode_step(model: int, x, logits, stream=None) -> None:
     _check("vbq_decode_step", _L().vbq_decode_step(model, _dptr(x), _dptr(logits), _stream(stream)))
+
+
+def vbq_decode_step_noalloc(model: int, x, logits, stream=None) -> None:
+    _check("vbq_decode_step_noalloc",
+           _L().vbq_decode_step_noalloc(model, _dptr(x), _dptr(logits), _stream(stream)))
 
 
 def _hptr(a) -> int:
