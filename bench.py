@@ -223,7 +223,7 @@ def dominant_kernel_roofline(V, pm, stream, peak_gbs, reps=3):
     achieved = tot_b / (tot_ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
             "frac": round(achieved / peak_gbs, 4), "traffic": None,
-            "kernel": "vbq_gemv_kernel<1,8>", "launches": launches,
+            "kernel": "vbq_gemv_kernel<1,16,8>", "launches": launches,
             "avg_launch_us": round(tot_ms * 1e3 / launches, 2),
             "alg_bytes_per_launch": round(tot_b / launches),
             "note": "each projection of the 9B stack launched alone; algorithmic bytes = codes + 2.25 B/group + 2K + 4N"}

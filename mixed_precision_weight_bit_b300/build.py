@@ -17,7 +17,7 @@ LIB = os.path.join(OUT_DIR, "libvbq.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 CUDA_LIB = "/usr/local/cuda/lib64"
 
-SOURCES = ["pack.cpp", "kernels.cu", "model.cu"]
+SOURCES = ["pack.cpp", "plan.cpp", "kernels.cu", "model.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr"]
 
@@ -57,7 +57,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         logs = list(ex.map(run, cmds))
     link = [NVCC, *GENCODE, "-shared", "-cudart", "shared", "-o", LIB + ".tmp", *objs,
-            "-Xlinker", f"-rpath,{CUDA_LIB}", "-L" + CUDA_LIB]
+            "-Xlinker", f"-rpath,{CUDA_LIB}", "-Xlinker", "--no-undefined", "-L" + CUDA_LIB]
     logs.append(run(link))
     os.replace(LIB + ".tmp", LIB)
     if verbose:

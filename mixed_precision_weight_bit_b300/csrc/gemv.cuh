@@ -5,44 +5,52 @@
 // The abstract's kernels ran on Apple silicon. This kernel is this library's
 // own design for sm_103a:
 //
-//  * One thread-block cluster per row tile. The C CTAs of the cluster split the
-//    tile's step stream evenly, and the warps of a CTA split the CTA's steps.
-//  * Each warp streams its contiguous byte range of step records into a private
-//    4 KB shared-memory ring with 1 KB cp.async.bulk copies, completed on
-//    mbarriers. Every wait is bounded.
-//  * Activations: per group column g, each warp builds a "prep" block in shared
-//    memory from the 64 values of x in that group:
-//      - 1-bit: 16 nibble tables T_j[n] = sum_i (bit_i(n) - 1/2) x_{4j+i}.
-//        One lookup covers 4 weights; 16 entries sit in 16 distinct banks, so
-//        lookups are conflict-free.
-//      - 2/4/8-bit: x'_m = x_m * 2^(8 - f_m*b), where f_m is the field
-//        position of code m inside its byte, and C = sum (x'_m + c_b x_m)
-//        over each lane slice.
-//  * 2/4/8-bit decode: each code byte is shifted to bits 15..22 of a word, and
-//    a field at bit p becomes the float 1 + q*2^(p-23) in one LOP3 (OR
-//    0x3F800000). Then sum x'_m * f_m - C = sum x_m (q_m - c_b), with packed
-//    f32x2 FMAs.
+//  * A host-built plan (layout.h) gives each CTA one contiguous, equal-byte
+//    range of the packed stream. The range is cut into units at tile borders,
+//    and each unit into one slice per warp.
+//  * Each warp streams its slices, unit after unit, through a private ring of
+//    NSLOT 4 KB slots in shared memory with cp.async.bulk copies completed on
+//    mbarriers. The copies start before griddepcontrol.wait, because the packed
+//    weights never depend on the previous kernel. Every wait is bounded. The
+//    first 512 bytes of each copy into slot 0 are also written past the ring's
+//    end, so a record that crosses the end of the ring reads on without
+//    wrapping.
+//  * The warp walks its slice run by run. A run has one group column g and one
+//    bit-class, so each step loop is compiled for its class.
+//  * 1-, 2- and 4-bit groups are stored as bit-planes (layout.h), and
+//    q - (2^b - 1)/2 = sum_p 2^p (q_p - 1/2). So every lane decodes one 64-bit
+//    plane as if it were a 1-bit group, and the b lanes of an entry add their
+//    plane sums with weights 2^p.
+//  * A plane is decoded with the warp shuffle as a lookup table. Per group
+//    column g, lane l holds T_k[l] = sum_{i<5} (bit_i(l) - 1/2) x_{5k+i} for
+//    k = 0..12 (the last table covers 4 values). A 5-bit field of the plane
+//    selects the lane to read from (shfl.idx uses only the low 5 bits of the
+//    lane index), so one shift, one shuffle and one add cover 5 weights.
+//  * 8-bit groups keep one byte per code. A byte permute turns code q into the
+//    float 1 + q*2^-15, so sum x'_m f_m - C = sum x_m (q_m - 127.5), with
+//    x'_m = 2^15 x_m, C = sum (x'_m + 127.5 x_m) per 8-code lane slice, and
+//    packed f32x2 FMAs.
 //  * Per entry, the lanes of the entry are summed with shuffles, then scaled by
 //    the fp16 group scale and added into the warp's fp32 row accumulator in
 //    shared memory. Rows are distinct within a step, so no atomics are needed.
-//  * Warps, then the cluster's CTAs (through DSMEM), are summed in a fixed
-//    order. Results are deterministic.
+//  * At the end of a unit, the CTA sums its warps in a fixed order. A tile cut
+//    between CTAs writes one partial per unit, and the last CTA to arrive adds
+//    them in split order. Results are therefore deterministic.
 #pragma once
 
-#include <cooperative_groups.h>
+#include <type_traits>
 
 #include "layout.h"
 #include "ptx.cuh"
 
 namespace vbq {
 
-namespace cg = cooperative_groups;
-
-constexpr int RING = 4096;           // bytes per warp
-constexpr int CHUNK = 1024;          // bytes per bulk copy
-constexpr int NSLOT = RING / CHUNK;  // chunks in flight per warp
-constexpr int XPF = 464;             // floats of activation prep per (warp, column)
-constexpr int XP_LUT = 0, XP_2 = 256, XP_4 = 320, XP_8 = 384, XC_2 = 448, XC_4 = 450, XC_8 = 454;
+constexpr int CH = 4096;             // bytes per bulk copy and per ring slot
+constexpr int LOG_CH = 12;
+constexpr int SPILL = 512;           // bytes past the ring's end (>= the largest record, 352 B)
+constexpr int XPF = 144;             // floats of activation prep per (warp, column)
+constexpr int XP_X = 0, XP_8 = 64, XC_8 = 128;  // x (64), 2^15 x (64), 8-bit slice constants (8)
+constexpr int NLUT = 13;             // 5-bit lookup tables per group (the last covers 4 codes)
 constexpr int MAX_SEG = 3;
 
 enum XMode : int { X_BF16 = 0, X_RMSNORM = 1, X_GQA = 2, X_SWIGLU = 3 };
@@ -50,15 +58,18 @@ enum EpMode : int { EP_STORE = 0, EP_RESID = 1 };
 
 struct MatView {
   const uint8_t* data;
-  const uint32_t* desc;
-  const uint32_t* off;
-  const uint32_t* row0;
-  const uint32_t* step0;
-  int32_t n_tiles;
-  int32_t N;
-  float* y;        // output rows of this segment, column j at y + j*y_ld
+  const uint32_t* run_desc;
+  float* y;        // output rows of this matrix, column j at y + j*y_ld
   int32_t y_ld;
   float* trace_y;  // optional raw-output copy (decode-step trace)
+};
+
+struct PlanView {
+  const UnitRec* units;    // CTA c: slots [c*umax, (c+1)*umax)
+  const SliceRec* slices;  // SLICES per slot
+  int32_t umax;
+  float* partial;          // split-tile partial rows
+  uint32_t* counters;      // split-tile arrival counters, zero between launches
 };
 
 // Where the activation x (bf16 [NB][K]) comes from.
@@ -79,209 +90,332 @@ struct XSource {
 struct GemvArgs {
   MatView seg[MAX_SEG];
   int32_t nseg;
-  int32_t tile_base[MAX_SEG + 1];  // cumulative tiles: segment s owns [tile_base[s], tile_base[s+1])
+  PlanView plan;
   XSource xs;
   int32_t ep;
   const float* resid;  // EP_RESID: y = resid + acc (may alias seg[0].y)
   int* err;
 };
 
-template <int NB, int NWARPS>
+template <int NB, int W, int NSLOT>
 struct GemvSmem {
+  static constexpr int kRingBytes = NSLOT * CH;
+  static constexpr int kRingStride = kRingBytes + SPILL;
   static constexpr int kRing = 0;
-  static constexpr int kXp = kRing + NWARPS * RING;
-  static constexpr int kAcc = kXp + NWARPS * NB * XPF * 4;
-  static constexpr int kPart = kAcc + NWARPS * NB * TILE_MAX * 4;
-  static constexpr int kBar = kPart + NB * TILE_MAX * 4;
-  static constexpr int kMisc = kBar + NWARPS * NSLOT * 8;
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kXp = kRing + W * kRingStride;
+  static constexpr int kAcc = kXp + W * NB * XPF * 4;
+  static constexpr int kBar = kAcc + W * NB * TILE_MAX * 4;
+  static constexpr int kMisc = kBar + W * NSLOT * 8;
+  static constexpr int kBytes = kMisc + 64 * 4;
+  static_assert((kRingBytes & (kRingBytes - 1)) == 0, "ring must be a power of two");
+  static_assert(kXp % 64 == 0 && (XPF * 4) % 64 == 0, "prep blocks must be 64-byte aligned");
 };
+
+extern __shared__ __align__(1024) uint8_t vbq_smem[];
+
+template <typename T>
+__device__ __forceinline__ T lds(uint32_t off) {
+  return *reinterpret_cast<const T*>(vbq_smem + off);
+}
+template <typename T>
+__device__ __forceinline__ void sts(uint32_t off, T v) {
+  *reinterpret_cast<T*>(vbq_smem + off) = v;
+}
 
 // ---- activation values ---------------------------------------------------
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-// x[k], x[k+1] (k even) of batch column col, as the bf16 values the projection consumes.
-__device__ __forceinline__ float2 x_pair(const XSource& xs, int col, int k, float inv_rms) {
+// The inputs from which x[k], x[k+1] (k even) of column col are made.
+struct XRaw {
+  float a, b, c, d;
+};
+
+__device__ __forceinline__ XRaw x_load(const XSource& xs, int col, int k) {
+  XRaw r{0.f, 0.f, 0.f, 0.f};
   switch (xs.mode) {
     case X_BF16: {
       const uint32_t v = ldg_nc_u32(xs.x + static_cast<int64_t>(col) * xs.ldx + k);
-      return make_float2(bf16_lo(v), bf16_hi(v));
+      r.a = bf16_lo(v);
+      r.b = bf16_hi(v);
+      break;
     }
     case X_RMSNORM: {
       const float2 h = *reinterpret_cast<const float2*>(xs.h + k);
-      return make_float2(round_bf16(h.x * inv_rms), round_bf16(h.y * inv_rms));
+      r.a = h.x;
+      r.b = h.y;
+      break;
     }
     case X_GQA: {
       const int head = k / xs.head_dim, j = k - head * xs.head_dim;
       const float2 v = *reinterpret_cast<const float2*>(xs.v + (head / xs.group) * xs.head_dim + j);
-      return make_float2(round_bf16(v.x), round_bf16(v.y));
+      r.a = v.x;
+      r.b = v.y;
+      break;
     }
     default: {
       const float2 g = *reinterpret_cast<const float2*>(xs.gate + k);
       const float2 u = *reinterpret_cast<const float2*>(xs.up + k);
-      return make_float2(round_bf16(silu_f(g.x) * u.x), round_bf16(silu_f(g.y) * u.y));
+      r.a = g.x;
+      r.b = g.y;
+      r.c = u.x;
+      r.d = u.y;
+      break;
     }
+  }
+  return r;
+}
+
+// x[k], x[k+1] as the bf16 values the projection consumes.
+__device__ __forceinline__ float2 x_make(const XSource& xs, const XRaw& r, float inv_rms) {
+  switch (xs.mode) {
+    case X_BF16: return make_float2(r.a, r.b);
+    case X_RMSNORM: return make_float2(round_bf16(r.a * inv_rms), round_bf16(r.b * inv_rms));
+    case X_GQA: return make_float2(round_bf16(r.a), round_bf16(r.b));
+    default: return make_float2(round_bf16(silu_f(r.a) * r.c), round_bf16(silu_f(r.b) * r.d));
   }
 }
 
-// Builds the prep block of one column for group g (whole warp; lane owns x_{2l}, x_{2l+1}).
-__device__ __forceinline__ void build_prep(float* xp, float x0, float x1, int lane) {
-  // 1-bit nibble tables: lane covers table j = lane/2, entries n = 8h..8h+7.
-  const int j = lane >> 1, h = lane & 1;
-  const float a0 = __shfl_sync(0xffffffffu, x0, 2 * j), a1 = __shfl_sync(0xffffffffu, x1, 2 * j);
-  const float a2 = __shfl_sync(0xffffffffu, x0, 2 * j + 1), a3 = __shfl_sync(0xffffffffu, x1, 2 * j + 1);
-  const float s3 = h ? a3 : -a3;
-  float t[8];
+// Builds the prep of one column for group g (whole warp; lane owns x_{2l}, x_{2l+1}):
+// the 8-bit block in shared memory and this lane's lookup-table registers.
+__device__ __forceinline__ void build_prep(uint32_t xp, float x0, float x1, int lane, const float (&sgn)[5],
+                                           float (&lut)[NLUT]) {
+  sts(xp + (XP_X + 2 * lane) * 4, make_float2(x0, x1));
+  const float p0 = x0 * 32768.0f, p1 = x1 * 32768.0f;
+  sts(xp + (XP_8 + 2 * lane) * 4, make_float2(p0, p1));
+  float c8 = (p0 + p1) + 127.5f * (x0 + x1);
+  c8 += __shfl_xor_sync(0xffffffffu, c8, 1);
+  c8 += __shfl_xor_sync(0xffffffffu, c8, 2);
+  if ((lane & 3) == 0) sts(xp + (XC_8 + (lane >> 2)) * 4, c8);
+  __syncwarp();
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    t[k] = 0.5f * ((((k & 1) ? a0 : -a0) + ((k & 2) ? a1 : -a1)) + ((k & 4) ? a2 : -a2) + s3);
-  float4* dst = reinterpret_cast<float4*>(xp + XP_LUT + 16 * j + 8 * h);
-  dst[0] = make_float4(t[0], t[1], t[2], t[3]);
-  dst[1] = make_float4(t[4], t[5], t[6], t[7]);
-  // Pre-scaled copies for the 2/4/8-bit decode: field f of code m gets 2^(8 - f*b).
-  const float f2a = (lane & 1) ? 16.0f : 256.0f, f2b = (lane & 1) ? 4.0f : 64.0f;
-  const float p2a = x0 * f2a, p2b = x1 * f2b;
-  const float p4a = x0 * 256.0f, p4b = x1 * 16.0f;
-  const float p8a = x0 * 256.0f, p8b = x1 * 256.0f;
-  reinterpret_cast<float2*>(xp + XP_2)[lane] = make_float2(p2a, p2b);
-  reinterpret_cast<float2*>(xp + XP_4)[lane] = make_float2(p4a, p4b);
-  reinterpret_cast<float2*>(xp + XP_8)[lane] = make_float2(p8a, p8b);
-  // Slice constants C = sum over the slice of (x'_m + c_b x_m).
-  const float xs = x0 + x1;
-  float c2 = (p2a + p2b) + 1.5f * xs;
-  float c4 = (p4a + p4b) + 7.5f * xs;
-  float c8 = (p8a + p8b) + 127.5f * xs;
+  for (int k = 0; k < NLUT; ++k) lut[k] = 0.0f;
 #pragma unroll
-  for (int d = 1; d < 16; d <<= 1) c2 += __shfl_xor_sync(0xffffffffu, c2, d);
+  for (int q = 0; q < 16; ++q) {
+    const float4 v = lds<float4>(xp + (XP_X + 4 * q) * 4);
+    const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int d = 1; d < 8; d <<= 1) c4 += __shfl_xor_sync(0xffffffffu, c4, d);
-#pragma unroll
-  for (int d = 1; d < 4; d <<= 1) c8 += __shfl_xor_sync(0xffffffffu, c8, d);
-  if ((lane & 15) == 0) xp[XC_2 + (lane >> 4)] = c2;
-  if ((lane & 7) == 0) xp[XC_4 + (lane >> 3)] = c4;
-  if ((lane & 3) == 0) xp[XC_8 + (lane >> 2)] = c8;
+    for (int u = 0; u < 4; ++u) {
+      const int m = 4 * q + u;
+      lut[m / 5] = fmaf(sgn[m % 5], e[u], lut[m / 5]);
+    }
+  }
 }
 
 // ---- decode -------------------------------------------------------------
 
-// 1-bit entry: sum over 16 nibbles of T_j[nibble_j] = sum_m (q_m - 1/2) x_m.
+// One 64-bit plane (w1:w0) against the lookup tables: sum_m (bit_m - 1/2) x_m.
 template <int NB>
-__device__ __forceinline__ void decode_lut(uint2 cw, uint32_t xp_addr, float (&t)[NB]) {
-  float a[NB][4];
-#pragma unroll
-  for (int c = 0; c < NB; ++c) a[c][0] = a[c][1] = a[c][2] = a[c][3] = 0.0f;
-#pragma unroll
-  for (int wi = 0; wi < 2; ++wi) {
-    const uint32_t w = wi ? cw.y : cw.x;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t nib4 = (i == 0) ? (w << 2) : (w >> (4 * i - 2));
-      const uint32_t addr = (nib4 & 0x3Cu) | xp_addr;  // xp_addr is 64-byte aligned
-#pragma unroll
-      for (int c = 0; c < NB; ++c) a[c][i & 3] += lds_f32(addr + c * XPF * 4 + (wi * 8 + i) * 64);
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < NB; ++c) t[c] = (a[c][0] + a[c][1]) + (a[c][2] + a[c][3]);
-}
-
-// b-bit entry slice (b = 2, 4, 8): 64/b codes in the lane's 8 bytes.
-template <int NB, int BITS>
-__device__ __forceinline__ void decode_direct(uint2 cw, const float* xp, uint32_t sigma, float (&t)[NB]) {
-  constexpr int F = 8 / BITS;       // fields per byte
-  constexpr int NPER = 64 / BITS;   // codes per slice
-  constexpr uint32_t MK = (1u << BITS) - 1u;
-  constexpr int XOFF = BITS == 2 ? XP_2 : BITS == 4 ? XP_4 : XP_8;
-  constexpr int COFF = BITS == 2 ? XC_2 : BITS == 4 ? XC_4 : XC_8;
-  float fv[NPER];
-#pragma unroll
-  for (int wi = 0; wi < 2; ++wi) {
-    const uint32_t w = wi ? cw.y : cw.x;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t S = (i == 0) ? (w << 15) : (i == 1) ? (w << 7) : (i == 2) ? (w >> 1) : (w >> 9);
-#pragma unroll
-      for (int f = 0; f < F; ++f)
-        fv[(wi * 4 + i) * F + f] = __uint_as_float((S & (MK << (15 + f * BITS))) | 0x3F800000u);
-    }
-  }
+__device__ __forceinline__ void decode_plane(uint2 cw, const float (&lut)[NB][NLUT], float (&t)[NB]) {
+  const uint32_t w0 = cw.x, w1 = cw.y;
+  const uint32_t f[NLUT] = {w0,       w0 >> 5,  w0 >> 10, w0 >> 15, w0 >> 20, w0 >> 25, __funnelshift_r(w0, w1, 30),
+                            w1 >> 3,  w1 >> 8,  w1 >> 13, w1 >> 18, w1 >> 23, w1 >> 28};
 #pragma unroll
   for (int c = 0; c < NB; ++c) {
-    const float4* xs = reinterpret_cast<const float4*>(xp + c * XPF + XOFF + sigma * NPER);
-    float2 acc = make_float2(0.0f, 0.0f);
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int p = 0; p < NPER / 4; ++p) {
-      const float4 xv = xs[p];
-      acc = __ffma2_rn(make_float2(xv.x, xv.y), make_float2(fv[4 * p], fv[4 * p + 1]), acc);
-      acc = __ffma2_rn(make_float2(xv.z, xv.w), make_float2(fv[4 * p + 2], fv[4 * p + 3]), acc);
-    }
-    t[c] = (acc.x + acc.y) - xp[c * XPF + COFF + sigma];
+    for (int k = 0; k < NLUT; ++k) a[k & 3] += __shfl_sync(0xffffffffu, lut[c][k], static_cast<int>(f[k]));
+    t[c] = (a[0] + a[1]) + (a[2] + a[3]);
   }
 }
+
+// 8-bit entry slice: codes [8*sigma, 8*sigma + 8) in the lane's 8 bytes.
+template <int NB>
+__device__ __forceinline__ void decode_bytes(uint2 cw, uint32_t xp, uint32_t sigma, float (&t)[NB]) {
+  float fv[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    fv[i] = __uint_as_float(__byte_perm(cw.x, 0x3F800000u, 0x7604u | (i << 4)));
+    fv[4 + i] = __uint_as_float(__byte_perm(cw.y, 0x3F800000u, 0x7604u | (i << 4)));
+  }
+  const uint32_t xs = xp + (XP_8 + 8 * sigma) * 4;
+#pragma unroll
+  for (int c = 0; c < NB; ++c) {
+    const float4 xa = lds<float4>(xs + c * XPF * 4);
+    const float4 xb = lds<float4>(xs + c * XPF * 4 + 16);
+    float2 acc = make_float2(0.0f, 0.0f);
+    acc = __ffma2_rn(make_float2(xa.x, xa.y), make_float2(fv[0], fv[1]), acc);
+    acc = __ffma2_rn(make_float2(xa.z, xa.w), make_float2(fv[2], fv[3]), acc);
+    acc = __ffma2_rn(make_float2(xb.x, xb.y), make_float2(fv[4], fv[5]), acc);
+    acc = __ffma2_rn(make_float2(xb.z, xb.w), make_float2(fv[6], fv[7]), acc);
+    t[c] = (acc.x + acc.y) - lds<float>(xp + (c * XPF + XC_8 + sigma) * 4);
+  }
+}
+
+// One step of class CLS with e entries whose record starts at shared offset rb.
+// pw = 2^(plane) for the lane's plane (classes 1 and 2).
+template <int NB, int CLS>
+__device__ __forceinline__ void do_step(uint32_t rb, uint32_t e, uint32_t xp, uint32_t acc, int lane,
+                                        const float (&lut)[NB][NLUT], float pw) {
+  const uint32_t j = static_cast<uint32_t>(lane) >> CLS;
+  const uint32_t sigma = static_cast<uint32_t>(lane) & ((1u << CLS) - 1u);
+  const bool active = j < e;
+  uint2 cw = make_uint2(0u, 0u);
+  if (active) cw = lds<uint2>(rb + 8u * lane);
+  float tv[NB];
+  if (CLS == 3) {
+    decode_bytes<NB>(cw, xp, sigma, tv);
+  } else {
+    decode_plane<NB>(cw, lut, tv);
+    if (CLS > 0) {
+#pragma unroll
+      for (int c = 0; c < NB; ++c) tv[c] *= pw;
+    }
+  }
+#pragma unroll
+  for (int d = 1; d < (1 << CLS); d <<= 1) {
+#pragma unroll
+    for (int c = 0; c < NB; ++c) tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], d);
+  }
+  if (active && sigma == 0) {
+    const uint16_t sb = lds<uint16_t>(rb + rec_scale_off(CLS, e) + 2u * j);
+    const uint32_t row = lds<uint8_t>(rb + rec_row_off(CLS, e) + j);
+    const float sc = __half2float(__ushort_as_half(sb));
+#pragma unroll
+    for (int c = 0; c < NB; ++c) {
+      const uint32_t ao = acc + (c * TILE_MAX + row) * 4;
+      sts(ao, fmaf(sc, tv[c], lds<float>(ao)));
+    }
+  }
+}
+
+// Per-warp stream state: the ring, the chunks issued and landed.
+struct WarpStream {
+  uint32_t ring;      // shared offset of the ring
+  uint32_t bar;       // shared address of the first slot's mbarrier
+  uint32_t L;         // stream bytes
+  uint32_t nch;       // chunks
+  uint32_t issued, landed;
+  uint32_t avail;     // bytes known to have landed
+  uint32_t refill_at; // stream offset at which the next chunk may be issued
+  int pu;             // producer: unit being copied
+  uint32_t ppos;      // producer: bytes of it already copied
+  bool ok;
+};
 
 // ---- the kernel ---------------------------------------------------------
 
-template <int NB, int NWARPS>
-__global__ void __launch_bounds__(NWARPS * 32) vbq_gemv_kernel(const __grid_constant__ GemvArgs a) {
-  using L = GemvSmem<NB, NWARPS>;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = static_cast<int>(cluster.num_blocks());
-  const int rank = static_cast<int>(cluster.block_rank());
+template <int NB, int W, int NSLOT>
+__global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_constant__ GemvArgs a) {
+  using Lay = GemvSmem<NB, W, NSLOT>;
+  constexpr int SPW = SLICES / W;  // plan slices per warp
+  constexpr uint32_t RING = static_cast<uint32_t>(Lay::kRingBytes);
+  constexpr uint32_t RMASK = RING - 1u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tglob = blockIdx.x / C;
+  const int umax = a.plan.umax;
 
-  int sidx = 0;
+  // Lane i holds unit slot i of this CTA and this warp's slice of it.
+  uint32_t u_seg = 0, u_split = 0, u_nsplit = 0, u_pbase = 0, u_cnt = 0, u_r0 = 0, u_rows = 0;
+  uint32_t s_run0 = 0, s_k0 = 0, s_run1 = 0, s_k1 = 0, s_b0 = 0, s_b1 = 0, s_g0 = 0;
+  if (lane < umax) {
+    const size_t slot = static_cast<size_t>(blockIdx.x) * umax + lane;
+    const UnitRec ur = a.plan.units[slot];
+    u_seg = ur.seg;
+    u_split = ur.split;
+    u_nsplit = ur.nsplit;
+    u_pbase = ur.pbase;
+    u_cnt = ur.cnt;
+    u_r0 = ur.r0;
+    u_rows = ur.rows;
+    const SliceRec* sl = a.plan.slices + slot * SLICES + warp * SPW;
+    const SliceRec f = sl[0];
+    const SliceRec l = sl[SPW - 1];
+    s_run0 = f.run0;
+    s_k0 = f.k0;
+    s_b0 = f.b0;
+    s_g0 = f.g0;
+    s_run1 = l.run1;
+    s_k1 = l.k1;
+    s_b1 = l.b1;
+    if (SPW > 1 && f.b1 == f.b0) s_g0 = l.g0;  // the first slice is empty
+  }
+  const int nu = __popc(__ballot_sync(0xffffffffu, u_nsplit > 0u));
+  uint32_t len16 = lane < nu ? s_b1 - s_b0 : 0u;
 #pragma unroll
-  for (int s = 1; s < MAX_SEG; ++s)
-    if (s < a.nseg && tglob >= a.tile_base[s]) sidx = s;
-  const MatView& M = a.seg[sidx];
-  const int t = tglob - a.tile_base[sidx];
-  const uint32_t r0 = M.row0[t], rows = M.row0[t + 1] - r0;
-  const uint32_t s0 = M.step0[t], ns = M.step0[t + 1] - s0;
-  const uint32_t ca = s0 + static_cast<uint32_t>((static_cast<uint64_t>(ns) * rank) / C);
-  const uint32_t cb = s0 + static_cast<uint32_t>((static_cast<uint64_t>(ns) * (rank + 1)) / C);
-  const uint32_t wa = ca + static_cast<uint32_t>((static_cast<uint64_t>(cb - ca) * warp) / NWARPS);
-  const uint32_t wb = ca + static_cast<uint32_t>((static_cast<uint64_t>(cb - ca) * (warp + 1)) / NWARPS);
+  for (int d = 16; d >= 1; d >>= 1) len16 += __shfl_xor_sync(0xffffffffu, len16, d);
 
-  uint8_t* ring = smem + L::kRing + warp * RING;
-  const uint32_t ring_a = smem_u32(ring);
-  float* xp = reinterpret_cast<float*>(smem + L::kXp) + warp * NB * XPF;
-  const uint32_t xp_a = smem_u32(xp);
-  float* acc = reinterpret_cast<float*>(smem + L::kAcc) + warp * NB * TILE_MAX;
-  float* part = reinterpret_cast<float*>(smem + L::kPart);
-  const uint32_t bar_a = smem_u32(smem + L::kBar) + warp * NSLOT * 8;
-  float* misc = reinterpret_cast<float*>(smem + L::kMisc);
-
-  // Start streaming this warp's weights before waiting on the previous kernel:
-  // the packed weights never depend on it.
-  const uint64_t gbase = static_cast<uint64_t>(M.off[wa]) * 16u;
-  const uint32_t len = static_cast<uint32_t>(static_cast<uint64_t>(M.off[wb]) * 16u - gbase);
-  const uint32_t nch = (len + CHUNK - 1) / CHUNK;
+  WarpStream S;
+  S.ring = Lay::kRing + warp * Lay::kRingStride;
+  S.bar = smem_u32(vbq_smem + Lay::kBar) + warp * NSLOT * 8;
+  S.L = len16 * 16u;
+  S.nch = (S.L + CH - 1) >> LOG_CH;
+  S.issued = S.landed = S.avail = 0;
+  S.pu = 0;
+  S.ppos = 0;
+  S.ok = true;
+  const uint32_t ring_a = smem_u32(vbq_smem) + S.ring;
   const uint64_t pol = l2_evict_first_policy();
-  const uint8_t* gsrc = M.data + gbase;
-  uint32_t issued = nch < NSLOT ? nch : NSLOT;
+
+  auto issue_next = [&]() {  // warp-uniform; lane 0 issues the copies
+    const uint32_t slot = S.issued & (NSLOT - 1);
+    const uint32_t bytes = min(static_cast<uint32_t>(CH), S.L - S.issued * CH);
+    const uint32_t spill = (slot == 0 && S.issued > 0) ? min(static_cast<uint32_t>(SPILL), bytes) : 0u;
+    const uint32_t bar = S.bar + 8 * slot;
+    if (lane == 0) mbar_arrive_expect_tx(bar, bytes + spill);
+    uint32_t done = 0;
+    while (done < bytes && S.pu < nu) {
+      const uint32_t ub0 = __shfl_sync(0xffffffffu, s_b0, S.pu);
+      const uint32_t ub1 = __shfl_sync(0xffffffffu, s_b1, S.pu);
+      const uint32_t useg = __shfl_sync(0xffffffffu, u_seg, S.pu);
+      const uint32_t ulen = (ub1 - ub0) * 16u;
+      const uint32_t take = min(ulen - S.ppos, bytes - done);
+      if (take > 0 && lane == 0) {
+        const uint8_t* src = a.seg[useg].data + static_cast<uint64_t>(ub0) * 16u + S.ppos;
+        bulk_g2s(ring_a + slot * CH + done, src, take, bar, pol);
+        if (done < spill) bulk_g2s(ring_a + RING + done, src, min(take, spill - done), bar, pol);
+      }
+      done += take;
+      S.ppos += take;
+      if (S.ppos == ulen) {
+        ++S.pu;
+        S.ppos = 0;
+      }
+    }
+    ++S.issued;
+    S.refill_at = S.issued < S.nch ? (S.issued + 1 - NSLOT) * CH : 0xFFFFFFFFu;
+  };
+
   if (lane == 0) {
 #pragma unroll
-    for (int i = 0; i < NSLOT; ++i) mbar_init(bar_a + 8 * i, 1);
+    for (int i = 0; i < NSLOT; ++i) mbar_init(S.bar + 8 * i, 1);
     fence_mbarrier_init();
-    for (uint32_t i = 0; i < issued; ++i) {
-      const uint32_t bytes = min(static_cast<uint32_t>(CHUNK), len - i * CHUNK);
-      mbar_arrive_expect_tx(bar_a + 8 * i, bytes);
-      bulk_g2s(ring_a + i * CHUNK, gsrc + static_cast<uint64_t>(i) * CHUNK, bytes, bar_a + 8 * i, pol);
-    }
   }
-  for (int i = lane; i < NB * TILE_MAX; i += 32) acc[i] = 0.0f;
   __syncwarp();
+  S.refill_at = 0xFFFFFFFFu;
+  while (S.issued < S.nch && S.issued < static_cast<uint32_t>(NSLOT)) issue_next();
 
+  const uint32_t xp = Lay::kXp + warp * NB * XPF * 4;
+  float sgn[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) sgn[i] = ((lane >> i) & 1) ? 0.5f : -0.5f;
+  const float pw2 = (lane & 1) ? 2.0f : 1.0f;
+  const float pw4 = static_cast<float>(1 << (lane & 3));
+  float lut[NB][NLUT];
+#pragma unroll
+  for (int c = 0; c < NB; ++c)
+#pragma unroll
+    for (int k = 0; k < NLUT; ++k) lut[c][k] = 0.0f;
+  const uint32_t acc = Lay::kAcc + warp * NB * TILE_MAX * 4;
+  float* misc = reinterpret_cast<float*>(vbq_smem + Lay::kMisc);
+  for (int i = lane; i < NB * TILE_MAX; i += 32) sts(acc + i * 4, 0.0f);
+
+  // The next kernel may start streaming its own weights now.
+  grid_dep_launch();
   grid_dep_wait();
+
+  // Start loading x for the first group column before the RMSNorm reduction.
+  int pre_g = nu > 0 ? static_cast<int>(__shfl_sync(0xffffffffu, s_g0, 0)) : -1;
+  XRaw pre[NB];
+  if (pre_g >= 0) {
+#pragma unroll
+    for (int c = 0; c < NB; ++c) pre[c] = x_load(a.xs, c, pre_g * GROUP + 2 * lane);
+  }
 
   // RMSNorm scale, when the input is rmsnorm(h): every CTA reduces h in the same order.
   float inv_rms = 1.0f;
   if (a.xs.mode == X_RMSNORM) {
     float ss = 0.0f;
-    for (int k = threadIdx.x; k < a.xs.K; k += NWARPS * 32) {
+    for (int k = threadIdx.x; k < a.xs.K; k += W * 32) {
       const float v = a.xs.h[k];
       ss = fmaf(v, v, ss);
     }
@@ -291,143 +425,196 @@ __global__ void __launch_bounds__(NWARPS * 32) vbq_gemv_kernel(const __grid_cons
     __syncthreads();
     if (threadIdx.x == 0) {
       float tot = 0.0f;
-      for (int w = 0; w < NWARPS; ++w) tot += misc[w];
-      misc[NWARPS] = 1.0f / sqrtf(tot / static_cast<float>(a.xs.K) + a.xs.eps);
+      for (int w = 0; w < W; ++w) tot += misc[w];
+      misc[W] = 1.0f / sqrtf(tot / static_cast<float>(a.xs.K) + a.xs.eps);
     }
     __syncthreads();
-    inv_rms = misc[NWARPS];
+    inv_rms = misc[W];
   }
   if (a.xs.trace_x && blockIdx.x == 0) {
-    for (int k = 2 * threadIdx.x; k < a.xs.K; k += 2 * NWARPS * 32) {
-      const float2 v = x_pair(a.xs, 0, k, inv_rms);
+    for (int k = 2 * threadIdx.x; k < a.xs.K; k += 2 * W * 32) {
+      const float2 v = x_make(a.xs, x_load(a.xs, 0, k), inv_rms);
       a.xs.trace_x[k] = bf16_bits(v.x);
       a.xs.trace_x[k + 1] = bf16_bits(v.y);
     }
   }
 
-  // ---- main loop over this warp's steps ----
-  bool ok = true;
-  uint32_t waited = 0;
+  uint32_t o = 0;  // stream offset of the next record
   int cur_g = -1;
-  uint32_t my_desc = 0, my_off = 0, my_off1 = 0;
-  for (uint32_t s = wa; s < wb; ++s) {
-    const uint32_t k = (s - wa) & 31u;
-    if (k == 0) {
-      const uint32_t idx = s + lane;
-      my_desc = idx < wb ? M.desc[idx] : 0u;
-      my_off = idx < wb ? M.off[idx] : 0u;
-      my_off1 = idx < wb ? M.off[idx + 1] : 0u;
-    }
-    const uint32_t desc = __shfl_sync(0xffffffffu, my_desc, k);
-    const uint32_t o0 = static_cast<uint32_t>(static_cast<uint64_t>(__shfl_sync(0xffffffffu, my_off, k)) * 16u - gbase);
-    const uint32_t o1 = static_cast<uint32_t>(static_cast<uint64_t>(__shfl_sync(0xffffffffu, my_off1, k)) * 16u - gbase);
-    const uint32_t need = (o1 - 1) / CHUNK;
-    while (waited <= need) {
-      const bool done = mbar_wait(bar_a + 8 * (waited % NSLOT), (waited / NSLOT) & 1u);
-      if (!__all_sync(0xffffffffu, done)) {
-        ok = false;
-        break;
-      }
-      ++waited;
-    }
-    if (!ok) break;
+  int cur_seg = -1;
 
-    const int g = static_cast<int>(desc_g(desc));
-    const uint32_t cls = desc_cls(desc), e = desc_e(desc);
-    if (g != cur_g) {
-      __syncwarp();
+  // Makes group column g's prep current, and prefetches the inputs of g + 1.
+  auto prep_for = [&](int g) {
+    XRaw r[NB];
+    if (g == pre_g) {
 #pragma unroll
-      for (int c = 0; c < NB; ++c) {
-        const float2 xv = x_pair(a.xs, c, g * GROUP + 2 * lane, inv_rms);
-        build_prep(xp + c * XPF, xv.x, xv.y, lane);
-      }
-      __syncwarp();
-      cur_g = g;
-    }
-    const uint32_t j = static_cast<uint32_t>(lane) >> cls;
-    const uint32_t sigma = static_cast<uint32_t>(lane) & ((1u << cls) - 1u);
-    const bool active = j < e;
-    uint2 cw = make_uint2(0u, 0u);
-    if (active) cw = lds_v2(ring_a + ((o0 + 8u * lane) & (RING - 1)));
-    float tv[NB];
-    if (cls == 0) {
-      decode_lut<NB>(cw, xp_a, tv);
-    } else if (cls == 1) {
-      decode_direct<NB, 2>(cw, xp, sigma, tv);
-#pragma unroll
-      for (int c = 0; c < NB; ++c) tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 1);
-    } else if (cls == 2) {
-      decode_direct<NB, 4>(cw, xp, sigma, tv);
-#pragma unroll
-      for (int c = 0; c < NB; ++c) {
-        tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 1);
-        tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 2);
-      }
+      for (int c = 0; c < NB; ++c) r[c] = pre[c];
     } else {
-      decode_direct<NB, 8>(cw, xp, sigma, tv);
 #pragma unroll
-      for (int c = 0; c < NB; ++c) {
-        tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 1);
-        tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 2);
-        tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 4);
-      }
+      for (int c = 0; c < NB; ++c) r[c] = x_load(a.xs, c, g * GROUP + 2 * lane);
     }
-    if (active && sigma == 0) {
-      const float sc = half_bits_to_float(lds_u16(ring_a + ((o0 + rec_scale_off(cls, e) + 2u * j) & (RING - 1))));
-      const uint32_t row = lds_u8(ring_a + ((o0 + rec_row_off(cls, e) + j) & (RING - 1)));
+    pre_g = (g + 1) * GROUP < a.xs.K ? g + 1 : -1;
+    if (pre_g >= 0) {
 #pragma unroll
-      for (int c = 0; c < NB; ++c) acc[c * TILE_MAX + row] = fmaf(sc, tv[c], acc[c * TILE_MAX + row]);
-    }
-    // Refill the ring with chunks whose slots are now free.
-    __syncwarp();
-    if (lane == 0) {
-      const uint32_t lim = o1 / CHUNK + NSLOT - 1;
-      while (issued < nch && issued <= lim) {
-        const uint32_t slot = issued % NSLOT;
-        const uint32_t bytes = min(static_cast<uint32_t>(CHUNK), len - issued * CHUNK);
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar_a + 8 * slot, bytes);
-        bulk_g2s(ring_a + slot * CHUNK, gsrc + static_cast<uint64_t>(issued) * CHUNK, bytes, bar_a + 8 * slot, pol);
-        ++issued;
-      }
+      for (int c = 0; c < NB; ++c) pre[c] = x_load(a.xs, c, pre_g * GROUP + 2 * lane);
     }
     __syncwarp();
-  }
-  if (!ok) {
-    if (lane == 0) atomicExch(a.err, kErrRingTimeout);
-    // Drain this warp's copies in flight (bounded) before the shared memory is released.
-    for (uint32_t c = waited; c < issued; ++c)
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_a + 8 * (c % NSLOT), (c / NSLOT) & 1u))) break;
-  }
-  grid_dep_launch();
+#pragma unroll
+    for (int c = 0; c < NB; ++c) {
+      const float2 xv = x_make(a.xs, r[c], inv_rms);
+      build_prep(xp + c * XPF * 4, xv.x, xv.y, lane, sgn, lut[c]);
+    }
+    __syncwarp();
+    cur_g = g;
+  };
 
-  // ---- combine: warps (fixed order), then the cluster's CTAs (fixed order) ----
-  __syncthreads();
-  for (uint32_t r = threadIdx.x; r < rows; r += NWARPS * 32) {
-#pragma unroll
-    for (int c = 0; c < NB; ++c) {
-      float v = 0.0f;
-      const float* ac = reinterpret_cast<const float*>(smem + L::kAcc) + c * TILE_MAX + r;
-#pragma unroll
-      for (int w = 0; w < NWARPS; ++w) v += ac[w * NB * TILE_MAX];
-      part[c * TILE_MAX + r] = v;
+  // Waits until the bytes below `upto` have landed; false on a timeout.
+  auto wait_for = [&](uint32_t upto) {
+    while (S.avail < upto) {
+      const bool done = mbar_wait(S.bar + 8 * (S.landed & (NSLOT - 1)), (S.landed / NSLOT) & 1u);
+      if (!__all_sync(0xffffffffu, done)) {
+        S.ok = false;
+        return;
+      }
+      ++S.landed;
+      S.avail = min(S.landed * CH, S.L);
     }
-  }
-  cluster.sync();
-  const uint32_t lo = static_cast<uint32_t>((static_cast<uint64_t>(rows) * rank) / C);
-  const uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(rows) * (rank + 1)) / C);
-  for (uint32_t r = lo + threadIdx.x; r < hi; r += NWARPS * 32) {
-#pragma unroll
-    for (int c = 0; c < NB; ++c) {
-      float v = 0.0f;
-      for (int q = 0; q < C; ++q) v += cluster.map_shared_rank(part, q)[c * TILE_MAX + r];
-      const uint32_t row = r0 + r;
-      if (M.trace_y) M.trace_y[row] = v;
+  };
+
+  auto refill = [&]() {
+    if (o >= S.refill_at) {
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_smem();
+      while (o >= S.refill_at) issue_next();
+    }
+  };
+
+  // Steps [k, kend) of a run of class CLS with n entries.
+  auto run_steps = [&](auto cls_tag, uint32_t k, uint32_t kend, uint32_t n) {
+    constexpr int CLS = decltype(cls_tag)::value;
+    constexpr uint32_t EPS = entries_per_step(CLS);
+    constexpr uint32_t FULL = full_step_bytes(CLS);
+    const float pw = CLS == 1 ? pw2 : pw4;
+    const uint32_t kfull = min(kend, n / EPS);
+    for (; k < kfull; ++k) {
+      const uint32_t o1 = o + FULL;
+      if (S.avail < o1) {
+        wait_for(o1);
+        if (!S.ok) return;
+      }
+      do_step<NB, CLS>(S.ring + (o & RMASK), EPS, xp, acc, lane, lut, pw);
+      o = o1;
+      refill();
+    }
+    if (k < kend) {  // the run's last, partial step
+      const uint32_t e = n - k * EPS;
+      const uint32_t o1 = o + rec_bytes(CLS, e);
+      if (S.avail < o1) {
+        wait_for(o1);
+        if (!S.ok) return;
+      }
+      do_step<NB, CLS>(S.ring + (o & RMASK), e, xp, acc, lane, lut, pw);
+      o = o1;
+      refill();
+    }
+  };
+
+  for (int ui = 0; ui < nu; ++ui) {
+    const uint32_t seg = __shfl_sync(0xffffffffu, u_seg, ui);
+    const uint32_t run1 = __shfl_sync(0xffffffffu, s_run1, ui);
+    const uint32_t k1 = __shfl_sync(0xffffffffu, s_k1, ui);
+    uint32_t run = __shfl_sync(0xffffffffu, s_run0, ui);
+    uint32_t k = __shfl_sync(0xffffffffu, s_k0, ui);
+    const uint32_t run_end = run1 + (k1 > 0u ? 1u : 0u);
+    const uint32_t* rdesc = a.seg[seg].run_desc;
+    if (static_cast<int>(seg) != cur_seg) {
+      cur_seg = static_cast<int>(seg);
+      cur_g = -1;
+    }
+    uint32_t dbase = run;
+    uint32_t dcur = (run + lane < run_end) ? __ldg(rdesc + run + lane) : 0u;
+    uint32_t dnext = (run + 32 + lane < run_end) ? __ldg(rdesc + run + 32 + lane) : 0u;
+
+    for (; S.ok && run < run_end; ++run, k = 0) {
+      if (run - dbase >= 32u) {
+        dbase += 32;
+        dcur = dnext;
+        dnext = (dbase + 32 + lane < run_end) ? __ldg(rdesc + dbase + 32 + lane) : 0u;
+      }
+      const uint32_t d = __shfl_sync(0xffffffffu, dcur, run - dbase);
+      const int g = static_cast<int>(run_g(d));
+      const uint32_t cls = run_cls(d), n = run_n(d);
+      const uint32_t kend = (run == run1) ? k1 : (n + entries_per_step(cls) - 1u) / entries_per_step(cls);
+      if (g != cur_g) prep_for(g);
+      switch (cls) {
+        case 0: run_steps(std::integral_constant<int, 0>{}, k, kend, n); break;
+        case 1: run_steps(std::integral_constant<int, 1>{}, k, kend, n); break;
+        case 2: run_steps(std::integral_constant<int, 2>{}, k, kend, n); break;
+        default: run_steps(std::integral_constant<int, 3>{}, k, kend, n); break;
+      }
+    }
+
+    // ---- unit epilogue: warps in fixed order, then split tiles across CTAs ----
+    __syncthreads();
+    const uint32_t split = __shfl_sync(0xffffffffu, u_split, ui);
+    const uint32_t nsplit = __shfl_sync(0xffffffffu, u_nsplit, ui);
+    const uint32_t r0 = __shfl_sync(0xffffffffu, u_r0, ui);
+    const uint32_t rows = __shfl_sync(0xffffffffu, u_rows, ui);
+    const MatView& M = a.seg[seg];
+    auto store = [&](int c, uint32_t row, float v) {
+      if (c == 0 && M.trace_y) M.trace_y[row] = v;
       if (a.ep == EP_RESID) v += a.resid[row];
       M.y[static_cast<int64_t>(c) * M.y_ld + row] = v;
+    };
+    auto warp_sum = [&](int c, uint32_t r) {
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) v += lds<float>(Lay::kAcc + ((w * NB + c) * TILE_MAX + r) * 4);
+      return v;
+    };
+    if (nsplit <= 1u) {
+      for (uint32_t r = threadIdx.x; r < rows; r += W * 32) {
+#pragma unroll
+        for (int c = 0; c < NB; ++c) store(c, r0 + r, warp_sum(c, r));
+      }
+    } else {
+      const uint32_t pbase = __shfl_sync(0xffffffffu, u_pbase, ui);
+      const uint32_t cnt = __shfl_sync(0xffffffffu, u_cnt, ui);
+      float* part = a.plan.partial + static_cast<size_t>(pbase) * NB;
+      for (uint32_t r = threadIdx.x; r < rows; r += W * 32) {
+#pragma unroll
+        for (int c = 0; c < NB; ++c) part[(split * NB + c) * rows + r] = warp_sum(c, r);
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(a.plan.counters + cnt, 1u);
+        reinterpret_cast<uint32_t*>(misc)[32] = (prev == nsplit - 1u) ? 1u : 0u;
+      }
+      __syncthreads();
+      if (reinterpret_cast<const uint32_t*>(misc)[32]) {
+        __threadfence();
+        for (uint32_t r = threadIdx.x; r < rows; r += W * 32) {
+#pragma unroll
+          for (int c = 0; c < NB; ++c) {
+            float v = 0.0f;
+            for (uint32_t s = 0; s < nsplit; ++s) v += __ldcg(part + (s * NB + c) * rows + r);
+            store(c, r0 + r, v);
+          }
+        }
+        if (threadIdx.x == 0) a.plan.counters[cnt] = 0u;
+      }
     }
+    __syncthreads();
+    for (int i = lane; i < NB * TILE_MAX; i += 32) sts(acc + i * 4, 0.0f);
   }
-  cluster.sync();
+
+  if (!S.ok) {
+    if (lane == 0) atomicExch(a.err, kErrRingTimeout);
+    // Drain this warp's copies in flight (bounded) before the shared memory is released.
+    for (uint32_t c = S.landed; c < S.issued; ++c)
+      if (!__all_sync(0xffffffffu, mbar_wait(S.bar + 8 * (c & (NSLOT - 1)), (c / NSLOT) & 1u))) break;
+  }
 }
 
 }  // namespace vbq

@@ -9,22 +9,24 @@
 
 #include "../../include/vbq.h"
 #include "layout.h"
+#include "plan.h"
 
 struct vbq_matrix {
   int64_t N = 0, K = 0;
   int32_t G = 0;
-  int32_t n_tiles = 0, n_steps = 0;
-  int32_t max_tile_rows = 0;
+  int32_t n_tiles = 0, n_runs = 0;
+  int64_t n_steps = 0;
   int64_t code_bytes = 0, meta_bytes = 0, total_bytes = 0, data_bytes = 0;
   int64_t groups_by_bits[4] = {0, 0, 0, 0};
   int device = 0;
-  uint8_t* dev_base = nullptr;  // one allocation holding everything below
+  uint8_t* dev_base = nullptr;  // one allocation: records and side tables
   const uint8_t* data = nullptr;
-  const uint32_t* step_desc = nullptr;
-  const uint32_t* step_off = nullptr;
+  const uint32_t* run_desc = nullptr;
+  const uint32_t* run_off = nullptr;
   const uint32_t* tile_row0 = nullptr;
-  const uint32_t* tile_step0 = nullptr;
-  std::vector<uint32_t> h_tile_row0, h_tile_step0;
+  const uint32_t* tile_run0 = nullptr;
+  std::vector<uint32_t> h_run_desc, h_run_off, h_tile_row0, h_tile_run0;  // host copies, for planning
+  vbq::DevicePlan plan;  // plan of a GEMV over this matrix alone
 };
 
 namespace vbq {
@@ -43,6 +45,20 @@ struct GpuInfo {
   int max_smem_optin = 0;
 };
 const GpuInfo& gpu_info();
+
+// Widest batch a single GEMV launch covers (partial storage is sized for it).
+constexpr int MAX_NB = 4;
+
+inline SegTables seg_tables(const vbq_matrix* m) {
+  SegTables t;
+  t.run_desc = m->h_run_desc.data();
+  t.run_off = m->h_run_off.data();
+  t.tile_row0 = m->h_tile_row0.data();
+  t.tile_run0 = m->h_tile_run0.data();
+  t.n_tiles = m->n_tiles;
+  t.n_runs = m->n_runs;
+  return t;
+}
 
 }  // namespace vbq
 

@@ -64,65 +64,58 @@ const GpuInfo& gpu_info() {
 MatView view_of(const vbq_matrix* m, float* y, int32_t y_ld, float* trace_y) {
   MatView v{};
   v.data = m->data;
-  v.desc = m->step_desc;
-  v.off = m->step_off;
-  v.row0 = m->tile_row0;
-  v.step0 = m->tile_step0;
-  v.n_tiles = m->n_tiles;
-  v.N = static_cast<int32_t>(m->N);
+  v.run_desc = m->run_desc;
   v.y = y;
   v.y_ld = y_ld;
   v.trace_y = trace_y;
   return v;
 }
 
+PlanView plan_view(const DevicePlan& p) {
+  PlanView v{};
+  v.units = p.units;
+  v.slices = p.slices;
+  v.umax = p.umax;
+  v.partial = p.partial;
+  v.counters = p.counters;
+  return v;
+}
+
 // ---------------------------------------------------------------- GEMV launch
 
-template <int NB, int NWARPS>
+// Kernel shapes: batch columns, warps per CTA, ring slots per warp.
+template <int NB> struct GemvShape;
+template <> struct GemvShape<1> { static constexpr int W = 16, NSLOT = 2; };
+template <> struct GemvShape<2> { static constexpr int W = 16, NSLOT = 2; };
+template <> struct GemvShape<4> { static constexpr int W = 8, NSLOT = 4; };
+
+template <int NB>
 struct GemvKernel {
-  static constexpr int kThreads = NWARPS * 32;
-  static constexpr int kSmem = GemvSmem<NB, NWARPS>::kBytes;
-  static int slots() {  // resident CTAs on the whole GPU
+  static constexpr int W = GemvShape<NB>::W, NSLOT = GemvShape<NB>::NSLOT;
+  static constexpr int kThreads = W * 32;
+  static constexpr int kSmem = GemvSmem<NB, W, NSLOT>::kBytes;
+  static void prepare() {  // once per device
     static std::mutex mu;
-    static std::map<int, int> cache;
+    static std::map<int, bool> done;
     const GpuInfo& gi = gpu_info();
     std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(gi.device);
-    if (it != cache.end()) return it->second;
-    auto k = vbq_gemv_kernel<NB, NWARPS>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, kSmem);
-    if (per_sm < 1) per_sm = 1;
-    const int s = per_sm * gi.sms;
-    cache[gi.device] = s;
-    return s;
+    if (done[gi.device]) return;
+    cudaFuncSetAttribute(vbq_gemv_kernel<NB, W, NSLOT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    done[gi.device] = true;
   }
 };
 
-int choose_cluster(int tiles, int slots) {
-  for (int c : {8, 4, 2}) {
-    if (static_cast<int64_t>(tiles) * c <= slots) return c;
-  }
-  return 1;
-}
-
-template <int NB, int NWARPS>
-cudaError_t launch_gemv_t(const GemvArgs& a, int total_tiles, cudaStream_t st, bool pdl, int force_cluster) {
-  using K = GemvKernel<NB, NWARPS>;
-  const int C = force_cluster > 0 ? force_cluster : choose_cluster(total_tiles, K::slots());
+template <int NB>
+cudaError_t launch_gemv_t(const GemvArgs& a, int n_ctas, cudaStream_t st, bool pdl) {
+  using K = GemvKernel<NB>;
+  K::prepare();
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(total_tiles * C), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
   cfg.blockDim = dim3(K::kThreads, 1, 1);
   cfg.dynamicSmemBytes = K::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attrs[2];
+  cudaLaunchAttribute attrs[1];
   int na = 0;
-  attrs[na].id = cudaLaunchAttributeClusterDimension;
-  attrs[na].val.clusterDim.x = C;
-  attrs[na].val.clusterDim.y = 1;
-  attrs[na].val.clusterDim.z = 1;
-  ++na;
   if (pdl) {
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[na].val.programmaticStreamSerializationAllowed = 1;
@@ -131,53 +124,65 @@ cudaError_t launch_gemv_t(const GemvArgs& a, int total_tiles, cudaStream_t st, b
   cfg.attrs = attrs;
   cfg.numAttrs = na;
   note_launches(1);
-  return cudaLaunchKernelEx(&cfg, vbq_gemv_kernel<NB, NWARPS>, a);
+  return cudaLaunchKernelEx(&cfg, vbq_gemv_kernel<NB, K::W, K::NSLOT>, a);
 }
 
-cudaError_t launch_gemv(int nb, const GemvArgs& a, int total_tiles, cudaStream_t st, bool pdl, int force_cluster) {
+cudaError_t launch_gemv(int nb, const GemvArgs& a, int n_ctas, cudaStream_t st, bool pdl) {
+  if (n_ctas <= 0) return cudaSuccess;
   switch (nb) {
-    case 1: return launch_gemv_t<1, 8>(a, total_tiles, st, pdl, force_cluster);
-    case 2: return launch_gemv_t<2, 8>(a, total_tiles, st, pdl, force_cluster);
-    case 4: return launch_gemv_t<4, 4>(a, total_tiles, st, pdl, force_cluster);
-    case 8: return launch_gemv_t<8, 4>(a, total_tiles, st, pdl, force_cluster);
+    case 1: return launch_gemv_t<1>(a, n_ctas, st, pdl);
+    case 2: return launch_gemv_t<2>(a, n_ctas, st, pdl);
+    case 4: return launch_gemv_t<4>(a, n_ctas, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
 void warm_gemv(int nb) {
   switch (nb) {
-    case 1: GemvKernel<1, 8>::slots(); break;
-    case 2: GemvKernel<2, 8>::slots(); break;
-    case 4: GemvKernel<4, 4>::slots(); break;
-    default: GemvKernel<8, 4>::slots(); break;
+    case 1: GemvKernel<1>::prepare(); break;
+    case 2: GemvKernel<2>::prepare(); break;
+    default: GemvKernel<4>::prepare(); break;
   }
 }
 
 // ---------------------------------------------------------------- dequant
 
-// W[r][k] = s * (q - c_b) for every weight, exact in fp32. One CTA per tile.
-__global__ void __launch_bounds__(256) vbq_dequant_kernel(MatView M, int32_t K, float* W) {
+// W[r][k] = s * (q - c_b) for every weight, exact in fp32. One CTA per tile;
+// its warps take the tile's runs in turn.
+__global__ void __launch_bounds__(256) vbq_dequant_kernel(const uint8_t* __restrict__ data,
+                                                          const uint32_t* __restrict__ run_desc,
+                                                          const uint32_t* __restrict__ run_off,
+                                                          const uint32_t* __restrict__ tile_row0,
+                                                          const uint32_t* __restrict__ tile_run0, int32_t K,
+                                                          float* __restrict__ W) {
   const int t = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const uint32_t r0 = M.row0[t], s0 = M.step0[t], s1 = M.step0[t + 1];
-  for (uint32_t s = s0 + warp; s < s1; s += nw) {
-    const uint32_t d = M.desc[s];
-    const uint32_t cls = desc_cls(d), e = desc_e(d), g = desc_g(d);
-    const uint8_t* rec = M.data + static_cast<uint64_t>(M.off[s]) * 16u;
-    const uint32_t j = static_cast<uint32_t>(lane) >> cls;
-    const uint32_t sigma = static_cast<uint32_t>(lane) & ((1u << cls) - 1u);
-    if (j >= e) continue;
-    const uint2 cw = ldg_nc_v2(rec + 8 * lane);
-    const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rec + rec_scale_off(cls, e) + 2 * j));
-    const uint32_t row = rec[rec_row_off(cls, e) + j];
-    const uint32_t b = 1u << cls, nper = 64u >> cls, mask = (1u << b) - 1u;
-    const float c = static_cast<float>((1u << b) - 1u) * 0.5f;
-    float* dst = W + static_cast<int64_t>(r0 + row) * K + static_cast<int64_t>(g) * GROUP + sigma * nper;
-    for (uint32_t m = 0; m < nper; ++m) {
-      const uint32_t bit = m * b;
-      const uint32_t w = bit < 32 ? cw.x : cw.y;
-      const uint32_t q = (w >> (bit & 31u)) & mask;
-      dst[m] = __fmul_rn(sc, static_cast<float>(q) - c);
+  const uint32_t r0 = tile_row0[t];
+  for (uint32_t run = tile_run0[t] + warp; run < tile_run0[t + 1]; run += nw) {
+    const uint32_t d = run_desc[run];
+    const uint32_t cls = run_cls(d), n = run_n(d), g = run_g(d);
+    const uint32_t eps = entries_per_step(cls);
+    const uint8_t* rec = data + static_cast<uint64_t>(run_off[run]) * 16u;
+    for (uint32_t k = 0; k * eps < n; ++k, rec += full_step_bytes(cls)) {
+      const uint32_t e = min(eps, n - k * eps);
+      const uint32_t j = static_cast<uint32_t>(lane);  // one entry per lane
+      if (j >= e) continue;
+      const uint32_t b = 1u << cls;
+      const uint8_t* ent = rec + 8u * b * j;
+      const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rec + rec_scale_off(cls, e) + 2 * j));
+      const uint32_t row = rec[rec_row_off(cls, e) + j];
+      const float c = static_cast<float>((1u << b) - 1u) * 0.5f;
+      float* dst = W + static_cast<int64_t>(r0 + row) * K + static_cast<int64_t>(g) * GROUP;
+      for (uint32_t m = 0; m < GROUP; ++m) {
+        uint32_t q;
+        if (b == 8) {
+          q = ent[m];
+        } else {
+          q = 0;
+          for (uint32_t p = 0; p < b; ++p) q |= ((ent[8 * p + (m >> 3)] >> (m & 7)) & 1u) << p;
+        }
+        dst[m] = __fmul_rn(sc, static_cast<float>(q) - c);
+      }
     }
   }
 }
@@ -278,9 +283,9 @@ extern "C" vbq_status vbq_dequant(const vbq_matrix* m, float* W_dev, void* strea
   if (m->N * m->K == 0) return VBQ_OK;
   if (!W_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_dequant: NULL output");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MatView v = view_of(m, nullptr, 0, nullptr);
   note_launches(1);
-  vbq_dequant_kernel<<<m->n_tiles, 256, 0, st>>>(v, static_cast<int32_t>(m->K), W_dev);
+  vbq_dequant_kernel<<<m->n_tiles, 256, 0, st>>>(m->data, m->run_desc, m->run_off, m->tile_row0, m->tile_run0,
+                                                 static_cast<int32_t>(m->K), W_dev);
   VBQ_CUDA_TRY(cudaGetLastError());
   return VBQ_OK;
 }
@@ -296,20 +301,18 @@ static vbq_status gemv_columns(const vbq_matrix* m, const uint16_t* X, int32_t B
   int done = 0;
   while (done < B) {
     const int left = B - done;
-    const int nb = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
+    const int nb = left >= 4 ? 4 : left >= 2 ? 2 : 1;
     GemvArgs a{};
     a.seg[0] = view_of(m, Y + static_cast<int64_t>(done) * m->N, static_cast<int32_t>(m->N), nullptr);
     a.nseg = 1;
-    a.tile_base[0] = 0;
-    a.tile_base[1] = m->n_tiles;
-    a.tile_base[2] = a.tile_base[3] = m->n_tiles;
+    a.plan = plan_view(m->plan);
     a.xs.mode = X_BF16;
     a.xs.K = static_cast<int32_t>(m->K);
     a.xs.x = X + static_cast<int64_t>(done) * m->K;
     a.xs.ldx = static_cast<int32_t>(m->K);
     a.ep = EP_STORE;
     a.err = err;
-    VBQ_CUDA_TRY(launch_gemv(nb, a, m->n_tiles, st, false, 0));
+    VBQ_CUDA_TRY(launch_gemv(nb, a, m->plan.n_ctas, st, false));
     done += nb;
   }
   return VBQ_OK;

@@ -11,9 +11,11 @@
 // [q;k;v] GEMV (RMSNorm in its prologue), the o GEMV (GQA gather in its
 // prologue, residual add in its epilogue), the fused [gate;up] GEMV (RMSNorm
 // prologue), and the down GEMV (SwiGLU prologue, residual epilogue); then the
-// head GEMV. The sequence is captured once into a CUDA graph. Its edges are
-// programmatic: each GEMV starts streaming its weights while the previous one
-// finishes, and waits (griddepcontrol.wait) only before touching activations.
+// head GEMV. Each of these launches has its own work plan over its matrices,
+// made when the model is created. The sequence is captured once into a CUDA
+// graph. Its edges are programmatic: each GEMV starts streaming its weights
+// while the previous one finishes, and waits (griddepcontrol.wait) only before
+// touching activations.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -58,6 +60,9 @@ struct vbq_model {
   const uint16_t* g_x = nullptr;
   float* g_logits = nullptr;
   int64_t kernels_per_step = 0;
+  std::vector<DevicePlan> plans;  // per layer: [q;k;v], o, [gate;up], down; then the head
+  uint64_t max_partial_rows = 0;
+  uint32_t max_counters = 0;
 };
 
 namespace {
@@ -85,57 +90,78 @@ void free_graph(vbq_model* m) {
   m->exec = nullptr;
 }
 
-GemvArgs base_args(int* err) {
+
+void add_seg(GemvArgs& a, const vbq_matrix* m, float* y, float* trace_y) {
+  a.seg[a.nseg] = view_of(m, y, static_cast<int32_t>(m->N), trace_y);
+  a.nseg += 1;
+}
+
+enum { L_QKV = 0, L_O, L_GU, L_DOWN, L_PER_LAYER };
+
+// Where one step's activations live.
+struct StepBuffers {
+  float* h;
+  float* qkv;
+  float* gu;
+  // Split-tile scratch shared by every launch of the step (the launches run in
+  // stream order, and each touches it only after griddepcontrol.wait). When
+  // null, each launch uses its plan's own storage.
+  float* partial;
+  uint32_t* counters;
+};
+
+GemvArgs proj_args(const vbq_model* m, int launch, const StepBuffers& b, int* err) {
   GemvArgs a{};
   a.err = err;
   a.ep = EP_STORE;
+  a.plan = plan_view(m->plans[launch]);
+  if (b.partial) {
+    a.plan.partial = b.partial;
+    a.plan.counters = b.counters;
+  }
   return a;
 }
 
-void add_seg(GemvArgs& a, int& tiles, const vbq_matrix* m, float* y, float* trace_y) {
-  a.seg[a.nseg] = view_of(m, y, static_cast<int32_t>(m->N), trace_y);
-  a.tile_base[a.nseg] = tiles;
-  tiles += m->n_tiles;
-  a.nseg += 1;
-  for (int s = a.nseg; s <= MAX_SEG; ++s) a.tile_base[s] = tiles;
-}
-
 // Enqueues one step; every kernel after the first may launch programmatically.
-cudaError_t enqueue_step(vbq_model* m, const uint16_t* x, float* logits, cudaStream_t st, int* err) {
+// skip_init: the caller has already enqueued h = x.
+cudaError_t enqueue_step(const vbq_model* m, const uint16_t* x, float* logits, const StepBuffers& b, bool trace,
+                         cudaStream_t st, int* err, bool skip_init = false) {
   const vbq_model_desc& d = m->desc;
   const int L = d.n_layers;
   const int64_t nq = proj_n(d, P_Q), nkv = proj_n(d, P_K);
-  float* q_out = m->qkv;
-  float* k_out = m->qkv + nq;
-  float* v_out = m->qkv + nq + nkv;
-  auto tin = [&](int p) -> uint16_t* { return m->trace ? m->tr_in + m->in_off[p] : nullptr; };
-  auto tout = [&](int p) -> float* { return m->trace ? m->tr_out + m->out_off[p] : nullptr; };
+  float* q_out = b.qkv;
+  float* k_out = b.qkv + nq;
+  float* v_out = b.qkv + nq + nkv;
+  auto tin = [&](int p) -> uint16_t* { return trace ? m->tr_in + m->in_off[p] : nullptr; };
+  auto tout = [&](int p) -> float* { return trace ? m->tr_out + m->out_off[p] : nullptr; };
+  auto n_ctas = [&](int launch) { return m->plans[launch].n_ctas; };
 
-  note_launches(1);
-  init_h_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x, m->h, d.d);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!skip_init) {
+    note_launches(1);
+    init_h_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x, b.h, d.d);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 
   for (int l = 0; l < L; ++l) {
     const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
     const int p0 = l * P_PER_LAYER;
+    const int l0 = l * L_PER_LAYER;
     {  // [q; k; v] = W u, u = bf16(rmsnorm(h))
-      GemvArgs a = base_args(err);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_Q], q_out, tout(p0 + P_Q));
-      add_seg(a, tiles, W[P_K], k_out, tout(p0 + P_K));
-      add_seg(a, tiles, W[P_V], v_out, tout(p0 + P_V));
+      GemvArgs a = proj_args(m, l0 + L_QKV, b, err);
+      add_seg(a, W[P_Q], q_out, tout(p0 + P_Q));
+      add_seg(a, W[P_K], k_out, tout(p0 + P_K));
+      add_seg(a, W[P_V], v_out, tout(p0 + P_V));
       a.xs.mode = X_RMSNORM;
       a.xs.K = d.d;
-      a.xs.h = m->h;
+      a.xs.h = b.h;
       a.xs.eps = d.rms_eps;
       a.xs.trace_x = tin(p0 + P_Q);
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+      if ((e = launch_gemv(1, a, n_ctas(l0 + L_QKV), st, true)) != cudaSuccess) return e;
     }
     {  // h += Wo a, a = bf16(v of each head's kv group)
-      GemvArgs a = base_args(err);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_O], m->h, tout(p0 + P_O));
+      GemvArgs a = proj_args(m, l0 + L_O, b, err);
+      add_seg(a, W[P_O], b.h, tout(p0 + P_O));
       a.xs.mode = X_GQA;
       a.xs.K = static_cast<int32_t>(nq);
       a.xs.v = v_out;
@@ -143,46 +169,44 @@ cudaError_t enqueue_step(vbq_model* m, const uint16_t* x, float* logits, cudaStr
       a.xs.group = d.n_heads / d.n_kv_heads;
       a.xs.trace_x = tin(p0 + P_O);
       a.ep = EP_RESID;
-      a.resid = m->h;
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+      a.resid = b.h;
+      if ((e = launch_gemv(1, a, n_ctas(l0 + L_O), st, true)) != cudaSuccess) return e;
     }
     {  // [gate; up] = W u, u = bf16(rmsnorm(h))
-      GemvArgs a = base_args(err);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_GATE], m->gu, tout(p0 + P_GATE));
-      add_seg(a, tiles, W[P_UP], m->gu + d.d_ff, tout(p0 + P_UP));
+      GemvArgs a = proj_args(m, l0 + L_GU, b, err);
+      add_seg(a, W[P_GATE], b.gu, tout(p0 + P_GATE));
+      add_seg(a, W[P_UP], b.gu + d.d_ff, tout(p0 + P_UP));
       a.xs.mode = X_RMSNORM;
       a.xs.K = d.d;
-      a.xs.h = m->h;
+      a.xs.h = b.h;
       a.xs.eps = d.rms_eps;
       a.xs.trace_x = tin(p0 + P_GATE);
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+      if ((e = launch_gemv(1, a, n_ctas(l0 + L_GU), st, true)) != cudaSuccess) return e;
     }
     {  // h += Wdown bf16(silu(gate) * up)
-      GemvArgs a = base_args(err);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_DOWN], m->h, tout(p0 + P_DOWN));
+      GemvArgs a = proj_args(m, l0 + L_DOWN, b, err);
+      add_seg(a, W[P_DOWN], b.h, tout(p0 + P_DOWN));
       a.xs.mode = X_SWIGLU;
       a.xs.K = d.d_ff;
-      a.xs.gate = m->gu;
-      a.xs.up = m->gu + d.d_ff;
+      a.xs.gate = b.gu;
+      a.xs.up = b.gu + d.d_ff;
       a.xs.trace_x = tin(p0 + P_DOWN);
       a.ep = EP_RESID;
-      a.resid = m->h;
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+      a.resid = b.h;
+      if ((e = launch_gemv(1, a, n_ctas(l0 + L_DOWN), st, true)) != cudaSuccess) return e;
     }
   }
   {  // logits = Whead bf16(rmsnorm(h))
-    GemvArgs a = base_args(err);
-    int tiles = 0;
+    const int lh = L * L_PER_LAYER;
+    GemvArgs a = proj_args(m, lh, b, err);
     const int ph = L * P_PER_LAYER;
-    add_seg(a, tiles, m->mats[ph], logits, tout(ph));
+    add_seg(a, m->mats[ph], logits, tout(ph));
     a.xs.mode = X_RMSNORM;
     a.xs.K = d.d;
-    a.xs.h = m->h;
+    a.xs.h = b.h;
     a.xs.eps = d.rms_eps;
     a.xs.trace_x = tin(ph);
-    if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
+    if ((e = launch_gemv(1, a, n_ctas(lh), st, true)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -194,7 +218,8 @@ vbq_status build_graph(vbq_model* m, const uint16_t* x, float* logits) {
   warm_gemv(1);
   const int64_t before = vbq_launch_count(0);
   VBQ_CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
-  cudaError_t e = enqueue_step(m, x, logits, m->cap_stream, err);
+  const StepBuffers b{m->h, m->qkv, m->gu, nullptr, nullptr};
+  cudaError_t e = enqueue_step(m, x, logits, b, m->trace, m->cap_stream, err);
   cudaGraph_t graph = nullptr;
   cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &graph);
   // Capturing enqueues nothing: the counter tracks launches that actually run.
@@ -217,6 +242,8 @@ vbq_status build_graph(vbq_model* m, const uint16_t* x, float* logits) {
 }
 
 }  // namespace
+
+extern "C" void vbq_model_free(vbq_model* m);
 
 extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_matrix* const* mats, vbq_model** out) {
   if (!out) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_create: out is NULL");
@@ -286,6 +313,37 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   }
   m->in_total = io;
   m->out_total = oo;
+  // One plan per launch of the step, each over the launch's matrices.
+  const int sms = gpu_info().sms;
+  auto add_plan = [&](std::initializer_list<const vbq_matrix*> ms) -> cudaError_t {
+    std::vector<SegTables> segs;
+    uint64_t bytes = 0;
+    for (const vbq_matrix* w : ms) {
+      segs.push_back(seg_tables(w));
+      bytes += static_cast<uint64_t>(w->data_bytes);
+    }
+    Plan pl = make_plan(segs, plan_ctas(bytes, sms), MAX_UNITS_PER_CTA);
+    m->max_partial_rows = std::max<uint64_t>(m->max_partial_rows, pl.partial_rows);
+    m->max_counters = std::max<uint32_t>(m->max_counters, pl.n_counters);
+    DevicePlan dp;
+    cudaError_t err = upload_plan(pl, 1, nullptr, &dp);
+    if (err == cudaSuccess) m->plans.push_back(dp);
+    return err;
+  };
+  for (int l = 0; l <= d.n_layers; ++l) {
+    const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
+    cudaError_t err;
+    if (l == d.n_layers) {
+      err = add_plan({W[0]});
+    } else if ((err = add_plan({W[P_Q], W[P_K], W[P_V]})) == cudaSuccess && (err = add_plan({W[P_O]})) == cudaSuccess &&
+               (err = add_plan({W[P_GATE], W[P_UP]})) == cudaSuccess) {
+      err = add_plan({W[P_DOWN]});
+    }
+    if (err != cudaSuccess) {
+      vbq_model_free(m);
+      return cuda_fail(err, "vbq_model_create: plan upload");
+    }
+  }
   *out = m;
   return VBQ_OK;
 }
@@ -301,6 +359,7 @@ extern "C" void vbq_model_free(vbq_model* m) {
   cudaFree(m->ws);
   cudaFree(m->tr_in);
   cudaFree(m->tr_out);
+  for (DevicePlan& p : m->plans) free_plan(&p);
   cudaSetDevice(cur);
   delete m;
 }
@@ -378,10 +437,11 @@ extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host
 
 namespace {
 
-// Floats of g_step_scratch: a 64-float status block, then h [d], [q;k;v] and
-// [gate;up], each rounded up to 64 floats. 65536 + 64 floats = 256.25 KiB on
-// every device that loads this library, held until the process exits.
-constexpr int64_t kStepScratchFloats = 65536 + 64;
+// g_step_scratch holds, in 64-float blocks: a status block, the split-tile
+// arrival counters, h [d], [q;k;v], [gate;up], and the split-tile partial rows.
+// 262,144 floats = 1 MiB on every device that loads this library, held until
+// the process exits.
+constexpr int64_t kStepScratchFloats = 262144;
 static __device__ __align__(256) float g_step_scratch[kStepScratchFloats];
 
 std::mutex g_step_scratch_mu;
@@ -406,85 +466,16 @@ vbq_status step_scratch_address(int dev, float** out) {
   return VBQ_OK;
 }
 
-__global__ void init_h_status_kernel(const uint16_t* __restrict__ x, float* __restrict__ h, int32_t d,
-                                     int* __restrict__ status) {
+// h = x, after clearing the status word and the arrival counters (`nclear` words at `clear`).
+__global__ void init_h_clear_kernel(const uint16_t* __restrict__ x, float* __restrict__ h, int32_t d,
+                                    uint32_t* __restrict__ clear, int32_t nclear) {
   grid_dep_wait();
-  if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nclear; i += gridDim.x * blockDim.x) clear[i] = 0u;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x)
     h[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
 }
 
 int64_t round64(int64_t n) { return (n + 63) & ~int64_t(63); }
-
-// The launch sequence of enqueue_step with the activations at explicit addresses and no trace.
-cudaError_t enqueue_step_at(const vbq_model* m, const uint16_t* x, float* logits, float* h, float* qkv, float* gu,
-                            int* status, cudaStream_t st) {
-  const vbq_model_desc& d = m->desc;
-  const int64_t nq = proj_n(d, P_Q), nkv = proj_n(d, P_K);
-  note_launches(1);
-  init_h_status_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x, h, d.d, status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  for (int l = 0; l < d.n_layers; ++l) {
-    const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
-    {
-      GemvArgs a = base_args(status);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_Q], qkv, nullptr);
-      add_seg(a, tiles, W[P_K], qkv + nq, nullptr);
-      add_seg(a, tiles, W[P_V], qkv + nq + nkv, nullptr);
-      a.xs.mode = X_RMSNORM;
-      a.xs.K = d.d;
-      a.xs.h = h;
-      a.xs.eps = d.rms_eps;
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
-    }
-    {
-      GemvArgs a = base_args(status);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_O], h, nullptr);
-      a.xs.mode = X_GQA;
-      a.xs.K = static_cast<int32_t>(nq);
-      a.xs.v = qkv + nq + nkv;
-      a.xs.head_dim = d.head_dim;
-      a.xs.group = d.n_heads / d.n_kv_heads;
-      a.ep = EP_RESID;
-      a.resid = h;
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
-    }
-    {
-      GemvArgs a = base_args(status);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_GATE], gu, nullptr);
-      add_seg(a, tiles, W[P_UP], gu + d.d_ff, nullptr);
-      a.xs.mode = X_RMSNORM;
-      a.xs.K = d.d;
-      a.xs.h = h;
-      a.xs.eps = d.rms_eps;
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
-    }
-    {
-      GemvArgs a = base_args(status);
-      int tiles = 0;
-      add_seg(a, tiles, W[P_DOWN], h, nullptr);
-      a.xs.mode = X_SWIGLU;
-      a.xs.K = d.d_ff;
-      a.xs.gate = gu;
-      a.xs.up = gu + d.d_ff;
-      a.ep = EP_RESID;
-      a.resid = h;
-      if ((e = launch_gemv(1, a, tiles, st, true, 0)) != cudaSuccess) return e;
-    }
-  }
-  GemvArgs a = base_args(status);
-  int tiles = 0;
-  add_seg(a, tiles, m->mats[static_cast<size_t>(d.n_layers) * P_PER_LAYER], logits, nullptr);
-  a.xs.mode = X_RMSNORM;
-  a.xs.K = d.d;
-  a.xs.h = h;
-  a.xs.eps = d.rms_eps;
-  return launch_gemv(1, a, tiles, st, true, 0);
-}
 
 }  // namespace
 
@@ -493,25 +484,37 @@ extern "C" vbq_status vbq_decode_step_noalloc(vbq_model* m, const uint16_t* x_de
   if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 2)
     return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: misaligned buffer");
   const vbq_model_desc& d = m->desc;
+  const int64_t n_cnt = round64(m->max_counters);
   const int64_t n_h = round64(d.d);
   const int64_t n_qkv = round64(proj_n(d, P_Q) + 2 * proj_n(d, P_K));
   const int64_t n_gu = round64(2 * int64_t(d.d_ff));
-  const int64_t need = 64 + n_h + n_qkv + n_gu;
+  const int64_t n_part = round64(static_cast<int64_t>(m->max_partial_rows));
+  const int64_t need = 64 + n_cnt + n_h + n_qkv + n_gu + n_part;
   if (need > kStepScratchFloats)
     return fail(VBQ_ERR_SHAPE, "vbq_decode_step_noalloc: the step needs " + std::to_string(need) +
-                                   " scratch floats (d + q,k,v + 2*d_ff, each rounded up to 64, plus 64); the "
-                                   "static scratch holds " + std::to_string(kStepScratchFloats));
+                                   " scratch floats (status, counters, h, q/k/v, gate/up and split-tile partials, "
+                                   "each rounded up to 64); the static scratch holds " +
+                                   std::to_string(kStepScratchFloats));
   int dev = 0;
   VBQ_CUDA_TRY(cudaGetDevice(&dev));
   if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: model is on another device");
   float* base = nullptr;
   vbq_status s = step_scratch_address(dev, &base);
   if (s != VBQ_OK) return s;
-  float* h = base + 64;
-  float* qkv = h + n_h;
-  float* gu = qkv + n_qkv;
-  cudaError_t e = enqueue_step_at(m, x_dev, logits_dev, h, qkv, gu, reinterpret_cast<int*>(base),
-                                  static_cast<cudaStream_t>(stream));
+  StepBuffers b{};
+  uint32_t* counters = reinterpret_cast<uint32_t*>(base + 64);
+  b.counters = counters;
+  b.h = base + 64 + n_cnt;
+  b.qkv = b.h + n_h;
+  b.gu = b.qkv + n_qkv;
+  b.partial = b.gu + n_gu;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status word and the counters must start at zero; the first kernel clears them.
+  note_launches(1);
+  init_h_clear_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x_dev, b.h, d.d, reinterpret_cast<uint32_t*>(base),
+                                                         static_cast<int32_t>(64 + n_cnt));
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = enqueue_step(m, x_dev, logits_dev, b, false, st, reinterpret_cast<int*>(base), true);
   if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: launch");
   return VBQ_OK;
 }

@@ -17,14 +17,19 @@ using namespace vbq;
 
 inline int bits_to_cls(uint8_t b) { return b == 1 ? 0 : b == 2 ? 1 : b == 4 ? 2 : 3; }
 
-// Packs the 64 codes of one group LSB-first into 8*b bytes: code m at bits [m*b, m*b+b).
+// Packs the 64 codes of one group into 8*b bytes.
+//  b = 1, 2, 4: bit-planes. Plane p (bit p of every code) fills bytes [8p, 8p+8),
+//               with code m's bit at bit m of the plane (little-endian).
+//  b = 8:       one byte per code, code m in byte m.
 inline void pack_entry(const uint8_t* q, int b, uint8_t* dst) {
   const int nbytes = 8 * b;
   std::memset(dst, 0, nbytes);
-  for (int m = 0; m < GROUP; ++m) {
-    const int bit = m * b;
-    dst[bit >> 3] |= static_cast<uint8_t>(q[m] << (bit & 7));
+  if (b == 8) {
+    std::memcpy(dst, q, GROUP);
+    return;
   }
+  for (int p = 0; p < b; ++p)
+    for (int m = 0; m < GROUP; ++m) dst[8 * p + (m >> 3)] |= static_cast<uint8_t>(((q[m] >> p) & 1u) << (m & 7));
 }
 
 struct TilePlan {
@@ -58,18 +63,20 @@ TilePlan plan_tiles(const uint8_t* bits, int64_t N, int32_t G) {
 }
 
 struct TileCount {
-  uint32_t steps = 0;
+  uint32_t runs = 0, steps = 0;
   uint64_t bytes = 0;
 };
 
-// Step count and record bytes of one tile.
+// Run, step and record-byte counts of one tile.
 TileCount count_tile(const uint8_t* bits, int32_t G, uint32_t r0, uint32_t r1) {
   TileCount tc;
   for (int32_t g = 0; g < G; ++g) {
     uint32_t n[4] = {0, 0, 0, 0};
     for (uint32_t r = r0; r < r1; ++r) ++n[bits_to_cls(bits[static_cast<int64_t>(r) * G + g])];
     for (int c = 0; c < 4; ++c) {
+      if (!n[c]) continue;
       const uint32_t eps = entries_per_step(c);
+      tc.runs += 1;
       for (uint32_t done = 0; done < n[c]; done += eps) {
         const uint32_t e = std::min(eps, n[c] - done);
         tc.steps += 1;
@@ -80,10 +87,11 @@ TileCount count_tile(const uint8_t* bits, int32_t G, uint32_t r0, uint32_t r1) {
   return tc;
 }
 
+// Writes the runs of one tile: records into data, descriptors and offsets into desc/off.
 void fill_tile(const uint8_t* codes, const uint8_t* bits, const uint16_t* scales, int64_t K, int32_t G,
-               uint32_t r0, uint32_t r1, uint32_t step0, uint64_t byte0, uint8_t* data, uint32_t* desc,
+               uint32_t r0, uint32_t r1, uint32_t run0, uint64_t byte0, uint8_t* data, uint32_t* desc,
                uint32_t* off) {
-  uint32_t s = step0;
+  uint32_t ri = run0;
   uint64_t o = byte0;
   std::vector<uint32_t> rows[4];
   for (int c = 0; c < 4; ++c) rows[c].reserve(r1 - r0);
@@ -91,9 +99,13 @@ void fill_tile(const uint8_t* codes, const uint8_t* bits, const uint16_t* scales
     for (int c = 0; c < 4; ++c) rows[c].clear();
     for (uint32_t r = r0; r < r1; ++r) rows[bits_to_cls(bits[static_cast<int64_t>(r) * G + g])].push_back(r);
     for (int c = 0; c < 4; ++c) {
+      const uint32_t n = static_cast<uint32_t>(rows[c].size());
+      if (!n) continue;
+      desc[ri] = make_run(static_cast<uint32_t>(g), static_cast<uint32_t>(c), n);
+      off[ri] = static_cast<uint32_t>(o >> 4);
+      ++ri;
       const uint32_t eps = entries_per_step(c);
       const int b = cls_bits(c);
-      const uint32_t n = static_cast<uint32_t>(rows[c].size());
       for (uint32_t done = 0; done < n; done += eps) {
         const uint32_t e = std::min(eps, n - done);
         uint8_t* rec = data + o;
@@ -107,9 +119,6 @@ void fill_tile(const uint8_t* codes, const uint8_t* bits, const uint16_t* scales
           sc[j] = scales[static_cast<int64_t>(r) * G + g];
           rw[j] = static_cast<uint8_t>(r - r0);
         }
-        desc[s] = make_desc(static_cast<uint32_t>(g), static_cast<uint32_t>(c), e);
-        off[s] = static_cast<uint32_t>(o >> 4);
-        ++s;
         o += rb;
       }
     }
@@ -189,15 +198,15 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
   const int32_t nt = static_cast<int32_t>(plan.row0.size()) - 1;
   std::vector<TileCount> tcs(nt);
   parallel_for(nt, [&](int64_t t) { tcs[t] = count_tile(bits, G, plan.row0[t], plan.row0[t + 1]); });
-  std::vector<uint32_t> step0(nt + 1, 0);
+  std::vector<uint32_t> run0(nt + 1, 0);
   std::vector<uint64_t> byte0(nt + 1, 0);
-  int32_t max_rows = 0;
+  int64_t n_steps = 0;
   for (int32_t t = 0; t < nt; ++t) {
-    step0[t + 1] = step0[t] + tcs[t].steps;
+    run0[t + 1] = run0[t] + tcs[t].runs;
     byte0[t + 1] = byte0[t] + tcs[t].bytes;
-    max_rows = std::max<int32_t>(max_rows, plan.row0[t + 1] - plan.row0[t]);
+    n_steps += tcs[t].steps;
   }
-  const uint32_t S = step0[nt];
+  const uint32_t R = run0[nt];
   const uint64_t data_bytes = byte0[nt];
   if ((data_bytes >> 4) >= (uint64_t(1) << 32)) {
     delete m;
@@ -206,26 +215,28 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
 
   // One host staging buffer laid out exactly like the device allocation.
   const uint64_t o_desc = align256(std::max<uint64_t>(data_bytes, 16));
-  const uint64_t o_off = align256(o_desc + 4ull * std::max<uint32_t>(S, 1));
-  const uint64_t o_row0 = align256(o_off + 4ull * (S + 1));
-  const uint64_t o_step0 = align256(o_row0 + 4ull * (nt + 1));
-  const uint64_t total = align256(o_step0 + 4ull * (nt + 1));
+  const uint64_t o_off = align256(o_desc + 4ull * std::max<uint32_t>(R, 1));
+  const uint64_t o_row0 = align256(o_off + 4ull * (R + 1));
+  const uint64_t o_run0 = align256(o_row0 + 4ull * (nt + 1));
+  const uint64_t total = align256(o_run0 + 4ull * (nt + 1));
   std::vector<uint8_t> host;
   try {
     host.assign(total, 0);
+    m->h_run_desc.assign(R, 0);
+    m->h_run_off.assign(R + 1, 0);
   } catch (...) {
     delete m;
     return fail(VBQ_ERR_OOM, "vbq_pack: host staging buffer");
   }
-  uint32_t* h_desc = reinterpret_cast<uint32_t*>(host.data() + o_desc);
-  uint32_t* h_off = reinterpret_cast<uint32_t*>(host.data() + o_off);
   parallel_for(nt, [&](int64_t t) {
-    fill_tile(codes, bits, scales_f16, K, G, plan.row0[t], plan.row0[t + 1], step0[t], byte0[t], host.data(),
-              h_desc, h_off);
+    fill_tile(codes, bits, scales_f16, K, G, plan.row0[t], plan.row0[t + 1], run0[t], byte0[t], host.data(),
+              m->h_run_desc.data(), m->h_run_off.data());
   });
-  h_off[S] = static_cast<uint32_t>(data_bytes >> 4);
+  m->h_run_off[R] = static_cast<uint32_t>(data_bytes >> 4);
+  std::memcpy(host.data() + o_desc, m->h_run_desc.data(), 4ull * R);
+  std::memcpy(host.data() + o_off, m->h_run_off.data(), 4ull * (R + 1));
   std::memcpy(host.data() + o_row0, plan.row0.data(), 4ull * (nt + 1));
-  std::memcpy(host.data() + o_step0, step0.data(), 4ull * (nt + 1));
+  std::memcpy(host.data() + o_run0, run0.data(), 4ull * (nt + 1));
 
   int64_t cnt[4] = {0, 0, 0, 0};
   int64_t code_bytes = 0;
@@ -251,20 +262,29 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
     return cuda_fail(e, "vbq_pack: upload");
   }
   m->data = m->dev_base;
-  m->step_desc = reinterpret_cast<const uint32_t*>(m->dev_base + o_desc);
-  m->step_off = reinterpret_cast<const uint32_t*>(m->dev_base + o_off);
+  m->run_desc = reinterpret_cast<const uint32_t*>(m->dev_base + o_desc);
+  m->run_off = reinterpret_cast<const uint32_t*>(m->dev_base + o_off);
   m->tile_row0 = reinterpret_cast<const uint32_t*>(m->dev_base + o_row0);
-  m->tile_step0 = reinterpret_cast<const uint32_t*>(m->dev_base + o_step0);
+  m->tile_run0 = reinterpret_cast<const uint32_t*>(m->dev_base + o_run0);
   m->h_tile_row0 = plan.row0;
-  m->h_tile_step0 = step0;
+  m->h_tile_run0 = run0;
   m->n_tiles = nt;
-  m->n_steps = static_cast<int32_t>(S);
-  m->max_tile_rows = max_rows;
+  m->n_runs = static_cast<int32_t>(R);
+  m->n_steps = n_steps;
   m->data_bytes = static_cast<int64_t>(data_bytes);
   m->code_bytes = code_bytes;
-  m->total_bytes = static_cast<int64_t>(total);
-  m->meta_bytes = static_cast<int64_t>(total) - code_bytes;
   for (int c = 0; c < 4; ++c) m->groups_by_bits[c] = cnt[c];
+
+  // The plan of a GEMV over this matrix alone.
+  Plan pl = make_plan({seg_tables(m)}, plan_ctas(data_bytes, gpu_info().sms), MAX_UNITS_PER_CTA);
+  e = upload_plan(pl, MAX_NB, st, &m->plan);
+  if (e != cudaSuccess) {
+    cudaFree(m->dev_base);
+    delete m;
+    return cuda_fail(e, "vbq_pack: plan upload");
+  }
+  m->total_bytes = static_cast<int64_t>(total) + m->plan.bytes;
+  m->meta_bytes = m->total_bytes - code_bytes;
   *out = m;
   return VBQ_OK;
 }
@@ -277,6 +297,7 @@ extern "C" void vbq_matrix_free(vbq_matrix* m) {
     cudaSetDevice(m->device);
     cudaDeviceSynchronize();
     cudaFree(m->dev_base);
+    free_plan(&m->plan);
     cudaSetDevice(cur);
   }
   delete m;
@@ -291,7 +312,7 @@ extern "C" vbq_status vbq_matrix_info(const vbq_matrix* m, vbq_info* info) {
   info->total_bytes = m->total_bytes;
   info->mean_bits = (m->N * m->K) ? 8.0 * static_cast<double>(m->code_bytes) / static_cast<double>(m->N * m->K) : 0.0;
   info->n_tiles = m->n_tiles;
-  info->n_steps = m->n_steps;
+  info->n_steps = static_cast<int32_t>(std::min<int64_t>(m->n_steps, INT32_MAX));
   for (int c = 0; c < 4; ++c) info->groups_by_bits[c] = m->groups_by_bits[c];
   return VBQ_OK;
 }

@@ -1,0 +1,62 @@
+// Work plans for the GEMV kernels: which CTA and warp streams which bytes.
+//
+// A launch covers one or more packed matrices ("segments"). Their step records,
+// tile after tile, form one byte stream. make_plan cuts that stream at step
+// borders into n_ctas equal-byte CTA ranges, each range into units at tile
+// borders, and each unit into SLICES equal-byte warp slices (layout.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "layout.h"
+
+namespace vbq {
+
+// Host copies of one packed matrix's side tables.
+struct SegTables {
+  const uint32_t* run_desc = nullptr;
+  const uint32_t* run_off = nullptr;    // n_runs + 1 entries
+  const uint32_t* tile_row0 = nullptr;  // n_tiles + 1 entries
+  const uint32_t* tile_run0 = nullptr;  // n_tiles + 1 entries
+  int32_t n_tiles = 0;
+  int32_t n_runs = 0;
+};
+
+struct Plan {
+  std::vector<UnitRec> units;     // n_ctas * umax slots
+  std::vector<SliceRec> slices;   // SLICES per slot
+  int32_t n_ctas = 0;
+  int32_t umax = 0;               // unit slots per CTA
+  uint64_t partial_rows = 0;      // rows of partial storage per batch column
+  uint32_t n_counters = 0;
+};
+
+// Number of CTAs for a launch over total_bytes: one per SM at most, but no
+// fewer than 32 KB each, and never more than MAX_UNITS_PER_CTA units a CTA.
+int32_t plan_ctas(uint64_t total_bytes, int sms);
+
+// Builds the plan. If a CTA would get more than max_units units, the CTA count
+// grows until none does.
+Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units);
+
+// A plan's device copy: units, slices and CTA table, arrival counters (zeroed)
+// and partial rows for up to max_nb batch columns, in one allocation.
+struct DevicePlan {
+  void* base = nullptr;
+  const UnitRec* units = nullptr;
+  const SliceRec* slices = nullptr;
+  uint32_t* counters = nullptr;
+  float* partial = nullptr;
+  int32_t n_ctas = 0;
+  int32_t umax = 0;
+  int64_t bytes = 0;
+};
+
+// Allocates and uploads (synchronously on stream). Returns cudaSuccess or the error.
+cudaError_t upload_plan(const Plan& p, int max_nb, cudaStream_t stream, DevicePlan* out);
+void free_plan(DevicePlan* p);
+
+}  // namespace vbq

@@ -92,27 +92,48 @@ def glue_ulps(gpu_bits, ref_bits):
     return np.where((a <= UNDERFLOW) & (r <= UNDERFLOW), 0, d)
 
 
+def rmsnorm_input_ok(gpu_bits, h, err_h):
+    """The GPU's bf16(rmsnorm(h)) against the fp64 value, within rounding.
+
+    The GPU keeps h in fp32, and each residual add rounds once, so its h is off
+    by at most err_h per element (tracked by the caller). Where h nearly cancels,
+    that absolute error is a large relative one, so the bound is absolute:
+    one bf16 ulp of the exact value, plus err_h scaled by 1/rms, plus 2^-20
+    relative for the fp32 sum of squares.
+    """
+    ref = O.rmsnorm(h)
+    inv = 1.0 / np.sqrt(np.mean(h * h) + O.RMS_EPS)
+    got = O.bf16_bits_to_f64(gpu_bits)
+    _, e = np.frexp(ref)
+    ulp = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    tol = ulp + err_h * inv + 2.0 ** -20 * np.abs(ref)
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), (np.flatnonzero(bad)[:8], got[bad][:8], ref[bad][:8])
+    return int((O.f64_to_bf16_bits(ref) != gpu_bits).sum())
+
+
 def check_glue(b, per, x):
     """Each projection input is the oracle's glue applied to the GPU's own earlier outputs."""
     s = b.shape
     h = O.bf16_bits_to_f64(x)
+    err_h = np.zeros_like(h)      # bound on |h_gpu - h| from the fp32 residual adds
     near = 0
     total = 0
+
+    def residual(h, err_h, v):
+        v = v.astype(np.float64)
+        new = h + v
+        return new, err_h + 2.0 ** -24 * np.abs(new) + 2.0 ** -24 * err_h
+
     for layer in range(s.n_layers):
-        u = O.f64_to_bf16_bits(O.rmsnorm(h))
-        d = bf16_ulp_diff(per[(layer, "q")][0], u)
-        near += int((d > 0).sum())
-        total += d.size
-        assert d.max() <= 1
+        near += rmsnorm_input_ok(per[(layer, "q")][0], h, err_h)
+        total += h.size
         v = per[(layer, "v")][1].astype(np.float64)
         a = O.f64_to_bf16_bits(O.attention_pos0(v, s.n_heads, s.n_kv_heads, s.head_dim))
         assert np.array_equal(per[(layer, "o")][0], a)  # same fp32 v, same rounding
-        h = h + per[(layer, "o")][1].astype(np.float64)
-        u = O.f64_to_bf16_bits(O.rmsnorm(h))
-        d = bf16_ulp_diff(per[(layer, "gate")][0], u)
-        assert d.max() <= 1
-        near += int((d > 0).sum())
-        total += d.size
+        h, err_h = residual(h, err_h, per[(layer, "o")][1])
+        near += rmsnorm_input_ok(per[(layer, "gate")][0], h, err_h)
+        total += h.size
         g = per[(layer, "gate")][1].astype(np.float64)
         up = per[(layer, "up")][1].astype(np.float64)
         mm = O.f64_to_bf16_bits(O.silu(g) * up)
@@ -120,13 +141,10 @@ def check_glue(b, per, x):
         assert d.max() <= 1
         near += int((d > 0).sum())
         total += d.size
-        h = h + per[(layer, "down")][1].astype(np.float64)
-    u = O.f64_to_bf16_bits(O.rmsnorm(h))
-    d = bf16_ulp_diff(per[(s.n_layers, "head")][0], u)
-    assert d.max() <= 1
-    near += int((d > 0).sum())
-    total += d.size
-    # 1-ulp differences come only from fp32-vs-fp64 values that sit near a bf16 rounding tie
+        h, err_h = residual(h, err_h, per[(layer, "down")][1])
+    near += rmsnorm_input_ok(per[(s.n_layers, "head")][0], h, err_h)
+    total += h.size
+    # Rounding differences come only from fp32-vs-fp64 values that sit near a bf16 rounding tie
     assert near <= max(8, total // 200), (near, total)
 
 

@@ -66,7 +66,7 @@ def test_noalloc_step_rejects_models_over_the_scratch_limit(V):
     import dataclasses
     import torch
     big = dataclasses.replace(model_tiny(), name="wide-ffn", n_layers=1, d=64, n_heads=1, n_kv_heads=1,
-                              head_dim=64, d_ff=32768, vocab=64)
+                              head_dim=64, d_ff=131072, vocab=64)
     mats, handles, model = _build(V, big, seed=3)
     x = dev_u16(gen_x(big.d, seed=4))
     out = torch.zeros(big.vocab, device="cuda")
