@@ -224,25 +224,28 @@ VBQ_API int64_t vbq_launch_count(int32_t reset);
  * counterpart: this is an interface of this library.
  *
  * It launches the same kernels in the same order as vbq_decode_step, directly
- * on `stream` (no graph, no trace), and gives the same logits. The activations
- * (h, [q;k;v], [gate;up]) live in one static device array of 65,600 floats
- * (256.25 KiB) that every GPU loading this library holds until the process
- * exits. The call allocates nothing: no cudaMalloc, no cudaFree, no graph.
+ * on `stream` (no graph, no trace), and gives the same logits. Its scratch
+ * lives in one static device array of 262,144 floats (1 MiB) that every GPU
+ * loading this library holds until the process exits. The array holds, in
+ * 64-float blocks, a status word, the split-tile arrival counters, h [d],
+ * [q;k;v], [gate;up], and the split-tile partial rows of the model's work
+ * plans. The call allocates nothing: no cudaMalloc, no cudaFree, no graph.
  *
  *  model       from vbq_model_create, on the current device
  *  x_dev       device, bf16 [d]
  *  logits_dev  device, float [vocab]
  *
- * Size limit: 64 + r(d) + r(n_heads*head_dim + 2*n_kv_heads*head_dim) +
- * r(2*d_ff) <= 65,600 floats, where r() rounds up to a multiple of 64 (the
- * 9B-shaped stack needs 38,976). Larger models get VBQ_ERR_SHAPE and nothing
- * is enqueued.
+ * Size limit: 64 + r(counters) + r(d) + r(n_heads*head_dim + 2*n_kv_heads*head_dim)
+ * + r(2*d_ff) + r(partial rows) <= 262,144 floats, where r() rounds up to a
+ * multiple of 64 and the counters and partial rows are the largest over the
+ * model's launch plans. Larger models get VBQ_ERR_SHAPE, the detail text gives
+ * the count, and nothing is enqueued.
  * Set-up: the first call on each device looks up the array's device address
  * with cudaGetSymbolAddress and sets the GEMV kernel attributes, with that
  * device current. Make that first call before any stream capture begins.
  * Sharing: every call on a device uses the same array, and the array keeps
- * the last call's contents. Each call writes h, q/k/v and gate/up before it
- * reads them, so stale contents do no harm. Calls that overlap on the GPU
+ * the last call's contents. Each call's first kernel clears the status word
+ * and the counters, and every other value is written before it is read. Calls that overlap on the GPU
  * (two streams, or two host threads) race on the array and give undefined
  * results; serialize them.
  * Errors: VBQ_ERR_INVALID_ARG (NULL or misaligned pointers, model on another

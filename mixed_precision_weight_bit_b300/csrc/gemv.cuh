@@ -31,11 +31,14 @@
 //    x'_m = 2^15 x_m, C = sum (x'_m + 127.5 x_m) per 8-code lane slice, and
 //    packed f32x2 FMAs.
 //  * Per entry, the lanes of the entry are summed with shuffles, then scaled by
-//    the fp16 group scale and added into the warp's fp32 row accumulator in
-//    shared memory. Rows are distinct within a step, so no atomics are needed.
-//  * At the end of a unit, the CTA sums its warps in a fixed order. A tile cut
-//    between CTAs writes one partial per unit, and the last CTA to arrive adds
-//    them in split order. Results are therefore deterministic.
+//    the fp16 group scale and added (red.shared.add) into the warp's private
+//    fp32 row accumulator. Each warp adds to a row in program order, so the
+//    sums do not depend on timing.
+//  * Accumulators are double-buffered by unit parity, and no barrier spans the
+//    CTA. The last warp to finish a unit (a shared-memory counter) sums the
+//    warps' accumulators in warp order while the others go on to the next
+//    unit. A tile cut between CTAs gets one partial per unit, and the last CTA
+//    to arrive adds them in split order. Results are therefore deterministic.
 #pragma once
 
 #include <type_traits>
@@ -103,8 +106,9 @@ struct GemvSmem {
   static constexpr int kRingStride = kRingBytes + SPILL;
   static constexpr int kRing = 0;
   static constexpr int kXp = kRing + W * kRingStride;
-  static constexpr int kAcc = kXp + W * NB * XPF * 4;
-  static constexpr int kBar = kAcc + W * NB * TILE_MAX * 4;
+  static constexpr int kAcc = kXp + W * NB * XPF * 4;          // [2 parities][W][NB][TILE_MAX]
+  static constexpr int kAccParity = W * NB * TILE_MAX * 4;
+  static constexpr int kBar = kAcc + 2 * kAccParity;
   static constexpr int kMisc = kBar + W * NSLOT * 8;
   static constexpr int kBytes = kMisc + 64 * 4;
   static_assert((kRingBytes & (kRingBytes - 1)) == 0, "ring must be a power of two");
@@ -272,10 +276,8 @@ __device__ __forceinline__ void do_step(uint32_t rb, uint32_t e, uint32_t xp, ui
     const uint32_t row = lds<uint8_t>(rb + rec_row_off(CLS, e) + j);
     const float sc = __half2float(__ushort_as_half(sb));
 #pragma unroll
-    for (int c = 0; c < NB; ++c) {
-      const uint32_t ao = acc + (c * TILE_MAX + row) * 4;
-      sts(ao, fmaf(sc, tv[c], lds<float>(ao)));
-    }
+    for (int c = 0; c < NB; ++c)
+      atomicAdd(reinterpret_cast<float*>(vbq_smem + acc + (c * TILE_MAX + row) * 4), sc * tv[c]);
   }
 }
 
@@ -395,9 +397,14 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
   for (int c = 0; c < NB; ++c)
 #pragma unroll
     for (int k = 0; k < NLUT; ++k) lut[c][k] = 0.0f;
-  const uint32_t acc = Lay::kAcc + warp * NB * TILE_MAX * 4;
+  // This warp's accumulator for unit parity p: acc_base + p * kAccParity.
+  const uint32_t acc_base = Lay::kAcc + warp * NB * TILE_MAX * 4;
   float* misc = reinterpret_cast<float*>(vbq_smem + Lay::kMisc);
-  for (int i = lane; i < NB * TILE_MAX; i += 32) sts(acc + i * 4, 0.0f);
+  // misc words 32..35: arrivals[2], reductions done[2], as uint32.
+  uint32_t* ucount = reinterpret_cast<uint32_t*>(misc) + 32;
+  if (threadIdx.x < 4) ucount[threadIdx.x] = 0u;
+
+  __syncthreads();  // the unit counters are initialized
 
   // The next kernel may start streaming its own weights now.
   grid_dep_launch();
@@ -440,6 +447,7 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
   }
 
   uint32_t o = 0;  // stream offset of the next record
+  uint32_t acc = acc_base;
   int cur_g = -1;
   int cur_seg = -1;
 
@@ -520,6 +528,21 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
   };
 
   for (int ui = 0; ui < nu; ++ui) {
+    const uint32_t par = static_cast<uint32_t>(ui) & 1u;
+    acc = acc_base + par * Lay::kAccParity;
+    if (ui >= 2) {  // the reduction of unit ui - 2 must have read this buffer (bounded wait)
+      const uint32_t need = static_cast<uint32_t>(ui) >> 1;
+      const long long t0 = clock64();
+      while (*reinterpret_cast<volatile uint32_t*>(ucount + 2 + par) < need) {
+        if (clock64() - t0 > 8000000000LL) {
+          S.ok = false;
+          break;
+        }
+      }
+      S.ok = __all_sync(0xffffffffu, S.ok);
+    }
+    for (int i = lane; i < NB * TILE_MAX; i += 32) sts(acc + i * 4, 0.0f);
+    __syncwarp();
     const uint32_t seg = __shfl_sync(0xffffffffu, u_seg, ui);
     const uint32_t run1 = __shfl_sync(0xffffffffu, s_run1, ui);
     const uint32_t k1 = __shfl_sync(0xffffffffu, s_k1, ui);
@@ -554,59 +577,66 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
       }
     }
 
-    // ---- unit epilogue: warps in fixed order, then split tiles across CTAs ----
-    __syncthreads();
-    const uint32_t split = __shfl_sync(0xffffffffu, u_split, ui);
-    const uint32_t nsplit = __shfl_sync(0xffffffffu, u_nsplit, ui);
-    const uint32_t r0 = __shfl_sync(0xffffffffu, u_r0, ui);
-    const uint32_t rows = __shfl_sync(0xffffffffu, u_rows, ui);
-    const MatView& M = a.seg[seg];
-    auto store = [&](int c, uint32_t row, float v) {
-      if (c == 0 && M.trace_y) M.trace_y[row] = v;
-      if (a.ep == EP_RESID) v += a.resid[row];
-      M.y[static_cast<int64_t>(c) * M.y_ld + row] = v;
-    };
-    auto warp_sum = [&](int c, uint32_t r) {
-      float v = 0.0f;
+    // ---- unit epilogue: the last warp to finish sums the warps in fixed order ----
+    __syncwarp();
+    __threadfence_block();
+    uint32_t arrived = 0;
+    if (lane == 0) arrived = atomicAdd(ucount + par, 1u);
+    arrived = __shfl_sync(0xffffffffu, arrived, 0);
+    if (arrived % W == W - 1) {
+      __threadfence_block();
+      const uint32_t split = __shfl_sync(0xffffffffu, u_split, ui);
+      const uint32_t nsplit = __shfl_sync(0xffffffffu, u_nsplit, ui);
+      const uint32_t r0 = __shfl_sync(0xffffffffu, u_r0, ui);
+      const uint32_t rows = __shfl_sync(0xffffffffu, u_rows, ui);
+      const MatView& M = a.seg[seg];
+      const uint32_t accp = Lay::kAcc + par * Lay::kAccParity;
+      auto store = [&](int c, uint32_t row, float v) {
+        if (c == 0 && M.trace_y) M.trace_y[row] = v;
+        if (a.ep == EP_RESID) v += a.resid[row];
+        M.y[static_cast<int64_t>(c) * M.y_ld + row] = v;
+      };
+      auto warp_sum = [&](int c, uint32_t r) {
+        float v = 0.0f;
 #pragma unroll
-      for (int w = 0; w < W; ++w) v += lds<float>(Lay::kAcc + ((w * NB + c) * TILE_MAX + r) * 4);
-      return v;
-    };
-    if (nsplit <= 1u) {
-      for (uint32_t r = threadIdx.x; r < rows; r += W * 32) {
+        for (int w = 0; w < W; ++w) v += lds<float>(accp + ((w * NB + c) * TILE_MAX + r) * 4);
+        return v;
+      };
+      if (nsplit <= 1u) {
+        for (uint32_t r = lane; r < rows; r += 32) {
 #pragma unroll
-        for (int c = 0; c < NB; ++c) store(c, r0 + r, warp_sum(c, r));
-      }
-    } else {
-      const uint32_t pbase = __shfl_sync(0xffffffffu, u_pbase, ui);
-      const uint32_t cnt = __shfl_sync(0xffffffffu, u_cnt, ui);
-      float* part = a.plan.partial + static_cast<size_t>(pbase) * NB;
-      for (uint32_t r = threadIdx.x; r < rows; r += W * 32) {
-#pragma unroll
-        for (int c = 0; c < NB; ++c) part[(split * NB + c) * rows + r] = warp_sum(c, r);
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const uint32_t prev = atomicAdd(a.plan.counters + cnt, 1u);
-        reinterpret_cast<uint32_t*>(misc)[32] = (prev == nsplit - 1u) ? 1u : 0u;
-      }
-      __syncthreads();
-      if (reinterpret_cast<const uint32_t*>(misc)[32]) {
-        __threadfence();
-        for (uint32_t r = threadIdx.x; r < rows; r += W * 32) {
-#pragma unroll
-          for (int c = 0; c < NB; ++c) {
-            float v = 0.0f;
-            for (uint32_t s = 0; s < nsplit; ++s) v += __ldcg(part + (s * NB + c) * rows + r);
-            store(c, r0 + r, v);
-          }
+          for (int c = 0; c < NB; ++c) store(c, r0 + r, warp_sum(c, r));
         }
-        if (threadIdx.x == 0) a.plan.counters[cnt] = 0u;
+      } else {
+        const uint32_t pbase = __shfl_sync(0xffffffffu, u_pbase, ui);
+        const uint32_t cnt = __shfl_sync(0xffffffffu, u_cnt, ui);
+        float* part = a.plan.partial + static_cast<size_t>(pbase) * NB;
+        for (uint32_t r = lane; r < rows; r += 32) {
+#pragma unroll
+          for (int c = 0; c < NB; ++c) part[(split * NB + c) * rows + r] = warp_sum(c, r);
+        }
+        __threadfence();
+        __syncwarp();
+        uint32_t prev = 0;
+        if (lane == 0) prev = atomicAdd(a.plan.counters + cnt, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == nsplit - 1u) {
+          __threadfence();
+          for (uint32_t r = lane; r < rows; r += 32) {
+#pragma unroll
+            for (int c = 0; c < NB; ++c) {
+              float v = 0.0f;
+              for (uint32_t s = 0; s < nsplit; ++s) v += __ldcg(part + (s * NB + c) * rows + r);
+              store(c, r0 + r, v);
+            }
+          }
+          if (lane == 0) a.plan.counters[cnt] = 0u;
+        }
       }
+      __syncwarp();
+      __threadfence_block();
+      if (lane == 0) atomicAdd(ucount + 2 + par, 1u);
     }
-    __syncthreads();
-    for (int i = lane; i < NB * TILE_MAX; i += 32) sts(acc + i * 4, 0.0f);
   }
 
   if (!S.ok) {

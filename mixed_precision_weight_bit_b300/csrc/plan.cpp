@@ -16,57 +16,82 @@ struct Pos {
   int seg = 0;
   uint32_t run = 0, k = 0;
   uint64_t gbyte = 0;  // offset in the launch's stream
+  uint64_t gcost = 0;  // estimated work before this position
 };
 
 struct Stream {
   const std::vector<SegTables>& segs;
-  std::vector<uint64_t> base;  // stream offset of each segment, plus the total
+  std::vector<uint64_t> base;   // stream byte offset of each segment, plus the total
+  std::vector<uint64_t> cbase;  // stream cost offset of each segment, plus the total
+  std::vector<std::vector<uint64_t>> cpre;  // per segment: cost before each run (n_runs + 1)
 
   explicit Stream(const std::vector<SegTables>& s) : segs(s) {
     base.assign(s.size() + 1, 0);
-    for (size_t i = 0; i < s.size(); ++i)
+    cbase.assign(s.size() + 1, 0);
+    cpre.resize(s.size());
+    for (size_t i = 0; i < s.size(); ++i) {
       base[i + 1] = base[i] + (s[i].n_runs ? uint64_t(s[i].run_off[s[i].n_runs]) * 16u : 0u);
+      std::vector<uint64_t>& c = cpre[i];
+      c.assign(static_cast<size_t>(s[i].n_runs) + 1, 0);
+      for (int32_t r = 0; r < s[i].n_runs; ++r) {
+        const uint32_t d = s[i].run_desc[r];
+        const bool col_start = r == 0 || run_g(s[i].run_desc[r - 1]) != run_g(d) || is_tile_start(i, r);
+        c[r + 1] = c[r] + head_cost(d, col_start) + uint64_t(run_steps(d)) * kCostStep[run_cls(d)];
+      }
+      cbase[i + 1] = cbase[i] + c.back();
+    }
+  }
+  static uint64_t head_cost(uint32_t, bool col_start) { return kCostRun + (col_start ? kCostColumn : 0u); }
+  bool is_tile_start(size_t seg, int32_t r) const {
+    const SegTables& S = segs[seg];
+    return std::binary_search(S.tile_run0, S.tile_run0 + S.n_tiles + 1, static_cast<uint32_t>(r));
   }
   uint64_t total() const { return base.back(); }
+  uint64_t total_cost() const { return cbase.back(); }
 
   uint64_t run_start(int seg, uint32_t run) const { return uint64_t(segs[seg].run_off[run]) * 16u; }
 
-  // Nearest step border to local byte t of segment seg.
-  Pos snap_local(int seg, uint64_t t) const {
+  Pos at(int seg, uint32_t run, uint32_t k) const {
     const SegTables& S = segs[seg];
     Pos p;
     p.seg = seg;
-    if (t >= run_start(seg, S.n_runs)) {
+    if (run >= static_cast<uint32_t>(S.n_runs)) {
       p.run = S.n_runs;
       p.gbyte = base[seg] + run_start(seg, S.n_runs);
+      p.gcost = cbase[seg] + cpre[seg].back();
       return p;
     }
-    // last run whose start <= t
-    uint32_t lo = 0, hi = S.n_runs;  // invariant: start(lo) <= t < start(hi)
-    while (hi - lo > 1) {
-      const uint32_t mid = (lo + hi) / 2;
-      if (run_start(seg, mid) <= t) lo = mid; else hi = mid;
-    }
-    const uint32_t d = S.run_desc[lo];
-    const uint64_t full = full_step_bytes(run_cls(d));
-    const uint32_t nst = run_steps(d);
-    uint64_t k = (t - run_start(seg, lo) + full / 2) / full;
-    if (k >= nst) {
-      p.run = lo + 1;
-      p.k = 0;
-      p.gbyte = base[seg] + run_start(seg, lo + 1);
-    } else {
-      p.run = lo;
-      p.k = static_cast<uint32_t>(k);
-      p.gbyte = base[seg] + run_start(seg, lo) + k * full;
-    }
+    const uint32_t d = S.run_desc[run];
+    if (k >= run_steps(d)) return at(seg, run + 1, 0);
+    p.run = run;
+    p.k = k;
+    p.gbyte = base[seg] + run_start(seg, run) + uint64_t(k) * full_step_bytes(run_cls(d));
+    p.gcost = cbase[seg] + cpre[seg][run] + (k ? (cpre[seg][run + 1] - cpre[seg][run] -
+                                                  uint64_t(run_steps(d)) * kCostStep[run_cls(d)]) +
+                                                     uint64_t(k) * kCostStep[run_cls(d)]
+                                               : 0u);
     return p;
   }
 
-  // Nearest step border to stream byte t.
+  // Nearest step border to local cost t of segment seg.
+  Pos snap_local(int seg, uint64_t t) const {
+    const SegTables& S = segs[seg];
+    const std::vector<uint64_t>& c = cpre[seg];
+    if (t >= c.back()) return at(seg, S.n_runs, 0);
+    // last run whose cost start <= t
+    const uint32_t r = static_cast<uint32_t>(std::upper_bound(c.begin(), c.end(), t) - c.begin()) - 1u;
+    const uint32_t d = S.run_desc[r];
+    const uint64_t head = c[r + 1] - c[r] - uint64_t(run_steps(d)) * kCostStep[run_cls(d)];
+    const uint64_t step = kCostStep[run_cls(d)];
+    const uint64_t into = t - c[r];
+    const uint64_t k = into <= head ? 0u : (into - head + step / 2) / step;
+    return at(seg, r, static_cast<uint32_t>(std::min<uint64_t>(k, run_steps(d))));
+  }
+
+  // Nearest step border to stream cost t.
   Pos snap(uint64_t t) const {
     for (size_t s = 0; s < segs.size(); ++s)
-      if (t < base[s + 1]) return snap_local(static_cast<int>(s), t - base[s]);
+      if (t < cbase[s + 1]) return snap_local(static_cast<int>(s), t - cbase[s]);
     return end();
   }
 
@@ -75,6 +100,7 @@ struct Stream {
     p.seg = static_cast<int>(segs.size()) - 1;
     p.run = segs.empty() ? 0 : segs.back().n_runs;
     p.gbyte = total();
+    p.gcost = total_cost();
     return p;
   }
 
@@ -110,7 +136,7 @@ SliceRec slice_of(const Stream& st, const Pos& a, const Pos& b) {
 }
 
 bool build(const Stream& st, int32_t P, int max_units, Plan* out) {
-  const uint64_t total = st.total();
+  const uint64_t total = st.total_cost();
   std::vector<Pos> cut(P + 1);
   cut[0] = st.normalize(st.snap(0));
   cut[P] = st.end();
@@ -130,10 +156,7 @@ bool build(const Stream& st, int32_t P, int max_units, Plan* out) {
       pos = st.normalize(pos);
       const SegTables& S = st.segs[pos.seg];
       const uint32_t t = st.tile_of(pos.seg, pos.run);
-      Pos tend;
-      tend.seg = pos.seg;
-      tend.run = S.tile_run0[t + 1];
-      tend.gbyte = st.base[pos.seg] + st.run_start(pos.seg, tend.run);
+      const Pos tend = st.at(pos.seg, S.tile_run0[t + 1], 0);
       const Pos uend = cut[c + 1].gbyte < tend.gbyte ? cut[c + 1] : tend;
       UnitRec u{};
       u.seg = static_cast<uint32_t>(pos.seg);
@@ -149,8 +172,8 @@ bool build(const Stream& st, int32_t P, int max_units, Plan* out) {
         if (j == SLICES) {
           nx = uend;
         } else {
-          const uint64_t tgt = pos.gbyte + (uend.gbyte - pos.gbyte) * static_cast<uint64_t>(j) / SLICES;
-          nx = st.snap_local(pos.seg, tgt - st.base[pos.seg]);
+          const uint64_t tgt = pos.gcost + (uend.gcost - pos.gcost) * static_cast<uint64_t>(j) / SLICES;
+          nx = st.snap_local(pos.seg, tgt - st.cbase[pos.seg]);
           if (nx.gbyte < prev.gbyte) nx = prev;
           if (nx.gbyte > uend.gbyte) nx = uend;
         }
@@ -215,7 +238,7 @@ Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units
   Stream st(segs);
   Plan p;
   int32_t P = std::max<int32_t>(1, n_ctas);
-  if (st.total() == 0) {
+  if (st.total() == 0 || st.total_cost() == 0) {
     p.n_ctas = 0;
     p.umax = 0;
     return p;

@@ -34,6 +34,12 @@ struct Plan {
   uint32_t n_counters = 0;
 };
 
+// Work model used to balance CTAs and warps: estimated warp instructions per
+// step of each bit class, per run, and per group column a warp has to prepare.
+constexpr uint32_t kCostStep[4] = {62, 64, 66, 50};
+constexpr uint32_t kCostRun = 6;
+constexpr uint32_t kCostColumn = 110;
+
 // Number of CTAs for a launch over total_bytes: one per SM at most, but no
 // fewer than 32 KB each, and never more than MAX_UNITS_PER_CTA units a CTA.
 int32_t plan_ctas(uint64_t total_bytes, int sms);

@@ -14,6 +14,7 @@
 // Exit status 0 on success; the first failed check is printed.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -113,6 +114,7 @@ static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::ve
   CHECK(pl.units.size() == static_cast<size_t>(pl.n_ctas) * pl.umax, "unit slots");
   CHECK(dp.n_ctas == pl.n_ctas && dp.umax == pl.umax, "device plan shape");
   std::vector<uint64_t> cta_bytes(pl.n_ctas, 0);
+  std::vector<uint64_t> cta_cost(pl.n_ctas, 0);  // the planner's work model over what each CTA walks
   std::vector<uint32_t> cnt_units(pl.n_counters, 0);
   std::vector<uint32_t> cta_units(pl.n_ctas, 0);
   for (int32_t c = 0; c < pl.n_ctas; ++c) {
@@ -171,6 +173,12 @@ static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::ve
           const uint32_t cls = run_cls(d), n = run_n(d), eps = entries_per_step(cls);
           const uint32_t kend = (run == l.run1) ? l.k1 : (n + eps - 1) / eps;
           if (k == 0 && kend > 0) CHECK(o == uint64_t(M->h_run_off[run]) * 16, "run start offset");
+          if (k == 0 && kend > 0) {
+            const bool col = run == 0 || run_g(M->h_run_desc[run - 1]) != run_g(d) ||
+                             std::binary_search(M->h_tile_run0.begin(), M->h_tile_run0.end(), run);
+            cta_cost[c] += kCostRun + (col ? kCostColumn : 0u);
+          }
+          if (kend > k) cta_cost[c] += uint64_t(kend - k) * kCostStep[cls];
           for (; k < kend; ++k) {
             CHECK(k < seen[ur.seg][run].size(), "step index");
             seen[ur.seg][run][k] += 1;
@@ -215,12 +223,15 @@ static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::ve
       for (size_t k = 0; k < seen[s][r].size(); ++k)
         CHECK(seen[s][r][k] == 1, "seg %zu run %d step %zu walked %d times", s, r, k, seen[s][r][k]);
   for (uint32_t i = 0; i < pl.n_counters; ++i) CHECK(cnt_units[i] >= 2, "split tile with <2 units");
-  // Balance: no CTA far above the mean (one step of slack per unit).
-  if (pl.n_ctas > 1 && total > 0) {
-    const double mean = static_cast<double>(total) / pl.n_ctas;
+  // Balance: no CTA far above the mean of the work model (one step and one
+  // column of slack per unit, since cuts fall on step borders).
+  if (pl.n_ctas > 1 && W == 16) {
+    uint64_t tot = 0;
+    for (uint64_t v : cta_cost) tot += v;
+    const double mean = static_cast<double>(tot) / pl.n_ctas;
     for (int32_t c = 0; c < pl.n_ctas; ++c)
-      CHECK(cta_bytes[c] <= mean * 1.02 + 2048.0 + 400.0 * cta_units[c],
-            "CTA %d carries %llu bytes, mean %.0f", c, static_cast<unsigned long long>(cta_bytes[c]), mean);
+      CHECK(cta_cost[c] <= mean * 1.02 + 200.0 + 250.0 * cta_units[c], "CTA %d carries cost %llu, mean %.0f", c,
+            static_cast<unsigned long long>(cta_cost[c]), mean);
   }
 }
 
