@@ -46,6 +46,7 @@ def parse():
     p.add_argument("--no-1b", action="store_true", help="skip the 1B-shaped step")
     p.add_argument("--no-dense", action="store_true", help="skip the dense bf16 baseline")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    p.add_argument("--no-sweep", action="store_true", help="skip the batch sweep and the stress matrices")
     return p.parse_args()
 
 
@@ -259,6 +260,63 @@ def dense_baseline(V, shape, stream, steps=3):
             "weight_bytes": nbytes}
 
 
+def time_cold(fn, stream, reps=10):
+    """Median device time of fn() over reps runs, with a 512 MiB write between runs to evict L2."""
+    import torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        fn()
+    ts = []
+    for _ in range(reps):
+        with torch.cuda.stream(stream):   # the flush is ordered before the timed call on the same stream
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    del flush
+    return float(np.median(ts)) * 1e3
+
+
+def batch_sweep(V, stream):
+    """14336x4096 at the config-0 allocation, batch 1..64, cold L2 (CUDA-core path to 8, tensor cores from 16)."""
+    import torch
+    from synth import CONFIG0_PROBS, gen_matrix, gen_x
+    m = gen_matrix(14336, 4096, CONFIG0_PROBS, seed=0)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    info = mat.info()
+    out = {}
+    for B in (1, 2, 4, 8, 16, 32, 64):
+        X = torch.from_numpy(gen_x(4096, seed=100 + B, batch=B).view(np.int16)).cuda()
+        Y = torch.empty(B, 14336, device="cuda")
+        us = time_cold(lambda: V.vbq_gemm_smallbatch(mat.handle, X, B, Y, stream), stream)
+        alg = algorithmic_bytes(14336, 4096, info["code_bytes"]) + 2.0 * 4096 * (B - 1) + 4.0 * 14336 * (B - 1)
+        out[str(B)] = {"us": round(us, 1), "GB/s": round(alg / us / 1e3, 1),
+                       "TFLOP/s": round(2.0 * 14336 * 4096 * B / us / 1e6, 2)}
+    mat.close()
+    return out
+
+
+def stress_8192(V, stream):
+    """The 8192x8192 allocation-stress matrices (a)-(e), batch 1, cold L2."""
+    import torch
+    from synth import gen_stress, gen_x
+    x = torch.from_numpy(gen_x(8192, seed=21).view(np.int16)).cuda()
+    y = torch.empty(8192, device="cuda")
+    out = {}
+    for case in "abcde":
+        m = gen_stress(case, 8192, 8192)
+        mat = V.Matrix(m.codes, m.bits, m.scales)
+        info = mat.info()
+        us = time_cold(lambda: V.vbq_gemv(mat.handle, x, y, stream), stream)
+        alg = algorithmic_bytes(8192, 8192, info["code_bytes"])
+        out[case] = {"us": round(us, 1), "GB/s": round(alg / us / 1e3, 1), "mean_bits": round(info["mean_bits"], 3)}
+        mat.close()
+    return out
+
+
 # --------------------------------------------------------------------------- CPU oracle
 
 def cpu_oracle_sample(shape, budget_s: float):
@@ -392,6 +450,9 @@ def run_vbq(args, ws, rank, local):
         extra["GB/s_1b"] = round(pm1.alg_bytes / (ms1 * 1e-3) / 1e9, 1)
         pm1.close()
         torch.cuda.empty_cache()
+    if not args.no_sweep:
+        extra["batch_sweep_14336x4096"] = batch_sweep(V, stream)
+        extra["stress_8192"] = stress_8192(V, stream)
     if not args.no_dense:
         extra["dense_bf16_9b"] = dense_baseline(V, shape, stream)
         extra["dense_bf16_9b"]["speedup_vbq"] = round(extra["dense_bf16_9b"]["us_per_step"] / (ms * 1e3), 2)

@@ -27,6 +27,8 @@ struct vbq_matrix {
   const uint32_t* tile_run0 = nullptr;
   std::vector<uint32_t> h_run_desc, h_run_off, h_tile_row0, h_tile_run0;  // host copies, for planning
   vbq::DevicePlan plan;  // plan of a GEMV over this matrix alone
+  float tc_max_scale = 0.0f;  // largest |s_g|: the tensor-core path needs s * 127.5 inside fp16
+  int64_t max_col_bytes = 0;  // largest (tile, group column) record span
 };
 
 namespace vbq {
@@ -48,6 +50,11 @@ const GpuInfo& gpu_info();
 
 // Widest batch a single GEMV launch covers (partial storage is sized for it).
 constexpr int MAX_NB = 4;
+
+// Tensor-core dequant-MMA for 16..64 batch columns (gemm_tc.cu).
+bool tc_eligible(const vbq_matrix* m);
+vbq_status launch_gemm_tc(const vbq_matrix* m, const uint16_t* X, int32_t B, float* Y, cudaStream_t st);
+void tc_forget(const vbq_matrix* m);
 
 inline SegTables seg_tables(const vbq_matrix* m) {
   SegTables t;

@@ -334,6 +334,9 @@ extern "C" vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X
   if (m->N > 0 && m->K > 0 && !X_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm_smallbatch: NULL X");
   if (!aligned(X_dev, 4) || !aligned(Y_dev, 4))
     return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm_smallbatch: X and Y must be 4-byte aligned");
+  // 16 or more columns form a dense contraction: the tensor-core dequant-MMA.
+  if (B >= 16 && m->N > 0 && m->K > 0 && aligned(X_dev, 16) && tc_eligible(m))
+    return launch_gemm_tc(m, X_dev, B, Y_dev, static_cast<cudaStream_t>(stream));
   return gemv_columns(m, X_dev, B, Y_dev, static_cast<cudaStream_t>(stream));
 }
 

@@ -5,6 +5,7 @@
 // tile plan and class ordering are this library's own design.
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <thread>
 #include <vector>
@@ -240,10 +241,13 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
 
   int64_t cnt[4] = {0, 0, 0, 0};
   int64_t code_bytes = 0;
+  uint16_t max_mag = 0;  // largest |s| as fp16 magnitude bits (monotone in the value for finite fp16)
   for (int64_t i = 0; i < N * G; ++i) {
     const int c = bits_to_cls(bits[i]);
     ++cnt[c];
     code_bytes += 8 * cls_bits(c);
+    const uint16_t mag = scales_f16[i] & 0x7FFFu;
+    if (mag > max_mag) max_mag = mag;
   }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -274,6 +278,25 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
   m->data_bytes = static_cast<int64_t>(data_bytes);
   m->code_bytes = code_bytes;
   for (int c = 0; c < 4; ++c) m->groups_by_bits[c] = cnt[c];
+  {  // the largest (tile, column) record span
+    int64_t best = 0;
+    for (int32_t t = 0; t < nt; ++t) {
+      uint32_t r = run0[t];
+      while (r < run0[t + 1]) {
+        uint32_t e = r + 1;
+        while (e < run0[t + 1] && run_g(m->h_run_desc[e]) == run_g(m->h_run_desc[r])) ++e;
+        best = std::max<int64_t>(best, 16ll * (m->h_run_off[e] - m->h_run_off[r]));
+        r = e;
+      }
+    }
+    m->max_col_bytes = best;
+  }
+  {  // fp16 magnitude bits to float (exact)
+    const uint32_t e = (max_mag >> 10) & 31u, f = max_mag & 1023u;
+    m->tc_max_scale = e == 31 ? 1e30f
+                      : e == 0 ? std::ldexp(static_cast<float>(f), -24)
+                               : std::ldexp(static_cast<float>(f | 1024u), static_cast<int>(e) - 25);
+  }
 
   // The plan of a GEMV over this matrix alone.
   Plan pl = make_plan({seg_tables(m)}, plan_ctas(data_bytes, gpu_info().sms), MAX_UNITS_PER_CTA);
@@ -298,6 +321,7 @@ extern "C" void vbq_matrix_free(vbq_matrix* m) {
     cudaDeviceSynchronize();
     cudaFree(m->dev_base);
     free_plan(&m->plan);
+    tc_forget(m);
     cudaSetDevice(cur);
   }
   delete m;

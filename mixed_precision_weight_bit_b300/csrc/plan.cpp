@@ -24,8 +24,10 @@ struct Stream {
   std::vector<uint64_t> base;   // stream byte offset of each segment, plus the total
   std::vector<uint64_t> cbase;  // stream cost offset of each segment, plus the total
   std::vector<std::vector<uint64_t>> cpre;  // per segment: cost before each run (n_runs + 1)
+  std::vector<std::vector<uint32_t>> cols;  // per segment: first run of every (tile, column), then n_runs
+  bool whole_columns = false;
 
-  explicit Stream(const std::vector<SegTables>& s) : segs(s) {
+  explicit Stream(const std::vector<SegTables>& s, bool by_columns = false) : segs(s), whole_columns(by_columns) {
     base.assign(s.size() + 1, 0);
     cbase.assign(s.size() + 1, 0);
     cpre.resize(s.size());
@@ -39,6 +41,13 @@ struct Stream {
         c[r + 1] = c[r] + head_cost(d, col_start) + uint64_t(run_steps(d)) * kCostStep[run_cls(d)];
       }
       cbase[i + 1] = cbase[i] + c.back();
+    }
+    cols.resize(s.size());
+    for (size_t i = 0; i < s.size(); ++i) {
+      for (int32_t r = 0; r < s[i].n_runs; ++r)
+        if (r == 0 || run_g(s[i].run_desc[r - 1]) != run_g(s[i].run_desc[r]) || is_tile_start(i, r))
+          cols[i].push_back(static_cast<uint32_t>(r));
+      cols[i].push_back(static_cast<uint32_t>(s[i].n_runs));
     }
   }
   static uint64_t head_cost(uint32_t, bool col_start) { return kCostRun + (col_start ? kCostColumn : 0u); }
@@ -73,11 +82,22 @@ struct Stream {
     return p;
   }
 
-  // Nearest step border to local cost t of segment seg.
+  // Nearest step border (or column start, in whole-column mode) to local cost t of segment seg.
   Pos snap_local(int seg, uint64_t t) const {
     const SegTables& S = segs[seg];
     const std::vector<uint64_t>& c = cpre[seg];
     if (t >= c.back()) return at(seg, S.n_runs, 0);
+    if (whole_columns) {
+      const std::vector<uint32_t>& cs = cols[seg];
+      // last column start whose cost <= t, and the next one
+      size_t lo = 0, hi = cs.size() - 1;
+      while (hi - lo > 1) {
+        const size_t mid = (lo + hi) / 2;
+        if (c[cs[mid]] <= t) lo = mid; else hi = mid;
+      }
+      const uint64_t a = c[cs[lo]], b = c[cs[hi]];
+      return at(seg, (t - a <= b - t) ? cs[lo] : cs[hi], 0);
+    }
     // last run whose cost start <= t
     const uint32_t r = static_cast<uint32_t>(std::upper_bound(c.begin(), c.end(), t) - c.begin()) - 1u;
     const uint32_t d = S.run_desc[r];
@@ -234,8 +254,8 @@ int32_t plan_ctas(uint64_t total_bytes, int sms) {
   return static_cast<int32_t>(std::max<uint64_t>(1, std::min<uint64_t>(static_cast<uint64_t>(sms), by_bytes)));
 }
 
-Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units) {
-  Stream st(segs);
+Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units, bool whole_columns) {
+  Stream st(segs, whole_columns);
   Plan p;
   int32_t P = std::max<int32_t>(1, n_ctas);
   if (st.total() == 0 || st.total_cost() == 0) {

@@ -45,8 +45,10 @@ constexpr uint32_t kCostColumn = 110;
 int32_t plan_ctas(uint64_t total_bytes, int sms);
 
 // Builds the plan. If a CTA would get more than max_units units, the CTA count
-// grows until none does.
-Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units);
+// grows until none does. With whole_columns, every cut falls at the start of a
+// (tile, group column), so each unit covers whole columns (the tensor-core
+// path dequantizes one column of a tile at a time).
+Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units, bool whole_columns = false);
 
 // A plan's device copy: units, slices and CTA table, arrival counters (zeroed)
 // and partial rows for up to max_nb batch columns, in one allocation.

@@ -44,6 +44,7 @@ static std::string g_err;
 vbq_status fail(vbq_status s, const std::string& d) { g_err = d; return s; }
 vbq_status cuda_fail(cudaError_t, const char* w) { g_err = w; return VBQ_ERR_CUDA; }
 void note_launches(int64_t) {}
+void tc_forget(const vbq_matrix*) {}
 static int g_sms = 148;
 const GpuInfo& gpu_info() {
   static GpuInfo gi;
@@ -101,7 +102,7 @@ static Logical make_matrix(int64_t N, int64_t K, const double p[4], uint32_t see
 
 // Replays the kernel's walk over one launch's plan. segs[i] is the packed matrix i.
 static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::vector<const Logical*>& logi,
-                       const Plan& pl, const DevicePlan& dp, int W) {
+                       const Plan& pl, const DevicePlan& dp, int W, bool balance = true) {
   const int SPW = SLICES / W;
   // Every step of every run of every matrix: visit count.
   std::vector<std::vector<std::vector<uint8_t>>> seen(mats.size());
@@ -225,7 +226,7 @@ static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::ve
   for (uint32_t i = 0; i < pl.n_counters; ++i) CHECK(cnt_units[i] >= 2, "split tile with <2 units");
   // Balance: no CTA far above the mean of the work model (one step and one
   // column of slack per unit, since cuts fall on step borders).
-  if (pl.n_ctas > 1 && W == 16) {
+  if (balance && pl.n_ctas > 1 && W == 16) {
     uint64_t tot = 0;
     for (uint64_t v : cta_cost) tot += v;
     const double mean = static_cast<double>(tot) / pl.n_ctas;
@@ -262,6 +263,26 @@ int main() {
     Plan pl = make_plan({seg_tables(m)}, m->plan.n_ctas, MAX_UNITS_PER_CTA);
     check_plan({m}, {&L}, pl, m->plan, 16);
     check_plan({m}, {&L}, pl, m->plan, 8);
+    // Whole-column plans (the tensor-core path): every unit starts and ends at a column start.
+    for (int P : {1, 148}) {
+      Plan pc = make_plan({seg_tables(m)}, P, MAX_UNITS_PER_CTA, true);
+      DevicePlan dc;
+      CHECK(upload_plan(pc, 64, nullptr, &dc) == cudaSuccess, "upload");
+      check_plan({m}, {&L}, pc, dc, 16, /*balance=*/false);  // cuts fall only on column starts
+      for (size_t u = 0; u < pc.units.size(); ++u) {
+        if (pc.units[u].nsplit == 0) continue;
+        const SliceRec& a0 = pc.slices[u * SLICES];
+        const SliceRec& a1 = pc.slices[u * SLICES + SLICES - 1];
+        auto col_start = [&](uint32_t r) {
+          return r == 0 || r >= static_cast<uint32_t>(m->n_runs) ||
+                 run_g(m->h_run_desc[r - 1]) != run_g(m->h_run_desc[r]) ||
+                 std::binary_search(m->h_tile_run0.begin(), m->h_tile_run0.end(), r);
+        };
+        CHECK(a0.k0 == 0 && a1.k1 == 0 && col_start(a0.run0) && col_start(a1.run1), "unit %zu not on columns", u);
+      }
+      CHECK(m->max_col_bytes <= 17408, "column span %lld", static_cast<long long>(m->max_col_bytes));
+      free_plan(&dc);
+    }
     // Other CTA counts, including more CTAs than tiles and a single CTA.
     for (int P : {1, 7, 148, 600}) {
       Plan p2 = make_plan({seg_tables(m)}, P, MAX_UNITS_PER_CTA);

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 from oracle import vbq_oracle as O
-from synth import (CONFIG0_PROBS, gen_matrix, gen_matrix_with_bits, gen_stress, gen_x, stress_bits)
+from synth import (CONFIG0_PROBS, bf16_bits_to_f32, gen_matrix, gen_matrix_with_bits, gen_stress, gen_x, stress_bits)
 from tests.gpu_util import TOL, dev_u16, gemv_err, gpu_dequant, gpu_gemm, gpu_gemv, lib
 
 pytestmark = pytest.mark.gpu
@@ -167,3 +167,59 @@ def test_full_stress_8192(V, case):
 
 def test_device_check_clean(V):
     assert V.vbq_device_check() == 0
+
+
+# ---- batches of 16..64: the tensor-core dequant-MMA ----
+
+TC_CASES = {
+    "mix300x1024": lambda: gen_matrix(300, 1024, CONFIG0_PROBS, seed=30),      # tiles of < 256 rows, both halves
+    "mix100x512": lambda: gen_matrix(100, 512, CONFIG0_PROBS, seed=31),        # one tile of <= 128 rows
+    "mix777x64": lambda: gen_matrix(777, 64, CONFIG0_PROBS, seed=32),          # one group per row
+    "all8_256x512": lambda: _one_class(256, 512, 8, 33),                       # the largest column span
+    "all1_512x256": lambda: _one_class(512, 256, 1, 34),
+    "stress_e_1024": lambda: gen_stress("e", 1024, 1024),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TC_CASES))
+@pytest.mark.parametrize("B", [16, 17, 31, 48, 64])
+def test_tensor_core_batches(V, name, B):
+    m = TC_CASES[name]()
+    X = gen_x(m.K, seed=40 + B, batch=B)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    V.vbq_launch_count(reset=True)
+    Y = gpu_gemm(V, mat, X)
+    assert V.vbq_launch_count() == 2  # the x-scale kernel and one tensor-core launch for all B columns
+    assert np.isfinite(Y).all()
+    assert gemv_err(m, X, Y) <= TOL
+    mat.close()
+    assert V.vbq_device_check() == 0
+
+
+def test_tensor_core_large_x_and_repeat(V):
+    """x far outside fp16's range is scaled by a power of two per column; two calls agree bit for bit."""
+    m = gen_matrix(512, 1024, CONFIG0_PROBS, seed=35)
+    X = gen_x(m.K, seed=36, batch=24)
+    Xf = bf16_bits_to_f32(X) * np.float32(2.0 ** 40)
+    Xf[3] *= np.float32(2.0 ** -80)            # one column tiny
+    from synth import f32_to_bf16_bits
+    X = f32_to_bf16_bits(Xf)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    Y1 = gpu_gemm(V, mat, X)
+    Y2 = gpu_gemm(V, mat, X)
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+    assert gemv_err(m, X, Y1) <= TOL
+    mat.close()
+
+
+def test_large_scales_take_the_cuda_core_path(V):
+    """Scales whose products would overflow fp16 are served by the CUDA-core kernel, still within tolerance."""
+    m = gen_matrix(200, 512, CONFIG0_PROBS, seed=37)
+    scales = np.full_like(m.scales, np.float16(1000.0).view(np.uint16))
+    X = gen_x(m.K, seed=38, batch=20)
+    mat = V.Matrix(m.codes, m.bits, scales)
+    Y = gpu_gemm(V, mat, X)
+    from synth import VbqMatrixInputs
+    ref = VbqMatrixInputs(codes=m.codes, bits=m.bits, scales=scales)
+    assert gemv_err(ref, X, Y) <= TOL
+    mat.close()
