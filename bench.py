@@ -23,7 +23,6 @@ from __future__ import annotations
 import argparse
 import json
 import os
-import subprocess
 import sys
 import threading
 import time
@@ -47,6 +46,8 @@ def parse():
     p.add_argument("--no-dense", action="store_true", help="skip the dense bf16 baseline")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
     p.add_argument("--no-sweep", action="store_true", help="skip the batch sweep and the stress matrices")
+    p.add_argument("--workload", choices=["9b", "1b"], default="9b",
+                   help="decode-step shape of the headline (1b: a smaller case for profiling)")
     return p.parse_args()
 
 
@@ -125,54 +126,129 @@ class PackedModel:
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons over the timed region.
 
-    def __init__(self, index: int):
-        self.index = index
+    NVML (pynvml) is sampled every 2 ms from a thread when it is importable.
+    Otherwise nvidia-smi runs with a 20 ms period from before the warm-up
+    (prepare()), and only the samples that arrive inside the timed region, plus
+    the first one after it, are kept."""
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40, "sw_power_cap": 0x4}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []      # (host time, sm MHz, set of reasons)
+        self.max_mhz = None
+        self.err = None
+        self.mode = None
+        self.t0 = self.t1 = None
+        self._stop = threading.Event()
+        self.thread = None
         self.proc = None
-        self.lines = []
+
+    # -- NVML
+    def _nvml(self):
+        import pynvml as N
+        import torch
+        N.nvmlInit()
+        try:
+            p = torch.cuda.get_device_properties(self.cuda_index)
+            h = N.nvmlDeviceGetHandleByPciBusId(f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0")
+        except Exception:
+            h = N.nvmlDeviceGetHandleByIndex(self.cuda_index)
+        self.max_mhz = float(N.nvmlDeviceGetMaxClockInfo(h, N.NVML_CLOCK_SM))
+        get_r = getattr(N, "nvmlDeviceGetCurrentClocksEventReasons", None) or N.nvmlDeviceGetCurrentClocksThrottleReasons
+
+        def sample():
+            sm = float(N.nvmlDeviceGetClockInfo(h, N.NVML_CLOCK_SM))
+            r = int(get_r(h))
+            self.samples.append((time.perf_counter(), sm, {n for n, b in self.REASONS.items() if r & b}))
+
+        def run():
+            while not self._stop.is_set():
+                try:
+                    sample()
+                except Exception as e:
+                    self.err = str(e)
+                    return
+                self._stop.wait(0.002)
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+
+    # -- nvidia-smi
+    def _smi(self):
+        import subprocess
+        import torch
+        try:
+            p = torch.cuda.get_device_properties(self.cuda_index)
+            dev = f"--id={p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except Exception:
+            dev = f"--id={self.cuda_index}"
+        self.proc = subprocess.Popen(["nvidia-smi", dev, f"--query-gpu={self.SMI_FIELDS}",
+                                      "--format=csv,noheader,nounits", "-lms", "20"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+        def run():
+            for line in self.proc.stdout:
+                parts = [q.strip() for q in line.split(",")]
+                if len(parts) < 6:
+                    continue
+                try:
+                    sm, mx = float(parts[0]), float(parts[1])
+                except ValueError:
+                    continue
+                self.max_mhz = mx
+                self.samples.append((time.perf_counter(), sm,
+                                     {n for n, v in zip(names, parts[2:6]) if v.lower().startswith("active")}))
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+
+    def prepare(self):
+        """Starts sampling (call before the warm-up)."""
+        try:
+            self._nvml()
+            self.mode = "nvml, every 2 ms"
+        except Exception as e:
+            self.err = f"nvml: {e}"
+            try:
+                self._smi()
+                self.mode = "nvidia-smi, every 20 ms"
+                deadline = time.perf_counter() + 10.0
+                while not self.samples and time.perf_counter() < deadline:
+                    time.sleep(0.01)
+            except OSError as e2:
+                self.err += f"; nvidia-smi: {e2}"
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except OSError:
-            self.proc = None
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+        self.t0 = time.perf_counter()
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
+        self.t1 = time.perf_counter()
+        if self.mode is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
+        if self.mode.startswith("nvidia-smi"):
+            deadline = time.perf_counter() + 1.0
+            while not any(t > self.t1 for t, _, _ in self.samples) and time.perf_counter() < deadline:
+                time.sleep(0.005)
+        self._stop.set()
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        inside = [q for q in self.samples if self.t0 <= q[0] <= self.t1]
+        after = [q for q in self.samples if q[0] > self.t1][:1]
+        use = inside + after
+        sm = [q[1] for q in use]
+        reasons = sorted(set().union(*[q[2] for q in use])) if use else []
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm), "source": self.mode}
 
 
 # --------------------------------------------------------------------------- GPU timings
@@ -195,7 +271,33 @@ def time_steps(fn, steps, warmup, stream, ws):
     return ms
 
 
-def dominant_kernel_roofline(V, pm, stream, peak_gbs, reps=3):
+def decode_kernel_roofline(V, pm, x, logits, stream, peak_gbs, steps):
+    """The decode step is one launch of vbq_decode_kernel; each launch bracketed by events on its stream."""
+    import torch
+    ev = []
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            V.vbq_decode_step(pm.model.handle, x, logits, stream)
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            V.vbq_decode_step(pm.model.handle, x, logits, stream)
+            b.record(stream)
+            ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    avg = sum(ms) / len(ms)
+    achieved = pm.alg_bytes / (avg * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(achieved / peak_gbs, 4), "traffic": None,
+            "kernel": "vbq_decode_kernel<16,2>", "launches": len(ms),
+            "avg_launch_us": round(avg * 1e3, 2), "min_launch_us": round(min(ms) * 1e3, 2),
+            "alg_bytes_per_launch": round(pm.alg_bytes),
+            "note": "one launch per 9B decode step; algorithmic bytes = sum over the 225 projections of "
+                    "codes + 2.25 B/group + 2K + 4N"}
+
+
+def standalone_gemv(V, pm, stream, peak_gbs, reps=3):
     """Each projection as its own vbq_gemv launch, bracketed by events on the launching stream."""
     import torch
     from synth import gen_x
@@ -222,12 +324,11 @@ def dominant_kernel_roofline(V, pm, stream, peak_gbs, reps=3):
     tot_b = sum(ab for _, _, ab in ev)
     launches = len(ev)
     achieved = tot_b / (tot_ms * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
-            "frac": round(achieved / peak_gbs, 4), "traffic": None,
-            "kernel": "vbq_gemv_kernel<1,16,8>", "launches": launches,
+    return {"achieved": round(achieved, 1), "unit": "GB/s", "frac": round(achieved / peak_gbs, 4),
+            "kernel": "vbq_gemv_kernel<1,16,2>", "launches": launches,
             "avg_launch_us": round(tot_ms * 1e3 / launches, 2),
             "alg_bytes_per_launch": round(tot_b / launches),
-            "note": "each projection of the 9B stack launched alone; algorithmic bytes = codes + 2.25 B/group + 2K + 4N"}
+            "note": "each projection of the 9B stack launched alone through vbq_gemv"}
 
 
 def dense_baseline(V, shape, stream, steps=3):
@@ -360,11 +461,19 @@ def peaks():
         return 6400.0, "fallback"
 
 
+def workload_text(shape):
+    size = {"vbq-9b": "9B", "vbq-1b": "1B"}.get(shape.name, shape.name)
+    att = (f"GQA {shape.n_heads}/{shape.n_kv_heads}x{shape.head_dim}" if shape.n_kv_heads != shape.n_heads
+           else f"MHA {shape.n_heads}x{shape.head_dim}")
+    return (f"{size}-shaped decode step, batch 1 ({shape.n_layers} layers, d={shape.d}, {att}, SwiGLU "
+            f"{shape.d_ff}, vocab {shape.vocab}), per-group {{1,2,4,8}}-bit weights, seed 0")
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
-    from synth import model_9b
-    shape = model_9b()
+    from synth import model_1b, model_9b
+    shape = model_9b() if args.workload == "9b" else model_1b()
     vals = []
     last = None
     for _ in range(args.warmup):
@@ -376,8 +485,7 @@ def run_reference(args, ws, rank):
     line = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "9B-shaped decode step, batch 1 (32 layers, d=4096, GQA 32/8x128, SwiGLU "
-                                   "14336, vocab 128256), per-group {1,2,4,8}-bit weights, seed 0"},
+            "config": {"workload": workload_text(shape)},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
                              "sample": last["sample"]},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -393,7 +501,7 @@ def run_vbq(args, ws, rank, local):
     stream = torch.cuda.Stream()
     peak, peak_kind = peaks()
 
-    shape = model_9b()
+    shape = model_9b() if args.workload == "9b" else model_1b()
     t0 = time.perf_counter()
     pm = PackedModel(V, shape, seed=0)
     pack_s = time.perf_counter() - t0
@@ -403,11 +511,12 @@ def run_vbq(args, ws, rank, local):
     def step():
         V.vbq_decode_step(pm.model.handle, x, logits, stream)
 
+    clocks = ClockSampler(local)
+    clocks.prepare()
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
             step()
         torch.cuda.synchronize()
-        clocks = ClockSampler(local)
         clocks.start()
         launches0 = V.vbq_launch_count()
         ms = time_steps(step, args.steps, 0, stream, ws)
@@ -429,15 +538,19 @@ def run_vbq(args, ws, rank, local):
     e2e_s = (time.perf_counter() - t1) / args.steps
     e2e_s = max_over_ranks(e2e_s, ws)
 
-    roof = dominant_kernel_roofline(V, pm, stream, peak)
+    roof = decode_kernel_roofline(V, pm, x, logits, stream, peak, args.steps)
     roof["peak_kind"] = peak_kind
-    extra = {"decode_step_us_9b": round(ms * 1e3, 1), "pack_seconds_9b": round(pack_s, 1),
-             "weights_9b": pm.weights, "alg_bytes_per_step_9b": round(pm.alg_bytes),
-             "device_bytes_9b": pm.total_bytes, "code_bytes_9b": pm.code_bytes}
+    standalone = standalone_gemv(V, pm, stream, peak)
+    w = "_" + args.workload
+    alg_step = pm.alg_bytes
+    extra = {"decode_step_us" + w: round(ms * 1e3, 1), "pack_seconds" + w: round(pack_s, 1),
+             "weights" + w: pm.weights, "alg_bytes_per_step" + w: round(pm.alg_bytes),
+             "device_bytes" + w: pm.total_bytes, "code_bytes" + w: pm.code_bytes,
+             "standalone_gemv" + w: standalone}
     pm.close()
     torch.cuda.empty_cache()
 
-    if not args.no_1b:
+    if not args.no_1b and args.workload == "9b":
         s1 = model_1b()
         pm1 = PackedModel(V, s1, seed=0)
         x1 = torch.from_numpy(gen_x(s1.d, seed=7).view(np.int16)).cuda()
@@ -454,8 +567,8 @@ def run_vbq(args, ws, rank, local):
         extra["batch_sweep_14336x4096"] = batch_sweep(V, stream)
         extra["stress_8192"] = stress_8192(V, stream)
     if not args.no_dense:
-        extra["dense_bf16_9b"] = dense_baseline(V, shape, stream)
-        extra["dense_bf16_9b"]["speedup_vbq"] = round(extra["dense_bf16_9b"]["us_per_step"] / (ms * 1e3), 2)
+        extra["dense_bf16" + w] = dense_baseline(V, shape, stream)
+        extra["dense_bf16" + w]["speedup_vbq"] = round(extra["dense_bf16" + w]["us_per_step"] / (ms * 1e3), 2)
 
     cpu = None
     if rank == 0:
@@ -466,24 +579,20 @@ def run_vbq(args, ws, rank, local):
                 "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32 accumulate (bf16 x, packed 1/2/4/8-bit codes, fp16 scales)", "data": "synthetic",
-                "config": {"workload": "9B-shaped decode step, batch 1 (32 layers, d=4096, GQA 32/8x128, "
-                                       "SwiGLU 14336, vocab 128256), per-group {1,2,4,8}-bit weights, seed 0",
-                           "l2": "inputs larger than L2: 1.9 GB of packed weights streamed per step",
+                "config": {"workload": workload_text(shape),
+                           "l2": f"inputs larger than L2: {pm.total_bytes / 1e9:.2f} GB of packed weights "
+                                 "streamed per step",
                            "parallelism": f"replicas x{ws}"},
                 "frac_of_peak": round(value / ws / peak, 4), "peak_gbs": peak,
                 "roofline": roof,
                 "cpu_baseline": cpu,
-                "e2e": {"value": round(ws * pm_bytes(extra) / e2e_s / 1e9, 1), "unit": "GB/s",
+                "e2e": {"value": round(ws * alg_step / e2e_s / 1e9, 1), "unit": "GB/s",
                         "h2d_bytes_per_step": 2 * shape.d, "d2h_bytes_per_step": 4 * shape.vocab,
                         "us_per_step": round(e2e_s * 1e6, 1)},
                 "gpu_launches": int(launches),
                 "clocks": clk,
                 **extra}
         print(json.dumps(line), flush=True)
-
-
-def pm_bytes(extra):
-    return extra["alg_bytes_per_step_9b"]
 
 
 def main():

@@ -93,8 +93,8 @@ VBQ_API const char* vbq_last_error(void);
 
 /*
  * vbq_pack: logical codes + per-group bit map + scales -> device layout.
- * Source: the VBQ abstract ("maps directly to packed low-bit storage"). The
- * layout is this library's own design.
+ * Source: the VBQ abstract (a fixed per-group allocation is stored as packed
+ * low-bit codes). The layout is this library's own design.
  *
  *  codes      host, uint8 [N][K] row-major; codes[r][k] < 2^bits[r][k/64]
  *  bits       host, uint8 [N][K/64]; each value in {1,2,4,8}
@@ -127,7 +127,7 @@ VBQ_API vbq_status vbq_dequant(const vbq_matrix* m, float* W_dev, void* stream);
 
 /*
  * vbq_gemv: y = W x for one bf16 activation vector, fp32 accumulation.
- * Source: the VBQ abstract ("custom fused dequantize-and-multiply kernels",
+ * Source: the VBQ abstract (dequantization fused with the multiply, for
  * batch-1 autoregressive decode).
  *  x_dev  device, bf16 [K] (uint16 bit patterns)
  *  y_dev  device, float [N]; every element is written (zeros when K == 0)
@@ -153,7 +153,9 @@ VBQ_API vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X_de
  *        down (in that order), then the LM head. The handles must stay alive
  *        while the model exists. The model does not own them.
  *  out   receives the model. It owns a device workspace for the activations
- *        and a CUDA graph built on the first step.
+ *        and one work plan per GEMV of the step, built here once.
+ * Limits: d, d_ff and n_heads*head_dim at most 16384 (the decode kernel keeps
+ * each projection's input in shared memory); VBQ_ERR_UNSUPPORTED otherwise.
  */
 VBQ_API vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_matrix* const* mats, vbq_model** out);
 
@@ -161,7 +163,7 @@ VBQ_API void vbq_model_free(vbq_model* model);
 
 /*
  * vbq_decode_step: one batch-1 decode step (position 0) through the stack.
- * Source: the VBQ abstract ("memory-bandwidth-bound autoregressive decode").
+ * Source: the VBQ abstract (decode whose speed is set by memory bandwidth).
  * The glue between projections is this library's reading, since the pages
  * give no architecture:
  *   h = x;  per layer:  u = bf16(rmsnorm(h)); q,k,v = Wq u, Wk u, Wv u;
@@ -170,6 +172,9 @@ VBQ_API void vbq_model_free(vbq_model* model);
  *                       h += Wdown bf16(silu(Wgate u) * Wup u)
  *   logits = Whead bf16(rmsnorm(h))
  * The residual h is fp32. Every projection accumulates in fp32.
+ * The step is one cooperative launch of a persistent kernel (one CTA per SM)
+ * with a grid barrier between dependent projections; its activations live in
+ * the model's workspace, so steps on the same model must not overlap.
  *  x_dev       device, bf16 [d]
  *  logits_dev  device, float [vocab]
  */
@@ -187,7 +192,7 @@ VBQ_API vbq_status vbq_decode_step_host(vbq_model* model, const uint16_t* x_host
  * projection p (layer-major, q..down per layer, then the head), the bf16
  * input it consumed and its fp32 output. vbq_model_trace_info gives the
  * offsets. The buffers live in the model, so nothing is recorded unless
- * enabled. Enabling rebuilds the step's graph.
+ * enabled. Enabling re-uploads the step's item list (it synchronizes the device).
  */
 VBQ_API vbq_status vbq_model_set_trace(vbq_model* model, int32_t enable);
 /* in_off/out_off: host int64 [n_layers*7+1]; element offsets into the buffers below. */
@@ -216,43 +221,40 @@ VBQ_API int64_t vbq_launch_count(int32_t reset);
 
 /*
  * vbq_decode_step_noalloc: the step of vbq_decode_step for callers that may not
- * allocate device memory while stepping. Examples are code running while
- * another component captures the stream into its own CUDA graph (cudaMalloc
- * is illegal during capture, and vbq_decode_step instantiates a graph of its
- * own), loops whose device memory is fixed before they start, and hosts that
- * hand out device memory only from their own pool. The pages have no
- * counterpart: this is an interface of this library.
+ * tie step memory to the model they step. Examples are code running while
+ * another component captures the stream into its own CUDA graph, loops whose
+ * device memory is fixed before they start, and hosts that hand out device
+ * memory only from their own pool. The pages have no counterpart: this is an
+ * interface of this library.
  *
- * It launches the same kernels in the same order as vbq_decode_step, directly
- * on `stream` (no graph, no trace), and gives the same logits. Its scratch
- * lives in one static device array of 262,144 floats (1 MiB) that every GPU
- * loading this library holds until the process exits. The array holds, in
- * 64-float blocks, a status word, the split-tile arrival counters, h [d],
- * [q;k;v], [gate;up], and the split-tile partial rows of the model's work
- * plans. The call allocates nothing: no cudaMalloc, no cudaFree, no graph.
+ * It launches the same kernel as vbq_decode_step, with the step's activations
+ * in one static device array instead of the model's workspace, and gives the
+ * same logits bit for bit. The array has 65,536 floats (256 KiB) on every GPU
+ * that loads this library and lives until the process exits. In 64-float
+ * blocks it holds the grid-barrier counters, h [d], [q;k;v] and [gate;up]. The
+ * call allocates nothing: no cudaMalloc, no cudaFree. Split-tile partial rows
+ * and their counters stay in the model's own work plans.
  *
  *  model       from vbq_model_create, on the current device
  *  x_dev       device, bf16 [d]
  *  logits_dev  device, float [vocab]
  *
- * Size limit: 64 + r(counters) + r(d) + r(n_heads*head_dim + 2*n_kv_heads*head_dim)
- * + r(2*d_ff) + r(partial rows) <= 262,144 floats, where r() rounds up to a
- * multiple of 64 and the counters and partial rows are the largest over the
- * model's launch plans. Larger models get VBQ_ERR_SHAPE, the detail text gives
- * the count, and nothing is enqueued.
- * Set-up: the first call on each device looks up the array's device address
- * with cudaGetSymbolAddress and sets the GEMV kernel attributes, with that
- * device current. Make that first call before any stream capture begins.
- * Sharing: every call on a device uses the same array, and the array keeps
- * the last call's contents. Each call's first kernel clears the status word
- * and the counters, and every other value is written before it is read. Calls that overlap on the GPU
- * (two streams, or two host threads) race on the array and give undefined
- * results; serialize them.
+ * Size limit: 64 + r(d) + r(n_heads*head_dim + 2*n_kv_heads*head_dim)
+ * + r(2*d_ff) <= 65,536 floats, where r() rounds up to a multiple of 64.
+ * Larger models get VBQ_ERR_SHAPE, the detail text gives the count, and
+ * nothing is enqueued.
+ * Set-up: vbq_model_create looks up the array's device address with
+ * cudaGetSymbolAddress on the model's device (once per device, with that
+ * device current) and clears it, so the calls themselves do neither.
+ * Sharing: every call on a device uses the same array. The counters must be
+ * zero when a step starts; every step leaves them at zero, and every other
+ * value is written before it is read. Calls that overlap on the GPU (two
+ * streams, or two host threads), with each other or with vbq_decode_step on
+ * the same model, race and give undefined results; serialize them.
  * Errors: VBQ_ERR_INVALID_ARG (NULL or misaligned pointers, model on another
- * device), VBQ_ERR_SHAPE (over the limit), VBQ_ERR_CUDA (a launch failed). A
- * kernel's bounded wait that runs out is recorded in the array's status word,
- * which each call clears first. This call does not read it back, because that
- * would need a synchronization.
+ * device), VBQ_ERR_SHAPE (over the limit), VBQ_ERR_CUDA (the launch failed). A
+ * bounded wait that runs out is recorded in the device check word; read it
+ * with vbq_device_check.
  */
 VBQ_API vbq_status vbq_decode_step_noalloc(vbq_model* model, const uint16_t* x_dev, float* logits_dev,
                                            void* stream);

@@ -442,7 +442,7 @@ static vbq_status tc_state(const vbq_matrix* m, TcState** out) {
   if (!s.ok) {
     Plan pl = make_plan({seg_tables(m)}, plan_ctas(static_cast<uint64_t>(m->data_bytes), gpu_info().sms),
                         MAX_UNITS_PER_CTA, true);
-    cudaError_t e = upload_plan(pl, TC_NMAX, nullptr, &s.plan);
+    cudaError_t e = upload_plan(pl, TC_NMAX, {m->data}, nullptr, &s.plan);
     if (e != cudaSuccess) return cuda_fail(e, "vbq_gemm_smallbatch: tensor-core plan");
     e = cudaMalloc(&s.sx, TC_NMAX * sizeof(float));
     if (e != cudaSuccess) {

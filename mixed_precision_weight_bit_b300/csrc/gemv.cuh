@@ -55,6 +55,7 @@ constexpr int XPF = 144;             // floats of activation prep per (warp, col
 constexpr int XP_X = 0, XP_8 = 64, XC_8 = 128;  // x (64), 2^15 x (64), 8-bit slice constants (8)
 constexpr int NLUT = 13;             // 5-bit lookup tables per group (the last covers 4 codes)
 constexpr int MAX_SEG = 3;
+constexpr int XCAP = 16384;          // largest K the decode kernel stages in shared memory
 
 enum XMode : int { X_BF16 = 0, X_RMSNORM = 1, X_GQA = 2, X_SWIGLU = 3 };
 enum EpMode : int { EP_STORE = 0, EP_RESID = 1 };
@@ -62,7 +63,8 @@ enum EpMode : int { EP_STORE = 0, EP_RESID = 1 };
 struct MatView {
   const uint8_t* data;
   const uint32_t* run_desc;
-  float* y;        // output rows of this matrix, column j at y + j*y_ld
+  float* y;        // output rows of this matrix, column j at y + j*y_ld (null: the launch's output)
+  int64_t y_off;   // when y is null: offset of the output in the launch's output buffer
   int32_t y_ld;
   float* trace_y;  // optional raw-output copy (decode-step trace)
 };
@@ -79,7 +81,7 @@ struct PlanView {
 struct XSource {
   int32_t mode;
   int32_t K;
-  const uint16_t* x;  // X_BF16: bf16 [NB][ldx]
+  const uint16_t* x;  // X_BF16: bf16 [NB][ldx] (null: the launch's x)
   int32_t ldx;
   const float* h;     // X_RMSNORM: fp32 residual [K]
   float eps;
@@ -90,13 +92,22 @@ struct XSource {
   uint16_t* trace_x;  // optional: CTA 0 writes the bf16 x it used ([K])
 };
 
-struct GemvArgs {
+// One GEMV over one or more matrices (a "launch item").
+struct Item {
   MatView seg[MAX_SEG];
   int32_t nseg;
   PlanView plan;
   XSource xs;
   int32_t ep;
   const float* resid;  // EP_RESID: y = resid + acc (may alias seg[0].y)
+};
+
+// A single-item launch: the item plus this plan's per-warp piece lists.
+struct GemvArgs {
+  Item it;
+  const uint64_t* pieces;
+  const uint32_t* pstart;  // [n_ctas * W + 1]
+  const uint32_t* pbytes;  // [n_ctas * W]
   int* err;
 };
 
@@ -111,6 +122,10 @@ struct GemvSmem {
   static constexpr int kBar = kAcc + 2 * kAccParity;
   static constexpr int kMisc = kBar + W * NSLOT * 8;
   static constexpr int kBytes = kMisc + 64 * 4;
+  // The decode kernel stages each item's x here (bf16, XCAP values); the
+  // single-GEMV kernel reads x from global memory and does not reserve it.
+  static constexpr int kX = kBytes;
+  static constexpr int kBytesStaged = kX + XCAP * 2;
   static_assert((kRingBytes & (kRingBytes - 1)) == 0, "ring must be a power of two");
   static_assert(kXp % 64 == 0 && (XPF * 4) % 64 == 0, "prep blocks must be 64-byte aligned");
 };
@@ -144,22 +159,23 @@ __device__ __forceinline__ XRaw x_load(const XSource& xs, int col, int k) {
       r.b = bf16_hi(v);
       break;
     }
+    // Activations written by another SM earlier in the same launch are read through L2 (ld.cg).
     case X_RMSNORM: {
-      const float2 h = *reinterpret_cast<const float2*>(xs.h + k);
+      const float2 h = __ldcg(reinterpret_cast<const float2*>(xs.h + k));
       r.a = h.x;
       r.b = h.y;
       break;
     }
     case X_GQA: {
       const int head = k / xs.head_dim, j = k - head * xs.head_dim;
-      const float2 v = *reinterpret_cast<const float2*>(xs.v + (head / xs.group) * xs.head_dim + j);
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(xs.v + (head / xs.group) * xs.head_dim + j));
       r.a = v.x;
       r.b = v.y;
       break;
     }
     default: {
-      const float2 g = *reinterpret_cast<const float2*>(xs.gate + k);
-      const float2 u = *reinterpret_cast<const float2*>(xs.up + k);
+      const float2 g = __ldcg(reinterpret_cast<const float2*>(xs.gate + k));
+      const float2 u = __ldcg(reinterpret_cast<const float2*>(xs.up + k));
       r.a = g.x;
       r.b = g.y;
       r.c = u.x;
@@ -281,220 +297,356 @@ __device__ __forceinline__ void do_step(uint32_t rb, uint32_t e, uint32_t xp, ui
   }
 }
 
-// Per-warp stream state: the ring, the chunks issued and landed.
-struct WarpStream {
-  uint32_t ring;      // shared offset of the ring
-  uint32_t bar;       // shared address of the first slot's mbarrier
-  uint32_t L;         // stream bytes
-  uint32_t nch;       // chunks
-  uint32_t issued, landed;
-  uint32_t avail;     // bytes known to have landed
-  uint32_t refill_at; // stream offset at which the next chunk may be issued
-  int pu;             // producer: unit being copied
-  uint32_t ppos;      // producer: bytes of it already copied
-  bool ok;
-};
-
-// ---- the kernel ---------------------------------------------------------
-
-template <int NB, int W, int NSLOT>
-__global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_constant__ GemvArgs a) {
-  using Lay = GemvSmem<NB, W, NSLOT>;
-  constexpr int SPW = SLICES / W;  // plan slices per warp
-  constexpr uint32_t RING = static_cast<uint32_t>(Lay::kRingBytes);
-  constexpr uint32_t RMASK = RING - 1u;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int umax = a.plan.umax;
-
-  // Lane i holds unit slot i of this CTA and this warp's slice of it.
-  uint32_t u_seg = 0, u_split = 0, u_nsplit = 0, u_pbase = 0, u_cnt = 0, u_r0 = 0, u_rows = 0;
-  uint32_t s_run0 = 0, s_k0 = 0, s_run1 = 0, s_k1 = 0, s_b0 = 0, s_b1 = 0, s_g0 = 0;
-  if (lane < umax) {
-    const size_t slot = static_cast<size_t>(blockIdx.x) * umax + lane;
-    const UnitRec ur = a.plan.units[slot];
-    u_seg = ur.seg;
-    u_split = ur.split;
-    u_nsplit = ur.nsplit;
-    u_pbase = ur.pbase;
-    u_cnt = ur.cnt;
-    u_r0 = ur.r0;
-    u_rows = ur.rows;
-    const SliceRec* sl = a.plan.slices + slot * SLICES + warp * SPW;
-    const SliceRec f = sl[0];
-    const SliceRec l = sl[SPW - 1];
-    s_run0 = f.run0;
-    s_k0 = f.k0;
-    s_b0 = f.b0;
-    s_g0 = f.g0;
-    s_run1 = l.run1;
-    s_k1 = l.k1;
-    s_b1 = l.b1;
-    if (SPW > 1 && f.b1 == f.b0) s_g0 = l.g0;  // the first slice is empty
-  }
-  const int nu = __popc(__ballot_sync(0xffffffffu, u_nsplit > 0u));
-  uint32_t len16 = lane < nu ? s_b1 - s_b0 : 0u;
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) len16 += __shfl_xor_sync(0xffffffffu, len16, d);
-
-  WarpStream S;
-  S.ring = Lay::kRing + warp * Lay::kRingStride;
-  S.bar = smem_u32(vbq_smem + Lay::kBar) + warp * NSLOT * 8;
-  S.L = len16 * 16u;
-  S.nch = (S.L + CH - 1) >> LOG_CH;
-  S.issued = S.landed = S.avail = 0;
-  S.pu = 0;
-  S.ppos = 0;
-  S.ok = true;
-  const uint32_t ring_a = smem_u32(vbq_smem) + S.ring;
-  const uint64_t pol = l2_evict_first_policy();
-
-  auto issue_next = [&]() {  // warp-uniform; lane 0 issues the copies
-    const uint32_t slot = S.issued & (NSLOT - 1);
-    const uint32_t bytes = min(static_cast<uint32_t>(CH), S.L - S.issued * CH);
-    const uint32_t spill = (slot == 0 && S.issued > 0) ? min(static_cast<uint32_t>(SPILL), bytes) : 0u;
-    const uint32_t bar = S.bar + 8 * slot;
-    if (lane == 0) mbar_arrive_expect_tx(bar, bytes + spill);
-    uint32_t done = 0;
-    while (done < bytes && S.pu < nu) {
-      const uint32_t ub0 = __shfl_sync(0xffffffffu, s_b0, S.pu);
-      const uint32_t ub1 = __shfl_sync(0xffffffffu, s_b1, S.pu);
-      const uint32_t useg = __shfl_sync(0xffffffffu, u_seg, S.pu);
-      const uint32_t ulen = (ub1 - ub0) * 16u;
-      const uint32_t take = min(ulen - S.ppos, bytes - done);
-      if (take > 0 && lane == 0) {
-        const uint8_t* src = a.seg[useg].data + static_cast<uint64_t>(ub0) * 16u + S.ppos;
-        bulk_g2s(ring_a + slot * CH + done, src, take, bar, pol);
-        if (done < spill) bulk_g2s(ring_a + RING + done, src, min(take, spill - done), bar, pol);
-      }
-      done += take;
-      S.ppos += take;
-      if (S.ppos == ulen) {
-        ++S.pu;
-        S.ppos = 0;
-      }
-    }
-    ++S.issued;
-    S.refill_at = S.issued < S.nch ? (S.issued + 1 - NSLOT) * CH : 0xFFFFFFFFu;
+// Stages the x of a decode item in shared memory at sx as the bf16 values the
+// projection consumes, for K <= XCAP (K a multiple of 64). All threads of the
+// CTA call it; it ends with a CTA barrier. Every CTA computes the same values
+// in the same order. Returns the RMSNorm scale (1 for other modes).
+template <int W>
+__device__ __forceinline__ float stage_x(const XSource& xs, uint32_t sx, float* misc, int lane, int warp) {
+  constexpr int NT = W * 32;
+  const int K = xs.K;
+  const int t = threadIdx.x;
+  auto put8 = [&](int k, const float (&v)[8]) {
+    uint4 q;
+    q.x = bf16_bits(v[0]) | (static_cast<uint32_t>(bf16_bits(v[1])) << 16);
+    q.y = bf16_bits(v[2]) | (static_cast<uint32_t>(bf16_bits(v[3])) << 16);
+    q.z = bf16_bits(v[4]) | (static_cast<uint32_t>(bf16_bits(v[5])) << 16);
+    q.w = bf16_bits(v[6]) | (static_cast<uint32_t>(bf16_bits(v[7])) << 16);
+    sts(sx + 2 * k, q);
   };
-
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < NSLOT; ++i) mbar_init(S.bar + 8 * i, 1);
-    fence_mbarrier_init();
-  }
-  __syncwarp();
-  S.refill_at = 0xFFFFFFFFu;
-  while (S.issued < S.nch && S.issued < static_cast<uint32_t>(NSLOT)) issue_next();
-
-  const uint32_t xp = Lay::kXp + warp * NB * XPF * 4;
-  float sgn[5];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) sgn[i] = ((lane >> i) & 1) ? 0.5f : -0.5f;
-  const float pw2 = (lane & 1) ? 2.0f : 1.0f;
-  const float pw4 = static_cast<float>(1 << (lane & 3));
-  float lut[NB][NLUT];
-#pragma unroll
-  for (int c = 0; c < NB; ++c)
-#pragma unroll
-    for (int k = 0; k < NLUT; ++k) lut[c][k] = 0.0f;
-  // This warp's accumulator for unit parity p: acc_base + p * kAccParity.
-  const uint32_t acc_base = Lay::kAcc + warp * NB * TILE_MAX * 4;
-  float* misc = reinterpret_cast<float*>(vbq_smem + Lay::kMisc);
-  // misc words 32..35: arrivals[2], reductions done[2], as uint32.
-  uint32_t* ucount = reinterpret_cast<uint32_t*>(misc) + 32;
-  if (threadIdx.x < 4) ucount[threadIdx.x] = 0u;
-
-  __syncthreads();  // the unit counters are initialized
-
-  // The next kernel may start streaming its own weights now.
-  grid_dep_launch();
-  grid_dep_wait();
-
-  // Start loading x for the first group column before the RMSNorm reduction.
-  int pre_g = nu > 0 ? static_cast<int>(__shfl_sync(0xffffffffu, s_g0, 0)) : -1;
-  XRaw pre[NB];
-  if (pre_g >= 0) {
-#pragma unroll
-    for (int c = 0; c < NB; ++c) pre[c] = x_load(a.xs, c, pre_g * GROUP + 2 * lane);
-  }
-
-  // RMSNorm scale, when the input is rmsnorm(h): every CTA reduces h in the same order.
+  auto ld8 = [&](const float* p, float (&v)[8]) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  };
   float inv_rms = 1.0f;
-  if (a.xs.mode == X_RMSNORM) {
+  if (xs.mode == X_RMSNORM) {
+    // Pass 1: sum of squares; the first chunk of each thread stays in registers.
+    float h0[8];
     float ss = 0.0f;
-    for (int k = threadIdx.x; k < a.xs.K; k += W * 32) {
-      const float v = a.xs.h[k];
-      ss = fmaf(v, v, ss);
+    const int k0 = 8 * t;
+    if (k0 < K) {
+      ld8(xs.h + k0, h0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(h0[i], h0[i], ss);
+    }
+    for (int k = k0 + 8 * NT; k < K; k += 8 * NT) {
+      float v[8];
+      ld8(xs.h + k, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
     }
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
     if (lane == 0) misc[warp] = ss;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (t == 0) {
       float tot = 0.0f;
       for (int w = 0; w < W; ++w) tot += misc[w];
-      misc[W] = 1.0f / sqrtf(tot / static_cast<float>(a.xs.K) + a.xs.eps);
+      misc[W] = 1.0f / sqrtf(tot / static_cast<float>(K) + xs.eps);
     }
     __syncthreads();
     inv_rms = misc[W];
+    // Pass 2: bf16(h * inv_rms).
+    if (k0 < K) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h0[i] *= inv_rms;
+      put8(k0, h0);
+    }
+    for (int k = k0 + 8 * NT; k < K; k += 8 * NT) {
+      float v[8];
+      ld8(xs.h + k, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] *= inv_rms;
+      put8(k, v);
+    }
+  } else if (xs.mode == X_SWIGLU) {
+    // bf16(silu(gate) * up); two chunks of loads in flight per thread.
+    for (int k = 8 * t; k < K; k += 16 * NT) {
+      const int k2 = k + 8 * NT;
+      float g0[8], u0[8], g1[8], u1[8];
+      ld8(xs.gate + k, g0);
+      ld8(xs.up + k, u0);
+      if (k2 < K) {
+        ld8(xs.gate + k2, g1);
+        ld8(xs.up + k2, u1);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g0[i] = silu_f(g0[i]) * u0[i];
+      put8(k, g0);
+      if (k2 < K) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g1[i] = silu_f(g1[i]) * u1[i];
+        put8(k2, g1);
+      }
+    }
+  } else if (xs.mode == X_GQA) {
+    // bf16(v of the head's kv group), two values at a time (head_dim is even).
+#pragma unroll 4
+    for (int k = 2 * t; k < K; k += 2 * NT) {
+      const int head = k / xs.head_dim, j = k - head * xs.head_dim;
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(xs.v + (head / xs.group) * xs.head_dim + j));
+      sts(sx + 2 * k, static_cast<uint32_t>(bf16_bits(v.x)) | (static_cast<uint32_t>(bf16_bits(v.y)) << 16));
+    }
+  } else {  // X_BF16
+#pragma unroll 4
+    for (int k = 2 * t; k < K; k += 2 * NT) sts(sx + 2 * k, ldg_nc_u32(xs.x + k));
   }
-  if (a.xs.trace_x && blockIdx.x == 0) {
-    for (int k = 2 * threadIdx.x; k < a.xs.K; k += 2 * W * 32) {
-      const float2 v = x_make(a.xs, x_load(a.xs, 0, k), inv_rms);
-      a.xs.trace_x[k] = bf16_bits(v.x);
-      a.xs.trace_x[k + 1] = bf16_bits(v.y);
+  __syncthreads();
+  if (xs.trace_x && blockIdx.x == 0) {
+    for (int k = 2 * t; k < K; k += 2 * NT)
+      *reinterpret_cast<uint32_t*>(xs.trace_x + k) = lds<uint32_t>(sx + 2 * k);
+  }
+  return inv_rms;
+}
+
+// Per-warp stream of packed bytes: the ring, the chunks issued and landed, and
+// the producer's place in the warp's piece list. Lane 0 issues the copies; the
+// bookkeeping is warp-uniform.
+template <int NSLOT>
+struct WarpStream {
+  uint32_t ring;       // shared offset of the ring
+  uint32_t ring_a;     // shared address of the ring
+  uint32_t bar;        // shared address of the first slot's mbarrier
+  uint32_t L;          // stream bytes
+  uint32_t nch;        // chunks
+  uint32_t issued, landed;
+  uint32_t avail;      // bytes known to have landed
+  uint32_t refill_at;  // stream offset at which the next chunk may be issued
+  const uint64_t* pieces;  // this warp's piece list
+  uint32_t npieces;
+  uint32_t pi;         // producer: piece being copied
+  uint32_t ppos;       // producer: bytes of it already copied
+  uint64_t pcur, pnext;  // lane i: piece (base + i) and (base + 32 + i) of the list
+  uint32_t pbase;      // index of the first piece held in pcur
+  uint64_t pol;
+  bool ok;
+
+  __device__ __forceinline__ void init(uint32_t ring_off, uint32_t bar_addr, const uint64_t* list, uint32_t n,
+                                       uint32_t bytes, int lane) {
+    ring = ring_off;
+    ring_a = smem_u32(vbq_smem) + ring_off;
+    bar = bar_addr;
+    L = bytes;
+    nch = (bytes + CH - 1) >> LOG_CH;
+    issued = landed = avail = 0;
+    refill_at = 0xFFFFFFFFu;
+    pieces = list;
+    npieces = n;
+    pi = ppos = 0;
+    pbase = 0;
+    pcur = lane < static_cast<int>(n) ? __ldg(list + lane) : 0ull;
+    pnext = lane + 32 < static_cast<int>(n) ? __ldg(list + 32 + lane) : 0ull;
+    pol = l2_evict_first_policy();
+    ok = true;
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < NSLOT; ++i) mbar_init(bar + 8 * i, 1);
+      fence_mbarrier_init();
+    }
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void issue_next(int lane) {
+    constexpr uint32_t RING = NSLOT * CH;
+    const uint32_t slot = issued & (NSLOT - 1);
+    const uint32_t bytes = min(static_cast<uint32_t>(CH), L - issued * CH);
+    const uint32_t spill = (slot == 0 && issued > 0) ? min(static_cast<uint32_t>(SPILL), bytes) : 0u;
+    const uint32_t b = bar + 8 * slot;
+    if (lane == 0) mbar_arrive_expect_tx(b, bytes + spill);
+    uint32_t done = 0;
+    while (done < bytes && pi < npieces) {
+      if (pi - pbase >= 32u) {  // next batch of 32 pieces
+        pbase += 32;
+        pcur = pnext;
+        pnext = pbase + 32 + lane < npieces ? __ldg(pieces + pbase + 32 + lane) : 0ull;
+      }
+      const uint64_t pc = __shfl_sync(0xffffffffu, pcur, static_cast<int>(pi - pbase));
+      const uint32_t plen = static_cast<uint32_t>(pc & 0xFFFFFu) << 4;
+      const uint32_t take = min(plen - ppos, bytes - done);
+      if (lane == 0) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>((pc >> 20) << 4) + ppos;
+        bulk_g2s(ring_a + slot * CH + done, src, take, b, pol);
+        if (done < spill) bulk_g2s(ring_a + RING + done, src, min(take, spill - done), b, pol);
+      }
+      done += take;
+      ppos += take;
+      if (ppos == plen) {
+        ++pi;
+        ppos = 0;
+      }
+    }
+    ++issued;
+    refill_at = issued < nch ? (issued + 1 - NSLOT) * CH : 0xFFFFFFFFu;
+  }
+
+  __device__ __forceinline__ void start(int lane) {
+    while (issued < nch && issued < static_cast<uint32_t>(NSLOT)) issue_next(lane);
+  }
+
+  // Waits until the bytes below `upto` have landed; sets ok = false on a timeout.
+  __device__ __forceinline__ void wait_for(uint32_t upto) {
+    while (avail < upto) {
+      const bool done = mbar_wait(bar + 8 * (landed & (NSLOT - 1)), (landed / NSLOT) & 1u);
+      if (!__all_sync(0xffffffffu, done)) {
+        ok = false;
+        return;
+      }
+      ++landed;
+      avail = min(landed * CH, L);
     }
   }
 
-  uint32_t o = 0;  // stream offset of the next record
-  uint32_t acc = acc_base;
+  // Issues the chunks whose slots the bytes below `o` have freed.
+  __device__ __forceinline__ void refill(uint32_t o, int lane) {
+    if (o >= refill_at) {
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_smem();
+      while (o >= refill_at) issue_next(lane);
+    }
+  }
+
+  // After an error: waits (bounded) for the copies still in flight.
+  __device__ __forceinline__ void drain() {
+    for (uint32_t c = landed; c < issued; ++c)
+      if (!__all_sync(0xffffffffu, mbar_wait(bar + 8 * (c & (NSLOT - 1)), (c / NSLOT) & 1u))) break;
+  }
+};
+
+// Per-warp consumer state that lives across the items of a launch.
+template <int NB>
+struct Worker {
+  uint32_t xp;        // shared offset of this warp's prep block
+  uint32_t acc_base;  // shared offset of this warp's accumulators (parity 0)
+  float sgn[5];
+  float pw2, pw4;
+  float lut[NB][NLUT];
+  uint32_t o;         // stream offset of the next record
+  uint32_t gunit;     // units this CTA has processed, over all items (accumulator parity)
+};
+
+// Unit and slice records of one item for this CTA: lane i holds slot i.
+struct UnitRegs {
+  uint32_t seg, split, nsplit, pbase, cnt, r0, rows;
+  uint32_t run0, k0, run1, k1, g0;
+};
+
+template <int W>
+__device__ __forceinline__ UnitRegs load_units(const PlanView& P, int warp, int lane) {
+  constexpr int SPW = SLICES / W;
+  UnitRegs u{};
+  if (lane < P.umax) {
+    const size_t slot = static_cast<size_t>(blockIdx.x) * P.umax + lane;
+    const UnitRec ur = P.units[slot];
+    u.seg = ur.seg;
+    u.split = ur.split;
+    u.nsplit = ur.nsplit;
+    u.pbase = ur.pbase;
+    u.cnt = ur.cnt;
+    u.r0 = ur.r0;
+    u.rows = ur.rows;
+    const SliceRec* sl = P.slices + slot * SLICES + warp * SPW;
+    const SliceRec f = sl[0];
+    const SliceRec l = sl[SPW - 1];
+    u.run0 = f.run0;
+    u.k0 = f.k0;
+    u.g0 = (SPW > 1 && f.b1 == f.b0) ? l.g0 : f.g0;
+    u.run1 = l.run1;
+    u.k1 = l.k1;
+  }
+  return u;
+}
+
+// Runs one item for this CTA. All threads of the CTA call it. out/xarg are the
+// launch's output and x buffers for matrices and sources that name them.
+template <int NB, int W, int NSLOT, bool STAGED>
+__device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, WarpStream<NSLOT>& S, Worker<NB>& K,
+                                         float* out, const uint16_t* xarg, int lane, int warp) {
+  static_assert(!STAGED || NB == 1, "staged x is for one column");
+  using Lay = GemvSmem<NB, W, NSLOT>;
+  constexpr uint32_t RMASK = NSLOT * CH - 1u;
+  float* misc = reinterpret_cast<float*>(vbq_smem + Lay::kMisc);
+  uint32_t* ucount = reinterpret_cast<uint32_t*>(misc) + 32;
+  XSource xs = it.xs;
+  if (xs.mode == X_BF16 && xs.x == nullptr) xs.x = xarg;
+  const int nu = __popc(__ballot_sync(0xffffffffu, ur.nsplit > 0u));
+
+  // Start loading x for the first group column before the RMSNorm reduction.
+  int pre_g = -1;
+  XRaw pre[NB];
+  float inv_rms = 1.0f;
+  if constexpr (STAGED) {
+    stage_x<W>(xs, Lay::kX, misc, lane, warp);
+  } else {
+    pre_g = nu > 0 ? static_cast<int>(__shfl_sync(0xffffffffu, ur.g0, 0)) : -1;
+    if (pre_g >= 0) {
+#pragma unroll
+      for (int c = 0; c < NB; ++c) pre[c] = x_load(xs, c, pre_g * GROUP + 2 * lane);
+    }
+    // RMSNorm scale, when the input is rmsnorm(h): every CTA reduces h in the same order.
+    if (xs.mode == X_RMSNORM) {
+      float ss = 0.0f;
+      for (int k = threadIdx.x; k < xs.K; k += W * 32) {
+        const float v = __ldcg(xs.h + k);
+        ss = fmaf(v, v, ss);
+      }
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+      if (lane == 0) misc[warp] = ss;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float tot = 0.0f;
+        for (int w = 0; w < W; ++w) tot += misc[w];
+        misc[W] = 1.0f / sqrtf(tot / static_cast<float>(xs.K) + xs.eps);
+      }
+      __syncthreads();
+      inv_rms = misc[W];
+    }
+    if (xs.trace_x && blockIdx.x == 0) {
+      for (int k = 2 * threadIdx.x; k < xs.K; k += 2 * W * 32) {
+        const float2 v = x_make(xs, x_load(xs, 0, k), inv_rms);
+        xs.trace_x[k] = bf16_bits(v.x);
+        xs.trace_x[k + 1] = bf16_bits(v.y);
+      }
+    }
+  }
+
   int cur_g = -1;
   int cur_seg = -1;
+  uint32_t acc = K.acc_base;
 
   // Makes group column g's prep current, and prefetches the inputs of g + 1.
   auto prep_for = [&](int g) {
+    if constexpr (STAGED) {
+      const uint32_t v = lds<uint32_t>(Lay::kX + (g * GROUP + 2 * lane) * 2);
+      __syncwarp();
+      build_prep(K.xp, bf16_lo(v), bf16_hi(v), lane, K.sgn, K.lut[0]);
+      __syncwarp();
+      cur_g = g;
+      return;
+    }
     XRaw r[NB];
     if (g == pre_g) {
 #pragma unroll
       for (int c = 0; c < NB; ++c) r[c] = pre[c];
     } else {
 #pragma unroll
-      for (int c = 0; c < NB; ++c) r[c] = x_load(a.xs, c, g * GROUP + 2 * lane);
+      for (int c = 0; c < NB; ++c) r[c] = x_load(xs, c, g * GROUP + 2 * lane);
     }
-    pre_g = (g + 1) * GROUP < a.xs.K ? g + 1 : -1;
+    pre_g = (g + 1) * GROUP < xs.K ? g + 1 : -1;
     if (pre_g >= 0) {
 #pragma unroll
-      for (int c = 0; c < NB; ++c) pre[c] = x_load(a.xs, c, pre_g * GROUP + 2 * lane);
+      for (int c = 0; c < NB; ++c) pre[c] = x_load(xs, c, pre_g * GROUP + 2 * lane);
     }
     __syncwarp();
 #pragma unroll
     for (int c = 0; c < NB; ++c) {
-      const float2 xv = x_make(a.xs, r[c], inv_rms);
-      build_prep(xp + c * XPF * 4, xv.x, xv.y, lane, sgn, lut[c]);
+      const float2 xv = x_make(xs, r[c], inv_rms);
+      build_prep(K.xp + c * XPF * 4, xv.x, xv.y, lane, K.sgn, K.lut[c]);
     }
     __syncwarp();
     cur_g = g;
-  };
-
-  // Waits until the bytes below `upto` have landed; false on a timeout.
-  auto wait_for = [&](uint32_t upto) {
-    while (S.avail < upto) {
-      const bool done = mbar_wait(S.bar + 8 * (S.landed & (NSLOT - 1)), (S.landed / NSLOT) & 1u);
-      if (!__all_sync(0xffffffffu, done)) {
-        S.ok = false;
-        return;
-      }
-      ++S.landed;
-      S.avail = min(S.landed * CH, S.L);
-    }
-  };
-
-  auto refill = [&]() {
-    if (o >= S.refill_at) {
-      __syncwarp();
-      if (lane == 0) fence_proxy_async_smem();
-      while (o >= S.refill_at) issue_next();
-    }
   };
 
   // Steps [k, kend) of a run of class CLS with n entries.
@@ -502,54 +654,55 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
     constexpr int CLS = decltype(cls_tag)::value;
     constexpr uint32_t EPS = entries_per_step(CLS);
     constexpr uint32_t FULL = full_step_bytes(CLS);
-    const float pw = CLS == 1 ? pw2 : pw4;
+    const float pw = CLS == 1 ? K.pw2 : K.pw4;
     const uint32_t kfull = min(kend, n / EPS);
     for (; k < kfull; ++k) {
-      const uint32_t o1 = o + FULL;
+      const uint32_t o1 = K.o + FULL;
       if (S.avail < o1) {
-        wait_for(o1);
+        S.wait_for(o1);
         if (!S.ok) return;
       }
-      do_step<NB, CLS>(S.ring + (o & RMASK), EPS, xp, acc, lane, lut, pw);
-      o = o1;
-      refill();
+      do_step<NB, CLS>(S.ring + (K.o & RMASK), EPS, K.xp, acc, lane, K.lut, pw);
+      K.o = o1;
+      S.refill(K.o, lane);
     }
     if (k < kend) {  // the run's last, partial step
       const uint32_t e = n - k * EPS;
-      const uint32_t o1 = o + rec_bytes(CLS, e);
+      const uint32_t o1 = K.o + rec_bytes(CLS, e);
       if (S.avail < o1) {
-        wait_for(o1);
+        S.wait_for(o1);
         if (!S.ok) return;
       }
-      do_step<NB, CLS>(S.ring + (o & RMASK), e, xp, acc, lane, lut, pw);
-      o = o1;
-      refill();
+      do_step<NB, CLS>(S.ring + (K.o & RMASK), e, K.xp, acc, lane, K.lut, pw);
+      K.o = o1;
+      S.refill(K.o, lane);
     }
   };
 
-  for (int ui = 0; ui < nu; ++ui) {
-    const uint32_t par = static_cast<uint32_t>(ui) & 1u;
-    acc = acc_base + par * Lay::kAccParity;
-    if (ui >= 2) {  // the reduction of unit ui - 2 must have read this buffer (bounded wait)
-      const uint32_t need = static_cast<uint32_t>(ui) >> 1;
+  for (int ui = 0; ui < nu; ++ui, ++K.gunit) {
+    const uint32_t par = K.gunit & 1u;
+    acc = K.acc_base + par * Lay::kAccParity;
+    if (K.gunit >= 2) {  // the reduction of unit gunit - 2 must have read this buffer (bounded wait)
+      const uint32_t need = K.gunit >> 1;
       const long long t0 = clock64();
+      bool timed_out = false;
       while (*reinterpret_cast<volatile uint32_t*>(ucount + 2 + par) < need) {
-        if (clock64() - t0 > 8000000000LL) {
-          S.ok = false;
+        if (clock64() - t0 > kSpinCycles) {
+          timed_out = true;
           break;
         }
       }
-      S.ok = __all_sync(0xffffffffu, S.ok);
+      if (__any_sync(0xffffffffu, timed_out)) S.ok = false;
     }
     for (int i = lane; i < NB * TILE_MAX; i += 32) sts(acc + i * 4, 0.0f);
     __syncwarp();
-    const uint32_t seg = __shfl_sync(0xffffffffu, u_seg, ui);
-    const uint32_t run1 = __shfl_sync(0xffffffffu, s_run1, ui);
-    const uint32_t k1 = __shfl_sync(0xffffffffu, s_k1, ui);
-    uint32_t run = __shfl_sync(0xffffffffu, s_run0, ui);
-    uint32_t k = __shfl_sync(0xffffffffu, s_k0, ui);
+    const uint32_t seg = __shfl_sync(0xffffffffu, ur.seg, ui);
+    const uint32_t run1 = __shfl_sync(0xffffffffu, ur.run1, ui);
+    const uint32_t k1 = __shfl_sync(0xffffffffu, ur.k1, ui);
+    uint32_t run = __shfl_sync(0xffffffffu, ur.run0, ui);
+    uint32_t k = __shfl_sync(0xffffffffu, ur.k0, ui);
     const uint32_t run_end = run1 + (k1 > 0u ? 1u : 0u);
-    const uint32_t* rdesc = a.seg[seg].run_desc;
+    const uint32_t* rdesc = it.seg[seg].run_desc;
     if (static_cast<int>(seg) != cur_seg) {
       cur_seg = static_cast<int>(seg);
       cur_g = -1;
@@ -578,6 +731,9 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
     }
 
     // ---- unit epilogue: the last warp to finish sums the warps in fixed order ----
+    // Every global load of the epilogue is issued before the values are used:
+    // it runs while the other SMs stream at full rate, when an L2 round trip
+    // takes about a microsecond.
     __syncwarp();
     __threadfence_block();
     uint32_t arrived = 0;
@@ -585,52 +741,94 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
     arrived = __shfl_sync(0xffffffffu, arrived, 0);
     if (arrived % W == W - 1) {
       __threadfence_block();
-      const uint32_t split = __shfl_sync(0xffffffffu, u_split, ui);
-      const uint32_t nsplit = __shfl_sync(0xffffffffu, u_nsplit, ui);
-      const uint32_t r0 = __shfl_sync(0xffffffffu, u_r0, ui);
-      const uint32_t rows = __shfl_sync(0xffffffffu, u_rows, ui);
-      const MatView& M = a.seg[seg];
+      constexpr int RPL = TILE_MAX / 32;  // rows per lane: lane + 32 j
+      const uint32_t split = __shfl_sync(0xffffffffu, ur.split, ui);
+      const uint32_t nsplit = __shfl_sync(0xffffffffu, ur.nsplit, ui);
+      const uint32_t r0 = __shfl_sync(0xffffffffu, ur.r0, ui);
+      const uint32_t rows = __shfl_sync(0xffffffffu, ur.rows, ui);
+      const MatView& M = it.seg[seg];
       const uint32_t accp = Lay::kAcc + par * Lay::kAccParity;
-      auto store = [&](int c, uint32_t row, float v) {
-        if (c == 0 && M.trace_y) M.trace_y[row] = v;
-        if (a.ep == EP_RESID) v += a.resid[row];
-        M.y[static_cast<int64_t>(c) * M.y_ld + row] = v;
-      };
-      auto warp_sum = [&](int c, uint32_t r) {
-        float v = 0.0f;
+      float v[NB][RPL];
 #pragma unroll
-        for (int w = 0; w < W; ++w) v += lds<float>(accp + ((w * NB + c) * TILE_MAX + r) * 4);
-        return v;
-      };
-      if (nsplit <= 1u) {
-        for (uint32_t r = lane; r < rows; r += 32) {
+      for (int j = 0; j < RPL; ++j) {
+        const uint32_t r = lane + 32u * j;
 #pragma unroll
-          for (int c = 0; c < NB; ++c) store(c, r0 + r, warp_sum(c, r));
+        for (int c = 0; c < NB; ++c) {
+          float t = 0.0f;
+          if (r < rows) {
+#pragma unroll
+            for (int w = 0; w < W; ++w) t += lds<float>(accp + ((w * NB + c) * TILE_MAX + r) * 4);
+          }
+          v[c][j] = t;
         }
-      } else {
-        const uint32_t pbase = __shfl_sync(0xffffffffu, u_pbase, ui);
-        const uint32_t cnt = __shfl_sync(0xffffffffu, u_cnt, ui);
-        float* part = a.plan.partial + static_cast<size_t>(pbase) * NB;
-        for (uint32_t r = lane; r < rows; r += 32) {
+      }
+      bool mine = true;  // this warp writes the rows
+      if (nsplit > 1u) {
+        const uint32_t pb = __shfl_sync(0xffffffffu, ur.pbase, ui);
+        const uint32_t cnt = __shfl_sync(0xffffffffu, ur.cnt, ui);
+        float* part = it.plan.partial + static_cast<size_t>(pb) * NB;
 #pragma unroll
-          for (int c = 0; c < NB; ++c) part[(split * NB + c) * rows + r] = warp_sum(c, r);
+        for (int j = 0; j < RPL; ++j) {
+          const uint32_t r = lane + 32u * j;
+#pragma unroll
+          for (int c = 0; c < NB; ++c)
+            if (r < rows) part[(split * NB + c) * rows + r] = v[c][j];
         }
         __threadfence();
         __syncwarp();
         uint32_t prev = 0;
-        if (lane == 0) prev = atomicAdd(a.plan.counters + cnt, 1u);
+        if (lane == 0) prev = atomicAdd(it.plan.counters + cnt, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == nsplit - 1u) {
+        mine = prev == nsplit - 1u;
+        if (mine) {  // the last split to arrive adds all of them, in split order
           __threadfence();
-          for (uint32_t r = lane; r < rows; r += 32) {
+          constexpr int SB = NB == 1 ? 4 : 1;  // splits whose loads are in flight together
+#pragma unroll
+          for (int j = 0; j < RPL; ++j)
+#pragma unroll
+            for (int c = 0; c < NB; ++c) v[c][j] = 0.0f;
+          for (uint32_t s0 = 0; s0 < nsplit; s0 += SB) {
+            float a[SB][NB][RPL];
+#pragma unroll
+            for (int q = 0; q < SB; ++q)
+#pragma unroll
+              for (int j = 0; j < RPL; ++j) {
+                const uint32_t r = lane + 32u * j;
+#pragma unroll
+                for (int c = 0; c < NB; ++c)
+                  a[q][c][j] = (s0 + q < nsplit && r < rows) ? __ldcg(part + ((s0 + q) * NB + c) * rows + r) : 0.0f;
+              }
+#pragma unroll
+            for (int q = 0; q < SB; ++q)
+#pragma unroll
+              for (int j = 0; j < RPL; ++j)
+#pragma unroll
+                for (int c = 0; c < NB; ++c)
+                  if (s0 + q < nsplit) v[c][j] += a[q][c][j];
+          }
+          if (lane == 0) it.plan.counters[cnt] = 0u;
+        }
+      }
+      if (mine) {
+        float* const ybase = M.y ? M.y : out + M.y_off;
+        float rv[RPL];
+#pragma unroll
+        for (int j = 0; j < RPL; ++j) {
+          const uint32_t r = lane + 32u * j;
+          rv[j] = (it.ep == EP_RESID && r < rows) ? __ldcg(it.resid + r0 + r) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < RPL; ++j) {
+          const uint32_t r = lane + 32u * j;
+          if (r < rows) {
 #pragma unroll
             for (int c = 0; c < NB; ++c) {
-              float v = 0.0f;
-              for (uint32_t s = 0; s < nsplit; ++s) v += __ldcg(part + (s * NB + c) * rows + r);
-              store(c, r0 + r, v);
+              float t = v[c][j];
+              if (c == 0 && M.trace_y) M.trace_y[r0 + r] = t;
+              if (it.ep == EP_RESID) t += rv[j];
+              ybase[static_cast<int64_t>(c) * M.y_ld + r0 + r] = t;
             }
           }
-          if (lane == 0) a.plan.counters[cnt] = 0u;
         }
       }
       __syncwarp();
@@ -638,12 +836,139 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_consta
       if (lane == 0) atomicAdd(ucount + 2 + par, 1u);
     }
   }
+}
 
+// Sets up this warp's stream and consumer state.
+template <int NB, int W, int NSLOT>
+__device__ __forceinline__ void worker_init(WarpStream<NSLOT>& S, Worker<NB>& K, const uint64_t* pieces,
+                                            const uint32_t* pstart, const uint32_t* pbytes, int lane, int warp) {
+  using Lay = GemvSmem<NB, W, NSLOT>;
+  const size_t wi = static_cast<size_t>(blockIdx.x) * W + warp;
+  const uint32_t p0 = pstart[wi], p1 = pstart[wi + 1];
+  S.init(Lay::kRing + warp * Lay::kRingStride, smem_u32(vbq_smem + Lay::kBar) + warp * NSLOT * 8, pieces + p0,
+         p1 - p0, pbytes[wi], lane);
+  S.start(lane);
+  K.xp = Lay::kXp + warp * NB * XPF * 4;
+  K.acc_base = Lay::kAcc + warp * NB * TILE_MAX * 4;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) K.sgn[i] = ((lane >> i) & 1) ? 0.5f : -0.5f;
+  K.pw2 = (lane & 1) ? 2.0f : 1.0f;
+  K.pw4 = static_cast<float>(1 << (lane & 3));
+#pragma unroll
+  for (int c = 0; c < NB; ++c)
+#pragma unroll
+    for (int k = 0; k < NLUT; ++k) K.lut[c][k] = 0.0f;
+  K.o = 0;
+  K.gunit = 0;
+  uint32_t* ucount = reinterpret_cast<uint32_t*>(vbq_smem + Lay::kMisc) + 32;
+  if (threadIdx.x < 4) ucount[threadIdx.x] = 0u;
+}
+
+// ---- the single-item kernel ---------------------------------------------
+
+template <int NB, int W, int NSLOT>
+__global__ void __launch_bounds__(W * 32, 1) vbq_gemv_kernel(const __grid_constant__ GemvArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WarpStream<NSLOT> S;
+  Worker<NB> K;
+  const UnitRegs ur = load_units<W>(a.it.plan, warp, lane);
+  worker_init<NB, W, NSLOT>(S, K, a.pieces, a.pstart, a.pbytes, lane, warp);
+  __syncthreads();  // the unit counters are initialized
+
+  // The next kernel may start streaming its own weights now.
+  grid_dep_launch();
+  grid_dep_wait();
+
+  run_item<NB, W, NSLOT, false>(a.it, ur, S, K, nullptr, nullptr, lane, warp);
   if (!S.ok) {
     if (lane == 0) atomicExch(a.err, kErrRingTimeout);
-    // Drain this warp's copies in flight (bounded) before the shared memory is released.
-    for (uint32_t c = S.landed; c < S.issued; ++c)
-      if (!__all_sync(0xffffffffu, mbar_wait(S.bar + 8 * (c & (NSLOT - 1)), (c / NSLOT) & 1u))) break;
+    S.drain();
+  }
+}
+
+// ---- the persistent decode-step kernel ----------------------------------
+
+// A sequence of items with a grid barrier between each and the next. Items
+// name their activations by pointer into one workspace; the launch's x and
+// output are substituted for items that leave them null.
+struct Program {
+  const Item* items;
+  int32_t n_items;
+  const uint64_t* pieces;   // per-warp piece lists over all items
+  const uint32_t* pstart;
+  const uint32_t* pbytes;
+  float* h;                 // h = x is written before the first item
+  int32_t d;
+  uint32_t* grid_bar;       // [0]: barrier arrivals, [1]: CTAs done; both zero at launch, and reset at exit
+  int* err;
+};
+
+struct DecodeArgs {
+  Program prog;
+  const uint16_t* x;
+  float* out;
+};
+
+// Grid barrier number k (0-based) of this launch. Bounded: on a timeout it
+// records kErrGridTimeout and lets the CTA go on; once any wait has recorded
+// an error (the check word is non-zero) it stops waiting at once, so a failed
+// step ends in about one wait limit rather than one per barrier.
+__device__ __forceinline__ void grid_barrier(uint32_t* bar, uint32_t k, int* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    const uint32_t target = (k + 1u) * gridDim.x;
+    const long long t0 = clock64();
+    uint32_t v;
+    int e;
+    do {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
+      if (v >= target) break;
+      asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(e) : "l"(err) : "memory");
+      if (e != 0) break;
+      if (clock64() - t0 > kSpinCycles) {
+        atomicExch(err, kErrGridTimeout);
+        break;
+      }
+    } while (true);
+  }
+  __syncthreads();
+}
+
+template <int W, int NSLOT>
+__global__ void __launch_bounds__(W * 32, 1) vbq_decode_kernel(const __grid_constant__ DecodeArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Program& P = a.prog;
+  WarpStream<NSLOT> S;
+  Worker<1> K;
+  UnitRegs ur = load_units<W>(P.items[0].plan, warp, lane);
+  worker_init<1, W, NSLOT>(S, K, P.pieces, P.pstart, P.pbytes, lane, warp);
+  // h = x (bf16 -> fp32)
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < P.d; i += gridDim.x * blockDim.x)
+    P.h[i] = __uint_as_float(static_cast<uint32_t>(a.x[i]) << 16);
+  grid_barrier(P.grid_bar, 0, P.err);
+  for (int i = 0; i < P.n_items; ++i) {
+    const Item& it = P.items[i];
+    run_item<1, W, NSLOT, true>(it, ur, S, K, a.out, a.x, lane, warp);
+    if (i + 1 < P.n_items) {
+      ur = load_units<W>(P.items[i + 1].plan, warp, lane);  // in flight across the barrier
+      grid_barrier(P.grid_bar, static_cast<uint32_t>(i + 1), P.err);
+    }
+  }
+  if (!S.ok) {
+    if (lane == 0) atomicExch(P.err, kErrRingTimeout);
+    S.drain();
+  }
+  // The last CTA to finish has seen every CTA leave every barrier, so it can
+  // return both counters to zero for the next launch in stream order.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(P.grid_bar + 1, 1u) == gridDim.x - 1u) {
+      atomicExch(P.grid_bar, 0u);
+      atomicExch(P.grid_bar + 1, 0u);
+    }
   }
 }
 

@@ -66,6 +66,7 @@ MatView view_of(const vbq_matrix* m, float* y, int32_t y_ld, float* trace_y) {
   v.data = m->data;
   v.run_desc = m->run_desc;
   v.y = y;
+  v.y_off = 0;
   v.y_ld = y_ld;
   v.trace_y = trace_y;
   return v;
@@ -303,15 +304,19 @@ static vbq_status gemv_columns(const vbq_matrix* m, const uint16_t* X, int32_t B
     const int left = B - done;
     const int nb = left >= 4 ? 4 : left >= 2 ? 2 : 1;
     GemvArgs a{};
-    a.seg[0] = view_of(m, Y + static_cast<int64_t>(done) * m->N, static_cast<int32_t>(m->N), nullptr);
-    a.nseg = 1;
-    a.plan = plan_view(m->plan);
-    a.xs.mode = X_BF16;
-    a.xs.K = static_cast<int32_t>(m->K);
-    a.xs.x = X + static_cast<int64_t>(done) * m->K;
-    a.xs.ldx = static_cast<int32_t>(m->K);
-    a.ep = EP_STORE;
+    a.it.seg[0] = view_of(m, Y + static_cast<int64_t>(done) * m->N, static_cast<int32_t>(m->N), nullptr);
+    a.it.nseg = 1;
+    a.it.plan = plan_view(m->plan);
+    a.it.xs.mode = X_BF16;
+    a.it.xs.K = static_cast<int32_t>(m->K);
+    a.it.xs.x = X + static_cast<int64_t>(done) * m->K;
+    a.it.xs.ldx = static_cast<int32_t>(m->K);
+    a.it.ep = EP_STORE;
     a.err = err;
+    const bool w8 = nb == 4;  // the 4-column kernel has 8 warps
+    a.pieces = w8 ? m->plan.pieces8 : m->plan.pieces16;
+    a.pstart = w8 ? m->plan.start8 : m->plan.start16;
+    a.pbytes = w8 ? m->plan.bytes8 : m->plan.bytes16;
     VBQ_CUDA_TRY(launch_gemv(nb, a, m->plan.n_ctas, st, false));
     done += nb;
   }

@@ -1,8 +1,8 @@
 // Packed VBQ layout: one definition shared by the host packer, the planner and the kernels.
 //
-// The pages ("Variable Bit-width Quantization ...", abstract) say only that the
-// per-group allocation "maps directly to packed low-bit storage". Everything
-// below is this library's own design for sm_103a.
+// The pages ("Variable Bit-width Quantization ...", abstract) state only that a
+// fixed per-group bit allocation can be stored as packed low-bit codes; they
+// give no format. Everything below is this library's own design for sm_103a.
 //
 // Rows are cut into tiles of at most TILE_MAX rows. Tiles are cut where the
 // running byte count reaches a target, so tiles carry about equal bytes. Within

@@ -7,15 +7,15 @@
 // head returns its kv group's v), SwiGLU, fp32 residual, and bf16 at every
 // projection input.
 //
-// Each step is 1 + 4*n_layers + 1 kernels: h = x; per layer the fused
-// [q;k;v] GEMV (RMSNorm in its prologue), the o GEMV (GQA gather in its
-// prologue, residual add in its epilogue), the fused [gate;up] GEMV (RMSNorm
-// prologue), and the down GEMV (SwiGLU prologue, residual epilogue); then the
-// head GEMV. Each of these launches has its own work plan over its matrices,
-// made when the model is created. The sequence is captured once into a CUDA
-// graph. Its edges are programmatic: each GEMV starts streaming its weights
-// while the previous one finishes, and waits (griddepcontrol.wait) only before
-// touching activations.
+// A step is one persistent kernel (vbq_decode_kernel in gemv.cuh): one CTA per
+// SM runs h = x, then per layer four GEMV items, then the head:
+//   [q;k;v] (RMSNorm in its prologue), o (GQA gather in its prologue, residual
+//   in its epilogue), [gate;up] (RMSNorm prologue), down (SwiGLU prologue,
+//   residual epilogue),
+// with a grid barrier between items. Each warp streams its share of every
+// item's packed weights back to back, so the next item's weights are already
+// arriving while the CTAs wait at a barrier. The items, their work plans and
+// the per-warp piece lists are built once, when the model is created.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -31,41 +31,10 @@ using namespace vbq;
 namespace {
 
 enum { P_Q = 0, P_K, P_V, P_O, P_GATE, P_UP, P_DOWN, P_PER_LAYER };
+enum { L_QKV = 0, L_O, L_GU, L_DOWN, L_PER_LAYER };
 
-__global__ void init_h_kernel(const uint16_t* __restrict__ x, float* __restrict__ h, int32_t d) {
-  grid_dep_wait();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x)
-    h[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
-}
-
-}  // namespace
-
-struct vbq_model {
-  vbq_model_desc desc{};
-  std::vector<const vbq_matrix*> mats;
-  int device = 0;
-  void* ws = nullptr;
-  float* h = nullptr;
-  float* qkv = nullptr;
-  float* gu = nullptr;
-  uint16_t* x_stage = nullptr;
-  float* logits_stage = nullptr;
-  bool trace = false;
-  uint16_t* tr_in = nullptr;
-  float* tr_out = nullptr;
-  std::vector<int64_t> in_off, out_off;
-  int64_t in_total = 0, out_total = 0;
-  cudaStream_t cap_stream = nullptr;
-  cudaGraphExec_t exec = nullptr;
-  const uint16_t* g_x = nullptr;
-  float* g_logits = nullptr;
-  int64_t kernels_per_step = 0;
-  std::vector<DevicePlan> plans;  // per layer: [q;k;v], o, [gate;up], down; then the head
-  uint64_t max_partial_rows = 0;
-  uint32_t max_counters = 0;
-};
-
-namespace {
+constexpr int DEC_W = 16;     // warps per CTA of the decode kernel
+constexpr int DEC_NSLOT = 2;  // ring slots per warp
 
 int64_t proj_n(const vbq_model_desc& d, int p) {
   switch (p) {
@@ -85,160 +54,191 @@ int64_t proj_k(const vbq_model_desc& d, int p) {
   }
 }
 
-void free_graph(vbq_model* m) {
-  if (m->exec) cudaGraphExecDestroy(m->exec);
-  m->exec = nullptr;
-}
+int64_t round64(int64_t n) { return (n + 63) & ~int64_t(63); }
 
-
-void add_seg(GemvArgs& a, const vbq_matrix* m, float* y, float* trace_y) {
-  a.seg[a.nseg] = view_of(m, y, static_cast<int32_t>(m->N), trace_y);
-  a.nseg += 1;
-}
-
-enum { L_QKV = 0, L_O, L_GU, L_DOWN, L_PER_LAYER };
-
-// Where one step's activations live.
-struct StepBuffers {
-  float* h;
-  float* qkv;
-  float* gu;
-  // Split-tile scratch shared by every launch of the step (the launches run in
-  // stream order, and each touches it only after griddepcontrol.wait). When
-  // null, each launch uses its plan's own storage.
-  float* partial;
-  uint32_t* counters;
+// Float offsets of one step's activations inside a region: the grid-barrier
+// counters, h, [q;k;v] and [gate;up]. The counters must be zero before a step;
+// each step leaves them so. (Split-tile partial rows and arrival counters live
+// in each item's work plan, which the model owns.)
+struct Layout {
+  int64_t bar = 0, h = 0, qkv = 0, gu = 0, total = 0;
 };
 
-GemvArgs proj_args(const vbq_model* m, int launch, const StepBuffers& b, int* err) {
-  GemvArgs a{};
-  a.err = err;
-  a.ep = EP_STORE;
-  a.plan = plan_view(m->plans[launch]);
-  if (b.partial) {
-    a.plan.partial = b.partial;
-    a.plan.counters = b.counters;
-  }
-  return a;
+Layout layout_of(const vbq_model_desc& d) {
+  Layout L;
+  L.bar = 0;
+  L.h = 64;
+  L.qkv = L.h + round64(d.d);
+  L.gu = L.qkv + round64(proj_n(d, P_Q) + 2 * proj_n(d, P_K));
+  L.total = L.gu + round64(2 * int64_t(d.d_ff));
+  return L;
 }
 
-// Enqueues one step; every kernel after the first may launch programmatically.
-// skip_init: the caller has already enqueued h = x.
-cudaError_t enqueue_step(const vbq_model* m, const uint16_t* x, float* logits, const StepBuffers& b, bool trace,
-                         cudaStream_t st, int* err, bool skip_init = false) {
+}  // namespace
+
+struct vbq_model {
+  vbq_model_desc desc{};
+  std::vector<const vbq_matrix*> mats;
+  int device = 0;
+  int sms = 0;
+  Layout lay;
+  float* ws = nullptr;              // this model's step scratch (Layout), then the host-step staging
+  uint16_t* x_stage = nullptr;
+  float* logits_stage = nullptr;
+  bool trace = false;
+  uint16_t* tr_in = nullptr;
+  float* tr_out = nullptr;
+  std::vector<int64_t> in_off, out_off;
+  int64_t in_total = 0, out_total = 0;
+  std::vector<DevicePlan> plans;    // per item
+  void* prog_mem = nullptr;         // piece lists and the items of both programs
+  const uint64_t* pieces = nullptr;
+  const uint32_t* pstart = nullptr;
+  const uint32_t* pbytes = nullptr;
+  Item* items_ws = nullptr;         // items over ws
+  Item* items_static = nullptr;     // items over the static scratch (null if the model does not fit it)
+  float* static_base = nullptr;
+  int32_t n_items = 0;
+  int* err = nullptr;               // the device check word of the model's device
+};
+
+namespace {
+
+// The static scratch of vbq_decode_step_noalloc (defined at the bottom of this file).
+vbq_status step_scratch_address(int dev, float** out);
+constexpr int64_t kStepScratchFloats = 65536;
+
+// The items of one step over the scratch at `base`.
+std::vector<Item> make_items(const vbq_model* m, float* base, bool trace) {
   const vbq_model_desc& d = m->desc;
-  const int L = d.n_layers;
+  const Layout& L = m->lay;
+  float* h = base + L.h;
+  float* qkv = base + L.qkv;
+  float* gu = base + L.gu;
   const int64_t nq = proj_n(d, P_Q), nkv = proj_n(d, P_K);
-  float* q_out = b.qkv;
-  float* k_out = b.qkv + nq;
-  float* v_out = b.qkv + nq + nkv;
   auto tin = [&](int p) -> uint16_t* { return trace ? m->tr_in + m->in_off[p] : nullptr; };
   auto tout = [&](int p) -> float* { return trace ? m->tr_out + m->out_off[p] : nullptr; };
-  auto n_ctas = [&](int launch) { return m->plans[launch].n_ctas; };
-
-  cudaError_t e = cudaSuccess;
-  if (!skip_init) {
-    note_launches(1);
-    init_h_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x, b.h, d.d);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-
-  for (int l = 0; l < L; ++l) {
+  std::vector<Item> items;
+  auto item_for = [&](int li) {
+    Item it{};
+    it.plan = plan_view(m->plans[li]);
+    it.ep = EP_STORE;
+    return it;
+  };
+  auto add_seg = [&](Item& it, const vbq_matrix* w, float* y, float* ty) {
+    it.seg[it.nseg] = view_of(w, y, static_cast<int32_t>(w->N), ty);
+    it.nseg += 1;
+  };
+  for (int l = 0; l < d.n_layers; ++l) {
     const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
-    const int p0 = l * P_PER_LAYER;
-    const int l0 = l * L_PER_LAYER;
+    const int p0 = l * P_PER_LAYER, l0 = l * L_PER_LAYER;
     {  // [q; k; v] = W u, u = bf16(rmsnorm(h))
-      GemvArgs a = proj_args(m, l0 + L_QKV, b, err);
-      add_seg(a, W[P_Q], q_out, tout(p0 + P_Q));
-      add_seg(a, W[P_K], k_out, tout(p0 + P_K));
-      add_seg(a, W[P_V], v_out, tout(p0 + P_V));
-      a.xs.mode = X_RMSNORM;
-      a.xs.K = d.d;
-      a.xs.h = b.h;
-      a.xs.eps = d.rms_eps;
-      a.xs.trace_x = tin(p0 + P_Q);
-      if ((e = launch_gemv(1, a, n_ctas(l0 + L_QKV), st, true)) != cudaSuccess) return e;
+      Item it = item_for(l0 + L_QKV);
+      add_seg(it, W[P_Q], qkv, tout(p0 + P_Q));
+      add_seg(it, W[P_K], qkv + nq, tout(p0 + P_K));
+      add_seg(it, W[P_V], qkv + nq + nkv, tout(p0 + P_V));
+      it.xs.mode = X_RMSNORM;
+      it.xs.K = d.d;
+      it.xs.h = h;
+      it.xs.eps = d.rms_eps;
+      it.xs.trace_x = tin(p0 + P_Q);
+      items.push_back(it);
     }
     {  // h += Wo a, a = bf16(v of each head's kv group)
-      GemvArgs a = proj_args(m, l0 + L_O, b, err);
-      add_seg(a, W[P_O], b.h, tout(p0 + P_O));
-      a.xs.mode = X_GQA;
-      a.xs.K = static_cast<int32_t>(nq);
-      a.xs.v = v_out;
-      a.xs.head_dim = d.head_dim;
-      a.xs.group = d.n_heads / d.n_kv_heads;
-      a.xs.trace_x = tin(p0 + P_O);
-      a.ep = EP_RESID;
-      a.resid = b.h;
-      if ((e = launch_gemv(1, a, n_ctas(l0 + L_O), st, true)) != cudaSuccess) return e;
+      Item it = item_for(l0 + L_O);
+      add_seg(it, W[P_O], h, tout(p0 + P_O));
+      it.xs.mode = X_GQA;
+      it.xs.K = static_cast<int32_t>(nq);
+      it.xs.v = qkv + nq + nkv;
+      it.xs.head_dim = d.head_dim;
+      it.xs.group = d.n_heads / d.n_kv_heads;
+      it.xs.trace_x = tin(p0 + P_O);
+      it.ep = EP_RESID;
+      it.resid = h;
+      items.push_back(it);
     }
     {  // [gate; up] = W u, u = bf16(rmsnorm(h))
-      GemvArgs a = proj_args(m, l0 + L_GU, b, err);
-      add_seg(a, W[P_GATE], b.gu, tout(p0 + P_GATE));
-      add_seg(a, W[P_UP], b.gu + d.d_ff, tout(p0 + P_UP));
-      a.xs.mode = X_RMSNORM;
-      a.xs.K = d.d;
-      a.xs.h = b.h;
-      a.xs.eps = d.rms_eps;
-      a.xs.trace_x = tin(p0 + P_GATE);
-      if ((e = launch_gemv(1, a, n_ctas(l0 + L_GU), st, true)) != cudaSuccess) return e;
+      Item it = item_for(l0 + L_GU);
+      add_seg(it, W[P_GATE], gu, tout(p0 + P_GATE));
+      add_seg(it, W[P_UP], gu + d.d_ff, tout(p0 + P_UP));
+      it.xs.mode = X_RMSNORM;
+      it.xs.K = d.d;
+      it.xs.h = h;
+      it.xs.eps = d.rms_eps;
+      it.xs.trace_x = tin(p0 + P_GATE);
+      items.push_back(it);
     }
     {  // h += Wdown bf16(silu(gate) * up)
-      GemvArgs a = proj_args(m, l0 + L_DOWN, b, err);
-      add_seg(a, W[P_DOWN], b.h, tout(p0 + P_DOWN));
-      a.xs.mode = X_SWIGLU;
-      a.xs.K = d.d_ff;
-      a.xs.gate = b.gu;
-      a.xs.up = b.gu + d.d_ff;
-      a.xs.trace_x = tin(p0 + P_DOWN);
-      a.ep = EP_RESID;
-      a.resid = b.h;
-      if ((e = launch_gemv(1, a, n_ctas(l0 + L_DOWN), st, true)) != cudaSuccess) return e;
+      Item it = item_for(l0 + L_DOWN);
+      add_seg(it, W[P_DOWN], h, tout(p0 + P_DOWN));
+      it.xs.mode = X_SWIGLU;
+      it.xs.K = d.d_ff;
+      it.xs.gate = gu;
+      it.xs.up = gu + d.d_ff;
+      it.xs.trace_x = tin(p0 + P_DOWN);
+      it.ep = EP_RESID;
+      it.resid = h;
+      items.push_back(it);
     }
   }
-  {  // logits = Whead bf16(rmsnorm(h))
-    const int lh = L * L_PER_LAYER;
-    GemvArgs a = proj_args(m, lh, b, err);
-    const int ph = L * P_PER_LAYER;
-    add_seg(a, m->mats[ph], logits, tout(ph));
-    a.xs.mode = X_RMSNORM;
-    a.xs.K = d.d;
-    a.xs.h = b.h;
-    a.xs.eps = d.rms_eps;
-    a.xs.trace_x = tin(ph);
-    if ((e = launch_gemv(1, a, n_ctas(lh), st, true)) != cudaSuccess) return e;
+  {  // logits = Whead bf16(rmsnorm(h)), into the launch's output
+    const int lh = d.n_layers * L_PER_LAYER, ph = d.n_layers * P_PER_LAYER;
+    Item it = item_for(lh);
+    add_seg(it, m->mats[ph], nullptr, tout(ph));
+    it.xs.mode = X_RMSNORM;
+    it.xs.K = d.d;
+    it.xs.h = h;
+    it.xs.eps = d.rms_eps;
+    it.xs.trace_x = tin(ph);
+    items.push_back(it);
   }
-  return cudaSuccess;
+  return items;
 }
 
-vbq_status build_graph(vbq_model* m, const uint16_t* x, float* logits) {
-  free_graph(m);
-  int* err = device_check_word();
-  if (!err) return fail(VBQ_ERR_CUDA, "device check word");
-  warm_gemv(1);
-  const int64_t before = vbq_launch_count(0);
-  VBQ_CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
-  const StepBuffers b{m->h, m->qkv, m->gu, nullptr, nullptr};
-  cudaError_t e = enqueue_step(m, x, logits, b, m->trace, m->cap_stream, err);
-  cudaGraph_t graph = nullptr;
-  cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &graph);
-  // Capturing enqueues nothing: the counter tracks launches that actually run.
-  m->kernels_per_step = vbq_launch_count(0) - before;
-  note_launches(-m->kernels_per_step);
-  if (e != cudaSuccess) {
-    if (graph) cudaGraphDestroy(graph);
-    return cuda_fail(e, "decode step capture");
-  }
-  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamEndCapture");
-  e = cudaGraphInstantiate(&m->exec, graph, 0);
-  cudaGraphDestroy(graph);
-  if (e != cudaSuccess) {
-    m->exec = nullptr;
-    return cuda_fail(e, "cudaGraphInstantiate");
-  }
-  m->g_x = x;
-  m->g_logits = logits;
-  return VBQ_OK;
+cudaError_t upload_items(const std::vector<Item>& items, Item* dst) {
+  return cudaMemcpy(dst, items.data(), sizeof(Item) * items.size(), cudaMemcpyHostToDevice);
+}
+
+cudaError_t launch_decode(const vbq_model* m, const Item* items, float* base, const uint16_t* x, float* out,
+                          cudaStream_t st, int* err) {
+  DecodeArgs a{};
+  a.prog.items = items;
+  a.prog.n_items = m->n_items;
+  a.prog.pieces = m->pieces;
+  a.prog.pstart = m->pstart;
+  a.prog.pbytes = m->pbytes;
+  a.prog.h = base + m->lay.h;
+  a.prog.d = m->desc.d;
+  a.prog.grid_bar = reinterpret_cast<uint32_t*>(base + m->lay.bar);
+  a.prog.err = err;
+  a.x = x;
+  a.out = out;
+  // The grid-barrier and split-tile counters are zero here: the scratch starts
+  // zeroed, and every launch leaves them at zero when it ends.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(m->sms), 1, 1);
+  cfg.blockDim = dim3(DEC_W * 32, 1, 1);
+  cfg.dynamicSmemBytes = GemvSmem<1, DEC_W, DEC_NSLOT>::kBytesStaged;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA is resident: the grid barriers need it
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  note_launches(1);
+  return cudaLaunchKernelEx(&cfg, vbq_decode_kernel<DEC_W, DEC_NSLOT>, a);
+}
+
+void prepare_decode_kernel() {
+  static std::mutex mu;
+  static std::map<int, bool> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return;
+  cudaFuncSetAttribute(vbq_decode_kernel<DEC_W, DEC_NSLOT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       GemvSmem<1, DEC_W, DEC_NSLOT>::kBytesStaged);
+  done[dev] = true;
 }
 
 }  // namespace
@@ -253,6 +253,9 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   if (d.n_layers < 0 || d.d <= 0 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.head_dim <= 0 || d.d_ff <= 0 ||
       d.vocab <= 0 || d.n_heads % d.n_kv_heads || d.head_dim % 2 || !(d.rms_eps >= 0.0f))
     return fail(VBQ_ERR_SHAPE, "vbq_model_create: invalid shapes");
+  if (d.d > XCAP || d.d_ff > XCAP || int64_t(d.n_heads) * d.head_dim > XCAP)
+    return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: d, d_ff and n_heads*head_dim must be at most " +
+                                         std::to_string(XCAP) + " (the decode kernel stages x in shared memory)");
   const int nm = d.n_layers * P_PER_LAYER + 1;
   int dev = 0;
   VBQ_CUDA_TRY(cudaGetDevice(&dev));
@@ -272,28 +275,13 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   if (!m) return fail(VBQ_ERR_OOM, "vbq_model_create");
   m->desc = d;
   m->device = dev;
+  m->sms = gpu_info().sms;
+  m->err = device_check_word();
+  if (!m->err) {
+    delete m;
+    return fail(VBQ_ERR_CUDA, "vbq_model_create: no device check word");
+  }
   m->mats.assign(mats, mats + nm);
-  const int64_t nqkv = proj_n(d, P_Q) + 2 * proj_n(d, P_K);
-  auto al = [](int64_t b) { return (b + 255) & ~int64_t(255); };
-  const int64_t b_h = al(4 * d.d), b_qkv = al(4 * nqkv), b_gu = al(8 * int64_t(d.d_ff));
-  const int64_t b_x = al(2 * d.d), b_lg = al(4 * int64_t(d.vocab));
-  cudaError_t e = cudaMalloc(&m->ws, b_h + b_qkv + b_gu + b_x + b_lg);
-  if (e != cudaSuccess) {
-    delete m;
-    return cuda_fail(e, "vbq_model_create: workspace");
-  }
-  char* p = static_cast<char*>(m->ws);
-  m->h = reinterpret_cast<float*>(p);
-  m->qkv = reinterpret_cast<float*>(p + b_h);
-  m->gu = reinterpret_cast<float*>(p + b_h + b_qkv);
-  m->x_stage = reinterpret_cast<uint16_t*>(p + b_h + b_qkv + b_gu);
-  m->logits_stage = reinterpret_cast<float*>(p + b_h + b_qkv + b_gu + b_x);
-  e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking);
-  if (e != cudaSuccess) {
-    cudaFree(m->ws);
-    delete m;
-    return cuda_fail(e, "vbq_model_create: stream");
-  }
   // Trace offsets: inputs shared by q/k/v and by gate/up.
   m->in_off.assign(nm, 0);
   m->out_off.assign(nm, 0);
@@ -313,37 +301,101 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   }
   m->in_total = io;
   m->out_total = oo;
-  // One plan per launch of the step, each over the launch's matrices.
-  const int sms = gpu_info().sms;
-  auto add_plan = [&](std::initializer_list<const vbq_matrix*> ms) -> cudaError_t {
+
+  // One plan per item, every one over exactly one CTA per SM; the piece lists of all items in turn.
+  std::vector<std::vector<uint64_t>> per_warp;
+  auto add_plan = [&](std::initializer_list<const vbq_matrix*> ms) -> vbq_status {
     std::vector<SegTables> segs;
-    uint64_t bytes = 0;
+    std::vector<const uint8_t*> data;
     for (const vbq_matrix* w : ms) {
       segs.push_back(seg_tables(w));
-      bytes += static_cast<uint64_t>(w->data_bytes);
+      data.push_back(w->data);
     }
-    Plan pl = make_plan(segs, plan_ctas(bytes, sms), MAX_UNITS_PER_CTA);
-    m->max_partial_rows = std::max<uint64_t>(m->max_partial_rows, pl.partial_rows);
-    m->max_counters = std::max<uint32_t>(m->max_counters, pl.n_counters);
+    Plan pl = make_plan(segs, m->sms, MAX_UNITS_PER_CTA);
+    if (pl.n_ctas != m->sms && pl.n_ctas != 0)
+      return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: a projection needs more than one CTA per SM");
+    if (pl.n_ctas == 0) {  // an empty projection: one empty slot per CTA
+      pl.n_ctas = m->sms;
+      pl.umax = 1;
+      pl.units.assign(m->sms, UnitRec{});
+      pl.slices.assign(static_cast<size_t>(m->sms) * SLICES, SliceRec{});
+    }
+    if (!append_pieces(pl, data, DEC_W, &per_warp))
+      return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: weight address beyond 2^48 or a warp piece of 16 MiB or more");
     DevicePlan dp;
-    cudaError_t err = upload_plan(pl, 1, nullptr, &dp);
-    if (err == cudaSuccess) m->plans.push_back(dp);
-    return err;
+    cudaError_t err = upload_plan(pl, 1, data, nullptr, &dp);
+    if (err != cudaSuccess) return cuda_fail(err, "vbq_model_create: plan upload");
+    m->plans.push_back(dp);
+    return VBQ_OK;
   };
-  for (int l = 0; l <= d.n_layers; ++l) {
+  vbq_status s = VBQ_OK;
+  for (int l = 0; l <= d.n_layers && s == VBQ_OK; ++l) {
     const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
-    cudaError_t err;
     if (l == d.n_layers) {
-      err = add_plan({W[0]});
-    } else if ((err = add_plan({W[P_Q], W[P_K], W[P_V]})) == cudaSuccess && (err = add_plan({W[P_O]})) == cudaSuccess &&
-               (err = add_plan({W[P_GATE], W[P_UP]})) == cudaSuccess) {
-      err = add_plan({W[P_DOWN]});
-    }
-    if (err != cudaSuccess) {
-      vbq_model_free(m);
-      return cuda_fail(err, "vbq_model_create: plan upload");
+      s = add_plan({W[0]});
+    } else if ((s = add_plan({W[P_Q], W[P_K], W[P_V]})) == VBQ_OK && (s = add_plan({W[P_O]})) == VBQ_OK &&
+               (s = add_plan({W[P_GATE], W[P_UP]})) == VBQ_OK) {
+      s = add_plan({W[P_DOWN]});
     }
   }
+  if (s != VBQ_OK) {
+    vbq_model_free(m);
+    return s;
+  }
+  m->n_items = static_cast<int32_t>(m->plans.size());
+  m->lay = layout_of(d);
+
+  // Device memory: the step scratch, the host-step staging, the piece lists and both item arrays.
+  const PieceSet ps = finish_pieces(per_warp);
+  auto al = [](int64_t b) { return (b + 255) & ~int64_t(255); };
+  const int64_t b_ws = al(4 * m->lay.total), b_x = al(2 * int64_t(d.d)), b_lg = al(4 * int64_t(d.vocab));
+  cudaError_t e = cudaMalloc(&m->ws, b_ws + b_x + b_lg);
+  if (e == cudaSuccess) e = cudaMemset(m->ws, 0, b_ws);
+  if (e != cudaSuccess) {
+    vbq_model_free(m);
+    return cuda_fail(e, "vbq_model_create: workspace");
+  }
+  m->x_stage = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(m->ws) + b_ws);
+  m->logits_stage = reinterpret_cast<float*>(reinterpret_cast<char*>(m->ws) + b_ws + b_x);
+  const int64_t o_p = 0, o_s = al(8 * int64_t(std::max<size_t>(1, ps.pieces.size())));
+  const int64_t o_b = o_s + al(4 * int64_t(ps.start.size()));
+  const int64_t o_i1 = o_b + al(4 * int64_t(std::max<size_t>(1, ps.bytes.size())));
+  const int64_t o_i2 = o_i1 + al(int64_t(sizeof(Item)) * m->n_items);
+  const int64_t total = o_i2 + al(int64_t(sizeof(Item)) * m->n_items);
+  e = cudaMalloc(&m->prog_mem, total);
+  char* pm = static_cast<char*>(m->prog_mem);
+  if (e == cudaSuccess && !ps.pieces.empty())
+    e = cudaMemcpy(pm + o_p, ps.pieces.data(), 8 * ps.pieces.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(pm + o_s, ps.start.data(), 4 * ps.start.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !ps.bytes.empty())
+    e = cudaMemcpy(pm + o_b, ps.bytes.data(), 4 * ps.bytes.size(), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    vbq_model_free(m);
+    return cuda_fail(e, "vbq_model_create: programs");
+  }
+  m->pieces = reinterpret_cast<const uint64_t*>(pm + o_p);
+  m->pstart = reinterpret_cast<const uint32_t*>(pm + o_s);
+  m->pbytes = reinterpret_cast<const uint32_t*>(pm + o_b);
+  m->items_ws = reinterpret_cast<Item*>(pm + o_i1);
+  e = upload_items(make_items(m, m->ws, false), m->items_ws);
+  // The program over the static scratch of vbq_decode_step_noalloc, when the model fits it. That entry
+  // point's set-up happens here, with the model's device current, so that its calls allocate nothing.
+  if (e == cudaSuccess && m->lay.total <= kStepScratchFloats) {
+    float* sb = nullptr;
+    vbq_status ss = step_scratch_address(dev, &sb);
+    if (ss != VBQ_OK) {
+      vbq_model_free(m);
+      return ss;
+    }
+    m->static_base = sb;
+    m->items_static = reinterpret_cast<Item*>(pm + o_i2);
+    e = upload_items(make_items(m, sb, false), m->items_static);
+  }
+  if (e != cudaSuccess) {
+    vbq_model_free(m);
+    return cuda_fail(e, "vbq_model_create: items");
+  }
+  prepare_decode_kernel();
   *out = m;
   return VBQ_OK;
 }
@@ -354,9 +406,8 @@ extern "C" void vbq_model_free(vbq_model* m) {
   cudaGetDevice(&cur);
   cudaSetDevice(m->device);
   cudaDeviceSynchronize();
-  free_graph(m);
-  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   cudaFree(m->ws);
+  cudaFree(m->prog_mem);
   cudaFree(m->tr_in);
   cudaFree(m->tr_out);
   for (DevicePlan& p : m->plans) free_plan(&p);
@@ -366,14 +417,9 @@ extern "C" void vbq_model_free(vbq_model* m) {
 
 extern "C" vbq_status vbq_decode_step(vbq_model* m, const uint16_t* x_dev, float* logits_dev, void* stream) {
   if (!m || !x_dev || !logits_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: NULL argument");
-  if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 2)
-    return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: misaligned buffer");
-  if (!m->exec || m->g_x != x_dev || m->g_logits != logits_dev) {
-    vbq_status s = build_graph(m, x_dev, logits_dev);
-    if (s != VBQ_OK) return s;
-  }
-  VBQ_CUDA_TRY(cudaGraphLaunch(m->exec, static_cast<cudaStream_t>(stream)));
-  note_launches(m->kernels_per_step);
+  if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 4)
+    return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: misaligned buffer (x and logits need 4-byte alignment)");
+  VBQ_CUDA_TRY(launch_decode(m, m->items_ws, m->ws, x_dev, logits_dev, static_cast<cudaStream_t>(stream), m->err));
   return VBQ_OK;
 }
 
@@ -396,7 +442,8 @@ extern "C" vbq_status vbq_model_set_trace(vbq_model* m, int32_t enable) {
     VBQ_CUDA_TRY(cudaMalloc(&m->tr_out, 4 * static_cast<size_t>(m->out_total)));
   }
   m->trace = enable != 0;
-  free_graph(m);
+  VBQ_CUDA_TRY(cudaDeviceSynchronize());  // no step may be reading the items
+  VBQ_CUDA_TRY(upload_items(make_items(m, m->ws, m->trace), m->items_ws));
   return VBQ_OK;
 }
 
@@ -424,32 +471,27 @@ extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host
 
 // ---------------------------------------------------------------- allocation-free decode step
 //
-// vbq_decode_step keeps its activations in a workspace that vbq_model_create
-// allocates, and it builds a CUDA graph on its first call and whenever the x or
-// logits pointers change; instantiating that graph allocates too. Some callers
-// cannot allow any allocation at step time: code that runs while another
-// component is capturing the stream into its own graph (cudaMalloc is illegal
-// during capture), real-time loops whose device memory is fixed before the loop
-// starts, or hosts that hand out device memory only from their own pool.
-// vbq_decode_step_noalloc serves them. It launches the same kernels in the same
-// order, directly on the caller's stream, and keeps the activations in the
-// file-scope array below.
+// vbq_decode_step keeps its step scratch (activations, split-tile partials and
+// counters, the grid-barrier counter) in memory that vbq_model_create
+// allocated for the model. Some callers cannot tie device memory to a model
+// they step: code that runs while another component is capturing the stream
+// into its own graph, real-time loops whose device memory is fixed before the
+// loop starts, or hosts that hand out device memory only from their own pool.
+// vbq_decode_step_noalloc serves them: it launches the same kernel with the
+// step's scratch in the file-scope array below, and allocates nothing.
 
 namespace {
 
-// g_step_scratch holds, in 64-float blocks: a status block, the split-tile
-// arrival counters, h [d], [q;k;v], [gate;up], and the split-tile partial rows.
-// 262,144 floats = 1 MiB on every device that loads this library, held until
-// the process exits.
-constexpr int64_t kStepScratchFloats = 262144;
+// Step scratch of vbq_decode_step_noalloc, in the Layout of the model: 65,536
+// floats = 256 KiB on every device that loads this library, held until the
+// process exits.
 static __device__ __align__(256) float g_step_scratch[kStepScratchFloats];
 
 std::mutex g_step_scratch_mu;
 std::map<int, float*> g_step_scratch_addr;  // device ordinal -> device address of g_step_scratch
 
-// Device address of g_step_scratch on the current device. The first call on a
-// device looks it up (and sets the GEMV kernel attributes); later calls only
-// read the cached address.
+// Device address of g_step_scratch on device dev, which must be current. The
+// first call on a device looks it up; later calls only read the cached value.
 vbq_status step_scratch_address(int dev, float** out) {
   std::lock_guard<std::mutex> lock(g_step_scratch_mu);
   auto it = g_step_scratch_addr.find(dev);
@@ -459,62 +501,34 @@ vbq_status step_scratch_address(int dev, float** out) {
   }
   void* p = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
-  if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: cudaGetSymbolAddress(g_step_scratch)");
-  warm_gemv(1);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_step_scratch)");
+  // Steps need the counters at zero; they leave them so.
+  e = cudaMemset(p, 0, sizeof(float) * kStepScratchFloats);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "clearing g_step_scratch");
   g_step_scratch_addr[dev] = static_cast<float*>(p);
   *out = static_cast<float*>(p);
   return VBQ_OK;
 }
 
-// h = x, after clearing the status word and the arrival counters (`nclear` words at `clear`).
-__global__ void init_h_clear_kernel(const uint16_t* __restrict__ x, float* __restrict__ h, int32_t d,
-                                    uint32_t* __restrict__ clear, int32_t nclear) {
-  grid_dep_wait();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nclear; i += gridDim.x * blockDim.x) clear[i] = 0u;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x)
-    h[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
-}
-
-int64_t round64(int64_t n) { return (n + 63) & ~int64_t(63); }
-
 }  // namespace
 
 extern "C" vbq_status vbq_decode_step_noalloc(vbq_model* m, const uint16_t* x_dev, float* logits_dev, void* stream) {
   if (!m || !x_dev || !logits_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: NULL argument");
-  if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 2)
-    return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: misaligned buffer");
-  const vbq_model_desc& d = m->desc;
-  const int64_t n_cnt = round64(m->max_counters);
-  const int64_t n_h = round64(d.d);
-  const int64_t n_qkv = round64(proj_n(d, P_Q) + 2 * proj_n(d, P_K));
-  const int64_t n_gu = round64(2 * int64_t(d.d_ff));
-  const int64_t n_part = round64(static_cast<int64_t>(m->max_partial_rows));
-  const int64_t need = 64 + n_cnt + n_h + n_qkv + n_gu + n_part;
-  if (need > kStepScratchFloats)
-    return fail(VBQ_ERR_SHAPE, "vbq_decode_step_noalloc: the step needs " + std::to_string(need) +
-                                   " scratch floats (status, counters, h, q/k/v, gate/up and split-tile partials, "
-                                   "each rounded up to 64); the static scratch holds " +
+  if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 4)
+    return fail(VBQ_ERR_INVALID_ARG,
+                "vbq_decode_step_noalloc: misaligned buffer (x and logits need 4-byte alignment)");
+  if (m->lay.total > kStepScratchFloats)
+    return fail(VBQ_ERR_SHAPE, "vbq_decode_step_noalloc: the step needs " + std::to_string(m->lay.total) +
+                                   " scratch floats (barrier block, h, q/k/v and gate/up, each rounded up to 64); the "
+                                   "static scratch holds " +
                                    std::to_string(kStepScratchFloats));
   int dev = 0;
   VBQ_CUDA_TRY(cudaGetDevice(&dev));
   if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: model is on another device");
-  float* base = nullptr;
-  vbq_status s = step_scratch_address(dev, &base);
-  if (s != VBQ_OK) return s;
-  StepBuffers b{};
-  uint32_t* counters = reinterpret_cast<uint32_t*>(base + 64);
-  b.counters = counters;
-  b.h = base + 64 + n_cnt;
-  b.qkv = b.h + n_h;
-  b.gu = b.qkv + n_qkv;
-  b.partial = b.gu + n_gu;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The status word and the counters must start at zero; the first kernel clears them.
-  note_launches(1);
-  init_h_clear_kernel<<<(d.d + 255) / 256, 256, 0, st>>>(x_dev, b.h, d.d, reinterpret_cast<uint32_t*>(base),
-                                                         static_cast<int32_t>(64 + n_cnt));
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = enqueue_step(m, x_dev, logits_dev, b, false, st, reinterpret_cast<int*>(base), true);
+  if (!m->items_static) return fail(VBQ_ERR_CUDA, "vbq_decode_step_noalloc: the static scratch was not set up");
+  cudaError_t e = launch_decode(m, m->items_static, m->static_base, x_dev, logits_dev,
+                                static_cast<cudaStream_t>(stream), m->err);
   if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: launch");
   return VBQ_OK;
 }

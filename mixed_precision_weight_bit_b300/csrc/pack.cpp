@@ -1,8 +1,8 @@
 // vbq_pack: logical codes + bit map + scales -> the packed device layout of layout.h.
 //
-// VBQ abstract ("Variable Bit-width Quantization ..."): the frozen per-group
-// allocation "maps directly to packed low-bit storage". The record format,
-// tile plan and class ordering are this library's own design.
+// VBQ abstract ("Variable Bit-width Quantization ..."): once the per-group bit
+// allocation is fixed, the weights can be stored as packed low-bit codes. The
+// record format, tile plan and class ordering are this library's own design.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -300,7 +300,7 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
 
   // The plan of a GEMV over this matrix alone.
   Plan pl = make_plan({seg_tables(m)}, plan_ctas(data_bytes, gpu_info().sms), MAX_UNITS_PER_CTA);
-  e = upload_plan(pl, MAX_NB, st, &m->plan);
+  e = upload_plan(pl, MAX_NB, {m->data}, st, &m->plan);
   if (e != cudaSuccess) {
     cudaFree(m->dev_base);
     delete m;

@@ -267,16 +267,75 @@ Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units
   return p;
 }
 
-cudaError_t upload_plan(const Plan& p, int max_nb, cudaStream_t stream, DevicePlan* out) {
+bool append_pieces(const Plan& p, const std::vector<const uint8_t*>& seg_data, int W,
+                   std::vector<std::vector<uint64_t>>* per_warp) {
+  const int spw = SLICES / W;
+  bool ok = true;
+  per_warp->resize(static_cast<size_t>(p.n_ctas) * W);
+  for (int32_t c = 0; c < p.n_ctas; ++c)
+    for (int32_t i = 0; i < p.umax; ++i) {
+      const size_t slot = static_cast<size_t>(c) * p.umax + i;
+      const UnitRec& u = p.units[slot];
+      if (u.nsplit == 0) break;
+      for (int w = 0; w < W; ++w) {
+        const SliceRec& f = p.slices[slot * SLICES + w * spw];
+        const SliceRec& l = p.slices[slot * SLICES + w * spw + spw - 1];
+        if (l.b1 > f.b0) {
+          const uint8_t* a = seg_data[u.seg] + uint64_t(f.b0) * 16u;
+          const uint64_t n = uint64_t(l.b1 - f.b0) * 16u;
+          ok = ok && piece_fits(a, n);
+          (*per_warp)[static_cast<size_t>(c) * W + w].push_back(make_piece(a, n));
+        }
+      }
+    }
+  return ok;
+}
+
+PieceSet finish_pieces(const std::vector<std::vector<uint64_t>>& per_warp) {
+  PieceSet ps;
+  ps.start.assign(per_warp.size() + 1, 0);
+  ps.bytes.assign(per_warp.size(), 0);
+  for (size_t i = 0; i < per_warp.size(); ++i) {
+    ps.start[i + 1] = ps.start[i] + static_cast<uint32_t>(per_warp[i].size());
+    uint64_t b = 0;
+    for (uint64_t q : per_warp[i]) {
+      ps.pieces.push_back(q);
+      b += (q & 0xFFFFFu) << 4;
+    }
+    ps.bytes[i] = static_cast<uint32_t>(b);
+  }
+  return ps;
+}
+
+cudaError_t upload_plan(const Plan& p, int max_nb, const std::vector<const uint8_t*>& seg_data,
+                        cudaStream_t stream, DevicePlan* out) {
   auto al = [](uint64_t b) { return (b + 255) & ~uint64_t(255); };
+  std::vector<std::vector<uint64_t>> w16, w8;
+  if (!append_pieces(p, seg_data, 16, &w16) || !append_pieces(p, seg_data, 8, &w8)) return cudaErrorInvalidValue;
+  const PieceSet p16 = finish_pieces(w16), p8 = finish_pieces(w8);
   const uint64_t o_units = 0;
   const uint64_t o_slices = al(o_units + sizeof(UnitRec) * std::max<size_t>(1, p.units.size()));
-  const uint64_t o_cnt = al(o_slices + sizeof(SliceRec) * std::max<size_t>(1, p.slices.size()));
+  const uint64_t o_p16 = al(o_slices + sizeof(SliceRec) * std::max<size_t>(1, p.slices.size()));
+  const uint64_t o_s16 = al(o_p16 + 8ull * std::max<size_t>(1, p16.pieces.size()));
+  const uint64_t o_b16 = al(o_s16 + 4ull * p16.start.size());
+  const uint64_t o_p8 = al(o_b16 + 4ull * std::max<size_t>(1, p16.bytes.size()));
+  const uint64_t o_s8 = al(o_p8 + 8ull * std::max<size_t>(1, p8.pieces.size()));
+  const uint64_t o_b8 = al(o_s8 + 4ull * p8.start.size());
+  const uint64_t o_cnt = al(o_b8 + 4ull * std::max<size_t>(1, p8.bytes.size()));
   const uint64_t o_part = al(o_cnt + 4ull * std::max<uint32_t>(1, p.n_counters));
   const uint64_t total = al(o_part + 4ull * std::max<uint64_t>(1, p.partial_rows * max_nb));
   std::vector<uint8_t> host(o_cnt, 0);
-  if (!p.units.empty()) std::memcpy(host.data() + o_units, p.units.data(), sizeof(UnitRec) * p.units.size());
-  if (!p.slices.empty()) std::memcpy(host.data() + o_slices, p.slices.data(), sizeof(SliceRec) * p.slices.size());
+  auto put = [&](uint64_t off, const void* src, size_t n) {
+    if (n) std::memcpy(host.data() + off, src, n);
+  };
+  put(o_units, p.units.data(), sizeof(UnitRec) * p.units.size());
+  put(o_slices, p.slices.data(), sizeof(SliceRec) * p.slices.size());
+  put(o_p16, p16.pieces.data(), 8 * p16.pieces.size());
+  put(o_s16, p16.start.data(), 4 * p16.start.size());
+  put(o_b16, p16.bytes.data(), 4 * p16.bytes.size());
+  put(o_p8, p8.pieces.data(), 8 * p8.pieces.size());
+  put(o_s8, p8.start.data(), 4 * p8.start.size());
+  put(o_b8, p8.bytes.data(), 4 * p8.bytes.size());
   uint8_t* d = nullptr;
   cudaError_t e = cudaMalloc(&d, total);
   if (e != cudaSuccess) return e;
@@ -290,6 +349,12 @@ cudaError_t upload_plan(const Plan& p, int max_nb, cudaStream_t stream, DevicePl
   out->base = d;
   out->units = reinterpret_cast<const UnitRec*>(d + o_units);
   out->slices = reinterpret_cast<const SliceRec*>(d + o_slices);
+  out->pieces16 = reinterpret_cast<const uint64_t*>(d + o_p16);
+  out->start16 = reinterpret_cast<const uint32_t*>(d + o_s16);
+  out->bytes16 = reinterpret_cast<const uint32_t*>(d + o_b16);
+  out->pieces8 = reinterpret_cast<const uint64_t*>(d + o_p8);
+  out->start8 = reinterpret_cast<const uint32_t*>(d + o_s8);
+  out->bytes8 = reinterpret_cast<const uint32_t*>(d + o_b8);
   out->counters = reinterpret_cast<uint32_t*>(d + o_cnt);
   out->partial = reinterpret_cast<float*>(d + o_part);
   out->n_ctas = p.n_ctas;

@@ -50,21 +50,54 @@ int32_t plan_ctas(uint64_t total_bytes, int sms);
 // path dequantizes one column of a tile at a time).
 Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units, bool whole_columns = false);
 
-// A plan's device copy: units, slices and CTA table, arrival counters (zeroed)
-// and partial rows for up to max_nb batch columns, in one allocation.
+// What each warp copies, in order: for CTA c and warp w of a W-warp CTA, the
+// byte ranges of its slices of every unit (and, for a program of several
+// launches, of every launch in turn). A piece is (address >> 4) << 20 | (bytes >> 4).
+struct PieceSet {
+  std::vector<uint64_t> pieces;
+  std::vector<uint32_t> start;  // [n_ctas * W + 1]: first piece of each warp
+  std::vector<uint32_t> bytes;  // [n_ctas * W]: bytes each warp copies
+};
+inline uint64_t make_piece(const uint8_t* addr, uint64_t bytes) {
+  return ((reinterpret_cast<uint64_t>(addr) >> 4) << 20) | (bytes >> 4);
+}
+// Whether (addr, bytes) survives that encoding: 16-byte aligned, addr below
+// 2^48 and bytes below 16 MiB.
+inline bool piece_fits(const uint8_t* addr, uint64_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(addr);
+  return (a & 15u) == 0 && (bytes & 15u) == 0 && a < (uint64_t(1) << 48) && bytes < (uint64_t(1) << 24);
+}
+// Appends, for each (CTA, warp), the pieces of plan p over segments whose data
+// bases are seg_data. With W = 8 a warp takes the plan's slices 2w and 2w+1.
+// Returns false if a piece does not fit the encoding (piece_fits).
+bool append_pieces(const Plan& p, const std::vector<const uint8_t*>& seg_data, int W,
+                   std::vector<std::vector<uint64_t>>* per_warp);
+PieceSet finish_pieces(const std::vector<std::vector<uint64_t>>& per_warp);
+
+// A plan's device copy: units, slices, arrival counters (zeroed) and partial
+// rows for up to max_nb batch columns, plus the piece lists of the 16-warp and
+// 8-warp kernels, in one allocation.
 struct DevicePlan {
   void* base = nullptr;
   const UnitRec* units = nullptr;
   const SliceRec* slices = nullptr;
   uint32_t* counters = nullptr;
   float* partial = nullptr;
+  const uint64_t* pieces16 = nullptr;
+  const uint32_t* start16 = nullptr;
+  const uint32_t* bytes16 = nullptr;
+  const uint64_t* pieces8 = nullptr;
+  const uint32_t* start8 = nullptr;
+  const uint32_t* bytes8 = nullptr;
   int32_t n_ctas = 0;
   int32_t umax = 0;
   int64_t bytes = 0;
 };
 
-// Allocates and uploads (synchronously on stream). Returns cudaSuccess or the error.
-cudaError_t upload_plan(const Plan& p, int max_nb, cudaStream_t stream, DevicePlan* out);
+// Allocates and uploads (synchronously on stream). seg_data are the device
+// bases of the plan's segments (for the piece lists). Returns cudaSuccess or the error.
+cudaError_t upload_plan(const Plan& p, int max_nb, const std::vector<const uint8_t*>& seg_data,
+                        cudaStream_t stream, DevicePlan* out);
 void free_plan(DevicePlan* p);
 
 }  // namespace vbq

@@ -9,13 +9,16 @@
 namespace vbq {
 
 // Bounded mbarrier waits: each try_wait may suspend for up to kTryWaitNs, and a
-// wait gives up after kMaxTries of them (several seconds in total).
+// wait gives up after kMaxTries of them (about a second in total).
 constexpr uint32_t kTryWaitNs = 1000000;   // 1 ms hint per try
-constexpr uint32_t kMaxTries = 4000;       // ~4 s worst case
+constexpr uint32_t kMaxTries = 1000;       // ~1 s worst case
+// Spin limit, in SM clock cycles, of the waits on counters in memory (~1 s).
+constexpr long long kSpinCycles = 2000000000LL;
 
 // Codes written to the device check word.
 constexpr int kErrRingTimeout = 1;
 constexpr int kErrMmaTimeout = 2;
+constexpr int kErrGridTimeout = 3;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

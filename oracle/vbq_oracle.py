@@ -14,8 +14,8 @@ What it follows:
   grid is the one this project fixes: w = s_g * (q - (2^b_g - 1)/2). Here s_g is
   an fp16 scale and q is an unsigned code in [0, 2^b_g - 1]. Group g of row r
   covers columns [64g, 64g + 63].
-* The projections of one decode step follow the same abstract ("autoregressive
-  decode"). The pages give no architecture, so the glue between projections is
+* The projections of one decode step follow the same abstract (token-by-token
+  decode). The pages give no architecture, so the glue between projections is
   this project's reading:
   - unit-gamma RMSNorm with eps 1e-5;
   - attention at position 0, where a softmax over one key is 1, so each head

@@ -132,6 +132,11 @@ static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::ve
     const uint32_t u0 = static_cast<uint32_t>(c) * pl.umax, u1 = u0 + nu;
     for (int w = 0; w < W; ++w) {
       uint64_t stream = 0;  // bytes this warp copies, in order
+      // The warp's piece list: one piece per unit with a non-empty slice, in unit order.
+      const uint64_t* pieces = W == 16 ? dp.pieces16 : dp.pieces8;
+      const uint32_t* pstart = W == 16 ? dp.start16 : dp.start8;
+      const uint32_t* pbytes = W == 16 ? dp.bytes16 : dp.bytes8;
+      uint32_t pi = pstart[c * W + w];
       for (uint32_t u = u0; u < u1; ++u) {
         const UnitRec ur = dp.units[u];
         CHECK(ur.seg < mats.size(), "unit seg");
@@ -155,6 +160,12 @@ static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::ve
         }
         const uint64_t b0 = uint64_t(f.b0) * 16, b1 = uint64_t(l.b1) * 16;
         CHECK(b1 >= b0, "slice bytes");
+        if (b1 > b0) {
+          CHECK(pi < pstart[c * W + w + 1], "CTA %d warp %d: too few pieces", c, w);
+          const uint64_t q = pieces[pi++];
+          CHECK(((q >> 20) << 4) == reinterpret_cast<uint64_t>(M->data + b0), "piece address");
+          CHECK(((q & 0xFFFFFu) << 4) == b1 - b0, "piece length");
+        }
         {  // the first group column the kernel prefetches
           const uint32_t g0 = (SPW > 1 && f.b1 == f.b0) ? l.g0 : f.g0;
           if (b1 > b0) {
@@ -216,7 +227,8 @@ static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::ve
               static_cast<unsigned long long>(b1));
         stream += b1 - b0;
       }
-      (void)stream;
+      CHECK(pi == pstart[c * W + w + 1], "CTA %d warp %d: extra pieces", c, w);
+      CHECK(pbytes[c * W + w] == stream, "CTA %d warp %d: piece bytes", c, w);
     }
   }
   for (size_t s = 0; s < mats.size(); ++s)
@@ -267,7 +279,7 @@ int main() {
     for (int P : {1, 148}) {
       Plan pc = make_plan({seg_tables(m)}, P, MAX_UNITS_PER_CTA, true);
       DevicePlan dc;
-      CHECK(upload_plan(pc, 64, nullptr, &dc) == cudaSuccess, "upload");
+      CHECK(upload_plan(pc, 64, {m->data}, nullptr, &dc) == cudaSuccess, "upload");
       check_plan({m}, {&L}, pc, dc, 16, /*balance=*/false);  // cuts fall only on column starts
       for (size_t u = 0; u < pc.units.size(); ++u) {
         if (pc.units[u].nsplit == 0) continue;
@@ -287,7 +299,7 @@ int main() {
     for (int P : {1, 7, 148, 600}) {
       Plan p2 = make_plan({seg_tables(m)}, P, MAX_UNITS_PER_CTA);
       DevicePlan d2;
-      CHECK(upload_plan(p2, 4, nullptr, &d2) == cudaSuccess, "upload");
+      CHECK(upload_plan(p2, 4, {m->data}, nullptr, &d2) == cudaSuccess, "upload");
       check_plan({m}, {&L}, p2, d2, 16);
       free_plan(&d2);
     }
@@ -301,7 +313,7 @@ int main() {
     for (int P : {1, 5, 148}) {
       Plan p = make_plan(segs, P, MAX_UNITS_PER_CTA);
       DevicePlan d;
-      CHECK(upload_plan(p, 1, nullptr, &d) == cudaSuccess, "upload");
+      CHECK(upload_plan(p, 1, {ms[0]->data, ms[1]->data, ms[2]->data}, nullptr, &d) == cudaSuccess, "upload");
       check_plan(ms, ls, p, d, 16);
       free_plan(&d);
     }

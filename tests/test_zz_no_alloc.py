@@ -3,7 +3,7 @@
 vbq_decode_step_noalloc is for callers that may not allocate device memory at
 step time (for example while another component captures the stream into a CUDA
 graph). It keeps its activations in a static device array instead of the model's
-workspace and launches without a graph. This file is named so that pytest
+workspace. This file is named so that pytest
 collects it last: if it fails, a run that stops at the first failure has
 already run every other test.
 """
@@ -65,8 +65,10 @@ def test_noalloc_step_matches_decode_step_twice(V):
 def test_noalloc_step_rejects_models_over_the_scratch_limit(V):
     import dataclasses
     import torch
-    big = dataclasses.replace(model_tiny(), name="wide-ffn", n_layers=1, d=64, n_heads=1, n_kv_heads=1,
-                              head_dim=64, d_ff=131072, vocab=64)
+    # 64 + 64 + 3*16384 ([q;k;v]) + 2*16384 ([gate;up]) = 82,048 floats > 65,536, with every
+    # dimension within the decode kernel's limit of 16384 and every matrix small.
+    big = dataclasses.replace(model_tiny(), name="wide", n_layers=1, d=64, n_heads=128, n_kv_heads=128,
+                              head_dim=128, d_ff=16384, vocab=64)
     mats, handles, model = _build(V, big, seed=3)
     x = dev_u16(gen_x(big.d, seed=4))
     out = torch.zeros(big.vocab, device="cuda")
