@@ -52,9 +52,13 @@ constexpr int CH = 4096;             // bytes per bulk copy and per ring slot
 constexpr int LOG_CH = 12;
 constexpr int SPILL = 512;           // bytes past the ring's end (>= the largest record, 352 B)
 constexpr int XPF = 144;             // floats of activation prep per (warp, column)
-constexpr int XP_X = 0, XP_8 = 64, XC_8 = 128;  // x (64), 2^15 x (64), 8-bit slice constants (8)
+// Prep block: x (64), 2^15 x (64) and the 8-bit slice constants (8). 2^15 x is
+// stored so that the 8 slices of 8 codes read 128 contiguous bytes per half:
+// x'_{8s+t} sits at XP_8 + 4s + t for t < 4 and at XP_8 + 32 + 4s + t - 4 after.
+constexpr int XP_X = 0, XP_8 = 64, XC_8 = 128;
 constexpr int NLUT = 13;             // 5-bit lookup tables per group (the last covers 4 codes)
 constexpr int MAX_SEG = 3;
+constexpr uint32_t kNoRefill = 0xFFFFFFFFu;  // WarpStream::refill_at once every chunk is issued
 constexpr int XCAP = 16384;          // largest K the decode kernel stages in shared memory
 
 enum XMode : int { X_BF16 = 0, X_RMSNORM = 1, X_GQA = 2, X_SWIGLU = 3 };
@@ -202,7 +206,10 @@ __device__ __forceinline__ void build_prep(uint32_t xp, float x0, float x1, int 
                                            float (&lut)[NLUT]) {
   sts(xp + (XP_X + 2 * lane) * 4, make_float2(x0, x1));
   const float p0 = x0 * 32768.0f, p1 = x1 * 32768.0f;
-  sts(xp + (XP_8 + 2 * lane) * 4, make_float2(p0, p1));
+  {
+    const int s8 = lane >> 2, t8 = 2 * (lane & 3);  // x_{2l} = x_{8 s8 + t8}
+    sts(xp + (XP_8 + (t8 < 4 ? 4 * s8 + t8 : 32 + 4 * s8 + t8 - 4)) * 4, make_float2(p0, p1));
+  }
   float c8 = (p0 + p1) + 127.5f * (x0 + x1);
   c8 += __shfl_xor_sync(0xffffffffu, c8, 1);
   c8 += __shfl_xor_sync(0xffffffffu, c8, 2);
@@ -248,11 +255,11 @@ __device__ __forceinline__ void decode_bytes(uint2 cw, uint32_t xp, uint32_t sig
     fv[i] = __uint_as_float(__byte_perm(cw.x, 0x3F800000u, 0x7604u | (i << 4)));
     fv[4 + i] = __uint_as_float(__byte_perm(cw.y, 0x3F800000u, 0x7604u | (i << 4)));
   }
-  const uint32_t xs = xp + (XP_8 + 8 * sigma) * 4;
+  const uint32_t xs = xp + (XP_8 + 4 * sigma) * 4;
 #pragma unroll
   for (int c = 0; c < NB; ++c) {
     const float4 xa = lds<float4>(xs + c * XPF * 4);
-    const float4 xb = lds<float4>(xs + c * XPF * 4 + 16);
+    const float4 xb = lds<float4>(xs + c * XPF * 4 + 128);
     float2 acc = make_float2(0.0f, 0.0f);
     acc = __ffma2_rn(make_float2(xa.x, xa.y), make_float2(fv[0], fv[1]), acc);
     acc = __ffma2_rn(make_float2(xa.z, xa.w), make_float2(fv[2], fv[3]), acc);
@@ -262,17 +269,23 @@ __device__ __forceinline__ void decode_bytes(uint2 cw, uint32_t xp, uint32_t sig
   }
 }
 
-// One step of class CLS with e entries whose record starts at shared offset rb.
-// pw = 2^(plane) for the lane's plane (classes 1 and 2).
+// acc[row] += v in shared memory when p: a predicated load, add and store.
+// Not atomic, and it need not be: a warp's accumulators are its own, and the
+// entries of one group column have distinct rows, so no two lanes of one
+// instruction, nor two steps in flight, touch the same row. (A shared-memory
+// fp32 atomic add is a compare-and-swap loop on this GPU.)
+__device__ __forceinline__ void acc_add_if(uint32_t addr, float v, bool p) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t.reg .f32 t;\n\tsetp.ne.u32 q, %2, 0;\n\t"
+      "@q ld.shared.f32 t, [%0];\n\t@q add.f32 t, t, %1;\n\t@q st.shared.f32 [%0], t;\n\t}" ::"r"(addr),
+      "f"(v), "r"(static_cast<uint32_t>(p)));
+}
+
+// Decodes one step of class CLS from its code words and reduces each entry's
+// lanes: on return, lane sigma == 0 of entry j holds the entry's dot products.
 template <int NB, int CLS>
-__device__ __forceinline__ void do_step(uint32_t rb, uint32_t e, uint32_t xp, uint32_t acc, int lane,
-                                        const float (&lut)[NB][NLUT], float pw) {
-  const uint32_t j = static_cast<uint32_t>(lane) >> CLS;
-  const uint32_t sigma = static_cast<uint32_t>(lane) & ((1u << CLS) - 1u);
-  const bool active = j < e;
-  uint2 cw = make_uint2(0u, 0u);
-  if (active) cw = lds<uint2>(rb + 8u * lane);
-  float tv[NB];
+__device__ __forceinline__ void step_dot(uint2 cw, uint32_t xp, uint32_t sigma, const float (&lut)[NB][NLUT],
+                                         float pw, float (&tv)[NB]) {
   if (CLS == 3) {
     decode_bytes<NB>(cw, xp, sigma, tv);
   } else {
@@ -287,14 +300,36 @@ __device__ __forceinline__ void do_step(uint32_t rb, uint32_t e, uint32_t xp, ui
 #pragma unroll
     for (int c = 0; c < NB; ++c) tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], d);
   }
-  if (active && sigma == 0) {
-    const uint16_t sb = lds<uint16_t>(rb + rec_scale_off(CLS, e) + 2u * j);
-    const uint32_t row = lds<uint8_t>(rb + rec_row_off(CLS, e) + j);
-    const float sc = __half2float(__ushort_as_half(sb));
+}
+
+// U consecutive steps of class CLS, the first at shared offset rb[0], each
+// with e entries (e < entries_per_step only for a run's last step). Every lane
+// loads and decodes; lanes past the last entry, and all but the first lane of
+// an entry, add nothing. The loads of all U steps are issued first.
+template <int NB, int CLS, int U>
+__device__ __forceinline__ void do_steps(const uint32_t (&rb)[U], uint32_t e, uint32_t xp, uint32_t acc,
+                                         uint32_t acc_a, int lane, const float (&lut)[NB][NLUT], float pw) {
+  const uint32_t j = static_cast<uint32_t>(lane) >> CLS;
+  const uint32_t sigma = static_cast<uint32_t>(lane) & ((1u << CLS) - 1u);
+  const bool add = j < e && sigma == 0;
+  uint2 cw[U];
+  uint32_t sb[U], row[U];
 #pragma unroll
-    for (int c = 0; c < NB; ++c)
-      atomicAdd(reinterpret_cast<float*>(vbq_smem + acc + (c * TILE_MAX + row) * 4), sc * tv[c]);
+  for (int u = 0; u < U; ++u) {
+    cw[u] = lds<uint2>(rb[u] + 8u * lane);
+    sb[u] = lds<uint16_t>(rb[u] + rec_scale_off(CLS, e) + 2u * j);
+    row[u] = lds<uint8_t>(rb[u] + rec_row_off(CLS, e) + j);
   }
+  float tv[U][NB];
+#pragma unroll
+  for (int u = 0; u < U; ++u) step_dot<NB, CLS>(cw[u], xp, sigma, lut, pw, tv[u]);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(sb[u])));
+#pragma unroll
+    for (int c = 0; c < NB; ++c) acc_add_if(acc_a + (c * TILE_MAX + row[u]) * 4, sc * tv[u][c], add);
+  }
+  (void)acc;
 }
 
 // Stages the x of a decode item in shared memory at sx as the bf16 values the
@@ -431,7 +466,7 @@ struct WarpStream {
     L = bytes;
     nch = (bytes + CH - 1) >> LOG_CH;
     issued = landed = avail = 0;
-    refill_at = 0xFFFFFFFFu;
+    refill_at = kNoRefill;
     pieces = list;
     npieces = n;
     pi = ppos = 0;
@@ -478,7 +513,7 @@ struct WarpStream {
       }
     }
     ++issued;
-    refill_at = issued < nch ? (issued + 1 - NSLOT) * CH : 0xFFFFFFFFu;
+    refill_at = issued < nch ? (issued + 1 - NSLOT) * CH : kNoRefill;
   }
 
   __device__ __forceinline__ void start(int lane) {
@@ -649,21 +684,39 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
     cur_g = g;
   };
 
-  // Steps [k, kend) of a run of class CLS with n entries.
+  // Steps [k, kend) of a run of class CLS with n entries. Full steps go in
+  // blocks that need no check inside: every step of a block has landed, and
+  // the block ends where the consumed bytes free a ring slot. Within a block,
+  // steps go in pairs, so two independent decodes are in flight.
   auto run_steps = [&](auto cls_tag, uint32_t k, uint32_t kend, uint32_t n) {
     constexpr int CLS = decltype(cls_tag)::value;
     constexpr uint32_t EPS = entries_per_step(CLS);
     constexpr uint32_t FULL = full_step_bytes(CLS);
     const float pw = CLS == 1 ? K.pw2 : K.pw4;
+    const uint32_t acc_a = smem_u32(vbq_smem) + acc;
     const uint32_t kfull = min(kend, n / EPS);
-    for (; k < kfull; ++k) {
-      const uint32_t o1 = K.o + FULL;
-      if (S.avail < o1) {
-        S.wait_for(o1);
+    while (k < kfull) {
+      if (S.avail < K.o + FULL) {
+        S.wait_for(K.o + FULL);
         if (!S.ok) return;
       }
-      do_step<NB, CLS>(S.ring + (K.o & RMASK), EPS, K.xp, acc, lane, K.lut, pw);
-      K.o = o1;
+      uint32_t nb = min(kfull - k, (S.avail - K.o) / FULL);
+      if (S.refill_at != kNoRefill) nb = min(nb, (S.refill_at - K.o + FULL - 1u) / FULL);
+      if (nb == 0u) {  // cannot happen: refill_at > K.o here; never spin without progress
+        S.ok = false;
+        return;
+      }
+      k += nb;
+      for (; nb >= 2u; nb -= 2u) {
+        const uint32_t rb[2] = {S.ring + (K.o & RMASK), S.ring + ((K.o + FULL) & RMASK)};
+        do_steps<NB, CLS, 2>(rb, EPS, K.xp, acc, acc_a, lane, K.lut, pw);
+        K.o += 2u * FULL;
+      }
+      if (nb) {
+        const uint32_t rb[1] = {S.ring + (K.o & RMASK)};
+        do_steps<NB, CLS, 1>(rb, EPS, K.xp, acc, acc_a, lane, K.lut, pw);
+        K.o += FULL;
+      }
       S.refill(K.o, lane);
     }
     if (k < kend) {  // the run's last, partial step
@@ -673,7 +726,8 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
         S.wait_for(o1);
         if (!S.ok) return;
       }
-      do_step<NB, CLS>(S.ring + (K.o & RMASK), e, K.xp, acc, lane, K.lut, pw);
+      const uint32_t rb[1] = {S.ring + (K.o & RMASK)};
+      do_steps<NB, CLS, 1>(rb, e, K.xp, acc, acc_a, lane, K.lut, pw);
       K.o = o1;
       S.refill(K.o, lane);
     }
@@ -720,7 +774,7 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
       const uint32_t d = __shfl_sync(0xffffffffu, dcur, run - dbase);
       const int g = static_cast<int>(run_g(d));
       const uint32_t cls = run_cls(d), n = run_n(d);
-      const uint32_t kend = (run == run1) ? k1 : (n + entries_per_step(cls) - 1u) / entries_per_step(cls);
+      const uint32_t kend = (run == run1) ? k1 : (n + entries_per_step(cls) - 1u) >> (LOG_STEP_LANES - cls);
       if (g != cur_g) prep_for(g);
       switch (cls) {
         case 0: run_steps(std::integral_constant<int, 0>{}, k, kend, n); break;

@@ -43,6 +43,7 @@ namespace vbq {
 constexpr int GROUP = 64;
 constexpr int TILE_MAX = 256;      // a row index in a tile fits one byte
 constexpr int STEP_LANES = 32;
+constexpr int LOG_STEP_LANES = 5;
 constexpr int LANE_BYTES = 8;      // code bytes per lane per step
 constexpr int MAX_G = 65535;       // group column fits 16 bits
 
