@@ -96,6 +96,20 @@ struct XSource {
   uint16_t* trace_x;  // optional: CTA 0 writes the bf16 x it used ([K])
 };
 
+// A range of floats to clear: ptr + off .. + n (ptr null: the launch's output).
+struct ZeroSpec {
+  float* ptr;
+  int64_t off;
+  int32_t n;
+};
+
+// A copy of n floats (the decode-step trace of a finished item's output).
+struct CopySpec {
+  const float* src;
+  float* dst;
+  int32_t n;
+};
+
 // One GEMV over one or more matrices (a "launch item").
 struct Item {
   MatView seg[MAX_SEG];
@@ -104,6 +118,8 @@ struct Item {
   XSource xs;
   int32_t ep;
   const float* resid;  // EP_RESID: y = resid + acc (may alias seg[0].y)
+  ZeroSpec zero;       // decode kernel: output of the item two later, cleared while this one runs
+  CopySpec tcopy;      // decode kernel: trace copy of the previous item's output (trace mode)
 };
 
 // A single-item launch: the item plus this plan's per-warp piece lists.
@@ -147,7 +163,9 @@ __device__ __forceinline__ void sts(uint32_t off, T v) {
 
 // ---- activation values ---------------------------------------------------
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and division: a few
+// 1e-7 of relative error, far below the bf16 rounding that follows.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // The inputs from which x[k], x[k+1] (k even) of column col are made.
 struct XRaw {
@@ -787,7 +805,10 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
     // ---- unit epilogue: the last warp to finish sums the warps in fixed order ----
     // Every global load of the epilogue is issued before the values are used:
     // it runs while the other SMs stream at full rate, when an L2 round trip
-    // takes about a microsecond.
+    // takes about a microsecond. In the decode kernel the CTA's last unit of
+    // the item is summed after the loop by all warps at once instead, so that
+    // no single warp adds the whole tile at the end of the item.
+    if (STAGED && ui == nu - 1) continue;
     __syncwarp();
     __threadfence_block();
     uint32_t arrived = 0;
@@ -795,7 +816,10 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
     arrived = __shfl_sync(0xffffffffu, arrived, 0);
     if (arrived % W == W - 1) {
       __threadfence_block();
-      constexpr int RPL = TILE_MAX / 32;  // rows per lane: lane + 32 j
+      // Rows per lane: 4 lane + j and 128 + 4 lane + j - 4 (j < 8), so that the
+      // warp sums read the accumulators 16 bytes at a time without bank conflicts.
+      constexpr int RPL = TILE_MAX / 32;
+      static_assert(RPL == 8, "the row mapping assumes 256-row tiles");
       const uint32_t split = __shfl_sync(0xffffffffu, ur.split, ui);
       const uint32_t nsplit = __shfl_sync(0xffffffffu, ur.nsplit, ui);
       const uint32_t r0 = __shfl_sync(0xffffffffu, ur.r0, ui);
@@ -804,90 +828,149 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
       const uint32_t accp = Lay::kAcc + par * Lay::kAccParity;
       float v[NB][RPL];
 #pragma unroll
-      for (int j = 0; j < RPL; ++j) {
-        const uint32_t r = lane + 32u * j;
+      for (int c = 0; c < NB; ++c) {
 #pragma unroll
-        for (int c = 0; c < NB; ++c) {
-          float t = 0.0f;
-          if (r < rows) {
+        for (int j = 0; j < RPL; ++j) v[c][j] = 0.0f;
 #pragma unroll
-            for (int w = 0; w < W; ++w) t += lds<float>(accp + ((w * NB + c) * TILE_MAX + r) * 4);
-          }
-          v[c][j] = t;
+        for (int w = 0; w < W; ++w) {  // in warp order
+          const uint32_t base = accp + ((w * NB + c) * TILE_MAX + 4u * lane) * 4;
+          const float4 lo = lds<float4>(base), hi = lds<float4>(base + 128 * 4);
+          v[c][0] += lo.x; v[c][1] += lo.y; v[c][2] += lo.z; v[c][3] += lo.w;
+          v[c][4] += hi.x; v[c][5] += hi.y; v[c][6] += hi.z; v[c][7] += hi.w;
         }
       }
-      bool mine = true;  // this warp writes the rows
-      if (nsplit > 1u) {
-        const uint32_t pb = __shfl_sync(0xffffffffu, ur.pbase, ui);
-        const uint32_t cnt = __shfl_sync(0xffffffffu, ur.cnt, ui);
-        float* part = it.plan.partial + static_cast<size_t>(pb) * NB;
-#pragma unroll
-        for (int j = 0; j < RPL; ++j) {
-          const uint32_t r = lane + 32u * j;
-#pragma unroll
-          for (int c = 0; c < NB; ++c)
-            if (r < rows) part[(split * NB + c) * rows + r] = v[c][j];
-        }
-        __threadfence();
-        __syncwarp();
-        uint32_t prev = 0;
-        if (lane == 0) prev = atomicAdd(it.plan.counters + cnt, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        mine = prev == nsplit - 1u;
-        if (mine) {  // the last split to arrive adds all of them, in split order
-          __threadfence();
-          constexpr int SB = NB == 1 ? 4 : 1;  // splits whose loads are in flight together
-#pragma unroll
-          for (int j = 0; j < RPL; ++j)
-#pragma unroll
-            for (int c = 0; c < NB; ++c) v[c][j] = 0.0f;
-          for (uint32_t s0 = 0; s0 < nsplit; s0 += SB) {
-            float a[SB][NB][RPL];
-#pragma unroll
-            for (int q = 0; q < SB; ++q)
-#pragma unroll
-              for (int j = 0; j < RPL; ++j) {
-                const uint32_t r = lane + 32u * j;
-#pragma unroll
-                for (int c = 0; c < NB; ++c)
-                  a[q][c][j] = (s0 + q < nsplit && r < rows) ? __ldcg(part + ((s0 + q) * NB + c) * rows + r) : 0.0f;
-              }
-#pragma unroll
-            for (int q = 0; q < SB; ++q)
-#pragma unroll
-              for (int j = 0; j < RPL; ++j)
-#pragma unroll
-                for (int c = 0; c < NB; ++c)
-                  if (s0 + q < nsplit) v[c][j] += a[q][c][j];
-          }
-          if (lane == 0) it.plan.counters[cnt] = 0u;
-        }
-      }
-      if (mine) {
+      // The accumulators are read: let the next unit of this parity have them
+      // before any global write (a fence here would wait for those too).
+      __syncwarp();
+      __threadfence_block();
+      if (lane == 0) atomicAdd(ucount + 2 + par, 1u);
+      if constexpr (STAGED) {
+        // Decode kernel: a whole tile stores its rows, or adds them onto the
+        // residual; each split of a tile adds its partial rows into y, which
+        // was cleared two items earlier. The adds are fire-and-forget, and the
+        // grid barrier after the item makes them visible. The order of the
+        // adds of a split tile's partials is not fixed, so those rows can
+        // differ in the last bits from one step to the next. (A traced output
+        // is added up the same way when the item adds onto the residual, and
+        // copied from y by the next item otherwise.)
         float* const ybase = M.y ? M.y : out + M.y_off;
-        float rv[RPL];
+        const bool add = nsplit > 1u || it.ep == EP_RESID;
 #pragma unroll
         for (int j = 0; j < RPL; ++j) {
-          const uint32_t r = lane + 32u * j;
-          rv[j] = (it.ep == EP_RESID && r < rows) ? __ldcg(it.resid + r0 + r) : 0.0f;
-        }
-#pragma unroll
-        for (int j = 0; j < RPL; ++j) {
-          const uint32_t r = lane + 32u * j;
+          const uint32_t r = (j < 4 ? 4u * lane : 124u + 4u * lane) + j;
           if (r < rows) {
+            const float t = v[0][j];
+            if (M.trace_y) red_add_f32(M.trace_y + r0 + r, t);
+            if (add) {
+              red_add_f32(ybase + r0 + r, t);
+            } else {
+              ybase[r0 + r] = t;
+            }
+          }
+        }
+      } else {
+        bool mine = true;  // this warp writes the rows
+        if (nsplit > 1u) {
+          const uint32_t pb = __shfl_sync(0xffffffffu, ur.pbase, ui);
+          const uint32_t cnt = __shfl_sync(0xffffffffu, ur.cnt, ui);
+          float* part = it.plan.partial + static_cast<size_t>(pb) * NB;
 #pragma unroll
-            for (int c = 0; c < NB; ++c) {
-              float t = v[c][j];
-              if (c == 0 && M.trace_y) M.trace_y[r0 + r] = t;
-              if (it.ep == EP_RESID) t += rv[j];
-              ybase[static_cast<int64_t>(c) * M.y_ld + r0 + r] = t;
+          for (int j = 0; j < RPL; ++j) {
+            const uint32_t r = (j < 4 ? 4u * lane : 124u + 4u * lane) + j;
+#pragma unroll
+            for (int c = 0; c < NB; ++c)
+              if (r < rows) part[(split * NB + c) * rows + r] = v[c][j];
+          }
+          __threadfence();
+          __syncwarp();
+          uint32_t prev = 0;
+          if (lane == 0) prev = atomicAdd(it.plan.counters + cnt, 1u);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          mine = prev == nsplit - 1u;
+          if (mine) {  // the last split to arrive adds all of them, in split order
+            __threadfence();
+            constexpr int SB = NB == 1 ? 4 : 1;  // splits whose loads are in flight together
+#pragma unroll
+            for (int j = 0; j < RPL; ++j)
+#pragma unroll
+              for (int c = 0; c < NB; ++c) v[c][j] = 0.0f;
+            for (uint32_t s0 = 0; s0 < nsplit; s0 += SB) {
+              float a[SB][NB][RPL];
+#pragma unroll
+              for (int q = 0; q < SB; ++q)
+#pragma unroll
+                for (int j = 0; j < RPL; ++j) {
+                  const uint32_t r = (j < 4 ? 4u * lane : 124u + 4u * lane) + j;
+#pragma unroll
+                  for (int c = 0; c < NB; ++c)
+                    a[q][c][j] = (s0 + q < nsplit && r < rows) ? __ldcg(part + ((s0 + q) * NB + c) * rows + r) : 0.0f;
+                }
+#pragma unroll
+              for (int q = 0; q < SB; ++q)
+#pragma unroll
+                for (int j = 0; j < RPL; ++j)
+#pragma unroll
+                  for (int c = 0; c < NB; ++c)
+                    if (s0 + q < nsplit) v[c][j] += a[q][c][j];
+            }
+            if (lane == 0) it.plan.counters[cnt] = 0u;
+          }
+        }
+        if (mine) {
+          float* const ybase = M.y ? M.y : out + M.y_off;
+          float rv[RPL];
+#pragma unroll
+          for (int j = 0; j < RPL; ++j) {
+            const uint32_t r = (j < 4 ? 4u * lane : 124u + 4u * lane) + j;
+            rv[j] = (it.ep == EP_RESID && r < rows) ? __ldcg(it.resid + r0 + r) : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < RPL; ++j) {
+            const uint32_t r = (j < 4 ? 4u * lane : 124u + 4u * lane) + j;
+            if (r < rows) {
+#pragma unroll
+              for (int c = 0; c < NB; ++c) {
+                float t = v[c][j];
+                if (c == 0 && M.trace_y) M.trace_y[r0 + r] = t;
+                if (it.ep == EP_RESID) t += rv[j];
+                ybase[static_cast<int64_t>(c) * M.y_ld + r0 + r] = t;
+              }
             }
           }
         }
       }
-      __syncwarp();
-      __threadfence_block();
-      if (lane == 0) atomicAdd(ucount + 2 + par, 1u);
+    }
+  }
+  if constexpr (STAGED) {
+    // The CTA's last unit of the item: warp w sums rows 16 w .. 16 w + 15 over
+    // the warps' accumulators, in warp order.
+    static_assert(!STAGED || W * 16 == TILE_MAX, "one warp per 16 rows");
+    __syncthreads();
+    if (nu > 0) {
+      const int ui = nu - 1;
+      const uint32_t par = (K.gunit - 1u) & 1u;
+      const uint32_t seg = __shfl_sync(0xffffffffu, ur.seg, ui);
+      const uint32_t nsplit = __shfl_sync(0xffffffffu, ur.nsplit, ui);
+      const uint32_t r0 = __shfl_sync(0xffffffffu, ur.r0, ui);
+      const uint32_t rows = __shfl_sync(0xffffffffu, ur.rows, ui);
+      const MatView& M = it.seg[seg];
+      const uint32_t accp = Lay::kAcc + par * Lay::kAccParity;
+      const uint32_t r = 16u * warp + (lane & 15);
+      float t = 0.0f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) t += lds<float>(accp + (w * TILE_MAX + r) * 4);
+      // (The next unit of this parity starts after the grid barrier, which
+      // orders these reads before its writes; the count only keeps the tally.)
+      if (threadIdx.x == 0) atomicAdd(ucount + 2 + par, 1u);
+      if (lane < 16 && r < rows) {
+        float* const ybase = M.y ? M.y : out + M.y_off;
+        if (M.trace_y) red_add_f32(M.trace_y + r0 + r, t);
+        if (nsplit > 1u || it.ep == EP_RESID) {
+          red_add_f32(ybase + r0 + r, t);
+        } else {
+          ybase[r0 + r] = t;
+        }
+      }
     }
   }
 }
@@ -953,6 +1036,7 @@ struct Program {
   const uint32_t* pbytes;
   float* h;                 // h = x is written before the first item
   int32_t d;
+  ZeroSpec pre[2];          // outputs of the first two items, cleared before the first barrier
   uint32_t* grid_bar;       // [0]: barrier arrivals, [1]: CTAs done; both zero at launch, and reset at exit
   int* err;
 };
@@ -962,6 +1046,20 @@ struct DecodeArgs {
   const uint16_t* x;
   float* out;
 };
+
+// All threads of the grid copy one range.
+__device__ __forceinline__ void grid_copy(const CopySpec& c) {
+  if (c.n <= 0) return;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < c.n; i += gridDim.x * blockDim.x)
+    c.dst[i] = __ldcg(c.src + i);
+}
+
+// All threads of the grid clear one range.
+__device__ __forceinline__ void grid_zero(const ZeroSpec& z, float* out) {
+  if (z.n <= 0) return;
+  float* p = (z.ptr ? z.ptr : out) + z.off;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < z.n; i += gridDim.x * blockDim.x) p[i] = 0.0f;
+}
 
 // Grid barrier number k (0-based) of this launch. Bounded: on a timeout it
 // records kErrGridTimeout and lets the CTA go on; once any wait has recorded
@@ -998,12 +1096,16 @@ __global__ void __launch_bounds__(W * 32, 1) vbq_decode_kernel(const __grid_cons
   Worker<1> K;
   UnitRegs ur = load_units<W>(P.items[0].plan, warp, lane);
   worker_init<1, W, NSLOT>(S, K, P.pieces, P.pstart, P.pbytes, lane, warp);
-  // h = x (bf16 -> fp32)
+  // h = x (bf16 -> fp32); the outputs that the first two items add into start at zero.
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < P.d; i += gridDim.x * blockDim.x)
     P.h[i] = __uint_as_float(static_cast<uint32_t>(a.x[i]) << 16);
+  grid_zero(P.pre[0], a.out);
+  grid_zero(P.pre[1], a.out);
   grid_barrier(P.grid_bar, 0, P.err);
   for (int i = 0; i < P.n_items; ++i) {
     const Item& it = P.items[i];
+    grid_zero(it.zero, a.out);
+    grid_copy(it.tcopy);
     run_item<1, W, NSLOT, true>(it, ur, S, K, a.out, a.x, lane, warp);
     if (i + 1 < P.n_items) {
       ur = load_units<W>(P.items[i + 1].plan, warp, lane);  // in flight across the barrier

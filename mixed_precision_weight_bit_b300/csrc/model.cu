@@ -97,6 +97,7 @@ struct vbq_model {
   const uint32_t* pbytes = nullptr;
   Item* items_ws = nullptr;         // items over ws
   Item* items_static = nullptr;     // items over the static scratch (null if the model does not fit it)
+  ZeroSpec pre_ws[2] = {}, pre_static[2] = {};  // what each program clears before its first barrier
   float* static_base = nullptr;
   int32_t n_items = 0;
   int* err = nullptr;               // the device check word of the model's device
@@ -108,8 +109,11 @@ namespace {
 vbq_status step_scratch_address(int dev, float** out);
 constexpr int64_t kStepScratchFloats = 65536;
 
-// The items of one step over the scratch at `base`.
-std::vector<Item> make_items(const vbq_model* m, float* base, bool trace) {
+// The items of one step over the scratch at `base`. Each item clears the
+// output of the item two after it (the outputs that split tiles add into);
+// pre receives the outputs of the first two items, cleared before the first
+// grid barrier.
+std::vector<Item> make_items(const vbq_model* m, float* base, bool trace, ZeroSpec pre[2]) {
   const vbq_model_desc& d = m->desc;
   const Layout& L = m->lay;
   float* h = base + L.h;
@@ -119,6 +123,8 @@ std::vector<Item> make_items(const vbq_model* m, float* base, bool trace) {
   auto tin = [&](int p) -> uint16_t* { return trace ? m->tr_in + m->in_off[p] : nullptr; };
   auto tout = [&](int p) -> float* { return trace ? m->tr_out + m->out_off[p] : nullptr; };
   std::vector<Item> items;
+  std::vector<ZeroSpec> outputs;  // per item: what its split tiles add into (n = 0: adds onto h)
+  std::vector<CopySpec> traces;   // per item: its traced output, copied by the next item
   auto item_for = [&](int li) {
     Item it{};
     it.plan = plan_view(m->plans[li]);
@@ -134,15 +140,17 @@ std::vector<Item> make_items(const vbq_model* m, float* base, bool trace) {
     const int p0 = l * P_PER_LAYER, l0 = l * L_PER_LAYER;
     {  // [q; k; v] = W u, u = bf16(rmsnorm(h))
       Item it = item_for(l0 + L_QKV);
-      add_seg(it, W[P_Q], qkv, tout(p0 + P_Q));
-      add_seg(it, W[P_K], qkv + nq, tout(p0 + P_K));
-      add_seg(it, W[P_V], qkv + nq + nkv, tout(p0 + P_V));
+      add_seg(it, W[P_Q], qkv, nullptr);
+      add_seg(it, W[P_K], qkv + nq, nullptr);
+      add_seg(it, W[P_V], qkv + nq + nkv, nullptr);
       it.xs.mode = X_RMSNORM;
       it.xs.K = d.d;
       it.xs.h = h;
       it.xs.eps = d.rms_eps;
       it.xs.trace_x = tin(p0 + P_Q);
       items.push_back(it);
+      outputs.push_back(ZeroSpec{qkv, 0, static_cast<int32_t>(nq + 2 * nkv)});
+      traces.push_back(CopySpec{qkv, tout(p0 + P_Q), trace ? static_cast<int32_t>(nq + 2 * nkv) : 0});
     }
     {  // h += Wo a, a = bf16(v of each head's kv group)
       Item it = item_for(l0 + L_O);
@@ -156,17 +164,21 @@ std::vector<Item> make_items(const vbq_model* m, float* base, bool trace) {
       it.ep = EP_RESID;
       it.resid = h;
       items.push_back(it);
+      outputs.push_back(ZeroSpec{nullptr, 0, 0});
+      traces.push_back(CopySpec{});
     }
     {  // [gate; up] = W u, u = bf16(rmsnorm(h))
       Item it = item_for(l0 + L_GU);
-      add_seg(it, W[P_GATE], gu, tout(p0 + P_GATE));
-      add_seg(it, W[P_UP], gu + d.d_ff, tout(p0 + P_UP));
+      add_seg(it, W[P_GATE], gu, nullptr);
+      add_seg(it, W[P_UP], gu + d.d_ff, nullptr);
       it.xs.mode = X_RMSNORM;
       it.xs.K = d.d;
       it.xs.h = h;
       it.xs.eps = d.rms_eps;
       it.xs.trace_x = tin(p0 + P_GATE);
       items.push_back(it);
+      outputs.push_back(ZeroSpec{gu, 0, 2 * d.d_ff});
+      traces.push_back(CopySpec{gu, tout(p0 + P_GATE), trace ? 2 * d.d_ff : 0});
     }
     {  // h += Wdown bf16(silu(gate) * up)
       Item it = item_for(l0 + L_DOWN);
@@ -179,19 +191,26 @@ std::vector<Item> make_items(const vbq_model* m, float* base, bool trace) {
       it.ep = EP_RESID;
       it.resid = h;
       items.push_back(it);
+      outputs.push_back(ZeroSpec{nullptr, 0, 0});
+      traces.push_back(CopySpec{});
     }
   }
   {  // logits = Whead bf16(rmsnorm(h)), into the launch's output
     const int lh = d.n_layers * L_PER_LAYER, ph = d.n_layers * P_PER_LAYER;
     Item it = item_for(lh);
-    add_seg(it, m->mats[ph], nullptr, tout(ph));
+    add_seg(it, m->mats[ph], nullptr, nullptr);  // traced by a copy after the launch
     it.xs.mode = X_RMSNORM;
     it.xs.K = d.d;
     it.xs.h = h;
     it.xs.eps = d.rms_eps;
     it.xs.trace_x = tin(ph);
     items.push_back(it);
+    outputs.push_back(ZeroSpec{nullptr, 0, d.vocab});  // the launch's logits
+    traces.push_back(CopySpec{});
   }
+  for (size_t i = 1; i < items.size(); ++i) items[i].tcopy = traces[i - 1];
+  for (size_t i = 0; i < items.size(); ++i) items[i].zero = i + 2 < items.size() ? outputs[i + 2] : ZeroSpec{};
+  for (int i = 0; i < 2; ++i) pre[i] = static_cast<size_t>(i) < outputs.size() ? outputs[i] : ZeroSpec{};
   return items;
 }
 
@@ -199,8 +218,8 @@ cudaError_t upload_items(const std::vector<Item>& items, Item* dst) {
   return cudaMemcpy(dst, items.data(), sizeof(Item) * items.size(), cudaMemcpyHostToDevice);
 }
 
-cudaError_t launch_decode(const vbq_model* m, const Item* items, float* base, const uint16_t* x, float* out,
-                          cudaStream_t st, int* err) {
+cudaError_t launch_decode(const vbq_model* m, const Item* items, const ZeroSpec* pre, float* base,
+                          const uint16_t* x, float* out, cudaStream_t st, int* err) {
   DecodeArgs a{};
   a.prog.items = items;
   a.prog.n_items = m->n_items;
@@ -211,6 +230,8 @@ cudaError_t launch_decode(const vbq_model* m, const Item* items, float* base, co
   a.prog.d = m->desc.d;
   a.prog.grid_bar = reinterpret_cast<uint32_t*>(base + m->lay.bar);
   a.prog.err = err;
+  a.prog.pre[0] = pre[0];
+  a.prog.pre[1] = pre[1];
   a.x = x;
   a.out = out;
   // The grid-barrier and split-tile counters are zero here: the scratch starts
@@ -377,7 +398,7 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   m->pstart = reinterpret_cast<const uint32_t*>(pm + o_s);
   m->pbytes = reinterpret_cast<const uint32_t*>(pm + o_b);
   m->items_ws = reinterpret_cast<Item*>(pm + o_i1);
-  e = upload_items(make_items(m, m->ws, false), m->items_ws);
+  e = upload_items(make_items(m, m->ws, false, m->pre_ws), m->items_ws);
   // The program over the static scratch of vbq_decode_step_noalloc, when the model fits it. That entry
   // point's set-up happens here, with the model's device current, so that its calls allocate nothing.
   if (e == cudaSuccess && m->lay.total <= kStepScratchFloats) {
@@ -389,7 +410,7 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
     }
     m->static_base = sb;
     m->items_static = reinterpret_cast<Item*>(pm + o_i2);
-    e = upload_items(make_items(m, sb, false), m->items_static);
+    e = upload_items(make_items(m, sb, false, m->pre_static), m->items_static);
   }
   if (e != cudaSuccess) {
     vbq_model_free(m);
@@ -419,7 +440,15 @@ extern "C" vbq_status vbq_decode_step(vbq_model* m, const uint16_t* x_dev, float
   if (!m || !x_dev || !logits_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: NULL argument");
   if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 4)
     return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: misaligned buffer (x and logits need 4-byte alignment)");
-  VBQ_CUDA_TRY(launch_decode(m, m->items_ws, m->ws, x_dev, logits_dev, static_cast<cudaStream_t>(stream), m->err));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (m->trace)  // traced outputs that add onto the residual are sums of adds
+    VBQ_CUDA_TRY(cudaMemsetAsync(m->tr_out, 0, 4 * static_cast<size_t>(m->out_total), st));
+  VBQ_CUDA_TRY(launch_decode(m, m->items_ws, m->pre_ws, m->ws, x_dev, logits_dev, st, m->err));
+  if (m->trace) {
+    const int64_t ph = int64_t(m->desc.n_layers) * P_PER_LAYER;
+    VBQ_CUDA_TRY(cudaMemcpyAsync(m->tr_out + m->out_off[ph], logits_dev, 4 * static_cast<size_t>(m->desc.vocab),
+                                 cudaMemcpyDeviceToDevice, st));
+  }
   return VBQ_OK;
 }
 
@@ -443,7 +472,7 @@ extern "C" vbq_status vbq_model_set_trace(vbq_model* m, int32_t enable) {
   }
   m->trace = enable != 0;
   VBQ_CUDA_TRY(cudaDeviceSynchronize());  // no step may be reading the items
-  VBQ_CUDA_TRY(upload_items(make_items(m, m->ws, m->trace), m->items_ws));
+  VBQ_CUDA_TRY(upload_items(make_items(m, m->ws, m->trace, m->pre_ws), m->items_ws));
   return VBQ_OK;
 }
 
@@ -527,7 +556,7 @@ extern "C" vbq_status vbq_decode_step_noalloc(vbq_model* m, const uint16_t* x_de
   VBQ_CUDA_TRY(cudaGetDevice(&dev));
   if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: model is on another device");
   if (!m->items_static) return fail(VBQ_ERR_CUDA, "vbq_decode_step_noalloc: the static scratch was not set up");
-  cudaError_t e = launch_decode(m, m->items_static, m->static_base, x_dev, logits_dev,
+  cudaError_t e = launch_decode(m, m->items_static, m->pre_static, m->static_base, x_dev, logits_dev,
                                 static_cast<cudaStream_t>(stream), m->err);
   if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: launch");
   return VBQ_OK;

@@ -115,6 +115,11 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   return v;
 }
 
+// y += v in global memory, without waiting for the result.
+__device__ __forceinline__ void red_add_f32(float* y, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(y), "f"(v) : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding grid's memory, and let
 // the next grid begin launching.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -121,9 +121,13 @@ def check_glue(b, per, x):
     total = 0
 
     def residual(h, err_h, v):
+        # The kernel adds each split of a tile's partial rows onto h with fp32
+        # atomic adds (up to 16 of them, in any order), while the trace holds the
+        # same partials summed on their own: allow one rounding of the partial
+        # sums and of h per add.
         v = v.astype(np.float64)
         new = h + v
-        return new, err_h + 2.0 ** -24 * np.abs(new) + 2.0 ** -24 * err_h
+        return new, err_h + 2.0 ** -20 * (np.abs(new) + np.abs(h) + np.abs(v)) + 2.0 ** -24 * err_h
 
     for layer in range(s.n_layers):
         near += rmsnorm_input_ok(per[(layer, "q")][0], h, err_h)
@@ -165,19 +169,29 @@ def test_tiny_decode_step_teacher_forced(V):
 
 
 def test_decode_step_repeatable_and_host_path(V):
+    """Steps on the same input agree within the parity bar: the partial rows of split tiles are added
+    with fp32 atomic adds in no fixed order, so the last bits can differ from one step to the next."""
     import torch
     b = Built(V, model_tiny(), seed=1)
     x = gen_x(b.shape.d, seed=4)
+    hm = b.get(b.shape.n_layers, "head")
+    norms = O.row_norms(*hm)
+    ones = O.f64_to_bf16_bits(np.ones(b.shape.d))  # the head's input bf16(rmsnorm(h)) has 2-norm ~ sqrt(d)
+
+    def close(a, ref):
+        assert np.isfinite(a).all()
+        assert O.normalized_error(a, ref.astype(np.float64), norms, ones) <= TOL
+
     l1, _ = run_step(V, b, x)
-    l2, _ = run_step(V, b, x)          # new device buffers: the graph is rebuilt
-    assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32))
+    l2, _ = run_step(V, b, x)          # new device buffers
+    close(l2, l1)
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
     lh = torch.empty(b.shape.vocab, dtype=torch.float32).pin_memory()
     V.vbq_decode_step_host(b.model.handle, xh, lh)
-    assert np.array_equal(lh.numpy().view(np.uint32), l1.view(np.uint32))
+    close(lh.numpy(), l1)
     # trace off and on give the same logits
     l3, _ = run_step(V, b, x, trace=True)
-    assert np.array_equal(l3.view(np.uint32), l1.view(np.uint32))
+    close(l3, l1)
     b.close()
 
 

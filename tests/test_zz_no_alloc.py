@@ -53,9 +53,9 @@ def test_noalloc_step_matches_decode_step_twice(V):
         # The parity bar of every GEMV test. The head's input is bf16(rmsnorm(h)), whose 2-norm is
         # sqrt(d), so a vector of ones stands in for it in the denominator.
         ones = O.f64_to_bf16_bits(np.ones(shape.d))
+        # The same kernel on the same inputs; split tiles add their partial rows with fp32 atomic adds
+        # in no fixed order, so the logits agree to the last bits only up to that order.
         assert O.normalized_error(o, r.astype(np.float64), norms, ones) <= TOL
-        # Same kernels in the same order on the same inputs: the logits are in fact bit-equal.
-        assert np.array_equal(o.view(np.uint32), r.view(np.uint32)), call
     assert V.vbq_device_check() == 0
     model.close()
     for h in handles:
