@@ -702,27 +702,36 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
     cur_g = g;
   };
 
-  // Steps [k, kend) of a run of class CLS with n entries. Full steps go in
-  // blocks that need no check inside: every step of a block has landed, and
-  // the block ends where the consumed bytes free a ring slot. Within a block,
-  // steps go in pairs, so two independent decodes are in flight.
+  // Steps [k, kend) of a run of class CLS with n entries. When every byte of
+  // the steps has landed (the usual case: a run is about a kilobyte and the
+  // ring holds 8), they run with no check at all, in pairs so that two
+  // decodes are in flight, and the freed ring slots are refilled after the
+  // run. Otherwise full steps go in blocks that need no check inside: every
+  // step of a block has landed, and the block ends where the consumed bytes
+  // free a ring slot.
   auto run_steps = [&](auto cls_tag, uint32_t k, uint32_t kend, uint32_t n) {
     constexpr int CLS = decltype(cls_tag)::value;
     constexpr uint32_t EPS = entries_per_step(CLS);
     constexpr uint32_t FULL = full_step_bytes(CLS);
     const float pw = CLS == 1 ? K.pw2 : K.pw4;
     const uint32_t acc_a = smem_u32(vbq_smem) + acc;
-    const uint32_t kfull = min(kend, n / EPS);
+    const uint32_t kfull = min(kend, n >> (LOG_STEP_LANES - CLS));
+    const uint32_t e_last = n - kfull * EPS;  // entries of the partial step, if kend > kfull
+    const uint32_t run_end = K.o + (kfull - k) * FULL + (kend > kfull ? rec_bytes(CLS, e_last) : 0u);
+    const bool landed = run_end <= S.avail;
     while (k < kfull) {
-      if (S.avail < K.o + FULL) {
-        S.wait_for(K.o + FULL);
-        if (!S.ok) return;
-      }
-      uint32_t nb = min(kfull - k, (S.avail - K.o) / FULL);
-      if (S.refill_at != kNoRefill) nb = min(nb, (S.refill_at - K.o + FULL - 1u) / FULL);
-      if (nb == 0u) {  // cannot happen: refill_at > K.o here; never spin without progress
-        S.ok = false;
-        return;
+      uint32_t nb = kfull - k;
+      if (!landed) {
+        if (S.avail < K.o + FULL) {
+          S.wait_for(K.o + FULL);
+          if (!S.ok) return;
+        }
+        nb = min(nb, (S.avail - K.o) / FULL);
+        if (S.refill_at != kNoRefill) nb = min(nb, (S.refill_at - K.o + FULL - 1u) / FULL);
+        if (nb == 0u) {  // cannot happen: refill_at > K.o here; never spin without progress
+          S.ok = false;
+          return;
+        }
       }
       k += nb;
       for (; nb >= 2u; nb -= 2u) {
@@ -735,20 +744,18 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
         do_steps<NB, CLS, 1>(rb, EPS, K.xp, acc, acc_a, lane, K.lut, pw);
         K.o += FULL;
       }
-      S.refill(K.o, lane);
+      if (!landed) S.refill(K.o, lane);
     }
-    if (k < kend) {  // the run's last, partial step
-      const uint32_t e = n - k * EPS;
-      const uint32_t o1 = K.o + rec_bytes(CLS, e);
-      if (S.avail < o1) {
-        S.wait_for(o1);
-        if (!S.ok) return;
-      }
+    if (S.avail < run_end) {
+      S.wait_for(run_end);
+      if (!S.ok) return;
+    }
+    if (kend > kfull) {  // the run's last, partial step
       const uint32_t rb[1] = {S.ring + (K.o & RMASK)};
-      do_steps<NB, CLS, 1>(rb, e, K.xp, acc, acc_a, lane, K.lut, pw);
-      K.o = o1;
-      S.refill(K.o, lane);
+      do_steps<NB, CLS, 1>(rb, e_last, K.xp, acc, acc_a, lane, K.lut, pw);
     }
+    K.o = run_end;
+    S.refill(K.o, lane);
   };
 
   for (int ui = 0; ui < nu; ++ui, ++K.gunit) {
