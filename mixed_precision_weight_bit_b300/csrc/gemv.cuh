@@ -949,9 +949,10 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
     }
   }
   if constexpr (STAGED) {
-    // The CTA's last unit of the item: warp w sums rows 16 w .. 16 w + 15 over
-    // the warps' accumulators, in warp order.
-    static_assert(!STAGED || W * 16 == TILE_MAX, "one warp per 16 rows");
+    // The CTA's last unit of the item: warp w sums rows RW w .. RW w + RW - 1
+    // (RW = TILE_MAX / W) over the warps' accumulators, in warp order.
+    constexpr uint32_t RW = TILE_MAX / W;
+    static_assert(!STAGED || (RW <= 32 && RW * W == TILE_MAX), "one lane per row");
     __syncthreads();
     if (nu > 0) {
       const int ui = nu - 1;
@@ -962,14 +963,14 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
       const uint32_t rows = __shfl_sync(0xffffffffu, ur.rows, ui);
       const MatView& M = it.seg[seg];
       const uint32_t accp = Lay::kAcc + par * Lay::kAccParity;
-      const uint32_t r = 16u * warp + (lane & 15);
+      const uint32_t r = RW * warp + (lane & (RW - 1u));
       float t = 0.0f;
 #pragma unroll
       for (int w = 0; w < W; ++w) t += lds<float>(accp + (w * TILE_MAX + r) * 4);
       // (The next unit of this parity starts after the grid barrier, which
       // orders these reads before its writes; the count only keeps the tally.)
       if (threadIdx.x == 0) atomicAdd(ucount + 2 + par, 1u);
-      if (lane < 16 && r < rows) {
+      if (static_cast<uint32_t>(lane) < RW && r < rows) {
         float* const ybase = M.y ? M.y : out + M.y_off;
         if (M.trace_y) red_add_f32(M.trace_y + r0 + r, t);
         if (nsplit > 1u || it.ep == EP_RESID) {

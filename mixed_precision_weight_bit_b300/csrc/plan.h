@@ -34,11 +34,15 @@ struct Plan {
   uint32_t n_counters = 0;
 };
 
-// Work model used to balance CTAs and warps: estimated warp instructions per
-// step of each bit class, per run, and per group column a warp has to prepare.
-constexpr uint32_t kCostStep[4] = {62, 64, 66, 50};
-constexpr uint32_t kCostRun = 6;
-constexpr uint32_t kCostColumn = 110;
+// Work model used to balance CTAs and warps: relative time per step of each
+// bit class, per run, and per group column a warp has to prepare. Fitted to
+// GEMV timings on a B300 (65536 x 4096 matrices of one class each, and the
+// mixed allocation): a 1-bit step costs about 2.4 8-bit steps (it adds 32
+// entries into the row accumulators, an 8-bit step 4), a run's set-up about
+// 1.6 1-bit steps, and a column's lookup tables about 1.9.
+constexpr uint32_t kCostStep[4] = {61, 47, 39, 25};
+constexpr uint32_t kCostRun = 99;
+constexpr uint32_t kCostColumn = 117;
 
 // Number of CTAs for a launch over total_bytes: one per SM at most, but no
 // fewer than 32 KB each, and never more than MAX_UNITS_PER_CTA units a CTA.
