@@ -82,75 +82,94 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
   return (row >> 3) * 1024u + (row & 7u) * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
-// Eight values s*(q - c) as fp16 into one 16-byte chunk of row `row` of A.
-__device__ __forceinline__ void put_chunk(uint8_t* sm, uint32_t a_base, uint32_t row, uint32_t chunk,
-                                          const float (&v)[8]) {
-  const uint32_t h = row >> 7, rr = row & 127u;
-  uint4 pk;
-  pk.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0]))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1]))) << 16);
-  pk.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2]))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3]))) << 16);
-  pk.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[4]))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[5]))) << 16);
-  pk.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[6]))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[7]))) << 16);
-  *reinterpret_cast<uint4*>(sm + a_base + h * (TC_ATILE / 2) + sw128(rr, chunk)) = pk;
+// K order inside one 64-wide group column (both A and B use it): position
+// 32*blk + 2*s + h holds code 32*blk + s + 16*h (s < 16, h < 2). A 32-bit code
+// plane then yields the pair (s, s + 16) with one shift and one mask, and an
+// 8-bit lane slice with one byte permute. The product does not depend on the
+// order of K.
+
+// Dequantization to fp16 without conversions: 0x6400 | q is the fp16 value
+// 1024 + q (q < 1024). With c = (2^b - 1)/2 = m0 + 1/2, (1024 + q) - (1024 + m0)
+// = q - m0 exactly, and fma(q - m0, s, -s/2) = s * (q - c) rounded once
+// (s/2 is exact in fp16).
+__device__ __forceinline__ uint32_t deq_pair(uint32_t h1024q, __half2 base, __half2 sc, __half2 nhs) {
+  const __half2 v = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&h1024q), base), sc, nhs);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Decodes one step of class cls (e entries) at shared offset rb into A.
-__device__ __forceinline__ void tc_step(uint8_t* sm, uint32_t rb, uint32_t cls, uint32_t e, uint32_t a_base,
-                                        int lane) {
-  const uint32_t j = static_cast<uint32_t>(lane) >> cls;
-  const uint32_t sg = static_cast<uint32_t>(lane) & ((1u << cls) - 1u);
+__device__ __forceinline__ void put16(uint8_t* sm, uint32_t a_base, uint32_t row, uint32_t chunk, uint4 v) {
+  *reinterpret_cast<uint4*>(sm + a_base + (row >> 7) * (TC_ATILE / 2) + sw128(row & 127u, chunk)) = v;
+}
+
+// Decodes one step of class CLS (e entries) at shared offset rb into A.
+template <int CLS>
+__device__ __forceinline__ void tc_step_cls(uint8_t* sm, uint32_t rb, uint32_t e, uint32_t a_base, int lane) {
+  constexpr uint32_t B = 1u << CLS;
+  const uint32_t j = static_cast<uint32_t>(lane) >> CLS;
+  const uint32_t sg = static_cast<uint32_t>(lane) & (B - 1u);
   const bool active = j < e;
-  uint2 cw = make_uint2(0u, 0u);
-  if (active) cw = *reinterpret_cast<const uint2*>(sm + rb + 8u * lane);
-  float sc = 0.0f;
-  uint32_t row = 0;
-  if (active) {
-    sc = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(sm + rb + rec_scale_off(cls, e) + 2u * j)));
-    row = sm[rb + rec_row_off(cls, e) + j];
-  }
-  if (cls == 3) {  // 8-bit: lane slice sg holds codes [8 sg, 8 sg + 8)
-    float v[8];
+  const uint2 cw = *reinterpret_cast<const uint2*>(sm + rb + 8u * lane);  // in the ring or its spill zone
+  const uint16_t sb = *reinterpret_cast<const uint16_t*>(sm + rb + rec_scale_off(CLS, e) + 2u * j);
+  const uint32_t row = sm[rb + rec_row_off(CLS, e) + j];
+  const __half2 sc = __half2half2(__ushort_as_half(sb));
+  const __half2 nhs = __hmul2(sc, __float2half2_rn(-0.5f));
+  const __half2 base = __float2half2_rn(static_cast<float>(1024u + (1u << (B - 1u)) - 1u));
+  if constexpr (CLS == 3) {
+    // Lane sg holds codes 8 sg .. 8 sg + 7; it writes chunk sg, which holds codes
+    // 32 blk + 4 t0 + i and those + 16 (blk = sg / 4, t0 = sg % 4, i < 4).
+    const int src = (lane & ~7) | static_cast<int>(4u * (sg >> 2) + ((sg & 3u) >> 1));
+    const uint32_t ax = __shfl_sync(0xffffffffu, cw.x, src), ay = __shfl_sync(0xffffffffu, cw.y, src);
+    const uint32_t bx = __shfl_sync(0xffffffffu, cw.x, src + 2), by = __shfl_sync(0xffffffffu, cw.y, src + 2);
+    const uint32_t a = (sg & 1u) ? ay : ax, b = (sg & 1u) ? by : bx;
+    uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      v[i] = sc * (static_cast<float>((cw.x >> (8 * i)) & 255u) - 127.5f);
-      v[4 + i] = sc * (static_cast<float>((cw.y >> (8 * i)) & 255u) - 127.5f);
+      const uint32_t pr = __byte_perm(a, b, static_cast<uint32_t>(i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12)));
+      o[i] = deq_pair((pr & 0x00FF00FFu) | 0x64006400u, base, sc, nhs);
     }
-    if (active) put_chunk(sm, a_base, row, sg, v);
-    return;
-  }
-  // Planes: gather all b planes of the entry, then lane sg writes codes [sg*64/b, (sg+1)*64/b).
-  const uint32_t b = 1u << cls;
-  uint2 pl[4];
+    if (active) put16(sm, a_base, row, sg, make_uint4(o[0], o[1], o[2], o[3]));
+  } else {
+    // Gather the entry's B planes; lane sg writes chunks sg * 8 / B .. + 8 / B - 1.
+    // Plane word w is kept as the 64-bit value w << 8 (hi:lo), so that one
+    // funnel shift right by s + 8 - p puts its bits s and s + 16 at bits p and
+    // 16 + p.
+    uint32_t lo[2][B], hi[2][B];
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const int src = (lane & ~static_cast<int>(b - 1u)) | (p & static_cast<int>(b - 1u));
-    pl[p].x = __shfl_sync(0xffffffffu, cw.x, src);
-    pl[p].y = __shfl_sync(0xffffffffu, cw.y, src);
-  }
-  if (!active) return;
-  const float c = 0.5f * static_cast<float>((1u << b) - 1u);  // c_b = (2^b - 1)/2
-  const uint32_t per = 64u >> cls;  // codes per lane
-  const uint32_t m0 = sg * per;
-  for (uint32_t ch = 0; ch < per / 8u; ++ch) {
-    float v[8];
+    for (uint32_t p = 0; p < B; ++p) {
+      const int src = (lane & ~static_cast<int>(B - 1u)) | static_cast<int>(p);
+      const uint32_t x = __shfl_sync(0xffffffffu, cw.x, src), y = __shfl_sync(0xffffffffu, cw.y, src);
+      lo[0][p] = x << 8;
+      hi[0][p] = x >> 24;
+      lo[1][p] = y << 8;
+      hi[1][p] = y >> 24;
+    }
+    if (!active) return;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t m = m0 + 8u * ch + i;
-      uint32_t q = 0;
+    for (uint32_t cc = 0; cc < 8u / B; ++cc) {
+      const uint32_t c = sg * (8u / B) + cc;
+      const uint32_t wsel = c >> 2, s0 = 4u * (c & 3u);
+      uint32_t o[4];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        if (p < static_cast<int>(b)) {
-          const uint32_t w = m < 32u ? pl[p].x : pl[p].y;
-          q |= ((w >> (m & 31u)) & 1u) << p;
-        }
+      for (uint32_t t = 0; t < 4; ++t) {
+        uint32_t q = 0x64006400u;
+#pragma unroll
+        for (uint32_t p = 0; p < B; ++p)
+          q |= __funnelshift_r(wsel ? lo[1][p] : lo[0][p], wsel ? hi[1][p] : hi[0][p], s0 + t + 8u - p) &
+               (0x00010001u << p);
+        o[t] = deq_pair(q, base, sc, nhs);
       }
-      v[i] = sc * (static_cast<float>(q) - c);
+      put16(sm, a_base, row, c, make_uint4(o[0], o[1], o[2], o[3]));
     }
-    put_chunk(sm, a_base, row, (m0 >> 3) + ch, v);
+  }
+}
+
+__device__ __forceinline__ void tc_step(uint8_t* sm, uint32_t rb, uint32_t cls, uint32_t e, uint32_t a_base,
+                                        int lane) {
+  switch (cls) {
+    case 0: tc_step_cls<0>(sm, rb, e, a_base, lane); break;
+    case 1: tc_step_cls<1>(sm, rb, e, a_base, lane); break;
+    case 2: tc_step_cls<2>(sm, rb, e, a_base, lane); break;
+    default: tc_step_cls<3>(sm, rb, e, a_base, lane); break;
   }
 }
 
@@ -285,14 +304,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) vbq_gemm_tc_kernel(const __grid
         const int bc = i >> 3, ch = i & 7;
         uint4 pk = make_uint4(0u, 0u, 0u, 0u);
         if (bc < a.B) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(a.X + static_cast<int64_t>(bc) * a.K + g * GROUP + ch * 8);
+          // Chunk ch holds codes 32 blk + s0 + t and those + 16 (t < 4), in pairs.
+          const uint16_t* xr = a.X + static_cast<int64_t>(bc) * a.K + g * GROUP + 32 * (ch >> 2) + 4 * (ch & 3);
+          const uint2 lo4 = *reinterpret_cast<const uint2*>(xr), hi4 = *reinterpret_cast<const uint2*>(xr + 16);
           const float s = sxs[bc];
-          const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+          const float xa[4] = {bf16_lo(lo4.x), bf16_hi(lo4.x), bf16_lo(lo4.y), bf16_hi(lo4.y)};
+          const float xb[4] = {bf16_lo(hi4.x), bf16_hi(hi4.x), bf16_lo(hi4.y), bf16_hi(hi4.y)};
           uint32_t o[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            o[q] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(bf16_lo(w[q]) * s))) |
-                   (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(bf16_hi(w[q]) * s))) << 16);
+          for (int t = 0; t < 4; ++t)
+            o[t] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(xa[t] * s))) |
+                   (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(xb[t] * s))) << 16);
           pk = make_uint4(o[0], o[1], o[2], o[3]);
         }
         *reinterpret_cast<uint4*>(sm + b_base + sw128(static_cast<uint32_t>(bc), static_cast<uint32_t>(ch))) = pk;
