@@ -299,24 +299,33 @@ __device__ __forceinline__ void acc_add_if(uint32_t addr, float v, bool p) {
       "f"(v), "r"(static_cast<uint32_t>(p)));
 }
 
-// Decodes one step of class CLS from its code words and reduces each entry's
-// lanes: on return, lane sigma == 0 of entry j holds the entry's dot products.
-template <int NB, int CLS>
-__device__ __forceinline__ void step_dot(uint2 cw, uint32_t xp, uint32_t sigma, const float (&lut)[NB][NLUT],
-                                         float pw, float (&tv)[NB]) {
-  if (CLS == 3) {
+// Decodes one step from its code words and reduces each entry's lanes: on
+// return, lane sigma == 0 of entry j holds the entry's dot products. BYTES is
+// the 8-bit class; otherwise cls (0, 1 or 2: 1, 2 or 4 bits) is a run-time
+// value, so that the three plane classes share one copy of the code (the
+// decode loop must stay small enough for the instruction cache).
+template <int NB, bool BYTES>
+__device__ __forceinline__ void step_dot(uint2 cw, uint32_t xp, uint32_t sigma, uint32_t cls,
+                                         const float (&lut)[NB][NLUT], float pw, float (&tv)[NB]) {
+  if constexpr (BYTES) {
     decode_bytes<NB>(cw, xp, sigma, tv);
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+#pragma unroll
+      for (int c = 0; c < NB; ++c) tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], d);
+    }
   } else {
     decode_plane<NB>(cw, lut, tv);
-    if (CLS > 0) {
 #pragma unroll
-      for (int c = 0; c < NB; ++c) tv[c] *= pw;
+    for (int c = 0; c < NB; ++c) tv[c] *= pw;  // 2^plane (1 for 1-bit entries)
+    if (cls >= 1u) {
+#pragma unroll
+      for (int c = 0; c < NB; ++c) tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 1);
     }
-  }
+    if (cls >= 2u) {
 #pragma unroll
-  for (int d = 1; d < (1 << CLS); d <<= 1) {
-#pragma unroll
-    for (int c = 0; c < NB; ++c) tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], d);
+      for (int c = 0; c < NB; ++c) tv[c] += __shfl_xor_sync(0xffffffffu, tv[c], 2);
+    }
   }
 }
 
@@ -324,23 +333,26 @@ __device__ __forceinline__ void step_dot(uint2 cw, uint32_t xp, uint32_t sigma, 
 // with e entries (e < entries_per_step only for a run's last step). Every lane
 // loads and decodes; lanes past the last entry, and all but the first lane of
 // an entry, add nothing. The loads of all U steps are issued first.
-template <int NB, int CLS, int U>
-__device__ __forceinline__ void do_steps(const uint32_t (&rb)[U], uint32_t e, uint32_t xp, uint32_t acc,
-                                         uint32_t acc_a, int lane, const float (&lut)[NB][NLUT], float pw) {
-  const uint32_t j = static_cast<uint32_t>(lane) >> CLS;
-  const uint32_t sigma = static_cast<uint32_t>(lane) & ((1u << CLS) - 1u);
+template <int NB, bool BYTES, int U>
+__device__ __forceinline__ void do_steps(const uint32_t (&rb)[U], uint32_t e, uint32_t cls, uint32_t xp,
+                                         uint32_t acc, uint32_t acc_a, int lane, const float (&lut)[NB][NLUT],
+                                         float pw) {
+  if constexpr (BYTES) cls = 3u;
+  const uint32_t j = static_cast<uint32_t>(lane) >> cls;
+  const uint32_t sigma = static_cast<uint32_t>(lane) & ((1u << cls) - 1u);
   const bool add = j < e && sigma == 0;
+  const uint32_t so = rec_scale_off(cls, e) + 2u * j, ro = rec_row_off(cls, e) + j;
   uint2 cw[U];
   uint32_t sb[U], row[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     cw[u] = lds<uint2>(rb[u] + 8u * lane);
-    sb[u] = lds<uint16_t>(rb[u] + rec_scale_off(CLS, e) + 2u * j);
-    row[u] = lds<uint8_t>(rb[u] + rec_row_off(CLS, e) + j);
+    sb[u] = lds<uint16_t>(rb[u] + so);
+    row[u] = lds<uint8_t>(rb[u] + ro);
   }
   float tv[U][NB];
 #pragma unroll
-  for (int u = 0; u < U; ++u) step_dot<NB, CLS>(cw[u], xp, sigma, lut, pw, tv[u]);
+  for (int u = 0; u < U; ++u) step_dot<NB, BYTES>(cw[u], xp, sigma, cls, lut, pw, tv[u]);
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(sb[u])));
@@ -709,15 +721,16 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
   // run. Otherwise full steps go in blocks that need no check inside: every
   // step of a block has landed, and the block ends where the consumed bytes
   // free a ring slot.
-  auto run_steps = [&](auto cls_tag, uint32_t k, uint32_t kend, uint32_t n) {
-    constexpr int CLS = decltype(cls_tag)::value;
-    constexpr uint32_t EPS = entries_per_step(CLS);
-    constexpr uint32_t FULL = full_step_bytes(CLS);
-    const float pw = CLS == 1 ? K.pw2 : K.pw4;
+  auto run_steps = [&](auto bytes_tag, uint32_t cls, uint32_t k, uint32_t kend, uint32_t n) {
+    constexpr bool BYTES = decltype(bytes_tag)::value;
+    if constexpr (BYTES) cls = 3u;
+    const uint32_t EPS = entries_per_step(cls);
+    const uint32_t FULL = full_step_bytes(cls);
+    const float pw = cls == 0u ? 1.0f : cls == 1u ? K.pw2 : K.pw4;
     const uint32_t acc_a = smem_u32(vbq_smem) + acc;
-    const uint32_t kfull = min(kend, n >> (LOG_STEP_LANES - CLS));
+    const uint32_t kfull = min(kend, n >> (LOG_STEP_LANES - cls));
     const uint32_t e_last = n - kfull * EPS;  // entries of the partial step, if kend > kfull
-    const uint32_t run_end = K.o + (kfull - k) * FULL + (kend > kfull ? rec_bytes(CLS, e_last) : 0u);
+    const uint32_t run_end = K.o + (kfull - k) * FULL + (kend > kfull ? rec_bytes(cls, e_last) : 0u);
     const bool landed = run_end <= S.avail;
     while (k < kfull) {
       uint32_t nb = kfull - k;
@@ -736,12 +749,12 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
       k += nb;
       for (; nb >= 2u; nb -= 2u) {
         const uint32_t rb[2] = {S.ring + (K.o & RMASK), S.ring + ((K.o + FULL) & RMASK)};
-        do_steps<NB, CLS, 2>(rb, EPS, K.xp, acc, acc_a, lane, K.lut, pw);
+        do_steps<NB, BYTES, 2>(rb, EPS, cls, K.xp, acc, acc_a, lane, K.lut, pw);
         K.o += 2u * FULL;
       }
       if (nb) {
         const uint32_t rb[1] = {S.ring + (K.o & RMASK)};
-        do_steps<NB, CLS, 1>(rb, EPS, K.xp, acc, acc_a, lane, K.lut, pw);
+        do_steps<NB, BYTES, 1>(rb, EPS, cls, K.xp, acc, acc_a, lane, K.lut, pw);
         K.o += FULL;
       }
       if (!landed) S.refill(K.o, lane);
@@ -752,7 +765,7 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
     }
     if (kend > kfull) {  // the run's last, partial step
       const uint32_t rb[1] = {S.ring + (K.o & RMASK)};
-      do_steps<NB, CLS, 1>(rb, e_last, K.xp, acc, acc_a, lane, K.lut, pw);
+      do_steps<NB, BYTES, 1>(rb, e_last, cls, K.xp, acc, acc_a, lane, K.lut, pw);
     }
     K.o = run_end;
     S.refill(K.o, lane);
@@ -801,11 +814,10 @@ __device__ __forceinline__ void run_item(const Item& it, const UnitRegs& ur, War
       const uint32_t cls = run_cls(d), n = run_n(d);
       const uint32_t kend = (run == run1) ? k1 : (n + entries_per_step(cls) - 1u) >> (LOG_STEP_LANES - cls);
       if (g != cur_g) prep_for(g);
-      switch (cls) {
-        case 0: run_steps(std::integral_constant<int, 0>{}, k, kend, n); break;
-        case 1: run_steps(std::integral_constant<int, 1>{}, k, kend, n); break;
-        case 2: run_steps(std::integral_constant<int, 2>{}, k, kend, n); break;
-        default: run_steps(std::integral_constant<int, 3>{}, k, kend, n); break;
+      if (cls == 3u) {
+        run_steps(std::true_type{}, cls, k, kend, n);
+      } else {
+        run_steps(std::false_type{}, cls, k, kend, n);
       }
     }
 
