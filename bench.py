@@ -275,7 +275,10 @@ def time_steps(fn, steps, warmup, stream, ws):
 # launch on the 9B-shaped step, from an ncu capture of the build whose kernel
 # sources hash to the key (the summary and command are in profiles/). Any other
 # build reports null.
-DECODE_TRAFFIC = {}
+DECODE_TRAFFIC = {
+    # profiles/vbq_decode_kernel_9b_decode_step.md: 2.08 GB read + 2.96 MB written in one launch
+    "329d270b03322a65": 2082960000,
+}
 KERNEL_SOURCES = ("gemv.cuh", "ptx.cuh", "layout.h", "model.cu", "plan.cpp", "plan.h", "pack.cpp")
 
 
@@ -308,7 +311,7 @@ def decode_kernel_roofline(V, pm, x, logits, stream, peak_gbs, ms_step, steps, w
     traffic = DECODE_TRAFFIC.get(key) if workload == "9b" else None
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
             "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
-            "kernel": "vbq_decode_kernel<8,2>", "launches_timed": steps,
+            "kernel": "vbq_decode_kernel<16,2>", "launches_timed": steps,
             "avg_launch_us": round(ms_step * 1e3, 2),
             "bracketed_launch_us": {"min": round(min(ms) * 1e3, 2), "avg": round(sum(ms) / len(ms) * 1e3, 2)},
             "alg_bytes_per_launch": round(pm.alg_bytes), "kernel_source_hash": key,

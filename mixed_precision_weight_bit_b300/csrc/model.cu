@@ -33,7 +33,7 @@ namespace {
 enum { P_Q = 0, P_K, P_V, P_O, P_GATE, P_UP, P_DOWN, P_PER_LAYER };
 enum { L_QKV = 0, L_O, L_GU, L_DOWN, L_PER_LAYER };
 
-constexpr int DEC_W = 8;      // warps per CTA of the decode kernel
+constexpr int DEC_W = 16;     // warps per CTA of the decode kernel
 constexpr int DEC_NSLOT = 2;  // ring slots per warp
 
 int64_t proj_n(const vbq_model_desc& d, int p) {
