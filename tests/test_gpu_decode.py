@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 from oracle import vbq_oracle as O
-from synth import PROJS, gen_model_matrix, gen_x, model_1b, model_matrix_list, model_matrix_shape, model_tiny
+from synth import PROJS, gen_model_matrix, gen_x, model_1b, model_9b, model_matrix_list, model_matrix_shape, model_tiny
 from tests.gpu_util import TOL, bf16_ulp_diff, dev_u16, lib
 
 pytestmark = pytest.mark.gpu
@@ -18,6 +18,7 @@ def V(cuda_device):
 class Built:
     def __init__(self, V, shape, seed=0, keep_inputs=True):
         self.shape = shape
+        self.seed = seed
         self.mats = {}
         self.handles = []
         for (layer, proj) in model_matrix_list(shape):
@@ -31,7 +32,9 @@ class Built:
         self.order = model_matrix_list(shape)
 
     def get(self, layer, proj):
-        m = self.mats[(layer, proj)]
+        m = self.mats.get((layer, proj))
+        if m is None:  # not kept: draw it again (the generator is deterministic)
+            m = gen_model_matrix(self.shape, layer, proj, seed=self.seed)
         return m.codes, m.bits, m.scales
 
     def close(self):
@@ -216,6 +219,19 @@ def test_1b_decode_step_sampled(V):
     logits, per = run_step(V, b, x, trace=True)
     assert np.isfinite(logits).all()
     check_projections(b, per, rows_per_proj=24)
+    check_glue(b, per, x)
+    b.close()
+    assert V.vbq_device_check() == 0
+
+
+def test_9b_decode_step_sampled(V):
+    """The full-size 9B-shaped step, in the launch configuration the bench times: every projection under
+    teacher forcing on sampled rows (the first, the last and random ones), and the glue between them."""
+    b = Built(V, model_9b(), keep_inputs=False)
+    x = gen_x(b.shape.d, seed=6)
+    logits, per = run_step(V, b, x, trace=True)
+    assert np.isfinite(logits).all()
+    check_projections(b, per, rows_per_proj=6)
     check_glue(b, per, x)
     b.close()
     assert V.vbq_device_check() == 0

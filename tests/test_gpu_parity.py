@@ -223,3 +223,24 @@ def test_large_scales_take_the_cuda_core_path(V):
     ref = VbqMatrixInputs(codes=m.codes, bits=m.bits, scales=scales)
     assert gemv_err(ref, X, Y) <= TOL
     mat.close()
+
+
+# ---- the dense bf16 baseline ----
+
+@pytest.mark.parametrize("N,K", [(1, 8), (3, 72), (300, 1024), (4099, 4096)])
+def test_dense_bf16_gemv(V, N, K):
+    """y = W x for bf16 W and x with fp32 accumulation, against the fp64 product of the same bf16 values."""
+    import torch
+    rng = np.random.default_rng(N * 7919 + K)
+    w_bits = O.f64_to_bf16_bits(rng.standard_normal((N, K)) * 0.05)
+    x_bits = gen_x(K, seed=N + K)
+    y = torch.full((N,), float("nan"), device="cuda")
+    V.vbq_dense_gemv_bf16(dev_u16(w_bits), dev_u16(x_bits), y, N, K)
+    torch.cuda.synchronize()
+    w = O.bf16_bits_to_f64(w_bits)
+    x = O.bf16_bits_to_f64(x_bits)
+    ref = w @ x
+    got = y.cpu().numpy().astype(np.float64)
+    norms = np.linalg.norm(w, axis=1) * np.linalg.norm(x)
+    assert np.isfinite(got).all()
+    assert np.max(np.abs(got - ref) / norms) <= TOL
