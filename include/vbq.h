@@ -2,13 +2,13 @@
  * vbq.h: C ABI of the VBQ mixed-bit decode library (sm_103a).
  *
  * VBQ (Variable Bit-width Quantization) stores a linear layer's weights packed.
- * Each contiguous group of 64 weights along the input dimension has its own
+ * Every run of 64 consecutive weights along the input dimension has its own
  * bit-width b_g from {1,2,4,8}. Source: "Variable Bit-width Quantization:
  * Learning Per-Group Precision for 'Bigger-but-Smaller' Language Models",
- * abstract. The abstract says the learned recipe "maps directly to packed
- * low-bit storage" and that fused dequantize-and-multiply kernels speed up
- * memory-bandwidth-bound autoregressive decode. The pages fix no code grid;
- * this library uses
+ * abstract: once learned, the per-group allocation is stored as packed low-bit
+ * codes, and kernels that dequantize inside the multiply speed up token-by-token
+ * decode, which memory bandwidth limits. The pages fix no code grid; this
+ * library uses
  *
  *     w = s_g * (q - (2^b_g - 1) / 2),   s_g fp16,   q unsigned in [0, 2^b_g - 1],
  *

@@ -1,22 +1,26 @@
-// Fused dequantize-and-multiply for the packed VBQ layout (layout.h), CUDA cores.
+// Fused dequantize-and-multiply for the packed VBQ layout (layout.h), CUDA cores:
+// the single-GEMV kernel and the persistent decode-step kernel.
 //
 // VBQ abstract ("Variable Bit-width Quantization ..."): decode is memory-bound,
 // and the packed per-group codes are dequantized and multiplied in one pass.
-// The abstract's kernels ran on Apple silicon. This kernel is this library's
-// own design for sm_103a:
+// The abstract's kernels ran on Apple silicon. These kernels are this
+// library's own design for sm_103a:
 //
-//  * A host-built plan (layout.h) gives each CTA one contiguous, equal-byte
-//    range of the packed stream. The range is cut into units at tile borders,
-//    and each unit into one slice per warp.
-//  * Each warp streams its slices, unit after unit, through a private ring of
-//    NSLOT 4 KB slots in shared memory with cp.async.bulk copies completed on
-//    mbarriers. The copies start before griddepcontrol.wait, because the packed
-//    weights never depend on the previous kernel. Every wait is bounded. The
-//    first 512 bytes of each copy into slot 0 are also written past the ring's
-//    end, so a record that crosses the end of the ring reads on without
-//    wrapping.
+//  * A host-built plan (plan.h) gives each CTA one contiguous range of the
+//    packed stream, balanced by a measured cost model. The range is cut into
+//    units at tile borders, and each unit into one slice per warp. Each warp
+//    has the list of byte ranges ("pieces") it streams, in order.
+//  * Each warp streams its pieces through a private ring of NSLOT 4 KB slots in
+//    shared memory with cp.async.bulk copies completed on mbarriers. Every wait
+//    is bounded. The first 512 bytes of each copy into slot 0 are also written
+//    past the ring's end, so a record that crosses the end of the ring reads on
+//    without wrapping. In the decode kernel the pieces of all projections of
+//    the step follow each other, so the next projection's weights arrive while
+//    the CTAs wait at a grid barrier.
 //  * The warp walks its slice run by run. A run has one group column g and one
-//    bit-class, so each step loop is compiled for its class.
+//    bit class. The step code exists twice, for the three bit-plane classes
+//    (their differences are run-time constants) and for bytes: the hot loop
+//    must stay small enough for the instruction cache.
 //  * 1-, 2- and 4-bit groups are stored as bit-planes (layout.h), and
 //    q - (2^b - 1)/2 = sum_p 2^p (q_p - 1/2). So every lane decodes one 64-bit
 //    plane as if it were a 1-bit group, and the b lanes of an entry add their
@@ -30,15 +34,19 @@
 //    float 1 + q*2^-15, so sum x'_m f_m - C = sum x_m (q_m - 127.5), with
 //    x'_m = 2^15 x_m, C = sum (x'_m + 127.5 x_m) per 8-code lane slice, and
 //    packed f32x2 FMAs.
-//  * Per entry, the lanes of the entry are summed with shuffles, then scaled by
-//    the fp16 group scale and added (red.shared.add) into the warp's private
-//    fp32 row accumulator. Each warp adds to a row in program order, so the
-//    sums do not depend on timing.
+//  * Per entry, the lanes of the entry are summed with shuffles, scaled by the
+//    fp16 group scale and added into the warp's private fp32 row accumulator
+//    with a predicated load-add-store (the rows of one group column are
+//    distinct, so no atomic is needed). Each warp adds to a row in program
+//    order. Full steps whose bytes have landed run two at a time.
 //  * Accumulators are double-buffered by unit parity, and no barrier spans the
-//    CTA. The last warp to finish a unit (a shared-memory counter) sums the
-//    warps' accumulators in warp order while the others go on to the next
-//    unit. A tile cut between CTAs gets one partial per unit, and the last CTA
-//    to arrive adds them in split order. Results are therefore deterministic.
+//    CTA within an item. The last warp to finish a unit sums the warps'
+//    accumulators in warp order while the others go on to the next unit (in
+//    the decode kernel, the CTA's last unit of an item is summed by all warps
+//    together). In the single-GEMV kernel a tile cut between CTAs writes one
+//    partial per unit and the last CTA to arrive adds them in split order, so
+//    its results are deterministic; the decode kernel adds the partials with
+//    fire-and-forget atomics instead.
 #pragma once
 
 #include <type_traits>

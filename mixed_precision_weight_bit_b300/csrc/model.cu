@@ -1,7 +1,7 @@
 // vbq_decode_step: one batch-1 decode step through a stack of VBQ projections.
 //
-// VBQ abstract ("Variable Bit-width Quantization ..."): the packed recipe makes
-// memory-bandwidth-bound autoregressive decode faster. The pages give no
+// VBQ abstract ("Variable Bit-width Quantization ..."): packed per-group codes
+// speed up token-by-token decode, whose speed memory bandwidth sets. The pages give no
 // architecture, so the glue below is this library's reading: unit-gamma
 // RMSNorm, attention at position 0 (a softmax over one key is 1, so each query
 // head returns its kv group's v), SwiGLU, fp32 residual, and bf16 at every
@@ -500,9 +500,8 @@ extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host
 
 // ---------------------------------------------------------------- allocation-free decode step
 //
-// vbq_decode_step keeps its step scratch (activations, split-tile partials and
-// counters, the grid-barrier counter) in memory that vbq_model_create
-// allocated for the model. Some callers cannot tie device memory to a model
+// vbq_decode_step keeps its step scratch (activations and the grid-barrier
+// counters) in memory that vbq_model_create allocated for the model. Some callers cannot tie device memory to a model
 // they step: code that runs while another component is capturing the stream
 // into its own graph, real-time loops whose device memory is fixed before the
 // loop starts, or hosts that hand out device memory only from their own pool.

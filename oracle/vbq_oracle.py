@@ -7,10 +7,10 @@ and it shares no code with the CUDA path.
 What it follows:
 
 * "Variable Bit-width Quantization: Learning Per-Group Precision for
-  'Bigger-but-Smaller' Language Models", abstract. Each contiguous group of 64
-  weights has its own bit-width from {1,2,4,8}. The recipe maps to packed
-  low-bit storage, and fused dequantize-and-multiply kernels speed up
-  memory-bound autoregressive decode. The abstract gives no code grid, so the
+  'Bigger-but-Smaller' Language Models", abstract. Every run of 64 consecutive
+  weights gets its own bit-width from {1,2,4,8}; the learned allocation is
+  stored as packed low-bit codes, and kernels that dequantize inside the
+  multiply speed up token-by-token decode. The abstract gives no code grid, so the
   grid is the one this project fixes: w = s_g * (q - (2^b_g - 1)/2). Here s_g is
   an fp16 scale and q is an unsigned code in [0, 2^b_g - 1]. Group g of row r
   covers columns [64g, 64g + 63].
