@@ -17,7 +17,7 @@ LIB = os.path.join(OUT_DIR, "libvbq.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 CUDA_LIB = "/usr/local/cuda/lib64"
 
-SOURCES = ["pack.cpp", "plan.cpp", "kernels.cu", "gemm_tc.cu", "model.cu"]
+SOURCES = ["pack.cpp", "plan.cpp", "gemv_plan.cpp", "kernels.cu", "gemm_tc.cu", "model.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr"]
 
@@ -36,17 +36,20 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines=None, out_dir: str = OUT_DIR) -> str:
+    """Compiles the sources and links <out_dir>/libvbq.so. defines: extra -D values for tuning builds."""
+    lib = os.path.join(out_dir, "libvbq.so")
+    if not force and out_dir == OUT_DIR and not defines and up_to_date():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     objs = []
     cmds = []
+    dflags = [f"-D{d}" for d in (defines or [])]
     for src in SOURCES:
-        obj = os.path.join(OUT_DIR, src.rsplit(".", 1)[0] + ".o")
+        obj = os.path.join(out_dir, src.rsplit(".", 1)[0] + ".o")
         objs.append(obj)
         lang = ["-x", "cu"] if src.endswith(".cu") else []
-        cmds.append([NVCC, *GENCODE, *FLAGS, *lang, "-c", os.path.join(CSRC, src), "-o", obj])
+        cmds.append([NVCC, *GENCODE, *FLAGS, *dflags, *lang, "-c", os.path.join(CSRC, src), "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -56,13 +59,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         logs = list(ex.map(run, cmds))
-    link = [NVCC, *GENCODE, "-shared", "-cudart", "shared", "-o", LIB + ".tmp", *objs,
+    link = [NVCC, *GENCODE, "-shared", "-cudart", "shared", "-o", lib + ".tmp", *objs,
             "-Xlinker", f"-rpath,{CUDA_LIB}", "-Xlinker", "--no-undefined", "-L" + CUDA_LIB]
     logs.append(run(link))
-    os.replace(LIB + ".tmp", LIB)
+    os.replace(lib + ".tmp", lib)
     if verbose:
         print("\n".join(l for l in logs if l.strip()))
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -11,24 +11,40 @@
 #include "layout.h"
 #include "plan.h"
 
+// Device data of a plan for one batch-1 GEMV over one matrix.
+struct GemvPlanDev {
+  void* base = nullptr;         // one allocation for everything below
+  const vbq::WarpPlan* warps = nullptr;
+  const vbq::CtaPlan* ctas = nullptr;
+  const uint32_t* arrivals = nullptr;  // per super-tile
+  uint32_t* counters = nullptr;        // per super-tile, zero between calls
+  unsigned long long* acc = nullptr;   // fixed-point row sums [n_super * 1024], zero between calls
+  const uint64_t* pieces = nullptr;
+  const uint32_t* pstart = nullptr;
+  const uint32_t* pbytes = nullptr;
+  int32_t n_ctas = 0;
+  int64_t bytes = 0;
+};
+
 struct vbq_matrix {
   int64_t N = 0, K = 0;
   int32_t G = 0;
-  int32_t n_tiles = 0, n_runs = 0;
+  int32_t n_tiles = 0;             // 256-row tiles
+  int32_t n_super = 0;             // 1024-row super-tiles
+  int64_t n_runs = 0;
   int64_t n_steps = 0;
   int64_t code_bytes = 0, meta_bytes = 0, total_bytes = 0, data_bytes = 0;
   int64_t groups_by_bits[4] = {0, 0, 0, 0};
   int device = 0;
-  uint8_t* dev_base = nullptr;  // one allocation: records and side tables
+  uint8_t* dev_base = nullptr;     // the packed stream
   const uint8_t* data = nullptr;
-  const uint32_t* run_desc = nullptr;
-  const uint32_t* run_off = nullptr;
-  const uint32_t* tile_row0 = nullptr;
-  const uint32_t* tile_run0 = nullptr;
-  std::vector<uint32_t> h_run_desc, h_run_off, h_tile_row0, h_tile_run0;  // host copies, for planning
-  vbq::DevicePlan plan;  // plan of a GEMV over this matrix alone
-  float tc_max_scale = 0.0f;  // largest |s_g|: the tensor-core path needs s * 127.5 inside fp16
-  int64_t max_col_bytes = 0;  // largest (tile, group column) record span
+  const uint64_t* st_byte0 = nullptr;  // device [n_super + 1]: first byte of each super-tile's runs
+  std::vector<vbq::RunInfo> runs;  // host copy of the run list, for planning
+  std::vector<uint32_t> block_run; // [n_super * G + 1]: first run of each (super-tile, group column)
+  float max_row_l1 = 0.0f;         // max over rows of sum_k |w_rk|, rounded up
+  uint16_t max_scale_bits = 0;     // largest |s_g| as fp16 magnitude bits
+  float max_scale = 0.0f;          // the same as a float
+  GemvPlanDev gemv;                // batch-1 GEMV plan and its accumulators
 };
 
 namespace vbq {
@@ -48,24 +64,10 @@ struct GpuInfo {
 };
 const GpuInfo& gpu_info();
 
-// Widest batch a single GEMV launch covers (partial storage is sized for it).
-constexpr int MAX_NB = 4;
-
-// Tensor-core dequant-MMA for 16..64 batch columns (gemm_tc.cu).
+// Tensor-core dequant-MMA for 2..256 batch columns (gemm_tc.cu).
 bool tc_eligible(const vbq_matrix* m);
 vbq_status launch_gemm_tc(const vbq_matrix* m, const uint16_t* X, int32_t B, float* Y, cudaStream_t st);
 void tc_forget(const vbq_matrix* m);
-
-inline SegTables seg_tables(const vbq_matrix* m) {
-  SegTables t;
-  t.run_desc = m->h_run_desc.data();
-  t.run_off = m->h_run_off.data();
-  t.tile_row0 = m->h_tile_row0.data();
-  t.tile_run0 = m->h_tile_run0.data();
-  t.n_tiles = m->n_tiles;
-  t.n_runs = m->n_runs;
-  return t;
-}
 
 }  // namespace vbq
 

@@ -9,7 +9,8 @@
 
 #include "gemv.cuh"
 #include "internal.h"
-#include "launch.h"
+#include <cstring>
+#include <vector>
 
 namespace vbq {
 
@@ -61,129 +62,182 @@ const GpuInfo& gpu_info() {
   return infos.emplace(dev, gi).first->second;
 }
 
-MatView view_of(const vbq_matrix* m, float* y, int32_t y_ld, float* trace_y) {
-  MatView v{};
-  v.data = m->data;
-  v.run_desc = m->run_desc;
-  v.y = y;
-  v.y_off = 0;
-  v.y_ld = y_ld;
-  v.trace_y = trace_y;
-  return v;
-}
+// ---- the single-GEMV kernel --------------------------------------------------
 
-PlanView plan_view(const DevicePlan& p) {
-  PlanView v{};
-  v.units = p.units;
-  v.slices = p.slices;
-  v.umax = p.umax;
-  v.partial = p.partial;
-  v.counters = p.counters;
-  return v;
-}
-
-// ---------------------------------------------------------------- GEMV launch
-
-// Kernel shapes: batch columns, warps per CTA, ring slots per warp.
-template <int NB> struct GemvShape;
-template <> struct GemvShape<1> { static constexpr int W = 16, NSLOT = 2; };
-template <> struct GemvShape<2> { static constexpr int W = 16, NSLOT = 2; };
-template <> struct GemvShape<4> { static constexpr int W = 8, NSLOT = 4; };
-
-template <int NB>
-struct GemvKernel {
-  static constexpr int W = GemvShape<NB>::W, NSLOT = GemvShape<NB>::NSLOT;
-  static constexpr int kThreads = W * 32;
-  static constexpr int kSmem = GemvSmem<NB, W, NSLOT>::kBytes;
-  static void prepare() {  // once per device
-    static std::mutex mu;
-    static std::map<int, bool> done;
-    const GpuInfo& gi = gpu_info();
-    std::lock_guard<std::mutex> lock(mu);
-    if (done[gi.device]) return;
-    cudaFuncSetAttribute(vbq_gemv_kernel<NB, W, NSLOT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    done[gi.device] = true;
-  }
+struct Gemv1Args {
+  const WarpPlan* warps;
+  const CtaPlan* ctas;
+  const uint32_t* arrivals;  // per super-tile
+  uint32_t* counters;        // per super-tile
+  unsigned long long* acc;   // [n_super * 1024] fixed-point sums, zero between calls
+  const uint64_t* pieces;
+  const uint32_t* pstart;
+  const uint32_t* pbytes;
+  const uint16_t* x;         // bf16 [K]
+  float* y;                  // [N]
+  int64_t N;
+  int32_t K;
+  int32_t ns;                // ring slots per warp
+  float max_row_l1;
+  int* err;
 };
 
-template <int NB>
-cudaError_t launch_gemv_t(const GemvArgs& a, int n_ctas, cudaStream_t st, bool pdl) {
-  using K = GemvKernel<NB>;
-  K::prepare();
+__global__ void __launch_bounds__(KW * 32, 1) vbq_gemv1_kernel(const __grid_constant__ Gemv1Args a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const SmemLayout L = smem_layout(a.ns);
+  WarpStream S;
+  Worker K;
+  worker_init(S, K, L, static_cast<uint32_t>(a.ns), a.pieces, a.pstart, a.pbytes, lane, warp);
+  for (uint32_t i = threadIdx.x; i < SLOTS_MAX * SROWS; i += KW * 32) sts<int>(L.acc + 4 * i, 0);
+  const CtaPlan cp = a.ctas[blockIdx.x];
+
+  // The weights do not depend on the previous kernel: the copies above already
+  // run. Wait for it before reading x or touching the accumulators.
+  grid_dep_launch();
+  grid_dep_wait();
+
+  float* red = reinterpret_cast<float*>(vbq_smem + L.misc);
+  const int F = fixed_exponent(a.max_row_l1, max_abs_bf16(a.x, a.K, red));
+  // Stage this CTA's columns; each warp issues all its loads first.
+  const uint32_t na = cp.a1 - cp.a0;
+  const uint32_t ncols = na + (cp.b1 - cp.b0);
+  {
+    constexpr int CPW = (CCAP + KW - 1) / KW;
+    uint32_t v[CPW];
+#pragma unroll
+    for (int q = 0; q < CPW; ++q) {
+      const uint32_t j = warp + q * KW;
+      const uint32_t g = j < na ? cp.a0 + j : cp.b0 + (j - na);
+      v[q] = j < ncols ? ldg_nc_u32(a.x + static_cast<size_t>(g) * GROUP + 2 * lane) : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < CPW; ++q) {
+      const uint32_t j = warp + q * KW;
+      if (j < ncols) put_column(L, static_cast<int>(j), bf16_lo(v[q]), bf16_hi(v[q]), F, lane);
+    }
+  }
+  __syncthreads();
+
+  if (cp.n_slots > 0) warp_item(L, a.warps + static_cast<size_t>(blockIdx.x) * KW + warp, nullptr, cp, S, K, lane);
+  if (!S.ok) {
+    if (lane == 0) atomicExch(a.err, kErrRingTimeout);
+    S.drain();
+  }
+  __syncthreads();
+  if (cp.n_slots == 0) return;
+  flush_slots(L, cp, a.acc);
+  __threadfence();
+  __syncthreads();
+  // The last CTA to add into a super-tile converts its rows and clears them for the next call.
+  uint32_t* fin = reinterpret_cast<uint32_t*>(vbq_smem + L.misc) + 16;
+  if (threadIdx.x == 0) {
+    uint32_t nf = 0;
+    for (uint32_t s = 0; s < cp.n_slots; ++s) {
+      const uint32_t t = cp.st_base + s;
+      if (atomicAdd(a.counters + t, 1u) == a.arrivals[t] - 1u) fin[1 + nf++] = t;
+    }
+    fin[0] = nf;
+  }
+  __syncthreads();
+  const uint32_t nf = fin[0];
+  if (nf == 0) return;
+  __threadfence();
+  for (uint32_t f = 0; f < nf; ++f) {
+    const uint32_t t = fin[1 + f];
+    for (uint32_t r = threadIdx.x; r < SROWS; r += KW * 32) {
+      const int64_t row = static_cast<int64_t>(t) * SROWS + r;
+      unsigned long long* p = a.acc + row;
+      const long long v = static_cast<long long>(__ldcg(p));
+      if (row < a.N) a.y[row] = scalbnf(__ll2float_rn(v), -F);
+      *p = 0ull;
+    }
+    if (threadIdx.x == 0) a.counters[t] = 0u;
+  }
+}
+
+
+static_assert(smem_layout(kRingSlots).total <= 232448, "shared memory");
+
+static void prepare_gemv1() {
+  static std::mutex mu;
+  static std::map<int, bool> done;
+  const GpuInfo& gi = gpu_info();
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[gi.device]) return;
+  cudaFuncSetAttribute(vbq_gemv1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_layout(kRingSlots).total);
+  done[gi.device] = true;
+}
+
+// One batch-1 GEMV launch over matrix m (K <= XCAP, N > 0, K > 0).
+static cudaError_t launch_gemv1(const vbq_matrix* m, const uint16_t* x, float* y, cudaStream_t st, int* err) {
+  prepare_gemv1();
+  const GemvPlanDev& P = m->gemv;
+  Gemv1Args a{};
+  a.warps = P.warps;
+  a.ctas = P.ctas;
+  a.arrivals = P.arrivals;
+  a.counters = P.counters;
+  a.acc = P.acc;
+  a.pieces = P.pieces;
+  a.pstart = P.pstart;
+  a.pbytes = P.pbytes;
+  a.x = x;
+  a.y = y;
+  a.N = m->N;
+  a.K = static_cast<int32_t>(m->K);
+  a.ns = kRingSlots;
+  a.max_row_l1 = m->max_row_l1;
+  a.err = err;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_ctas), 1, 1);
-  cfg.blockDim = dim3(K::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = K::kSmem;
+  cfg.gridDim = dim3(static_cast<unsigned>(P.n_ctas), 1, 1);
+  cfg.blockDim = dim3(KW * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem_layout(kRingSlots).total;
   cfg.stream = st;
   cudaLaunchAttribute attrs[1];
-  int na = 0;
-  if (pdl) {
-    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = na;
+  cfg.numAttrs = 1;
   note_launches(1);
-  return cudaLaunchKernelEx(&cfg, vbq_gemv_kernel<NB, K::W, K::NSLOT>, a);
-}
-
-cudaError_t launch_gemv(int nb, const GemvArgs& a, int n_ctas, cudaStream_t st, bool pdl) {
-  if (n_ctas <= 0) return cudaSuccess;
-  switch (nb) {
-    case 1: return launch_gemv_t<1>(a, n_ctas, st, pdl);
-    case 2: return launch_gemv_t<2>(a, n_ctas, st, pdl);
-    case 4: return launch_gemv_t<4>(a, n_ctas, st, pdl);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-void warm_gemv(int nb) {
-  switch (nb) {
-    case 1: GemvKernel<1>::prepare(); break;
-    case 2: GemvKernel<2>::prepare(); break;
-    default: GemvKernel<4>::prepare(); break;
-  }
+  return cudaLaunchKernelEx(&cfg, vbq_gemv1_kernel, a);
 }
 
 // ---------------------------------------------------------------- dequant
 
-// W[r][k] = s * (q - c_b) for every weight, exact in fp32. One CTA per tile;
-// its warps take the tile's runs in turn.
+// W[r][k] = s * (q - c_b) for every weight, exact in fp32. One CTA per
+// super-tile walks its runs in stream order; its threads share each step.
 __global__ void __launch_bounds__(256) vbq_dequant_kernel(const uint8_t* __restrict__ data,
-                                                          const uint32_t* __restrict__ run_desc,
-                                                          const uint32_t* __restrict__ run_off,
-                                                          const uint32_t* __restrict__ tile_row0,
-                                                          const uint32_t* __restrict__ tile_run0, int32_t K,
+                                                          const uint64_t* __restrict__ st_byte0, int32_t K,
                                                           float* __restrict__ W) {
   const int t = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const uint32_t r0 = tile_row0[t];
-  for (uint32_t run = tile_run0[t] + warp; run < tile_run0[t + 1]; run += nw) {
-    const uint32_t d = run_desc[run];
-    const uint32_t cls = run_cls(d), n = run_n(d), g = run_g(d);
+  uint64_t o = st_byte0[t];
+  const uint64_t end = st_byte0[t + 1];
+  while (o < end) {
+    const RunHeader h = *reinterpret_cast<const RunHeader*>(data + o);
+    o += HEADER_BYTES;
+    const uint32_t cls = h.cls, n = h.n, b = 1u << cls;
     const uint32_t eps = entries_per_step(cls);
-    const uint8_t* rec = data + static_cast<uint64_t>(run_off[run]) * 16u;
-    for (uint32_t k = 0; k * eps < n; ++k, rec += full_step_bytes(cls)) {
-      const uint32_t e = min(eps, n - k * eps);
-      const uint32_t j = static_cast<uint32_t>(lane);  // one entry per lane
-      if (j >= e) continue;
-      const uint32_t b = 1u << cls;
-      const uint8_t* ent = rec + 8u * b * j;
-      const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rec + rec_scale_off(cls, e) + 2 * j));
-      const uint32_t row = rec[rec_row_off(cls, e) + j];
-      const float c = static_cast<float>((1u << b) - 1u) * 0.5f;
-      float* dst = W + static_cast<int64_t>(r0 + row) * K + static_cast<int64_t>(g) * GROUP;
-      for (uint32_t m = 0; m < GROUP; ++m) {
+    const float c = static_cast<float>((1u << b) - 1u) * 0.5f;
+    for (uint32_t done = 0; done < n; done += eps) {
+      const uint32_t e = min(eps, n - done);
+      const uint8_t* rec = data + o;
+      for (uint32_t i = threadIdx.x; i < e * GROUP; i += blockDim.x) {
+        const uint32_t j = i / GROUP, m = i % GROUP;
+        const uint8_t* ent = rec + 8u * b * j;
         uint32_t q;
-        if (b == 8) {
-          q = ent[m];
+        if (b == 1) {
+          q = (ent[m >> 3] >> (m & 7)) & 1u;
         } else {
-          q = 0;
-          for (uint32_t p = 0; p < b; ++p) q |= ((ent[8 * p + (m >> 3)] >> (m & 7)) & 1u) << p;
+          const uint32_t per_slice = GROUP / b, per_word = per_slice / 2;
+          const uint32_t s = m / per_slice, within = m % per_slice, hw = within / per_word, r = within % per_word;
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(ent + 8 * s + 4 * hw);
+          q = (w >> code_bit(b, r)) & ((1u << b) - 1u);
         }
-        dst[m] = __fmul_rn(sc, static_cast<float>(q) - c);
+        const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rec + rec_scale_off(cls, e) + 2 * j));
+        const uint32_t row = h.row0 + entry_tile(h, done + j) * TILE + rec[rec_row_off(cls, e) + j];
+        W[static_cast<int64_t>(row) * K + static_cast<int64_t>(h.g) * GROUP + m] = __fmul_rn(sc, static_cast<float>(q) - c);
       }
+      o += rec_bytes(cls, e);
     }
   }
 }
@@ -285,41 +339,23 @@ extern "C" vbq_status vbq_dequant(const vbq_matrix* m, float* W_dev, void* strea
   if (!W_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_dequant: NULL output");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   note_launches(1);
-  vbq_dequant_kernel<<<m->n_tiles, 256, 0, st>>>(m->data, m->run_desc, m->run_off, m->tile_row0, m->tile_run0,
-                                                 static_cast<int32_t>(m->K), W_dev);
+  vbq_dequant_kernel<<<m->n_super, 256, 0, st>>>(m->data, m->st_byte0, static_cast<int32_t>(m->K), W_dev);
   VBQ_CUDA_TRY(cudaGetLastError());
   return VBQ_OK;
 }
 
+// Batch columns one at a time through the batch-1 kernel (each call streams the matrix once).
 static vbq_status gemv_columns(const vbq_matrix* m, const uint16_t* X, int32_t B, float* Y, cudaStream_t st) {
   if (m->N == 0) return VBQ_OK;
   if (m->K == 0) {
     VBQ_CUDA_TRY(cudaMemsetAsync(Y, 0, sizeof(float) * static_cast<size_t>(m->N) * B, st));
     return VBQ_OK;
   }
+  if (m->K > XCAP) return fail(VBQ_ERR_UNSUPPORTED, "K above 16384 on the batch-1 path");
   int* err = device_check_word();
   if (!err) return fail(VBQ_ERR_CUDA, "device check word");
-  int done = 0;
-  while (done < B) {
-    const int left = B - done;
-    const int nb = left >= 4 ? 4 : left >= 2 ? 2 : 1;
-    GemvArgs a{};
-    a.it.seg[0] = view_of(m, Y + static_cast<int64_t>(done) * m->N, static_cast<int32_t>(m->N), nullptr);
-    a.it.nseg = 1;
-    a.it.plan = plan_view(m->plan);
-    a.it.xs.mode = X_BF16;
-    a.it.xs.K = static_cast<int32_t>(m->K);
-    a.it.xs.x = X + static_cast<int64_t>(done) * m->K;
-    a.it.xs.ldx = static_cast<int32_t>(m->K);
-    a.it.ep = EP_STORE;
-    a.err = err;
-    const bool w8 = nb == 4;  // the 4-column kernel has 8 warps
-    a.pieces = w8 ? m->plan.pieces8 : m->plan.pieces16;
-    a.pstart = w8 ? m->plan.start8 : m->plan.start16;
-    a.pbytes = w8 ? m->plan.bytes8 : m->plan.bytes16;
-    VBQ_CUDA_TRY(launch_gemv(nb, a, m->plan.n_ctas, st, false));
-    done += nb;
-  }
+  for (int j = 0; j < B; ++j)
+    VBQ_CUDA_TRY(launch_gemv1(m, X + static_cast<int64_t>(j) * m->K, Y + static_cast<int64_t>(j) * m->N, st, err));
   return VBQ_OK;
 }
 
@@ -328,7 +364,15 @@ extern "C" vbq_status vbq_gemv(const vbq_matrix* m, const uint16_t* x_dev, float
   if (m->N > 0 && !y_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemv: NULL y");
   if (m->N > 0 && m->K > 0 && !x_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemv: NULL x");
   if (!aligned(x_dev, 4) || !aligned(y_dev, 4)) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemv: x and y must be 4-byte aligned");
-  return gemv_columns(m, x_dev, 1, y_dev, static_cast<cudaStream_t>(stream));
+  int dev = 0;
+  VBQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemv: matrix is on another device");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (m->K > XCAP && m->N > 0) {
+    if (!tc_eligible(m)) return fail(VBQ_ERR_UNSUPPORTED, "vbq_gemv: K above 16384 needs the tensor-core path");
+    return launch_gemm_tc(m, x_dev, 1, y_dev, st);
+  }
+  return gemv_columns(m, x_dev, 1, y_dev, st);
 }
 
 extern "C" vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X_dev, int32_t B, float* Y_dev,
@@ -339,10 +383,14 @@ extern "C" vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X
   if (m->N > 0 && m->K > 0 && !X_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm_smallbatch: NULL X");
   if (!aligned(X_dev, 4) || !aligned(Y_dev, 4))
     return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm_smallbatch: X and Y must be 4-byte aligned");
-  // 16 or more columns form a dense contraction: the tensor-core dequant-MMA.
-  if (B >= 16 && m->N > 0 && m->K > 0 && aligned(X_dev, 16) && tc_eligible(m))
-    return launch_gemm_tc(m, X_dev, B, Y_dev, static_cast<cudaStream_t>(stream));
-  return gemv_columns(m, X_dev, B, Y_dev, static_cast<cudaStream_t>(stream));
+  int dev = 0;
+  VBQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm_smallbatch: matrix is on another device");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Two or more columns form a dense contraction: the tensor-core dequant-MMA decodes each code once.
+  if (B >= 2 && m->N > 0 && m->K > 0 && tc_eligible(m)) return launch_gemm_tc(m, X_dev, B, Y_dev, st);
+  if (B == 1 && m->K > XCAP && m->N > 0 && tc_eligible(m)) return launch_gemm_tc(m, X_dev, 1, Y_dev, st);
+  return gemv_columns(m, X_dev, B, Y_dev, st);
 }
 
 extern "C" vbq_status vbq_dense_gemv_bf16(const uint16_t* W_dev, const uint16_t* x_dev, float* y_dev, int64_t N,

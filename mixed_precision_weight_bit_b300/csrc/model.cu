@@ -1,30 +1,27 @@
 // vbq_decode_step: one batch-1 decode step through a stack of VBQ projections.
 //
 // VBQ abstract ("Variable Bit-width Quantization ..."): packed per-group codes
-// speed up token-by-token decode, whose speed memory bandwidth sets. The pages give no
-// architecture, so the glue below is this library's reading: unit-gamma
-// RMSNorm, attention at position 0 (a softmax over one key is 1, so each query
-// head returns its kv group's v), SwiGLU, fp32 residual, and bf16 at every
-// projection input.
+// speed up token-by-token decode, whose speed memory bandwidth sets. The pages
+// give no architecture, so the glue is this library's reading (decode.cuh):
+// unit-gain RMSNorm, attention at position 0 (each query head returns its kv
+// group's v), SwiGLU, fp32 residual, and bf16 at every projection input.
 //
-// A step is one persistent kernel (vbq_decode_kernel in gemv.cuh): one CTA per
-// SM runs h = x, then per layer four GEMV items, then the head:
-//   [q;k;v] (RMSNorm in its prologue), o (GQA gather in its prologue, residual
-//   in its epilogue), [gate;up] (RMSNorm prologue), down (SwiGLU prologue,
-//   residual epilogue),
-// with a grid barrier between items. Each warp streams its share of every
-// item's packed weights back to back, so the next item's weights are already
-// arriving while the CTAs wait at a barrier. The items, their work plans and
-// the per-warp piece lists are built once, when the model is created.
+// A step is one persistent cooperative launch (vbq_decode_kernel): per layer
+// the items [q;k;v], o, [gate;up], down, then the head, with a grid barrier
+// between items. Each warp streams its share of every item's packed weights
+// back to back, so the next item's weights arrive while the CTAs wait at a
+// barrier. Items, work plans and per-warp piece lists are built once, here.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <string>
 #include <vector>
 
+#include "decode.cuh"
 #include "internal.h"
-#include "launch.h"
 
 using namespace vbq;
 
@@ -32,9 +29,6 @@ namespace {
 
 enum { P_Q = 0, P_K, P_V, P_O, P_GATE, P_UP, P_DOWN, P_PER_LAYER };
 enum { L_QKV = 0, L_O, L_GU, L_DOWN, L_PER_LAYER };
-
-constexpr int DEC_W = 16;     // warps per CTA of the decode kernel
-constexpr int DEC_NSLOT = 2;  // ring slots per warp
 
 int64_t proj_n(const vbq_model_desc& d, int p) {
   switch (p) {
@@ -54,23 +48,29 @@ int64_t proj_k(const vbq_model_desc& d, int p) {
   }
 }
 
-int64_t round64(int64_t n) { return (n + 63) & ~int64_t(63); }
+int64_t n_super_of(int64_t n) { return (n + SROWS - 1) / SROWS; }
+uint32_t decode_smem_bytes() { return smem_layout(kRingSlots).total + XT_MAX * 2; }
 
-// Float offsets of one step's activations inside a region: the grid-barrier
-// counters, h, [q;k;v] and [gate;up]. The counters must be zero before a step;
-// each step leaves them so. (Split-tile partial rows and arrival counters live
-// in each item's work plan, which the model owns.)
+// Offsets (in 8-byte words) of one step's scratch inside a region. All of it
+// must be zero before the first step; every step leaves the fixed-point sums
+// and counters so, and writes h and the per-item exponents before reading them.
 struct Layout {
-  int64_t bar = 0, h = 0, qkv = 0, gu = 0, total = 0;
+  int64_t bar = 0, F = 0, maxx = 0, h = 0, qkv = 0, o = 0, gu = 0, dn = 0, logits = 0, total = 0;
 };
 
-Layout layout_of(const vbq_model_desc& d) {
+Layout layout_of(const vbq_model_desc& d, int32_t n_items) {
   Layout L;
+  auto r8 = [](int64_t n) { return (n + 7) & ~int64_t(7); };
   L.bar = 0;
-  L.h = 64;
-  L.qkv = L.h + round64(d.d);
-  L.gu = L.qkv + round64(proj_n(d, P_Q) + 2 * proj_n(d, P_K));
-  L.total = L.gu + round64(2 * int64_t(d.d_ff));
+  L.F = 8;                                   // int [n_items]
+  L.maxx = L.F + r8((n_items + 1) / 2);      // float [n_items]
+  L.h = L.maxx + r8((n_items + 1) / 2);      // float [2][d]
+  L.qkv = L.h + r8(d.d);                     // u64 [1024 * (st(q) + st(k) + st(v))]
+  L.o = L.qkv + SROWS * (n_super_of(proj_n(d, P_Q)) + 2 * n_super_of(proj_n(d, P_K)));
+  L.gu = L.o + SROWS * n_super_of(d.d);
+  L.dn = L.gu + SROWS * 2 * n_super_of(d.d_ff);
+  L.logits = L.dn + SROWS * n_super_of(d.d);
+  L.total = L.logits + SROWS * n_super_of(d.vocab);
   return L;
 }
 
@@ -81,8 +81,9 @@ struct vbq_model {
   std::vector<const vbq_matrix*> mats;
   int device = 0;
   int sms = 0;
+  int32_t n_items = 0;
   Layout lay;
-  float* ws = nullptr;              // this model's step scratch (Layout), then the host-step staging
+  uint64_t* ws = nullptr;            // step scratch (Layout), then the host-step staging
   uint16_t* x_stage = nullptr;
   float* logits_stage = nullptr;
   bool trace = false;
@@ -90,156 +91,168 @@ struct vbq_model {
   float* tr_out = nullptr;
   std::vector<int64_t> in_off, out_off;
   int64_t in_total = 0, out_total = 0;
-  std::vector<DevicePlan> plans;    // per item
-  void* prog_mem = nullptr;         // piece lists and the items of both programs
+  std::vector<void*> plan_mem;       // per item: warp and CTA plans
+  std::vector<const WarpPlan*> item_warps;
+  std::vector<const CtaPlan*> item_ctas;
+  std::vector<std::vector<uint32_t>> item_st_off;
+  void* prog_mem = nullptr;          // piece lists and the item arrays
   const uint64_t* pieces = nullptr;
   const uint32_t* pstart = nullptr;
   const uint32_t* pbytes = nullptr;
-  Item* items_ws = nullptr;         // items over ws
-  Item* items_static = nullptr;     // items over the static scratch (null if the model does not fit it)
-  ZeroSpec pre_ws[2] = {}, pre_static[2] = {};  // what each program clears before its first barrier
-  float* static_base = nullptr;
-  int32_t n_items = 0;
-  int* err = nullptr;               // the device check word of the model's device
+  DItem* items_ws = nullptr;         // items over ws
+  DItem* items_static = nullptr;     // items over the static scratch (null if the model does not fit it)
+  uint64_t* static_base = nullptr;
+  int* err = nullptr;
 };
 
 namespace {
 
 // The static scratch of vbq_decode_step_noalloc (defined at the bottom of this file).
-vbq_status step_scratch_address(int dev, float** out);
-constexpr int64_t kStepScratchFloats = 65536;
+vbq_status step_scratch_address(int dev, uint64_t** out);
+constexpr int64_t kStepScratchWords = 262144;  // 2 MiB
 
-// The items of one step over the scratch at `base`. Each item clears the
-// output of the item two after it (the outputs that split tiles add into);
-// pre receives the outputs of the first two items, cleared before the first
-// grid barrier.
-std::vector<Item> make_items(const vbq_model* m, float* base, bool trace, ZeroSpec pre[2]) {
+float l1_of(std::initializer_list<const vbq_matrix*> ms) {
+  float v = 0.0f;
+  for (const vbq_matrix* m : ms) v = std::max(v, m->max_row_l1);
+  return v;
+}
+
+// The items of one step over the scratch at base.
+std::vector<DItem> make_items(const vbq_model* m, uint64_t* base, bool trace) {
   const vbq_model_desc& d = m->desc;
   const Layout& L = m->lay;
-  float* h = base + L.h;
-  float* qkv = base + L.qkv;
-  float* gu = base + L.gu;
+  int* Fs = reinterpret_cast<int*>(base + L.F);
+  float* mx = reinterpret_cast<float*>(base + L.maxx);
+  float* hb[2] = {reinterpret_cast<float*>(base + L.h), reinterpret_cast<float*>(base + L.h) + d.d};
+  unsigned long long* qkv = reinterpret_cast<unsigned long long*>(base + L.qkv);
+  unsigned long long* yo = reinterpret_cast<unsigned long long*>(base + L.o);
+  unsigned long long* gu = reinterpret_cast<unsigned long long*>(base + L.gu);
+  unsigned long long* yd = reinterpret_cast<unsigned long long*>(base + L.dn);
+  unsigned long long* lg = reinterpret_cast<unsigned long long*>(base + L.logits);
   const int64_t nq = proj_n(d, P_Q), nkv = proj_n(d, P_K);
+  const int64_t n_qkv = L.o - L.qkv, n_yo = L.gu - L.o, n_gu = L.dn - L.gu, n_yd = L.logits - L.dn;
   auto tin = [&](int p) -> uint16_t* { return trace ? m->tr_in + m->in_off[p] : nullptr; };
   auto tout = [&](int p) -> float* { return trace ? m->tr_out + m->out_off[p] : nullptr; };
-  std::vector<Item> items;
-  std::vector<ZeroSpec> outputs;  // per item: what its split tiles add into (n = 0: adds onto h)
-  std::vector<CopySpec> traces;   // per item: its traced output, copied by the next item
-  auto item_for = [&](int li) {
-    Item it{};
-    it.plan = plan_view(m->plans[li]);
-    it.ep = EP_STORE;
+  std::vector<DItem> items;
+  int cur = 0;  // h buffer holding the latest residual
+  auto base_item = [&](int idx, int mode, int K, float l1, unsigned long long* out) {
+    DItem it{};
+    it.warps = m->item_warps[idx];
+    it.ctas = m->item_ctas[idx];
+    for (size_t s = 0; s < m->item_st_off[idx].size() && s < static_cast<size_t>(MAX_SEG); ++s)
+      it.seg_st_off[s] = m->item_st_off[idx][s];
+    it.mode = mode;
+    it.K = K;
+    it.l1 = l1;
+    it.out = out;
+    it.F_out = Fs + idx;
+    it.maxx_out = mx + idx;
+    it.eps = d.rms_eps;
     return it;
-  };
-  auto add_seg = [&](Item& it, const vbq_matrix* w, float* y, float* ty) {
-    it.seg[it.nseg] = view_of(w, y, static_cast<int32_t>(w->N), ty);
-    it.nseg += 1;
   };
   for (int l = 0; l < d.n_layers; ++l) {
     const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
-    const int p0 = l * P_PER_LAYER, l0 = l * L_PER_LAYER;
-    {  // [q; k; v] = W u, u = bf16(rmsnorm(h))
-      Item it = item_for(l0 + L_QKV);
-      add_seg(it, W[P_Q], qkv, nullptr);
-      add_seg(it, W[P_K], qkv + nq, nullptr);
-      add_seg(it, W[P_V], qkv + nq + nkv, nullptr);
-      it.xs.mode = X_RMSNORM;
-      it.xs.K = d.d;
-      it.xs.h = h;
-      it.xs.eps = d.rms_eps;
-      it.xs.trace_x = tin(p0 + P_Q);
+    const int p0 = l * P_PER_LAYER, i0 = l * L_PER_LAYER;
+    {  // [q; k; v] = W bf16(rmsnorm(h)), h = h + y_down of the previous layer
+      DItem it = base_item(i0 + L_QKV, X_RMS, d.d, l1_of({W[P_Q], W[P_K], W[P_V]}), qkv);
+      it.h_prev = l == 0 ? nullptr : hb[cur];
+      it.y_add = l == 0 ? nullptr : yd;
+      it.F_add = l == 0 ? nullptr : Fs + (i0 - 1);
+      it.h_next = hb[1 - cur];
+      cur = 1 - cur;
+      it.zero[0] = ZeroSpec{gu, n_gu};
+      if (trace && l > 0) it.tcopy[0] = CopySpec{yd, Fs + (i0 - 1), tout(p0 - 1), d.d};
+      it.trace_x = tin(p0 + P_Q);
       items.push_back(it);
-      outputs.push_back(ZeroSpec{qkv, 0, static_cast<int32_t>(nq + 2 * nkv)});
-      traces.push_back(CopySpec{qkv, tout(p0 + P_Q), trace ? static_cast<int32_t>(nq + 2 * nkv) : 0});
     }
-    {  // h += Wo a, a = bf16(v of each head's kv group)
-      Item it = item_for(l0 + L_O);
-      add_seg(it, W[P_O], h, tout(p0 + P_O));
-      it.xs.mode = X_GQA;
-      it.xs.K = static_cast<int32_t>(nq);
-      it.xs.v = qkv + nq + nkv;
-      it.xs.head_dim = d.head_dim;
-      it.xs.group = d.n_heads / d.n_kv_heads;
-      it.xs.trace_x = tin(p0 + P_O);
-      it.ep = EP_RESID;
-      it.resid = h;
+    const std::vector<uint32_t>& so = m->item_st_off[i0 + L_QKV];
+    {  // h += W_o bf16(v of each head's kv group)
+      DItem it = base_item(i0 + L_O, X_GQA, static_cast<int>(nq), l1_of({W[P_O]}), yo);
+      it.src = qkv;
+      it.F_src = Fs + i0 + L_QKV;
+      it.v_off = int64_t(so[2]) * SROWS;
+      it.head_dim = d.head_dim;
+      it.group = d.n_heads / d.n_kv_heads;
+      it.zero[0] = ZeroSpec{yd, n_yd};
+      if (trace) {
+        it.tcopy[0] = CopySpec{qkv, Fs + i0, tout(p0 + P_Q), static_cast<int32_t>(nq)};
+        it.tcopy[1] = CopySpec{qkv + int64_t(so[1]) * SROWS, Fs + i0, tout(p0 + P_K), static_cast<int32_t>(nkv)};
+        it.tcopy[2] = CopySpec{qkv + int64_t(so[2]) * SROWS, Fs + i0, tout(p0 + P_V), static_cast<int32_t>(nkv)};
+      }
+      it.trace_x = tin(p0 + P_O);
       items.push_back(it);
-      outputs.push_back(ZeroSpec{nullptr, 0, 0});
-      traces.push_back(CopySpec{});
     }
-    {  // [gate; up] = W u, u = bf16(rmsnorm(h))
-      Item it = item_for(l0 + L_GU);
-      add_seg(it, W[P_GATE], gu, nullptr);
-      add_seg(it, W[P_UP], gu + d.d_ff, nullptr);
-      it.xs.mode = X_RMSNORM;
-      it.xs.K = d.d;
-      it.xs.h = h;
-      it.xs.eps = d.rms_eps;
-      it.xs.trace_x = tin(p0 + P_GATE);
+    {  // [gate; up] = W bf16(rmsnorm(h)), h = h + y_o
+      DItem it = base_item(i0 + L_GU, X_RMS, d.d, l1_of({W[P_GATE], W[P_UP]}), gu);
+      it.h_prev = hb[cur];
+      it.y_add = yo;
+      it.F_add = Fs + i0 + L_O;
+      it.h_next = hb[1 - cur];
+      cur = 1 - cur;
+      it.zero[0] = ZeroSpec{qkv, n_qkv};
+      if (trace) it.tcopy[0] = CopySpec{yo, Fs + i0 + L_O, tout(p0 + P_O), d.d};
+      it.trace_x = tin(p0 + P_GATE);
       items.push_back(it);
-      outputs.push_back(ZeroSpec{gu, 0, 2 * d.d_ff});
-      traces.push_back(CopySpec{gu, tout(p0 + P_GATE), trace ? 2 * d.d_ff : 0});
     }
-    {  // h += Wdown bf16(silu(gate) * up)
-      Item it = item_for(l0 + L_DOWN);
-      add_seg(it, W[P_DOWN], h, tout(p0 + P_DOWN));
-      it.xs.mode = X_SWIGLU;
-      it.xs.K = d.d_ff;
-      it.xs.gate = gu;
-      it.xs.up = gu + d.d_ff;
-      it.xs.trace_x = tin(p0 + P_DOWN);
-      it.ep = EP_RESID;
-      it.resid = h;
+    const std::vector<uint32_t>& sg = m->item_st_off[i0 + L_GU];
+    {  // h += W_down bf16(silu(gate) * up)
+      DItem it = base_item(i0 + L_DOWN, X_SWIGLU, d.d_ff, l1_of({W[P_DOWN]}), yd);
+      it.src = gu;
+      it.F_src = Fs + i0 + L_GU;
+      it.up_off = int64_t(sg[1]) * SROWS;
+      it.maxx_src = mx + i0 + L_GU;
+      it.l1_gate = W[P_GATE]->max_row_l1;
+      it.l1_up = W[P_UP]->max_row_l1;
+      it.zero[0] = ZeroSpec{yo, n_yo};
+      if (trace) {
+        it.tcopy[0] = CopySpec{gu, Fs + i0 + L_GU, tout(p0 + P_GATE), d.d_ff};
+        it.tcopy[1] = CopySpec{gu + it.up_off, Fs + i0 + L_GU, tout(p0 + P_UP), d.d_ff};
+      }
+      it.trace_x = tin(p0 + P_DOWN);
       items.push_back(it);
-      outputs.push_back(ZeroSpec{nullptr, 0, 0});
-      traces.push_back(CopySpec{});
     }
   }
-  {  // logits = Whead bf16(rmsnorm(h)), into the launch's output
-    const int lh = d.n_layers * L_PER_LAYER, ph = d.n_layers * P_PER_LAYER;
-    Item it = item_for(lh);
-    add_seg(it, m->mats[ph], nullptr, nullptr);  // traced by a copy after the launch
-    it.xs.mode = X_RMSNORM;
-    it.xs.K = d.d;
-    it.xs.h = h;
-    it.xs.eps = d.rms_eps;
-    it.xs.trace_x = tin(ph);
+  {  // logits = W_head bf16(rmsnorm(h + y_down))
+    const int ih = d.n_layers * L_PER_LAYER, ph = d.n_layers * P_PER_LAYER;
+    DItem it = base_item(ih, X_RMS, d.d, l1_of({m->mats[ph]}), lg);
+    it.h_prev = d.n_layers > 0 ? hb[cur] : nullptr;
+    it.y_add = d.n_layers > 0 ? yd : nullptr;
+    it.F_add = d.n_layers > 0 ? Fs + (ih - 1) : nullptr;
+    it.zero[0] = ZeroSpec{gu, n_gu};
+    if (trace && d.n_layers > 0) it.tcopy[0] = CopySpec{yd, Fs + (ih - 1), tout(ph - 1), d.d};
+    it.trace_x = tin(ph);
     items.push_back(it);
-    outputs.push_back(ZeroSpec{nullptr, 0, d.vocab});  // the launch's logits
-    traces.push_back(CopySpec{});
   }
-  for (size_t i = 1; i < items.size(); ++i) items[i].tcopy = traces[i - 1];
-  for (size_t i = 0; i < items.size(); ++i) items[i].zero = i + 2 < items.size() ? outputs[i + 2] : ZeroSpec{};
-  for (int i = 0; i < 2; ++i) pre[i] = static_cast<size_t>(i) < outputs.size() ? outputs[i] : ZeroSpec{};
   return items;
 }
 
-cudaError_t upload_items(const std::vector<Item>& items, Item* dst) {
-  return cudaMemcpy(dst, items.data(), sizeof(Item) * items.size(), cudaMemcpyHostToDevice);
+cudaError_t upload_items(const std::vector<DItem>& items, DItem* dst) {
+  return cudaMemcpy(dst, items.data(), sizeof(DItem) * items.size(), cudaMemcpyHostToDevice);
 }
 
-cudaError_t launch_decode(const vbq_model* m, const Item* items, const ZeroSpec* pre, float* base,
-                          const uint16_t* x, float* out, cudaStream_t st, int* err) {
+cudaError_t launch_decode(const vbq_model* m, const DItem* items, uint64_t* base, const uint16_t* x, float* out,
+                          cudaStream_t st, int* err) {
+  const Layout& L = m->lay;
   DecodeArgs a{};
-  a.prog.items = items;
-  a.prog.n_items = m->n_items;
-  a.prog.pieces = m->pieces;
-  a.prog.pstart = m->pstart;
-  a.prog.pbytes = m->pbytes;
-  a.prog.h = base + m->lay.h;
-  a.prog.d = m->desc.d;
-  a.prog.grid_bar = reinterpret_cast<uint32_t*>(base + m->lay.bar);
-  a.prog.err = err;
-  a.prog.pre[0] = pre[0];
-  a.prog.pre[1] = pre[1];
+  a.items = items;
+  a.n_items = m->n_items;
+  a.pieces = m->pieces;
+  a.pstart = m->pstart;
+  a.pbytes = m->pbytes;
   a.x = x;
-  a.out = out;
-  // The grid-barrier and split-tile counters are zero here: the scratch starts
-  // zeroed, and every launch leaves them at zero when it ends.
+  a.logits = out;
+  a.logits_acc = reinterpret_cast<const unsigned long long*>(base + L.logits);
+  a.logits_acc_w = reinterpret_cast<unsigned long long*>(base + L.logits);
+  a.F_head = reinterpret_cast<const int*>(base + L.F) + (m->n_items - 1);
+  a.vocab = m->desc.vocab;
+  a.final_zero = ZeroSpec{reinterpret_cast<unsigned long long*>(base + L.dn), L.logits - L.dn};
+  a.grid_bar = reinterpret_cast<uint32_t*>(base + L.bar);
+  a.ns = kRingSlots;
+  a.err = err;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(m->sms), 1, 1);
-  cfg.blockDim = dim3(DEC_W * 32, 1, 1);
-  cfg.dynamicSmemBytes = GemvSmem<1, DEC_W, DEC_NSLOT>::kBytesStaged;
+  cfg.blockDim = dim3(KW * 32, 1, 1);
+  cfg.dynamicSmemBytes = decode_smem_bytes();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // every CTA is resident: the grid barriers need it
@@ -247,7 +260,7 @@ cudaError_t launch_decode(const vbq_model* m, const Item* items, const ZeroSpec*
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   note_launches(1);
-  return cudaLaunchKernelEx(&cfg, vbq_decode_kernel<DEC_W, DEC_NSLOT>, a);
+  return cudaLaunchKernelEx(&cfg, vbq_decode_kernel, a);
 }
 
 void prepare_decode_kernel() {
@@ -257,8 +270,7 @@ void prepare_decode_kernel() {
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return;
-  cudaFuncSetAttribute(vbq_decode_kernel<DEC_W, DEC_NSLOT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       GemvSmem<1, DEC_W, DEC_NSLOT>::kBytesStaged);
+  cudaFuncSetAttribute(vbq_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes());
   done[dev] = true;
 }
 
@@ -272,11 +284,13 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   if (!desc || !mats) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_create: NULL desc or mats");
   const vbq_model_desc d = *desc;
   if (d.n_layers < 0 || d.d <= 0 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.head_dim <= 0 || d.d_ff <= 0 ||
-      d.vocab <= 0 || d.n_heads % d.n_kv_heads || d.head_dim % 2 || !(d.rms_eps >= 0.0f))
+      d.vocab <= 0 || d.n_heads % d.n_kv_heads || !(d.rms_eps >= 0.0f))
     return fail(VBQ_ERR_SHAPE, "vbq_model_create: invalid shapes");
-  if (d.d > XCAP || d.d_ff > XCAP || int64_t(d.n_heads) * d.head_dim > XCAP)
-    return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: d, d_ff and n_heads*head_dim must be at most " +
-                                         std::to_string(XCAP) + " (the decode kernel stages x in shared memory)");
+  if (d.d % GROUP || d.d_ff % GROUP || (int64_t(d.n_heads) * d.head_dim) % GROUP)
+    return fail(VBQ_ERR_SHAPE, "vbq_model_create: d, d_ff and n_heads*head_dim must be multiples of 64");
+  if (d.d > XT_MAX || int64_t(d.n_heads) * d.head_dim > XT_MAX || d.d_ff > XCAP)
+    return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: d and n_heads*head_dim must be at most " +
+                                         std::to_string(XT_MAX) + " and d_ff at most " + std::to_string(XCAP));
   const int nm = d.n_layers * P_PER_LAYER + 1;
   int dev = 0;
   VBQ_CUDA_TRY(cudaGetDevice(&dev));
@@ -323,30 +337,39 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   m->in_total = io;
   m->out_total = oo;
 
-  // One plan per item, every one over exactly one CTA per SM; the piece lists of all items in turn.
+  // One plan per item, each over exactly one CTA per SM; the piece lists of all items in turn.
   std::vector<std::vector<uint64_t>> per_warp;
   auto add_plan = [&](std::initializer_list<const vbq_matrix*> ms) -> vbq_status {
-    std::vector<SegTables> segs;
-    std::vector<const uint8_t*> data;
+    std::vector<SegPlanInput> segs;
     for (const vbq_matrix* w : ms) {
-      segs.push_back(seg_tables(w));
-      data.push_back(w->data);
+      SegPlanInput s;
+      s.runs = &w->runs;
+      s.data = w->data;
+      s.n_super = static_cast<uint32_t>(w->n_super);
+      s.G = static_cast<uint32_t>(w->G);
+      segs.push_back(s);
     }
-    Plan pl = make_plan(segs, m->sms, MAX_UNITS_PER_CTA);
-    if (pl.n_ctas != m->sms && pl.n_ctas != 0)
-      return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: a projection needs more than one CTA per SM");
-    if (pl.n_ctas == 0) {  // an empty projection: one empty slot per CTA
-      pl.n_ctas = m->sms;
-      pl.umax = 1;
-      pl.units.assign(m->sms, UnitRec{});
-      pl.slices.assign(static_cast<size_t>(m->sms) * SLICES, SliceRec{});
-    }
-    if (!append_pieces(pl, data, DEC_W, &per_warp))
-      return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: weight address beyond 2^48 or a warp piece of 16 MiB or more");
-    DevicePlan dp;
-    cudaError_t err = upload_plan(pl, 1, data, nullptr, &dp);
-    if (err != cudaSuccess) return cuda_fail(err, "vbq_model_create: plan upload");
-    m->plans.push_back(dp);
+    ItemPlan pl;
+    const char* why = "";
+    if (!make_item_plan(segs, m->sms, &pl, &why))
+      return fail(VBQ_ERR_UNSUPPORTED, std::string("vbq_model_create: ") + why);
+    if (!append_pieces(pl, segs, &per_warp))
+      return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: weight address beyond 2^48");
+    per_warp.resize(static_cast<size_t>(m->sms) * KW);
+    auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
+    const size_t bw = al(sizeof(WarpPlan) * pl.warps.size()), bc = al(sizeof(CtaPlan) * pl.ctas.size());
+    void* mem = nullptr;
+    cudaError_t e = cudaMalloc(&mem, bw + bc);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(mem, pl.warps.data(), sizeof(WarpPlan) * pl.warps.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(static_cast<char*>(mem) + bw, pl.ctas.data(), sizeof(CtaPlan) * pl.ctas.size(),
+                     cudaMemcpyHostToDevice);
+    if (mem) m->plan_mem.push_back(mem);
+    if (e != cudaSuccess) return cuda_fail(e, "vbq_model_create: plan upload");
+    m->item_warps.push_back(static_cast<const WarpPlan*>(mem));
+    m->item_ctas.push_back(reinterpret_cast<const CtaPlan*>(static_cast<char*>(mem) + bw));
+    m->item_st_off.push_back(pl.st_off);
     return VBQ_OK;
   };
   vbq_status s = VBQ_OK;
@@ -363,13 +386,13 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
     vbq_model_free(m);
     return s;
   }
-  m->n_items = static_cast<int32_t>(m->plans.size());
-  m->lay = layout_of(d);
+  m->n_items = static_cast<int32_t>(m->item_warps.size());
+  m->lay = layout_of(d, m->n_items);
 
   // Device memory: the step scratch, the host-step staging, the piece lists and both item arrays.
   const PieceSet ps = finish_pieces(per_warp);
   auto al = [](int64_t b) { return (b + 255) & ~int64_t(255); };
-  const int64_t b_ws = al(4 * m->lay.total), b_x = al(2 * int64_t(d.d)), b_lg = al(4 * int64_t(d.vocab));
+  const int64_t b_ws = al(8 * m->lay.total), b_x = al(2 * int64_t(d.d)), b_lg = al(4 * int64_t(d.vocab));
   cudaError_t e = cudaMalloc(&m->ws, b_ws + b_x + b_lg);
   if (e == cudaSuccess) e = cudaMemset(m->ws, 0, b_ws);
   if (e != cudaSuccess) {
@@ -381,8 +404,8 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   const int64_t o_p = 0, o_s = al(8 * int64_t(std::max<size_t>(1, ps.pieces.size())));
   const int64_t o_b = o_s + al(4 * int64_t(ps.start.size()));
   const int64_t o_i1 = o_b + al(4 * int64_t(std::max<size_t>(1, ps.bytes.size())));
-  const int64_t o_i2 = o_i1 + al(int64_t(sizeof(Item)) * m->n_items);
-  const int64_t total = o_i2 + al(int64_t(sizeof(Item)) * m->n_items);
+  const int64_t o_i2 = o_i1 + al(int64_t(sizeof(DItem)) * m->n_items);
+  const int64_t total = o_i2 + al(int64_t(sizeof(DItem)) * m->n_items);
   e = cudaMalloc(&m->prog_mem, total);
   char* pm = static_cast<char*>(m->prog_mem);
   if (e == cudaSuccess && !ps.pieces.empty())
@@ -397,20 +420,20 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   m->pieces = reinterpret_cast<const uint64_t*>(pm + o_p);
   m->pstart = reinterpret_cast<const uint32_t*>(pm + o_s);
   m->pbytes = reinterpret_cast<const uint32_t*>(pm + o_b);
-  m->items_ws = reinterpret_cast<Item*>(pm + o_i1);
-  e = upload_items(make_items(m, m->ws, false, m->pre_ws), m->items_ws);
+  m->items_ws = reinterpret_cast<DItem*>(pm + o_i1);
+  e = upload_items(make_items(m, m->ws, false), m->items_ws);
   // The program over the static scratch of vbq_decode_step_noalloc, when the model fits it. That entry
   // point's set-up happens here, with the model's device current, so that its calls allocate nothing.
-  if (e == cudaSuccess && m->lay.total <= kStepScratchFloats) {
-    float* sb = nullptr;
+  if (e == cudaSuccess && m->lay.total <= kStepScratchWords) {
+    uint64_t* sb = nullptr;
     vbq_status ss = step_scratch_address(dev, &sb);
     if (ss != VBQ_OK) {
       vbq_model_free(m);
       return ss;
     }
     m->static_base = sb;
-    m->items_static = reinterpret_cast<Item*>(pm + o_i2);
-    e = upload_items(make_items(m, sb, false, m->pre_static), m->items_static);
+    m->items_static = reinterpret_cast<DItem*>(pm + o_i2);
+    e = upload_items(make_items(m, sb, false), m->items_static);
   }
   if (e != cudaSuccess) {
     vbq_model_free(m);
@@ -431,7 +454,7 @@ extern "C" void vbq_model_free(vbq_model* m) {
   cudaFree(m->prog_mem);
   cudaFree(m->tr_in);
   cudaFree(m->tr_out);
-  for (DevicePlan& p : m->plans) free_plan(&p);
+  for (void* p : m->plan_mem) cudaFree(p);
   cudaSetDevice(cur);
   delete m;
 }
@@ -440,10 +463,11 @@ extern "C" vbq_status vbq_decode_step(vbq_model* m, const uint16_t* x_dev, float
   if (!m || !x_dev || !logits_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: NULL argument");
   if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 4)
     return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: misaligned buffer (x and logits need 4-byte alignment)");
+  int dev = 0;
+  VBQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step: model is on another device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (m->trace)  // traced outputs that add onto the residual are sums of adds
-    VBQ_CUDA_TRY(cudaMemsetAsync(m->tr_out, 0, 4 * static_cast<size_t>(m->out_total), st));
-  VBQ_CUDA_TRY(launch_decode(m, m->items_ws, m->pre_ws, m->ws, x_dev, logits_dev, st, m->err));
+  VBQ_CUDA_TRY(launch_decode(m, m->items_ws, m->ws, x_dev, logits_dev, st, m->err));
   if (m->trace) {
     const int64_t ph = int64_t(m->desc.n_layers) * P_PER_LAYER;
     VBQ_CUDA_TRY(cudaMemcpyAsync(m->tr_out + m->out_off[ph], logits_dev, 4 * static_cast<size_t>(m->desc.vocab),
@@ -472,7 +496,7 @@ extern "C" vbq_status vbq_model_set_trace(vbq_model* m, int32_t enable) {
   }
   m->trace = enable != 0;
   VBQ_CUDA_TRY(cudaDeviceSynchronize());  // no step may be reading the items
-  VBQ_CUDA_TRY(upload_items(make_items(m, m->ws, m->trace, m->pre_ws), m->items_ws));
+  VBQ_CUDA_TRY(upload_items(make_items(m, m->ws, m->trace), m->items_ws));
   return VBQ_OK;
 }
 
@@ -500,27 +524,30 @@ extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host
 
 // ---------------------------------------------------------------- allocation-free decode step
 //
-// vbq_decode_step keeps its step scratch (activations and the grid-barrier
-// counters) in memory that vbq_model_create allocated for the model. Some callers cannot tie device memory to a model
-// they step: code that runs while another component is capturing the stream
-// into its own graph, real-time loops whose device memory is fixed before the
-// loop starts, or hosts that hand out device memory only from their own pool.
-// vbq_decode_step_noalloc serves them: it launches the same kernel with the
-// step's scratch in the file-scope array below, and allocates nothing.
+// vbq_decode_step keeps its step scratch (fixed-point sums, the residual,
+// per-item exponents and the grid-barrier counters) in memory that
+// vbq_model_create allocated for the model. Some callers cannot tie device
+// memory to a model they step: code that runs while another component is
+// capturing the stream into its own graph, real-time loops whose device memory
+// is fixed before the loop starts, or hosts that hand out device memory only
+// from their own pool. vbq_decode_step_noalloc serves them: it launches the
+// same kernel with the step's scratch in the file-scope array below, and
+// allocates nothing.
 
 namespace {
 
-// Step scratch of vbq_decode_step_noalloc, in the Layout of the model: 65,536
-// floats = 256 KiB on every device that loads this library, held until the
+// Step scratch of vbq_decode_step_noalloc, in the Layout of the model: 262,144
+// 8-byte words = 2 MiB on every device that loads this library, held until the
 // process exits.
-static __device__ __align__(256) float g_step_scratch[kStepScratchFloats];
+static __device__ __align__(256) uint64_t g_step_scratch[kStepScratchWords];
 
 std::mutex g_step_scratch_mu;
-std::map<int, float*> g_step_scratch_addr;  // device ordinal -> device address of g_step_scratch
+std::map<int, uint64_t*> g_step_scratch_addr;  // device ordinal -> device address of g_step_scratch
 
 // Device address of g_step_scratch on device dev, which must be current. The
-// first call on a device looks it up; later calls only read the cached value.
-vbq_status step_scratch_address(int dev, float** out) {
+// first call on a device looks it up and clears the array; later calls only
+// read the cached value.
+vbq_status step_scratch_address(int dev, uint64_t** out) {
   std::lock_guard<std::mutex> lock(g_step_scratch_mu);
   auto it = g_step_scratch_addr.find(dev);
   if (it != g_step_scratch_addr.end()) {
@@ -530,12 +557,12 @@ vbq_status step_scratch_address(int dev, float** out) {
   void* p = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_step_scratch)");
-  // Steps need the counters at zero; they leave them so.
-  e = cudaMemset(p, 0, sizeof(float) * kStepScratchFloats);
+  // Steps need the sums and counters at zero; they leave them so.
+  e = cudaMemset(p, 0, sizeof(uint64_t) * kStepScratchWords);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "clearing g_step_scratch");
-  g_step_scratch_addr[dev] = static_cast<float*>(p);
-  *out = static_cast<float*>(p);
+  g_step_scratch_addr[dev] = static_cast<uint64_t*>(p);
+  *out = static_cast<uint64_t*>(p);
   return VBQ_OK;
 }
 
@@ -546,16 +573,16 @@ extern "C" vbq_status vbq_decode_step_noalloc(vbq_model* m, const uint16_t* x_de
   if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 4)
     return fail(VBQ_ERR_INVALID_ARG,
                 "vbq_decode_step_noalloc: misaligned buffer (x and logits need 4-byte alignment)");
-  if (m->lay.total > kStepScratchFloats)
+  if (m->lay.total > kStepScratchWords)
     return fail(VBQ_ERR_SHAPE, "vbq_decode_step_noalloc: the step needs " + std::to_string(m->lay.total) +
-                                   " scratch floats (barrier block, h, q/k/v and gate/up, each rounded up to 64); the "
-                                   "static scratch holds " +
-                                   std::to_string(kStepScratchFloats));
+                                   " scratch words of 8 bytes (counters, exponents, h, and the fixed-point sums of "
+                                   "q/k/v, o, gate/up, down and the head); the static scratch holds " +
+                                   std::to_string(kStepScratchWords));
   int dev = 0;
   VBQ_CUDA_TRY(cudaGetDevice(&dev));
   if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: model is on another device");
   if (!m->items_static) return fail(VBQ_ERR_CUDA, "vbq_decode_step_noalloc: the static scratch was not set up");
-  cudaError_t e = launch_decode(m, m->items_static, m->pre_static, m->static_base, x_dev, logits_dev,
+  cudaError_t e = launch_decode(m, m->items_static, m->static_base, x_dev, logits_dev,
                                 static_cast<cudaStream_t>(stream), m->err);
   if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: launch");
   return VBQ_OK;

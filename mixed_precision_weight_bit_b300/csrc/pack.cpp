@@ -2,7 +2,7 @@
 //
 // VBQ abstract ("Variable Bit-width Quantization ..."): once the per-group bit
 // allocation is fixed, the weights can be stored as packed low-bit codes. The
-// record format, tile plan and class ordering are this library's own design.
+// record format, tile order and class ordering are this library's own design.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -18,112 +18,38 @@ using namespace vbq;
 
 inline int bits_to_cls(uint8_t b) { return b == 1 ? 0 : b == 2 ? 1 : b == 4 ? 2 : 3; }
 
-// Packs the 64 codes of one group into 8*b bytes.
-//  b = 1, 2, 4: bit-planes. Plane p (bit p of every code) fills bytes [8p, 8p+8),
-//               with code m's bit at bit m of the plane (little-endian).
-//  b = 8:       one byte per code, code m in byte m.
+// Packs the 64 codes q of one group of b bits into 8*b bytes (layout.h).
 inline void pack_entry(const uint8_t* q, int b, uint8_t* dst) {
   const int nbytes = 8 * b;
   std::memset(dst, 0, nbytes);
-  if (b == 8) {
-    std::memcpy(dst, q, GROUP);
+  if (b == 1) {
+    for (int m = 0; m < GROUP; ++m) dst[m >> 3] |= static_cast<uint8_t>((q[m] & 1u) << (m & 7));
     return;
   }
-  for (int p = 0; p < b; ++p)
-    for (int m = 0; m < GROUP; ++m) dst[8 * p + (m >> 3)] |= static_cast<uint8_t>(((q[m] >> p) & 1u) << (m & 7));
+  const int per_slice = GROUP / b;     // codes in a lane slice
+  const int per_word = per_slice / 2;  // codes in a 32-bit word
+  for (int m = 0; m < GROUP; ++m) {
+    const int s = m / per_slice, within = m % per_slice;
+    const int h = within / per_word, r = within % per_word;
+    uint32_t* w = reinterpret_cast<uint32_t*>(dst + 8 * s + 4 * h);
+    *w |= static_cast<uint32_t>(q[m]) << code_bit(static_cast<uint32_t>(b), static_cast<uint32_t>(r));
+  }
 }
 
-struct TilePlan {
-  std::vector<uint32_t> row0;  // n_tiles + 1
-};
-
-// Equal-byte tiles of at most TILE_MAX rows. A row's weight is the bytes its
-// groups take in the stream (codes plus scale plus row index).
-TilePlan plan_tiles(const uint8_t* bits, int64_t N, int32_t G) {
-  TilePlan p;
-  std::vector<double> pre(static_cast<size_t>(N) + 1, 0.0);
-  for (int64_t r = 0; r < N; ++r) {
-    double rb = 0.0;
+// Entry counts of one super-tile, per group column and class.
+void count_super(const uint8_t* bits, int32_t G, int64_t r0, int64_t r1, std::vector<uint32_t>* cnt) {
+  cnt->assign(static_cast<size_t>(G) * 4, 0);
+  for (int64_t r = r0; r < r1; ++r) {
     const uint8_t* br = bits + r * G;
-    for (int32_t g = 0; g < G; ++g) rb += 8.0 * br[g] + 3.0;
-    pre[r + 1] = pre[r] + rb;
+    for (int32_t g = 0; g < G; ++g) (*cnt)[static_cast<size_t>(g) * 4 + bits_to_cls(br[g])] += 1;
   }
-  p.row0.push_back(0);
-  if (N == 0) return p;
-  const int64_t nominal = (N + TILE_MAX - 1) / TILE_MAX;
-  const double target = pre[N] / static_cast<double>(nominal);
-  int64_t start = 0;
-  while (start < N) {
-    const double thr = pre[start] + target;
-    int64_t end = start + 1;
-    while (end < N && end - start < TILE_MAX && pre[end] < thr) ++end;
-    p.row0.push_back(static_cast<uint32_t>(end));
-    start = end;
-  }
-  return p;
 }
 
-struct TileCount {
-  uint32_t runs = 0, steps = 0;
-  uint64_t bytes = 0;
-};
-
-// Run, step and record-byte counts of one tile.
-TileCount count_tile(const uint8_t* bits, int32_t G, uint32_t r0, uint32_t r1) {
-  TileCount tc;
-  for (int32_t g = 0; g < G; ++g) {
-    uint32_t n[4] = {0, 0, 0, 0};
-    for (uint32_t r = r0; r < r1; ++r) ++n[bits_to_cls(bits[static_cast<int64_t>(r) * G + g])];
-    for (int c = 0; c < 4; ++c) {
-      if (!n[c]) continue;
-      const uint32_t eps = entries_per_step(c);
-      tc.runs += 1;
-      for (uint32_t done = 0; done < n[c]; done += eps) {
-        const uint32_t e = std::min(eps, n[c] - done);
-        tc.steps += 1;
-        tc.bytes += rec_bytes(c, e);
-      }
-    }
-  }
-  return tc;
-}
-
-// Writes the runs of one tile: records into data, descriptors and offsets into desc/off.
-void fill_tile(const uint8_t* codes, const uint8_t* bits, const uint16_t* scales, int64_t K, int32_t G,
-               uint32_t r0, uint32_t r1, uint32_t run0, uint64_t byte0, uint8_t* data, uint32_t* desc,
-               uint32_t* off) {
-  uint32_t ri = run0;
-  uint64_t o = byte0;
-  std::vector<uint32_t> rows[4];
-  for (int c = 0; c < 4; ++c) rows[c].reserve(r1 - r0);
-  for (int32_t g = 0; g < G; ++g) {
-    for (int c = 0; c < 4; ++c) rows[c].clear();
-    for (uint32_t r = r0; r < r1; ++r) rows[bits_to_cls(bits[static_cast<int64_t>(r) * G + g])].push_back(r);
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t n = static_cast<uint32_t>(rows[c].size());
-      if (!n) continue;
-      desc[ri] = make_run(static_cast<uint32_t>(g), static_cast<uint32_t>(c), n);
-      off[ri] = static_cast<uint32_t>(o >> 4);
-      ++ri;
-      const uint32_t eps = entries_per_step(c);
-      const int b = cls_bits(c);
-      for (uint32_t done = 0; done < n; done += eps) {
-        const uint32_t e = std::min(eps, n - done);
-        uint8_t* rec = data + o;
-        const uint32_t rb = rec_bytes(c, e);
-        std::memset(rec, 0, rb);
-        uint16_t* sc = reinterpret_cast<uint16_t*>(rec + rec_scale_off(c, e));
-        uint8_t* rw = rec + rec_row_off(c, e);
-        for (uint32_t j = 0; j < e; ++j) {
-          const uint32_t r = rows[c][done + j];
-          pack_entry(codes + static_cast<int64_t>(r) * K + static_cast<int64_t>(g) * GROUP, b, rec + j * 8u * b);
-          sc[j] = scales[static_cast<int64_t>(r) * G + g];
-          rw[j] = static_cast<uint8_t>(r - r0);
-        }
-        o += rb;
-      }
-    }
-  }
+// |s| of an fp16 bit pattern, exactly.
+double f16_abs(uint16_t h) {
+  const uint32_t e = (h >> 10) & 31u, f = h & 1023u;
+  if (e == 31) return 1e300;
+  return e == 0 ? std::ldexp(static_cast<double>(f), -24) : std::ldexp(static_cast<double>(f | 1024u), static_cast<int>(e) - 25);
 }
 
 template <class F>
@@ -146,6 +72,14 @@ void parallel_for(int64_t n, F&& f) {
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
 }  // namespace
+
+namespace vbq {
+
+// The GEMV plan of a matrix alone (also used after a device change of sms).
+vbq_status build_gemv_plan(vbq_matrix* m, cudaStream_t st);
+void free_gemv_plan(vbq_matrix* m);
+
+}  // namespace vbq
 
 extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const uint16_t* scales_f16, int64_t N,
                                int64_t K, void* stream, vbq_matrix** out) {
@@ -194,50 +128,121 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
     delete m;
     return fail(VBQ_ERR_CUDA, "vbq_pack: no CUDA device");
   }
+  const int32_t nt = static_cast<int32_t>((N + TILE - 1) / TILE);
+  const int32_t ns = static_cast<int32_t>((N + SROWS - 1) / SROWS);
+  m->n_tiles = nt;
+  m->n_super = ns;
 
-  TilePlan plan = plan_tiles(bits, N, G);
-  const int32_t nt = static_cast<int32_t>(plan.row0.size()) - 1;
-  std::vector<TileCount> tcs(nt);
-  parallel_for(nt, [&](int64_t t) { tcs[t] = count_tile(bits, G, plan.row0[t], plan.row0[t + 1]); });
-  std::vector<uint32_t> run0(nt + 1, 0);
-  std::vector<uint64_t> byte0(nt + 1, 0);
+  // Pass 1: per super-tile, runs and bytes.
+  std::vector<std::vector<uint32_t>> counts(ns);
+  std::vector<uint64_t> st_bytes(ns, 0), st_runs(ns, 0), st_steps(ns, 0);
+  parallel_for(ns, [&](int64_t t) {
+    count_super(bits, G, t * SROWS, std::min<int64_t>(N, (t + 1) * SROWS), &counts[t]);
+    uint64_t b = 0, runs = 0, steps = 0;
+    for (int32_t g = 0; g < G; ++g)
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t n = counts[t][static_cast<size_t>(g) * 4 + c];
+        if (!n) continue;
+        b += run_bytes(c, n);
+        runs += 1;
+        steps += run_steps(c, n);
+      }
+    st_bytes[t] = b;
+    st_runs[t] = runs;
+    st_steps[t] = steps;
+  });
+  std::vector<uint64_t> byte0(ns + 1, 0), run0(ns + 1, 0);
   int64_t n_steps = 0;
-  for (int32_t t = 0; t < nt; ++t) {
-    run0[t + 1] = run0[t] + tcs[t].runs;
-    byte0[t + 1] = byte0[t] + tcs[t].bytes;
-    n_steps += tcs[t].steps;
+  for (int32_t t = 0; t < ns; ++t) {
+    byte0[t + 1] = byte0[t] + st_bytes[t];
+    run0[t + 1] = run0[t] + st_runs[t];
+    n_steps += static_cast<int64_t>(st_steps[t]);
   }
-  const uint32_t R = run0[nt];
-  const uint64_t data_bytes = byte0[nt];
-  if ((data_bytes >> 4) >= (uint64_t(1) << 32)) {
-    delete m;
-    return fail(VBQ_ERR_SHAPE, "vbq_pack: packed matrix exceeds 64 GiB");
-  }
+  const uint64_t data_bytes = byte0[ns];
+  const uint64_t o_tiles = align256(std::max<uint64_t>(data_bytes, 16));
+  const uint64_t total = align256(o_tiles + 8ull * (ns + 1));
 
-  // One host staging buffer laid out exactly like the device allocation.
-  const uint64_t o_desc = align256(std::max<uint64_t>(data_bytes, 16));
-  const uint64_t o_off = align256(o_desc + 4ull * std::max<uint32_t>(R, 1));
-  const uint64_t o_row0 = align256(o_off + 4ull * (R + 1));
-  const uint64_t o_run0 = align256(o_row0 + 4ull * (nt + 1));
-  const uint64_t total = align256(o_run0 + 4ull * (nt + 1));
   std::vector<uint8_t> host;
   try {
     host.assign(total, 0);
-    m->h_run_desc.assign(R, 0);
-    m->h_run_off.assign(R + 1, 0);
+    m->runs.assign(run0[ns], RunInfo{});
   } catch (...) {
     delete m;
     return fail(VBQ_ERR_OOM, "vbq_pack: host staging buffer");
   }
-  parallel_for(nt, [&](int64_t t) {
-    fill_tile(codes, bits, scales_f16, K, G, plan.row0[t], plan.row0[t + 1], run0[t], byte0[t], host.data(),
-              m->h_run_desc.data(), m->h_run_off.data());
+
+  // Pass 2: write the records.
+  parallel_for(ns, [&](int64_t t) {
+    const int64_t r0 = t * SROWS, r1 = std::min<int64_t>(N, (t + 1) * SROWS);
+    const uint32_t ntl = static_cast<uint32_t>((r1 - r0 + TILE - 1) / TILE);
+    uint64_t o = byte0[t];
+    uint64_t ri = run0[t];
+    std::vector<uint32_t> rows[4];
+    for (int32_t g = 0; g < G; ++g) {
+      for (int c = 0; c < 4; ++c) rows[c].clear();
+      for (int64_t r = r0; r < r1; ++r) rows[bits_to_cls(bits[r * G + g])].push_back(static_cast<uint32_t>(r));
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t n = static_cast<uint32_t>(rows[c].size());
+        if (!n) continue;
+        RunInfo& info = m->runs[ri++];
+        info.off = o;
+        RunHeader h{};
+        h.row0 = static_cast<uint32_t>(r0);
+        h.g = static_cast<uint16_t>(g);
+        h.cls = static_cast<uint8_t>(c);
+        h.ntl = static_cast<uint8_t>(ntl);
+        h.n = static_cast<uint16_t>(n);
+        uint16_t pc[3];
+        for (int q = 0; q < 3; ++q) {
+          const int64_t lim = r0 + int64_t(q + 1) * TILE;
+          pc[q] = static_cast<uint16_t>(std::lower_bound(rows[c].begin(), rows[c].end(), static_cast<uint32_t>(
+                                                             std::min<int64_t>(lim, int64_t(UINT32_MAX)))) -
+                                        rows[c].begin());
+        }
+        h.c1 = pc[0];
+        h.c2 = pc[1];
+        h.c3 = pc[2];
+        info.h = h;
+        std::memcpy(host.data() + o, &h, sizeof(h));
+        o += HEADER_BYTES;
+        const uint32_t eps = entries_per_step(c);
+        const int b = cls_bits(c);
+        for (uint32_t done = 0; done < n; done += eps) {
+          const uint32_t e = std::min(eps, n - done);
+          uint8_t* rec = host.data() + o;
+          uint16_t* sc = reinterpret_cast<uint16_t*>(rec + rec_scale_off(c, e));
+          uint8_t* rw = rec + rec_row_off(c, e);
+          for (uint32_t j = 0; j < e; ++j) {
+            const int64_t r = rows[c][done + j];
+            pack_entry(codes + r * K + static_cast<int64_t>(g) * GROUP, b, rec + j * 8u * b);
+            sc[j] = scales_f16[r * G + g];
+            rw[j] = static_cast<uint8_t>((r - r0) % TILE);
+          }
+          o += rec_bytes(c, e);
+        }
+      }
+    }
   });
-  m->h_run_off[R] = static_cast<uint32_t>(data_bytes >> 4);
-  std::memcpy(host.data() + o_desc, m->h_run_desc.data(), 4ull * R);
-  std::memcpy(host.data() + o_off, m->h_run_off.data(), 4ull * (R + 1));
-  std::memcpy(host.data() + o_row0, plan.row0.data(), 4ull * (nt + 1));
-  std::memcpy(host.data() + o_run0, run0.data(), 4ull * (nt + 1));
+  std::memcpy(host.data() + o_tiles, byte0.data(), 8ull * (ns + 1));
+
+  // Largest row L1 norm sum_k |w_rk| (exact in double, rounded up to float):
+  // every partial sum of a row's products is at most this times max|x|.
+  std::vector<double> l1(N, 0.0);
+  parallel_for(N, [&](int64_t r) {
+    double acc = 0.0;
+    for (int32_t g = 0; g < G; ++g) {
+      const int b = bits[r * G + g];
+      const double c = ((1 << b) - 1) * 0.5;
+      double sq = 0.0;
+      const uint8_t* q = codes + r * K + static_cast<int64_t>(g) * GROUP;
+      for (int mm = 0; mm < GROUP; ++mm) sq += std::fabs(q[mm] - c);
+      acc += f16_abs(scales_f16[r * G + g]) * sq;
+    }
+    l1[r] = acc;
+  });
+  double l1max = 0.0;
+  for (double v : l1) l1max = std::max(l1max, v);
+  m->max_row_l1 = l1max >= 3.0e38 ? 3.0e38f : std::nextafter(static_cast<float>(l1max), 3.0e38f);
 
   int64_t cnt[4] = {0, 0, 0, 0};
   int64_t code_bytes = 0;
@@ -266,47 +271,33 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
     return cuda_fail(e, "vbq_pack: upload");
   }
   m->data = m->dev_base;
-  m->run_desc = reinterpret_cast<const uint32_t*>(m->dev_base + o_desc);
-  m->run_off = reinterpret_cast<const uint32_t*>(m->dev_base + o_off);
-  m->tile_row0 = reinterpret_cast<const uint32_t*>(m->dev_base + o_row0);
-  m->tile_run0 = reinterpret_cast<const uint32_t*>(m->dev_base + o_run0);
-  m->h_tile_row0 = plan.row0;
-  m->h_tile_run0 = run0;
-  m->n_tiles = nt;
-  m->n_runs = static_cast<int32_t>(R);
+  m->st_byte0 = reinterpret_cast<const uint64_t*>(m->dev_base + o_tiles);
+  m->n_runs = static_cast<int64_t>(run0[ns]);
   m->n_steps = n_steps;
   m->data_bytes = static_cast<int64_t>(data_bytes);
   m->code_bytes = code_bytes;
   for (int c = 0; c < 4; ++c) m->groups_by_bits[c] = cnt[c];
-  {  // the largest (tile, column) record span
-    int64_t best = 0;
-    for (int32_t t = 0; t < nt; ++t) {
-      uint32_t r = run0[t];
-      while (r < run0[t + 1]) {
-        uint32_t e = r + 1;
-        while (e < run0[t + 1] && run_g(m->h_run_desc[e]) == run_g(m->h_run_desc[r])) ++e;
-        best = std::max<int64_t>(best, 16ll * (m->h_run_off[e] - m->h_run_off[r]));
-        r = e;
-      }
-    }
-    m->max_col_bytes = best;
-  }
+  m->max_scale_bits = max_mag;
   {  // fp16 magnitude bits to float (exact)
-    const uint32_t e = (max_mag >> 10) & 31u, f = max_mag & 1023u;
-    m->tc_max_scale = e == 31 ? 1e30f
-                      : e == 0 ? std::ldexp(static_cast<float>(f), -24)
-                               : std::ldexp(static_cast<float>(f | 1024u), static_cast<int>(e) - 25);
+    const uint32_t ex = (max_mag >> 10) & 31u, f = max_mag & 1023u;
+    m->max_scale = ex == 31 ? 1e30f
+                   : ex == 0 ? std::ldexp(static_cast<float>(f), -24)
+                             : std::ldexp(static_cast<float>(f | 1024u), static_cast<int>(ex) - 25);
+  }
+  // First run of each (super-tile, group column) block, for the tensor-core path.
+  m->block_run.assign(static_cast<size_t>(ns) * G + 1, static_cast<uint32_t>(m->n_runs));
+  for (int64_t r = static_cast<int64_t>(m->runs.size()) - 1; r >= 0; --r) {
+    const RunInfo& ri = m->runs[r];
+    m->block_run[static_cast<size_t>(ri.st()) * G + ri.h.g] = static_cast<uint32_t>(r);
   }
 
-  // The plan of a GEMV over this matrix alone.
-  Plan pl = make_plan({seg_tables(m)}, plan_ctas(data_bytes, gpu_info().sms), MAX_UNITS_PER_CTA);
-  e = upload_plan(pl, MAX_NB, {m->data}, st, &m->plan);
-  if (e != cudaSuccess) {
+  vbq_status s = build_gemv_plan(m, st);
+  if (s != VBQ_OK) {
     cudaFree(m->dev_base);
     delete m;
-    return cuda_fail(e, "vbq_pack: plan upload");
+    return s;
   }
-  m->total_bytes = static_cast<int64_t>(total) + m->plan.bytes;
+  m->total_bytes = static_cast<int64_t>(total);
   m->meta_bytes = m->total_bytes - code_bytes;
   *out = m;
   return VBQ_OK;
@@ -320,7 +311,7 @@ extern "C" void vbq_matrix_free(vbq_matrix* m) {
     cudaSetDevice(m->device);
     cudaDeviceSynchronize();
     cudaFree(m->dev_base);
-    free_plan(&m->plan);
+    free_gemv_plan(m);
     tc_forget(m);
     cudaSetDevice(cur);
   }

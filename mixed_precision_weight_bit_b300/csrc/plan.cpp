@@ -1,371 +1,259 @@
-// Work plans for the GEMV kernels (plan.h). Host code only.
+// Work plans for the batch-1 kernels (plan.h).
 #include "plan.h"
 
 #include <algorithm>
-#include <cstring>
+#include <cmath>
 
 namespace vbq {
 
 namespace {
 
-constexpr uint64_t kMinCtaBytes = 32 * 1024;
-
-// A step border in the stream of a launch: step k of run `run` of segment `seg`.
-// The end of a segment is (seg, n_runs, 0).
-struct Pos {
-  int seg = 0;
-  uint32_t run = 0, k = 0;
-  uint64_t gbyte = 0;  // offset in the launch's stream
-  uint64_t gcost = 0;  // estimated work before this position
+struct Flat {
+  int seg;
+  uint32_t run;        // run index in its segment
+  uint32_t item_st;    // item super-tile
+  uint32_t g;
+  uint64_t step0;      // item step index of the run's first step
+  uint32_t steps;
+  double cost0;        // cost of all steps before the run
+  double head;         // extra cost of the run's first step (run set-up, column preparation)
+  double step_cost;
 };
 
-struct Stream {
-  const std::vector<SegTables>& segs;
-  std::vector<uint64_t> base;   // stream byte offset of each segment, plus the total
-  std::vector<uint64_t> cbase;  // stream cost offset of each segment, plus the total
-  std::vector<std::vector<uint64_t>> cpre;  // per segment: cost before each run (n_runs + 1)
-  std::vector<std::vector<uint32_t>> cols;  // per segment: first run of every (tile, column), then n_runs
-  bool whole_columns = false;
+struct Flattened {
+  std::vector<Flat> runs;
+  uint64_t total_steps = 0;
+  double total_cost = 0.0;
+  uint32_t G = 0;
 
-  explicit Stream(const std::vector<SegTables>& s, bool by_columns = false) : segs(s), whole_columns(by_columns) {
-    base.assign(s.size() + 1, 0);
-    cbase.assign(s.size() + 1, 0);
-    cpre.resize(s.size());
-    for (size_t i = 0; i < s.size(); ++i) {
-      base[i + 1] = base[i] + (s[i].n_runs ? uint64_t(s[i].run_off[s[i].n_runs]) * 16u : 0u);
-      std::vector<uint64_t>& c = cpre[i];
-      c.assign(static_cast<size_t>(s[i].n_runs) + 1, 0);
-      for (int32_t r = 0; r < s[i].n_runs; ++r) {
-        const uint32_t d = s[i].run_desc[r];
-        const bool col_start = r == 0 || run_g(s[i].run_desc[r - 1]) != run_g(d) || is_tile_start(i, r);
-        c[r + 1] = c[r] + head_cost(d, col_start) + uint64_t(run_steps(d)) * kCostStep[run_cls(d)];
-      }
-      cbase[i + 1] = cbase[i] + c.back();
+  // Index of the run holding item step pos (pos < total_steps).
+  size_t run_of(uint64_t pos) const {
+    size_t lo = 0, hi = runs.size();
+    while (hi - lo > 1) {
+      const size_t mid = (lo + hi) / 2;
+      if (runs[mid].step0 <= pos) lo = mid; else hi = mid;
     }
-    cols.resize(s.size());
-    for (size_t i = 0; i < s.size(); ++i) {
-      for (int32_t r = 0; r < s[i].n_runs; ++r)
-        if (r == 0 || run_g(s[i].run_desc[r - 1]) != run_g(s[i].run_desc[r]) || is_tile_start(i, r))
-          cols[i].push_back(static_cast<uint32_t>(r));
-      cols[i].push_back(static_cast<uint32_t>(s[i].n_runs));
+    return lo;
+  }
+  double cost(uint64_t pos) const {
+    if (pos >= total_steps) return total_cost;
+    const Flat& f = runs[run_of(pos)];
+    const uint64_t k = pos - f.step0;
+    return f.cost0 + (k > 0 ? f.head + static_cast<double>(k) * f.step_cost : 0.0);
+  }
+  // The step border whose cost is nearest to c.
+  uint64_t pos_for(double c) const {
+    if (runs.empty() || c <= 0.0) return 0;
+    if (c >= total_cost) return total_steps;
+    size_t lo = 0, hi = runs.size();
+    while (hi - lo > 1) {
+      const size_t mid = (lo + hi) / 2;
+      if (runs[mid].cost0 <= c) lo = mid; else hi = mid;
     }
+    const Flat& f = runs[lo];
+    const double within = c - f.cost0 - f.head;
+    double k = within / f.step_cost;
+    if (within < 0.0) k = (c - f.cost0) < 0.5 * (f.head + f.step_cost) ? 0.0 : 1.0;
+    uint64_t ki = static_cast<uint64_t>(std::llround(std::max(0.0, k)));
+    ki = std::min<uint64_t>(ki, f.steps);
+    return f.step0 + ki;
   }
-  static uint64_t head_cost(uint32_t, bool col_start) { return kCostRun + (col_start ? kCostColumn : 0u); }
-  bool is_tile_start(size_t seg, int32_t r) const {
-    const SegTables& S = segs[seg];
-    return std::binary_search(S.tile_run0, S.tile_run0 + S.n_tiles + 1, static_cast<uint32_t>(r));
-  }
-  uint64_t total() const { return base.back(); }
-  uint64_t total_cost() const { return cbase.back(); }
-
-  uint64_t run_start(int seg, uint32_t run) const { return uint64_t(segs[seg].run_off[run]) * 16u; }
-
-  Pos at(int seg, uint32_t run, uint32_t k) const {
-    const SegTables& S = segs[seg];
-    Pos p;
-    p.seg = seg;
-    if (run >= static_cast<uint32_t>(S.n_runs)) {
-      p.run = S.n_runs;
-      p.gbyte = base[seg] + run_start(seg, S.n_runs);
-      p.gcost = cbase[seg] + cpre[seg].back();
-      return p;
+  // Super-tiles and group columns touched by steps [p0, p1) (p1 > p0).
+  void window(uint64_t p0, uint64_t p1, uint32_t* st0, uint32_t* nslots, uint32_t* ncols, uint32_t cols[4]) const {
+    const Flat& a = runs[run_of(p0)];
+    const Flat& b = runs[run_of(p1 - 1)];
+    *st0 = a.item_st;
+    *nslots = b.item_st - a.item_st + 1;
+    if (a.item_st == b.item_st) {
+      cols[0] = a.g; cols[1] = b.g + 1; cols[2] = 0; cols[3] = 0;
+    } else if (b.item_st == a.item_st + 1 && b.g + 1 < a.g) {
+      cols[0] = 0; cols[1] = b.g + 1; cols[2] = a.g; cols[3] = G;
+    } else {
+      cols[0] = 0; cols[1] = G; cols[2] = 0; cols[3] = 0;
     }
-    const uint32_t d = S.run_desc[run];
-    if (k >= run_steps(d)) return at(seg, run + 1, 0);
-    p.run = run;
-    p.k = k;
-    p.gbyte = base[seg] + run_start(seg, run) + uint64_t(k) * full_step_bytes(run_cls(d));
-    p.gcost = cbase[seg] + cpre[seg][run] + (k ? (cpre[seg][run + 1] - cpre[seg][run] -
-                                                  uint64_t(run_steps(d)) * kCostStep[run_cls(d)]) +
-                                                     uint64_t(k) * kCostStep[run_cls(d)]
-                                               : 0u);
-    return p;
+    *ncols = (cols[1] - cols[0]) + (cols[3] - cols[2]);
   }
-
-  // Nearest step border (or column start, in whole-column mode) to local cost t of segment seg.
-  Pos snap_local(int seg, uint64_t t) const {
-    const SegTables& S = segs[seg];
-    const std::vector<uint64_t>& c = cpre[seg];
-    if (t >= c.back()) return at(seg, S.n_runs, 0);
-    if (whole_columns) {
-      const std::vector<uint32_t>& cs = cols[seg];
-      // last column start whose cost <= t, and the next one
-      size_t lo = 0, hi = cs.size() - 1;
-      while (hi - lo > 1) {
-        const size_t mid = (lo + hi) / 2;
-        if (c[cs[mid]] <= t) lo = mid; else hi = mid;
-      }
-      const uint64_t a = c[cs[lo]], b = c[cs[hi]];
-      return at(seg, (t - a <= b - t) ? cs[lo] : cs[hi], 0);
-    }
-    // last run whose cost start <= t
-    const uint32_t r = static_cast<uint32_t>(std::upper_bound(c.begin(), c.end(), t) - c.begin()) - 1u;
-    const uint32_t d = S.run_desc[r];
-    const uint64_t head = c[r + 1] - c[r] - uint64_t(run_steps(d)) * kCostStep[run_cls(d)];
-    const uint64_t step = kCostStep[run_cls(d)];
-    const uint64_t into = t - c[r];
-    const uint64_t k = into <= head ? 0u : (into - head + step / 2) / step;
-    return at(seg, r, static_cast<uint32_t>(std::min<uint64_t>(k, run_steps(d))));
-  }
-
-  // Nearest step border to stream cost t.
-  Pos snap(uint64_t t) const {
-    for (size_t s = 0; s < segs.size(); ++s)
-      if (t < cbase[s + 1]) return snap_local(static_cast<int>(s), t - cbase[s]);
-    return end();
-  }
-
-  Pos end() const {
-    Pos p;
-    p.seg = static_cast<int>(segs.size()) - 1;
-    p.run = segs.empty() ? 0 : segs.back().n_runs;
-    p.gbyte = total();
-    p.gcost = total_cost();
-    return p;
-  }
-
-  // Moves a position at the end of a segment to the start of the next non-empty one.
-  Pos normalize(Pos p) const {
-    while (p.seg + 1 < static_cast<int>(segs.size()) && p.run >= static_cast<uint32_t>(segs[p.seg].n_runs)) {
-      ++p.seg;
-      p.run = 0;
-      p.k = 0;
-    }
-    return p;
-  }
-
-  uint32_t tile_of(int seg, uint32_t run) const {
-    const SegTables& S = segs[seg];
-    const uint32_t* b = S.tile_run0;
-    // last tile whose first run <= run
-    const uint32_t* it = std::upper_bound(b, b + S.n_tiles + 1, run);
-    return static_cast<uint32_t>((it - b) - 1);
+  bool fits(uint64_t p0, uint64_t p1) const {
+    uint32_t st0, ns, nc, cols[4];
+    window(p0, p1, &st0, &ns, &nc, cols);
+    return ns <= static_cast<uint32_t>(SLOTS_MAX) && nc <= static_cast<uint32_t>(CCAP);
   }
 };
 
-SliceRec slice_of(const Stream& st, const Pos& a, const Pos& b) {
-  SliceRec r{};
-  r.run0 = a.run;
-  r.k0 = a.k;
-  r.run1 = b.run;
-  r.k1 = b.k;
-  r.b0 = static_cast<uint32_t>((a.gbyte - st.base[a.seg]) >> 4);
-  r.b1 = static_cast<uint32_t>((b.gbyte - st.base[a.seg]) >> 4);
-  r.g0 = (b.gbyte > a.gbyte) ? run_g(st.segs[a.seg].run_desc[a.run]) : 0u;
-  return r;
-}
-
-bool build(const Stream& st, int32_t P, int max_units, Plan* out) {
-  const uint64_t total = st.total_cost();
-  std::vector<Pos> cut(P + 1);
-  cut[0] = st.normalize(st.snap(0));
-  cut[P] = st.end();
-  for (int32_t c = 1; c < P; ++c) {
-    cut[c] = st.normalize(st.snap(total * static_cast<uint64_t>(c) / static_cast<uint64_t>(P)));
-    if (cut[c].gbyte < cut[c - 1].gbyte) cut[c] = cut[c - 1];
+Flattened flatten(const std::vector<SegPlanInput>& segs, std::vector<uint32_t>* st_off, uint32_t* n_item_super) {
+  Flattened F;
+  uint32_t off = 0;
+  st_off->clear();
+  for (const SegPlanInput& s : segs) {
+    st_off->push_back(off);
+    off += s.n_super;
+    F.G = std::max(F.G, s.G);
   }
-  // Units in stream order, with their CTA and slices.
-  std::vector<UnitRec> units;
-  std::vector<SliceRec> slices;
-  std::vector<int32_t> owner;
-  int umax = 1;
-  for (int32_t c = 0; c < P; ++c) {
-    Pos pos = cut[c];
-    int nunits = 0;
-    while (pos.gbyte < cut[c + 1].gbyte) {
-      pos = st.normalize(pos);
-      const SegTables& S = st.segs[pos.seg];
-      const uint32_t t = st.tile_of(pos.seg, pos.run);
-      const Pos tend = st.at(pos.seg, S.tile_run0[t + 1], 0);
-      const Pos uend = cut[c + 1].gbyte < tend.gbyte ? cut[c + 1] : tend;
-      UnitRec u{};
-      u.seg = static_cast<uint32_t>(pos.seg);
-      u.tile = t;
-      u.r0 = S.tile_row0[t];
-      u.rows = S.tile_row0[t + 1] - S.tile_row0[t];
-      units.push_back(u);
-      owner.push_back(c);
-      // Warp slices: equal bytes, snapped to step borders inside the unit.
-      Pos prev = pos;
-      for (int j = 1; j <= SLICES; ++j) {
-        Pos nx;
-        if (j == SLICES) {
-          nx = uend;
-        } else {
-          const uint64_t tgt = pos.gcost + (uend.gcost - pos.gcost) * static_cast<uint64_t>(j) / SLICES;
-          nx = st.snap_local(pos.seg, tgt - st.cbase[pos.seg]);
-          if (nx.gbyte < prev.gbyte) nx = prev;
-          if (nx.gbyte > uend.gbyte) nx = uend;
-        }
-        SliceRec sr = slice_of(st, prev, nx);
-        if (nx.gbyte == prev.gbyte) {  // empty slice: start = end
-          sr.run1 = sr.run0;
-          sr.k1 = sr.k0;
-        }
-        slices.push_back(sr);
-        prev = nx;
-      }
-      ++nunits;
-      pos = uend;
+  *n_item_super = off;
+  double cost = 0.0;
+  uint64_t step = 0;
+  for (size_t si = 0; si < segs.size(); ++si) {
+    const std::vector<RunInfo>& rr = *segs[si].runs;
+    uint32_t last_st = UINT32_MAX, last_g = UINT32_MAX;
+    for (size_t r = 0; r < rr.size(); ++r) {
+      const RunInfo& ri = rr[r];
+      Flat f;
+      f.seg = static_cast<int>(si);
+      f.run = static_cast<uint32_t>(r);
+      f.item_st = (*st_off)[si] + ri.st();
+      f.g = ri.h.g;
+      f.step0 = step;
+      f.steps = run_steps(ri.h.cls, ri.h.n);
+      f.cost0 = cost;
+      f.step_cost = kCostStep[ri.h.cls];
+      f.head = kCostRun + ((ri.st() != last_st || ri.h.g != last_g) ? kCostColumn : 0.0);
+      last_st = ri.st();
+      last_g = ri.h.g;
+      F.runs.push_back(f);
+      step += f.steps;
+      cost += f.head + f.steps * f.step_cost;
     }
-    if (nunits > max_units) return false;
-    umax = std::max(umax, nunits);
   }
-
-  // Split tiles. Units of one tile are consecutive in stream order.
-  Plan pl;
-  pl.n_ctas = P;
-  pl.umax = umax;
-  size_t i = 0;
-  while (i < units.size()) {
-    size_t j = i + 1;
-    while (j < units.size() && units[j].seg == units[i].seg && units[j].tile == units[i].tile) ++j;
-    const uint32_t ns = static_cast<uint32_t>(j - i);
-    for (size_t q = i; q < j; ++q) {
-      units[q].split = static_cast<uint32_t>(q - i);
-      units[q].nsplit = ns;
-      units[q].pbase = ns > 1 ? static_cast<uint32_t>(pl.partial_rows) : 0u;
-      units[q].cnt = ns > 1 ? pl.n_counters : 0u;
-    }
-    if (ns > 1) {
-      pl.partial_rows += static_cast<uint64_t>(ns) * units[i].rows;
-      pl.n_counters += 1;
-    }
-    i = j;
-  }
-  // Slots: CTA c owns [c*umax, (c+1)*umax).
-  pl.units.assign(static_cast<size_t>(P) * umax, UnitRec{});
-  pl.slices.assign(static_cast<size_t>(P) * umax * SLICES, SliceRec{});
-  std::vector<int> fill(P, 0);
-  for (size_t u = 0; u < units.size(); ++u) {
-    const int32_t c = owner[u];
-    const size_t slot = static_cast<size_t>(c) * umax + fill[c]++;
-    pl.units[slot] = units[u];
-    for (int j = 0; j < SLICES; ++j) pl.slices[slot * SLICES + j] = slices[u * SLICES + j];
-  }
-  *out = std::move(pl);
-  return true;
+  F.total_steps = step;
+  F.total_cost = cost;
+  return F;
 }
 
 }  // namespace
 
-int32_t plan_ctas(uint64_t total_bytes, int sms) {
-  const uint64_t by_bytes = (total_bytes + kMinCtaBytes - 1) / kMinCtaBytes;
-  return static_cast<int32_t>(std::max<uint64_t>(1, std::min<uint64_t>(static_cast<uint64_t>(sms), by_bytes)));
-}
+bool make_item_plan(const std::vector<SegPlanInput>& segs, int32_t n_ctas, ItemPlan* out, const char** why) {
+  ItemPlan& P = *out;
+  P = ItemPlan{};
+  P.n_ctas = n_ctas;
+  Flattened F = flatten(segs, &P.st_off, &P.n_item_super);
+  P.total_cost = F.total_cost;
+  P.arrivals.assign(P.n_item_super, 0);
+  P.ctas.assign(n_ctas, CtaPlan{});
+  P.warps.assign(static_cast<size_t>(n_ctas) * KW, WarpPlan{});
+  P.sub_b0.assign(static_cast<size_t>(n_ctas) * KW * MAX_SEG, 0);
+  if (F.total_steps == 0) return true;
 
-Plan make_plan(const std::vector<SegTables>& segs, int32_t n_ctas, int max_units, bool whole_columns) {
-  Stream st(segs, whole_columns);
-  Plan p;
-  int32_t P = std::max<int32_t>(1, n_ctas);
-  if (st.total() == 0 || st.total_cost() == 0) {
-    p.n_ctas = 0;
-    p.umax = 0;
-    return p;
+  // CTA ranges: equal shares of the remaining cost, each kept inside the
+  // super-tile and column limits (the largest end that fits, found by bisection).
+  std::vector<uint64_t> cut(n_ctas + 1, 0);
+  uint64_t pos = 0;
+  for (int32_t c = 0; c < n_ctas; ++c) {
+    cut[c] = pos;
+    if (pos >= F.total_steps) continue;
+    const double c0 = F.cost(pos);
+    const double target = c0 + (F.total_cost - c0) / static_cast<double>(n_ctas - c);
+    uint64_t end = (c == n_ctas - 1) ? F.total_steps : std::max<uint64_t>(F.pos_for(target), pos + 1);
+    end = std::min<uint64_t>(end, F.total_steps);
+    if (!F.fits(pos, end)) {
+      uint64_t lo = pos + 1, hi = end;  // fits(pos, lo) holds: one step touches one super-tile and column
+      while (hi - lo > 1) {
+        const uint64_t mid = lo + (hi - lo) / 2;
+        if (F.fits(pos, mid)) lo = mid; else hi = mid;
+      }
+      end = lo;
+    }
+    pos = end;
   }
-  while (!build(st, P, max_units, &p)) P = P + P / 2 + 1;
-  return p;
+  cut[n_ctas] = pos;
+  if (pos < F.total_steps) {
+    *why = "the item needs more CTAs than given (each CTA may touch 2 super-tiles and 64 group columns)";
+    return false;
+  }
+
+  for (int32_t c = 0; c < n_ctas; ++c) {
+    const uint64_t p0 = cut[c], p1 = cut[c + 1];
+    CtaPlan& cp = P.ctas[c];
+    if (p1 <= p0) continue;
+    uint32_t st0, ns, nc, cols[4];
+    F.window(p0, p1, &st0, &ns, &nc, cols);
+    cp.st_base = st0;
+    cp.n_slots = ns;
+    cp.a0 = cols[0];
+    cp.a1 = cols[1];
+    cp.b0 = cols[2];
+    cp.b1 = cols[3];
+    for (uint32_t t = 0; t < ns; ++t) P.arrivals[st0 + t] += 1;
+    // Warp ranges: equal cost shares of the CTA range.
+    const double ca = F.cost(p0), cb = F.cost(p1);
+    uint64_t wa = p0;
+    for (int w = 0; w < KW; ++w) {
+      uint64_t wb = (w == KW - 1) ? p1 : F.pos_for(ca + (cb - ca) * (w + 1) / KW);
+      wb = std::min(std::max(wb, wa), p1);
+      WarpPlan& wp = P.warps[static_cast<size_t>(c) * KW + w];
+      // Sub-ranges: one per segment the range crosses.
+      uint64_t q = wa;
+      while (q < wb) {
+        const size_t fi = F.run_of(q);
+        const Flat& f = F.runs[fi];
+        const SegPlanInput& S = segs[f.seg];
+        const RunInfo& ri = (*S.runs)[f.run];
+        size_t fj = fi;
+        while (fj + 1 < F.runs.size() && F.runs[fj + 1].seg == f.seg && F.runs[fj + 1].step0 < wb) ++fj;
+        const uint64_t seg_end = std::min<uint64_t>(wb, F.runs[fj].step0 + F.runs[fj].steps);
+        if (wp.nsub >= MAX_SEG) {
+          *why = "a warp range crosses more segments than supported";
+          return false;
+        }
+        SubRange& sr = wp.sub[wp.nsub++];
+        sr.first = ri.h;
+        sr.seg = static_cast<uint32_t>(f.seg);
+        sr.k0 = static_cast<uint32_t>(q - f.step0);
+        sr.nsteps = static_cast<uint32_t>(seg_end - q);
+        const uint64_t b0 = sr.k0 == 0 ? ri.off : ri.off + HEADER_BYTES + uint64_t(sr.k0) * full_step_bytes(ri.h.cls);
+        const size_t fe = F.run_of(seg_end - 1);
+        const Flat& fl = F.runs[fe];
+        const RunInfo& re = (*S.runs)[fl.run];
+        const uint64_t ke = seg_end - fl.step0;  // steps of the last run inside the range (>= 1)
+        const uint64_t b1 = ke == fl.steps ? re.off + run_bytes(re.h.cls, re.h.n)
+                                           : re.off + HEADER_BYTES + ke * full_step_bytes(re.h.cls);
+        sr.bytes = static_cast<uint32_t>(b1 - b0);
+        P.sub_b0[(static_cast<size_t>(c) * KW + w) * MAX_SEG + (wp.nsub - 1)] = b0;
+        q = seg_end;
+      }
+      wa = wb;
+    }
+  }
+  return true;
 }
 
-bool append_pieces(const Plan& p, const std::vector<const uint8_t*>& seg_data, int W,
+bool append_pieces(const ItemPlan& p, const std::vector<SegPlanInput>& segs,
                    std::vector<std::vector<uint64_t>>* per_warp) {
-  const int spw = SLICES / W;
-  bool ok = true;
-  per_warp->resize(static_cast<size_t>(p.n_ctas) * W);
-  for (int32_t c = 0; c < p.n_ctas; ++c)
-    for (int32_t i = 0; i < p.umax; ++i) {
-      const size_t slot = static_cast<size_t>(c) * p.umax + i;
-      const UnitRec& u = p.units[slot];
-      if (u.nsplit == 0) break;
-      for (int w = 0; w < W; ++w) {
-        const SliceRec& f = p.slices[slot * SLICES + w * spw];
-        const SliceRec& l = p.slices[slot * SLICES + w * spw + spw - 1];
-        if (l.b1 > f.b0) {
-          const uint8_t* a = seg_data[u.seg] + uint64_t(f.b0) * 16u;
-          const uint64_t n = uint64_t(l.b1 - f.b0) * 16u;
-          ok = ok && piece_fits(a, n);
-          (*per_warp)[static_cast<size_t>(c) * W + w].push_back(make_piece(a, n));
-        }
+  const size_t nw = static_cast<size_t>(p.n_ctas) * KW;
+  if (per_warp->size() < nw) per_warp->resize(nw);
+  for (size_t w = 0; w < nw; ++w) {
+    const WarpPlan& wp = p.warps[w];
+    for (uint32_t s = 0; s < wp.nsub; ++s) {
+      const SubRange& sr = wp.sub[s];
+      if (sr.nsteps == 0) continue;
+      const SegPlanInput& S = segs[sr.seg];
+      const uint64_t b0 = p.sub_b0[w * MAX_SEG + s];
+      const uint8_t* a = S.data + b0;
+      uint64_t left = sr.bytes;
+      while (left > 0) {  // pieces below 16 MiB each
+        const uint64_t take = std::min<uint64_t>(left, uint64_t(1) << 23);
+        if (!piece_fits(a, take)) return false;
+        (*per_warp)[w].push_back(make_piece(a, take));
+        a += take;
+        left -= take;
       }
     }
-  return ok;
+  }
+  return true;
 }
 
 PieceSet finish_pieces(const std::vector<std::vector<uint64_t>>& per_warp) {
   PieceSet ps;
-  ps.start.assign(per_warp.size() + 1, 0);
-  ps.bytes.assign(per_warp.size(), 0);
-  for (size_t i = 0; i < per_warp.size(); ++i) {
-    ps.start[i + 1] = ps.start[i] + static_cast<uint32_t>(per_warp[i].size());
+  ps.start.push_back(0);
+  for (const auto& v : per_warp) {
     uint64_t b = 0;
-    for (uint64_t q : per_warp[i]) {
-      ps.pieces.push_back(q);
-      b += (q & 0xFFFFFu) << 4;
+    for (uint64_t pc : v) {
+      ps.pieces.push_back(pc);
+      b += (pc & 0xFFFFFu) << 4;
     }
-    ps.bytes[i] = static_cast<uint32_t>(b);
+    ps.start.push_back(static_cast<uint32_t>(ps.pieces.size()));
+    ps.bytes.push_back(static_cast<uint32_t>(b));
   }
   return ps;
-}
-
-cudaError_t upload_plan(const Plan& p, int max_nb, const std::vector<const uint8_t*>& seg_data,
-                        cudaStream_t stream, DevicePlan* out) {
-  auto al = [](uint64_t b) { return (b + 255) & ~uint64_t(255); };
-  std::vector<std::vector<uint64_t>> w16, w8;
-  if (!append_pieces(p, seg_data, 16, &w16) || !append_pieces(p, seg_data, 8, &w8)) return cudaErrorInvalidValue;
-  const PieceSet p16 = finish_pieces(w16), p8 = finish_pieces(w8);
-  const uint64_t o_units = 0;
-  const uint64_t o_slices = al(o_units + sizeof(UnitRec) * std::max<size_t>(1, p.units.size()));
-  const uint64_t o_p16 = al(o_slices + sizeof(SliceRec) * std::max<size_t>(1, p.slices.size()));
-  const uint64_t o_s16 = al(o_p16 + 8ull * std::max<size_t>(1, p16.pieces.size()));
-  const uint64_t o_b16 = al(o_s16 + 4ull * p16.start.size());
-  const uint64_t o_p8 = al(o_b16 + 4ull * std::max<size_t>(1, p16.bytes.size()));
-  const uint64_t o_s8 = al(o_p8 + 8ull * std::max<size_t>(1, p8.pieces.size()));
-  const uint64_t o_b8 = al(o_s8 + 4ull * p8.start.size());
-  const uint64_t o_cnt = al(o_b8 + 4ull * std::max<size_t>(1, p8.bytes.size()));
-  const uint64_t o_part = al(o_cnt + 4ull * std::max<uint32_t>(1, p.n_counters));
-  const uint64_t total = al(o_part + 4ull * std::max<uint64_t>(1, p.partial_rows * max_nb));
-  std::vector<uint8_t> host(o_cnt, 0);
-  auto put = [&](uint64_t off, const void* src, size_t n) {
-    if (n) std::memcpy(host.data() + off, src, n);
-  };
-  put(o_units, p.units.data(), sizeof(UnitRec) * p.units.size());
-  put(o_slices, p.slices.data(), sizeof(SliceRec) * p.slices.size());
-  put(o_p16, p16.pieces.data(), 8 * p16.pieces.size());
-  put(o_s16, p16.start.data(), 4 * p16.start.size());
-  put(o_b16, p16.bytes.data(), 4 * p16.bytes.size());
-  put(o_p8, p8.pieces.data(), 8 * p8.pieces.size());
-  put(o_s8, p8.start.data(), 4 * p8.start.size());
-  put(o_b8, p8.bytes.data(), 4 * p8.bytes.size());
-  uint8_t* d = nullptr;
-  cudaError_t e = cudaMalloc(&d, total);
-  if (e != cudaSuccess) return e;
-  e = cudaMemcpyAsync(d, host.data(), o_cnt, cudaMemcpyHostToDevice, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(d + o_cnt, 0, total - o_cnt, stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-  if (e != cudaSuccess) {
-    cudaFree(d);
-    return e;
-  }
-  out->base = d;
-  out->units = reinterpret_cast<const UnitRec*>(d + o_units);
-  out->slices = reinterpret_cast<const SliceRec*>(d + o_slices);
-  out->pieces16 = reinterpret_cast<const uint64_t*>(d + o_p16);
-  out->start16 = reinterpret_cast<const uint32_t*>(d + o_s16);
-  out->bytes16 = reinterpret_cast<const uint32_t*>(d + o_b16);
-  out->pieces8 = reinterpret_cast<const uint64_t*>(d + o_p8);
-  out->start8 = reinterpret_cast<const uint32_t*>(d + o_s8);
-  out->bytes8 = reinterpret_cast<const uint32_t*>(d + o_b8);
-  out->counters = reinterpret_cast<uint32_t*>(d + o_cnt);
-  out->partial = reinterpret_cast<float*>(d + o_part);
-  out->n_ctas = p.n_ctas;
-  out->umax = p.umax;
-  out->bytes = static_cast<int64_t>(total);
-  return cudaSuccess;
-}
-
-void free_plan(DevicePlan* p) {
-  if (p->base) cudaFree(p->base);
-  *p = DevicePlan{};
 }
 
 }  // namespace vbq

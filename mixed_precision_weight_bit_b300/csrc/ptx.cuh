@@ -19,6 +19,7 @@ constexpr long long kSpinCycles = 2000000000LL;
 constexpr int kErrRingTimeout = 1;
 constexpr int kErrMmaTimeout = 2;
 constexpr int kErrGridTimeout = 3;
+constexpr int kErrRange = 4;  // a fixed-point partial sum left its range
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -81,6 +82,9 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
   return v;
 }
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v));
+}
 __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
@@ -118,6 +122,28 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
 // y += v in global memory, without waiting for the result.
 __device__ __forceinline__ void red_add_f32(float* y, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(y), "f"(v) : "memory");
+}
+// 64-bit integer add in global memory (two's complement, so signed values add correctly).
+__device__ __forceinline__ void red_add_u64(unsigned long long* p, long long v) {
+  asm volatile("red.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Two-way dot products of signed 16-bit pairs with unsigned bytes, accumulated in 32 bits:
+// lo: c + a.lo16 * b.byte0 + a.hi16 * b.byte1;  hi: the same with bytes 2 and 3.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
 }
 
 // Programmatic dependent launch: wait for the preceding grid's memory, and let

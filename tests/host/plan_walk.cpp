@@ -1,17 +1,20 @@
-// Host check of the packed layout and the GEMV work plans (CPU only, no GPU).
+// Host check of the packed layout and the batch-1 work plans (CPU only, no GPU).
 //
-// Builds pack.cpp and plan.cpp against a stub CUDA runtime whose "device"
-// memory is host memory. It packs seeded random matrices, then replays what
-// each warp of the GEMV kernel walks: the units of its CTA, its slice of each
-// unit, run by run and step by step. It checks that
-//   * every warp's slices add up to the bytes it copies, and that the records it
-//     walks sit exactly at the offsets the copies put them;
-//   * every step of every tile is walked exactly once per launch;
-//   * decoding every walked record (codes, fp16 scale, row) gives back the
-//     logical codes and scales;
-//   * split tiles have consistent split/nsplit/pbase/counter numbers, no CTA has
-//     more than 32 units, and the CTA ranges have about equal bytes.
-// Exit status 0 on success; the first failed check is printed.
+// Builds pack.cpp, plan.cpp and gemv_plan.cpp against a stub CUDA runtime
+// whose "device" memory is host memory. It packs seeded random matrices and
+// checks that
+//   * walking the stream tile by tile (run header, then steps) decodes every
+//     (row, group) exactly once, back to its logical codes and fp16 scale,
+//     with runs in (tile, group column, class) order and rows increasing;
+//   * replaying every warp of every CTA of a plan exactly as the batch-1
+//     kernel does (its byte pieces concatenated into its stream, the first
+//     run header from the plan, later headers from the stream) visits every
+//     step once, consumes exactly the bytes the warp copies, and keeps each
+//     CTA inside its window of SLOTS_MAX super-tiles and CCAP staged columns;
+//     per-super-tile arrival counts match;
+//   * the same holds for plans over several matrices (as for [q; k; v]) and
+//     for several CTA counts.
+// Exit status 0 on success; the first failed checks are printed.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -58,14 +61,14 @@ const GpuInfo& gpu_info() {
 using namespace vbq;
 
 static int g_failures = 0;
-#define CHECK(cond, ...)                                   \
-  do {                                                     \
-    if (!(cond)) {                                         \
+#define CHECK(cond, ...)                                        \
+  do {                                                          \
+    if (!(cond)) {                                              \
       std::fprintf(stderr, "FAIL %s:%d: ", __FILE__, __LINE__); \
-      std::fprintf(stderr, __VA_ARGS__);                   \
-      std::fprintf(stderr, "\n");                          \
-      if (++g_failures > 10) std::exit(1);                 \
-    }                                                      \
+      std::fprintf(stderr, __VA_ARGS__);                        \
+      std::fprintf(stderr, "\n");                               \
+      if (++g_failures > 10) std::exit(1);                      \
+    }                                                           \
   } while (0)
 
 struct Logical {
@@ -100,229 +103,230 @@ static Logical make_matrix(int64_t N, int64_t K, const double p[4], uint32_t see
   return L;
 }
 
-// Replays the kernel's walk over one launch's plan. segs[i] is the packed matrix i.
-static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::vector<const Logical*>& logi,
-                       const Plan& pl, const DevicePlan& dp, int W, bool balance = true) {
-  const int SPW = SLICES / W;
-  // Every step of every run of every matrix: visit count.
-  std::vector<std::vector<std::vector<uint8_t>>> seen(mats.size());
-  uint64_t total = 0;
-  for (size_t s = 0; s < mats.size(); ++s) {
-    seen[s].resize(mats[s]->n_runs);
-    for (int32_t r = 0; r < mats[s]->n_runs; ++r) seen[s][r].assign(run_steps(mats[s]->h_run_desc[r]), 0);
-    total += mats[s]->data_bytes;
-  }
-  CHECK(pl.units.size() == static_cast<size_t>(pl.n_ctas) * pl.umax, "unit slots");
-  CHECK(dp.n_ctas == pl.n_ctas && dp.umax == pl.umax, "device plan shape");
-  std::vector<uint64_t> cta_bytes(pl.n_ctas, 0);
-  std::vector<uint64_t> cta_cost(pl.n_ctas, 0);  // the planner's work model over what each CTA walks
-  std::vector<uint32_t> cnt_units(pl.n_counters, 0);
-  std::vector<uint32_t> cta_units(pl.n_ctas, 0);
-  for (int32_t c = 0; c < pl.n_ctas; ++c) {
-    // The kernel counts a CTA's units as the non-empty slots, which come first.
-    uint32_t nu = 0;
-    bool gap = false;
-    for (int32_t i = 0; i < pl.umax; ++i) {
-      const bool used = dp.units[static_cast<size_t>(c) * pl.umax + i].nsplit > 0;
-      if (used && gap) CHECK(false, "CTA %d: used slot after an empty one", c);
-      if (used) ++nu; else gap = true;
-    }
-    cta_units[c] = nu;
-    CHECK(pl.umax <= MAX_UNITS_PER_CTA, "umax %d", pl.umax);
-    const uint32_t u0 = static_cast<uint32_t>(c) * pl.umax, u1 = u0 + nu;
-    for (int w = 0; w < W; ++w) {
-      uint64_t stream = 0;  // bytes this warp copies, in order
-      // The warp's piece list: one piece per unit with a non-empty slice, in unit order.
-      const uint64_t* pieces = W == 16 ? dp.pieces16 : dp.pieces8;
-      const uint32_t* pstart = W == 16 ? dp.start16 : dp.start8;
-      const uint32_t* pbytes = W == 16 ? dp.bytes16 : dp.bytes8;
-      uint32_t pi = pstart[c * W + w];
-      for (uint32_t u = u0; u < u1; ++u) {
-        const UnitRec ur = dp.units[u];
-        CHECK(ur.seg < mats.size(), "unit seg");
-        const vbq_matrix* M = mats[ur.seg];
-        const Logical& LG = *logi[ur.seg];
-        CHECK(ur.tile < static_cast<uint32_t>(M->n_tiles), "unit tile");
-        CHECK(ur.split < ur.nsplit, "split index");
-        const uint32_t r0 = M->h_tile_row0[ur.tile], rows = M->h_tile_row0[ur.tile + 1] - r0;
-        CHECK(ur.r0 == r0 && ur.rows == rows, "unit rows");
-        if (ur.nsplit > 1) {
-          CHECK(ur.cnt < pl.n_counters, "counter index");
-          CHECK(static_cast<uint64_t>(ur.pbase) + static_cast<uint64_t>(ur.nsplit) * rows <= pl.partial_rows,
-                "partial range");
-          if (w == 0) cnt_units[ur.cnt] += 1;
-        }
-        const SliceRec f = dp.slices[static_cast<size_t>(u) * SLICES + w * SPW];
-        const SliceRec l = dp.slices[static_cast<size_t>(u) * SLICES + w * SPW + SPW - 1];
-        if (SPW == 2) {
-          const SliceRec mid = dp.slices[static_cast<size_t>(u) * SLICES + w * SPW];
-          CHECK(mid.b1 == l.b0, "slices of a warp are contiguous");
-        }
-        const uint64_t b0 = uint64_t(f.b0) * 16, b1 = uint64_t(l.b1) * 16;
-        CHECK(b1 >= b0, "slice bytes");
-        if (b1 > b0) {
-          CHECK(pi < pstart[c * W + w + 1], "CTA %d warp %d: too few pieces", c, w);
-          const uint64_t q = pieces[pi++];
-          CHECK(((q >> 20) << 4) == reinterpret_cast<uint64_t>(M->data + b0), "piece address");
-          CHECK(((q & 0xFFFFFu) << 4) == b1 - b0, "piece length");
-        }
-        {  // the first group column the kernel prefetches
-          const uint32_t g0 = (SPW > 1 && f.b1 == f.b0) ? l.g0 : f.g0;
-          if (b1 > b0) {
-            const uint32_t r = (SPW > 1 && f.b1 == f.b0) ? l.run0 : f.run0;
-            CHECK(g0 == run_g(M->h_run_desc[r]), "slice g0");
-          }
-        }
-        cta_bytes[c] += b1 - b0;
-        // Walk runs and steps exactly as the kernel does.
-        uint64_t o = b0;
-        const uint32_t run_end = l.run1 + (l.k1 > 0 ? 1u : 0u);
-        uint32_t k = f.k0;
-        for (uint32_t run = f.run0; run < run_end; ++run, k = 0) {
-          CHECK(run < static_cast<uint32_t>(M->n_runs), "run index %u of %d", run, M->n_runs);
-          CHECK(run >= M->h_tile_run0[ur.tile] && run < M->h_tile_run0[ur.tile + 1], "run outside the unit's tile");
-          const uint32_t d = M->h_run_desc[run];
-          const uint32_t cls = run_cls(d), n = run_n(d), eps = entries_per_step(cls);
-          const uint32_t kend = (run == l.run1) ? l.k1 : (n + eps - 1) / eps;
-          if (k == 0 && kend > 0) CHECK(o == uint64_t(M->h_run_off[run]) * 16, "run start offset");
-          if (k == 0 && kend > 0) {
-            const bool col = run == 0 || run_g(M->h_run_desc[run - 1]) != run_g(d) ||
-                             std::binary_search(M->h_tile_run0.begin(), M->h_tile_run0.end(), run);
-            cta_cost[c] += kCostRun + (col ? kCostColumn : 0u);
-          }
-          if (kend > k) cta_cost[c] += uint64_t(kend - k) * kCostStep[cls];
-          for (; k < kend; ++k) {
-            CHECK(k < seen[ur.seg][run].size(), "step index");
-            seen[ur.seg][run][k] += 1;
-            const uint32_t e = std::min(eps, n - k * eps);
-            const uint8_t* rec = M->data + o;
-            const int b = 1 << cls;
-            const uint32_t g = run_g(d);
-            for (uint32_t j = 0; j < e; ++j) {
-              const uint32_t row = rec[rec_row_off(cls, e) + j];
-              CHECK(row < rows, "row in tile");
-              uint16_t sc;
-              std::memcpy(&sc, rec + rec_scale_off(cls, e) + 2 * j, 2);
-              const int64_t R = r0 + row;
-              CHECK(LG.bits[R * (LG.K / 64) + g] == b, "class of (row, g)");
-              CHECK(LG.scales[R * (LG.K / 64) + g] == sc, "scale of (row, g)");
-              const uint8_t* ent = rec + j * 8u * b;
-              for (int m = 0; m < 64; ++m) {
-                uint32_t q = 0;  // bit-planes for 1, 2 and 4 bits, bytes for 8 bits
-                if (b == 8) {
-                  q = ent[m];
-                } else {
-                  for (int p = 0; p < b; ++p) q |= ((ent[8 * p + (m >> 3)] >> (m & 7)) & 1u) << p;
-                }
-                if (q != LG.codes[R * LG.K + g * 64 + m]) {
-                  CHECK(false, "code mismatch row %lld g %u m %d", static_cast<long long>(R), g, m);
-                  break;
-                }
-              }
-            }
-            o += rec_bytes(cls, e);
-          }
-        }
-        CHECK(o == b1, "walked bytes %llu != slice end %llu", static_cast<unsigned long long>(o),
-              static_cast<unsigned long long>(b1));
-        stream += b1 - b0;
-      }
-      CHECK(pi == pstart[c * W + w + 1], "CTA %d warp %d: extra pieces", c, w);
-      CHECK(pbytes[c * W + w] == stream, "CTA %d warp %d: piece bytes", c, w);
-    }
-  }
-  for (size_t s = 0; s < mats.size(); ++s)
-    for (int32_t r = 0; r < mats[s]->n_runs; ++r)
-      for (size_t k = 0; k < seen[s][r].size(); ++k)
-        CHECK(seen[s][r][k] == 1, "seg %zu run %d step %zu walked %d times", s, r, k, seen[s][r][k]);
-  for (uint32_t i = 0; i < pl.n_counters; ++i) CHECK(cnt_units[i] >= 2, "split tile with <2 units");
-  // Balance: no CTA far above the mean of the work model (one step and one
-  // column of slack per unit, since cuts fall on step borders).
-  if (balance && pl.n_ctas > 1 && W == 16) {
-    uint64_t tot = 0;
-    for (uint64_t v : cta_cost) tot += v;
-    const double mean = static_cast<double>(tot) / pl.n_ctas;
-    for (int32_t c = 0; c < pl.n_ctas; ++c)
-      CHECK(cta_cost[c] <= mean * 1.02 + 200.0 + 250.0 * cta_units[c], "CTA %d carries cost %llu, mean %.0f", c,
-            static_cast<unsigned long long>(cta_cost[c]), mean);
+// Code m of entry j of a step record of class cls with e entries (layout.h).
+static uint32_t decode_code(const uint8_t* rec, uint32_t cls, uint32_t j, uint32_t m) {
+  const uint32_t b = 1u << cls;
+  const uint8_t* ent = rec + 8u * b * j;
+  if (b == 1) return (ent[m >> 3] >> (m & 7)) & 1u;
+  const uint32_t per_slice = 64 / b, per_word = per_slice / 2;
+  const uint32_t s = m / per_slice, within = m % per_slice, h = within / per_word, r = within % per_word;
+  uint32_t w;
+  std::memcpy(&w, ent + 8 * s + 4 * h, 4);
+  return (w >> code_bit(b, r)) & ((1u << b) - 1u);
+}
+
+// Checks the entries of one step (entries i0 .. i0+e-1 of its run) against the
+// logical matrix and marks them seen.
+static void check_step(const Logical& L, const RunHeader& h, const uint8_t* rec, uint32_t e, uint32_t i0,
+                       std::vector<uint8_t>* seen, int64_t* last_row) {
+  const int64_t G = L.K / 64;
+  const uint32_t cls = h.cls;
+  for (uint32_t j = 0; j < e; ++j) {
+    const uint16_t sc = *reinterpret_cast<const uint16_t*>(rec + rec_scale_off(cls, e) + 2 * j);
+    const uint32_t row_in = rec[rec_row_off(cls, e) + j];
+    const uint32_t tile = entry_tile(h, i0 + j);
+    CHECK(tile < h.ntl, "entry tile inside the super-tile");
+    const int64_t r = int64_t(h.row0) + int64_t(tile) * TILE + row_in;
+    CHECK(r < L.N, "row %lld beyond N", (long long)r);
+    if (r >= L.N) continue;
+    CHECK(r > *last_row, "rows of a run must increase");
+    *last_row = r;
+    const int64_t gi = r * G + h.g;
+    CHECK(L.bits[gi] == (1 << cls), "class of (%lld, %u)", (long long)r, h.g);
+    CHECK(L.scales[gi] == sc, "scale of (%lld, %u)", (long long)r, h.g);
+    for (uint32_t m = 0; m < 64; ++m)
+      CHECK(decode_code(rec, cls, j, m) == L.codes[r * L.K + int64_t(h.g) * 64 + m], "code %u of (%lld, %u)", m,
+            (long long)r, h.g);
+    (*seen)[gi] += 1;
   }
 }
 
+// Walks the whole stream super-tile by super-tile, as the dequant kernel does.
+static void check_stream(const vbq_matrix* M, const Logical& L) {
+  const int64_t G = L.K / 64;
+  std::vector<uint8_t> seen(L.N * G, 0);
+  std::vector<uint64_t> tb(M->n_super + 1);
+  std::memcpy(tb.data(), M->st_byte0, 8 * tb.size());
+  size_t run_index = 0;
+  for (int32_t t = 0; t < M->n_super; ++t) {
+    uint64_t o = tb[t];
+    int last_key = -1;
+    const int64_t rows = std::min<int64_t>(L.N - int64_t(t) * SROWS, SROWS);
+    while (o < tb[t + 1]) {
+      RunHeader h;
+      std::memcpy(&h, M->data + o, sizeof(h));
+      CHECK(run_index < M->runs.size() && M->runs[run_index].off == o &&
+                std::memcmp(&M->runs[run_index].h, &h, sizeof(h)) == 0, "run list entry");
+      CHECK(h.row0 == static_cast<uint32_t>(t) * SROWS, "header super-tile");
+      CHECK(h.ntl == (rows + TILE - 1) / TILE, "header tile count");
+      CHECK(h.c1 <= h.c2 && h.c2 <= h.c3 && h.c3 <= h.n, "prefix counts");
+      const int key = h.g * 4 + h.cls;
+      CHECK(key > last_key, "runs in (g, class) order");
+      last_key = key;
+      ++run_index;
+      o += HEADER_BYTES;
+      int64_t last_row = -1;
+      const uint32_t eps = entries_per_step(h.cls);
+      for (uint32_t done = 0; done < h.n; done += eps) {
+        const uint32_t e = std::min<uint32_t>(eps, h.n - done);
+        check_step(L, h, M->data + o, e, done, &seen, &last_row);
+        o += rec_bytes(h.cls, e);
+      }
+    }
+    CHECK(o == tb[t + 1], "super-tile %d ends at its table offset", t);
+  }
+  CHECK(run_index == M->runs.size(), "every run walked");
+  for (size_t i = 0; i < seen.size(); ++i) CHECK(seen[i] == 1, "group %zu seen %d times", i, seen[i]);
+  // Byte accounting.
+  int64_t cb = 0;
+  for (uint8_t b : L.bits) cb += 8 * b;
+  CHECK(cb == M->code_bytes, "code bytes");
+  CHECK(M->total_bytes == M->code_bytes + M->meta_bytes, "total = code + meta");
+}
+
+// Replays an item plan: every warp's stream (its pieces), walked like the kernel.
+static void check_plan(const std::vector<const vbq_matrix*>& mats, const std::vector<const Logical*>& logi,
+                       const ItemPlan& P, const std::vector<std::vector<uint64_t>>& pieces_per_warp) {
+  std::vector<std::vector<uint8_t>> seen(mats.size());
+  for (size_t s = 0; s < mats.size(); ++s) seen[s].assign(logi[s]->N * (logi[s]->K / 64), 0);
+  std::vector<uint32_t> arrivals(P.n_item_super, 0);
+  for (int32_t c = 0; c < P.n_ctas; ++c) {
+    const CtaPlan& cp = P.ctas[c];
+    CHECK(cp.n_slots <= static_cast<uint32_t>(SLOTS_MAX), "CTA %d touches %u super-tiles", c, cp.n_slots);
+    const uint32_t ncols = (cp.a1 - cp.a0) + (cp.b1 - cp.b0);
+    CHECK(ncols <= static_cast<uint32_t>(CCAP), "CTA %d stages %u columns", c, ncols);
+    for (uint32_t t = 0; t < cp.n_slots; ++t) arrivals[cp.st_base + t] += 1;
+    for (int w = 0; w < KW; ++w) {
+      const size_t wi = static_cast<size_t>(c) * KW + w;
+      // The warp's stream: its pieces concatenated.
+      std::vector<uint8_t> st;
+      for (uint64_t pc : pieces_per_warp[wi]) {
+        const uint8_t* a = reinterpret_cast<const uint8_t*>((pc >> 20) << 4);
+        const uint64_t n = (pc & 0xFFFFFu) << 4;
+        st.insert(st.end(), a, a + n);
+      }
+      const WarpPlan& wp = P.warps[wi];
+      uint64_t o = 0;
+      for (uint32_t si = 0; si < wp.nsub; ++si) {
+        const SubRange& sr = wp.sub[si];
+        CHECK(sr.seg < mats.size(), "sub-range segment");
+        const Logical& L = *logi[sr.seg];
+        RunHeader h = sr.first;
+        uint32_t k = sr.k0, left = sr.nsteps;
+        if (left == 0) continue;
+        if (k == 0) {
+          CHECK(o + HEADER_BYTES <= st.size(), "header inside the stream");
+          RunHeader sh;
+          std::memcpy(&sh, st.data() + o, sizeof(sh));
+          CHECK(std::memcmp(&sh, &h, sizeof(h)) == 0, "plan header equals the stream header");
+          o += HEADER_BYTES;
+        }
+        while (true) {
+          const uint32_t nrs = run_steps(h.cls, h.n);
+          CHECK(k < nrs, "start step inside the run");
+          const uint32_t kend = std::min(nrs, k + left);
+          const uint32_t item_st = P.st_off[sr.seg] + h.row0 / SROWS;
+          CHECK(item_st >= cp.st_base && item_st < cp.st_base + cp.n_slots, "super-tile inside the CTA window");
+          CHECK((h.g >= cp.a0 && h.g < cp.a1) || (h.g >= cp.b0 && h.g < cp.b1), "column %u staged by CTA %d", h.g, c);
+          CHECK(col_slot(cp, h.g) < ncols, "column slot");
+          const uint32_t eps = entries_per_step(h.cls), nfull = h.n / eps, e_last = h.n - nfull * eps;
+          int64_t last_row = -1;
+          const uint32_t k_start = k;
+          for (; k < kend; ++k) {
+            const uint32_t e = k < nfull ? eps : e_last;
+            CHECK(o + rec_bytes(h.cls, e) <= st.size(), "step inside the stream");
+            if (o + rec_bytes(h.cls, e) > st.size()) return;
+            check_step(L, h, st.data() + o, e, k * eps, &seen[sr.seg], &last_row);
+            o += rec_bytes(h.cls, e);
+          }
+          left -= kend - k_start;
+          if (left == 0) break;
+          CHECK(o + HEADER_BYTES <= st.size(), "next header inside the stream");
+          if (o + HEADER_BYTES > st.size()) return;
+          std::memcpy(&h, st.data() + o, sizeof(h));
+          o += HEADER_BYTES;
+          k = 0;
+        }
+      }
+      CHECK(o == st.size(), "CTA %d warp %d consumes %llu of %zu streamed bytes", c, w, (unsigned long long)o,
+            st.size());
+    }
+  }
+  for (size_t s = 0; s < mats.size(); ++s)
+    for (size_t i = 0; i < seen[s].size(); ++i) CHECK(seen[s][i] == 1, "seg %zu group %zu seen %d times", s, i, seen[s][i]);
+  for (uint32_t t = 0; t < P.n_item_super; ++t) CHECK(arrivals[t] == P.arrivals[t], "arrivals of super-tile %u", t);
+}
+
+static vbq_matrix* pack(const Logical& L) {
+  vbq_matrix* m = nullptr;
+  const vbq_status s = vbq_pack(L.codes.data(), L.bits.data(), L.scales.data(), L.N, L.K, nullptr, &m);
+  CHECK(s == VBQ_OK, "vbq_pack failed: %s", g_err.c_str());
+  return m;
+}
+
+static void plan_and_check(const std::vector<const vbq_matrix*>& mats, const std::vector<const Logical*>& logi,
+                           int32_t n_ctas) {
+  std::vector<SegPlanInput> segs;
+  for (const vbq_matrix* m : mats) {
+    SegPlanInput s;
+    s.runs = &m->runs;
+    s.data = m->data;
+    s.n_super = static_cast<uint32_t>(m->n_super);
+    s.G = static_cast<uint32_t>(m->G);
+    segs.push_back(s);
+  }
+  ItemPlan ip;
+  const char* why = "";
+  int32_t n = n_ctas;
+  while (!make_item_plan(segs, n, &ip, &why)) n *= 2;
+  std::vector<std::vector<uint64_t>> per_warp;
+  CHECK(append_pieces(ip, segs, &per_warp), "pieces");
+  per_warp.resize(static_cast<size_t>(ip.n_ctas) * KW);
+  check_plan(mats, logi, ip, per_warp);
+}
+
 int main() {
-  const double cfg0[4] = {0.69, 0.15, 0.11, 0.05};
-  const double all8[4] = {0, 0, 0, 1};
-  const double all1[4] = {1, 0, 0, 0};
+  const double p0[4] = {0.69, 0.15, 0.11, 0.05};
+  const double one[4][4] = {{1, 0, 0, 0}, {0, 1, 0, 0}, {0, 0, 1, 0}, {0, 0, 0, 1}};
   struct Case { int64_t N, K; const double* p; int mode; };
-  const Case cases[] = {
-      {768, 768, cfg0, 0},   {1, 64, cfg0, 0},     {3, 128, cfg0, 0},     {300, 1024, cfg0, 0},
-      {257, 640, cfg0, 0},   {4099, 128, cfg0, 0}, {200, 512, all8, 0},   {200, 512, all1, 0},
-      {1024, 1024, cfg0, 1}, {1024, 1024, cfg0, 2}, {2048, 4096, cfg0, 0}, {5000, 64, cfg0, 0},
-      {40000, 64, all1, 0},
+  std::vector<Case> cases = {
+      {1, 64, p0, 0},      {3, 128, p0, 0},     {257, 640, p0, 0},   {511, 192, p0, 0},   {768, 768, p0, 0},
+      {4099, 128, p0, 0},  {300, 1024, p0, 0},  {1024, 1024, p0, 1}, {1024, 1024, p0, 2}, {200, 512, one[0], 0},
+      {200, 512, one[1], 0}, {200, 512, one[2], 0}, {200, 512, one[3], 0}, {2048, 4096, p0, 0}, {20000, 128, p0, 0},
+      {5000, 8192, p0, 0}, {3000, 640, p0, 1},
   };
-  std::vector<Logical> keep;
-  keep.reserve(32);
-  std::vector<vbq_matrix*> packed;
   uint32_t seed = 1;
   for (const Case& cs : cases) {
-    keep.push_back(make_matrix(cs.N, cs.K, cs.p, seed++, cs.mode));
-    const Logical& L = keep.back();
+    const Logical L = make_matrix(cs.N, cs.K, cs.p, seed++, cs.mode);
+    vbq_matrix* m = pack(L);
+    if (!m) continue;
+    check_stream(m, L);
+    for (int32_t ctas : {1, 7, 148}) plan_and_check({m}, {&L}, ctas);
+    vbq_matrix_free(m);
+  }
+  {  // three matrices in one item, as [q; k; v]
+    const Logical q = make_matrix(600, 512, p0, 101, 0), k = make_matrix(130, 512, p0, 102, 0),
+                  v = make_matrix(257, 512, p0, 103, 0);
+    vbq_matrix *mq = pack(q), *mk = pack(k), *mv = pack(v);
+    for (int32_t ctas : {1, 5, 148}) plan_and_check({mq, mk, mv}, {&q, &k, &v}, ctas);
+    vbq_matrix_free(mq);
+    vbq_matrix_free(mk);
+    vbq_matrix_free(mv);
+  }
+  {  // invalid inputs are rejected before anything is allocated
+    Logical L = make_matrix(4, 128, p0, 7, 0);
     vbq_matrix* m = nullptr;
-    const vbq_status st = vbq_pack(L.codes.data(), L.bits.data(), L.scales.data(), L.N, L.K, nullptr, &m);
-    CHECK(st == VBQ_OK, "pack %lldx%lld: %s", static_cast<long long>(cs.N), static_cast<long long>(cs.K),
-          g_err.c_str());
-    packed.push_back(m);
-    // The matrix's own plan, as the 1- and 2-column kernels (16 warps) and the 4-column kernel (8 warps) read it.
-    Plan pl = make_plan({seg_tables(m)}, m->plan.n_ctas, MAX_UNITS_PER_CTA);
-    check_plan({m}, {&L}, pl, m->plan, 16);
-    check_plan({m}, {&L}, pl, m->plan, 8);
-    // Whole-column plans (the tensor-core path): every unit starts and ends at a column start.
-    for (int P : {1, 148}) {
-      Plan pc = make_plan({seg_tables(m)}, P, MAX_UNITS_PER_CTA, true);
-      DevicePlan dc;
-      CHECK(upload_plan(pc, 64, {m->data}, nullptr, &dc) == cudaSuccess, "upload");
-      check_plan({m}, {&L}, pc, dc, 16, /*balance=*/false);  // cuts fall only on column starts
-      for (size_t u = 0; u < pc.units.size(); ++u) {
-        if (pc.units[u].nsplit == 0) continue;
-        const SliceRec& a0 = pc.slices[u * SLICES];
-        const SliceRec& a1 = pc.slices[u * SLICES + SLICES - 1];
-        auto col_start = [&](uint32_t r) {
-          return r == 0 || r >= static_cast<uint32_t>(m->n_runs) ||
-                 run_g(m->h_run_desc[r - 1]) != run_g(m->h_run_desc[r]) ||
-                 std::binary_search(m->h_tile_run0.begin(), m->h_tile_run0.end(), r);
-        };
-        CHECK(a0.k0 == 0 && a1.k1 == 0 && col_start(a0.run0) && col_start(a1.run1), "unit %zu not on columns", u);
-      }
-      CHECK(m->max_col_bytes <= 17408, "column span %lld", static_cast<long long>(m->max_col_bytes));
-      free_plan(&dc);
-    }
-    // Other CTA counts, including more CTAs than tiles and a single CTA.
-    for (int P : {1, 7, 148, 600}) {
-      Plan p2 = make_plan({seg_tables(m)}, P, MAX_UNITS_PER_CTA);
-      DevicePlan d2;
-      CHECK(upload_plan(p2, 4, {m->data}, nullptr, &d2) == cudaSuccess, "upload");
-      check_plan({m}, {&L}, p2, d2, 16);
-      free_plan(&d2);
-    }
+    L.bits[3] = 3;
+    CHECK(vbq_pack(L.codes.data(), L.bits.data(), L.scales.data(), 4, 128, nullptr, &m) == VBQ_ERR_BITS && !m,
+          "bad bit-width");
+    L = make_matrix(4, 128, p0, 7, 0);
+    L.bits[0] = 1;
+    L.codes[5] = 2;
+    CHECK(vbq_pack(L.codes.data(), L.bits.data(), L.scales.data(), 4, 128, nullptr, &m) == VBQ_ERR_CODE_RANGE && !m,
+          "code out of range");
+    CHECK(vbq_pack(L.codes.data(), L.bits.data(), L.scales.data(), 4, 100, nullptr, &m) == VBQ_ERR_SHAPE, "K % 64");
   }
-  // Fused launches of several matrices (as the decode step's [q;k;v] and [gate;up]).
-  {
-    const std::vector<const vbq_matrix*> ms = {packed[3], packed[4], packed[6]};
-    const std::vector<const Logical*> ls = {&keep[3], &keep[4], &keep[6]};
-    std::vector<SegTables> segs;
-    for (const vbq_matrix* m : ms) segs.push_back(seg_tables(m));
-    for (int P : {1, 5, 148}) {
-      Plan p = make_plan(segs, P, MAX_UNITS_PER_CTA);
-      DevicePlan d;
-      CHECK(upload_plan(p, 1, {ms[0]->data, ms[1]->data, ms[2]->data}, nullptr, &d) == cudaSuccess, "upload");
-      check_plan(ms, ls, p, d, 16);
-      free_plan(&d);
-    }
-  }
-  for (vbq_matrix* m : packed) vbq_matrix_free(m);
-  if (g_failures) {
-    std::fprintf(stderr, "%d check(s) failed\n", g_failures);
-    return 1;
-  }
+  if (g_failures) return 1;
   std::printf("plan walk ok\n");
   return 0;
 }
