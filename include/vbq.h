@@ -259,6 +259,29 @@ VBQ_API int64_t vbq_launch_count(int32_t reset);
 VBQ_API vbq_status vbq_decode_step_noalloc(vbq_model* model, const uint16_t* x_dev, float* logits_dev,
                                            void* stream);
 
+/*
+ * Test hooks; they change how later decode steps (vbq_decode_step and
+ * vbq_decode_step_noalloc) behave in this process, and value 0 restores the
+ * default.
+ *  VBQ_DEBUG_WAIT_LIMIT     SM clock cycles a decode-step wait on another
+ *                           CTA's flag may take before the kernel records
+ *                           check code 3 and goes on (default 2e9, about a
+ *                           second at 2 GHz).
+ *  VBQ_DEBUG_NEVER_READY    nonzero: the waits look for a flag value that no
+ *                           launch writes, so the first one runs out after
+ *                           the limit and the rest give up at once. The step
+ *                           completes with wrong logits and check code 3.
+ *  VBQ_DEBUG_NOALLOC_WORDS  words of vbq_decode_step_noalloc's static array
+ *                           that it may use (to test its size check).
+ * Errors: VBQ_ERR_INVALID_ARG (unknown key, negative value).
+ */
+enum {
+  VBQ_DEBUG_WAIT_LIMIT = 1,
+  VBQ_DEBUG_NEVER_READY = 2,
+  VBQ_DEBUG_NOALLOC_WORDS = 3
+};
+VBQ_API vbq_status vbq_debug_set(int32_t key, int64_t value);
+
 #ifdef __cplusplus
 }
 #endif

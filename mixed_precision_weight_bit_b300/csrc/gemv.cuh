@@ -40,10 +40,13 @@
 
 namespace vbq {
 
-constexpr int CH = 4096;             // bytes per bulk copy and per ring slot
-constexpr int LOG_CH = 12;
-constexpr int NS_MAX = 6;            // ring slots per warp at most
-constexpr int SPILL = 512;           // bytes past the ring's end (>= header + the largest record)
+#ifndef VBQ_LOG_CH
+#define VBQ_LOG_CH 12
+#endif
+constexpr int LOG_CH = VBQ_LOG_CH;
+constexpr int CH = 1 << LOG_CH;      // bytes per bulk copy and per ring slot
+constexpr int NS_MAX = 16;           // ring slots per warp at most
+constexpr int SPILL = 2176;          // bytes past the ring's end (>= header + the largest record)
 constexpr int XL_FLOATS = 72;        // per column: 7 x 5 float2 in lookup order, padded to 16 bytes
 constexpr int NLUT = 13;             // 5-bit tables per group (the last covers 4 codes)
 constexpr int XCAP = 16384;          // largest K of the batch-1 kernels
@@ -55,15 +58,22 @@ constexpr uint32_t kNoRefill = 0xFFFFFFFFu;
 #define VBQ_NS 2
 #endif
 #ifndef VBQ_U1
-#define VBQ_U1 2
+#define VBQ_U1 1
 #endif
 #ifndef VBQ_UDP
-#define VBQ_UDP 2
+#define VBQ_UDP 1
 #endif
 constexpr int kRingSlots = VBQ_NS;
 constexpr int kU1 = VBQ_U1;
 constexpr int kUdp = VBQ_UDP;
-static_assert(kRingSlots >= 2 && kRingSlots <= 6, "ring slots");
+static_assert(kRingSlots >= 2 && kRingSlots <= NS_MAX, "ring slots");
+static_assert(CH >= 512 && (kRingSlots - 1) * CH >= 1024, "a few steps must fit ahead of the consumer");
+static_assert(SPILL % 16 == 0 && SPILL <= CH && SPILL >= HEADER_BYTES + full_step_bytes(3),
+              "a record that crosses the ring's end must fit in the mirrored bytes");
+// A warp waits for the bytes of U steps past its position; they must fit in
+// the slots other than the one being read.
+static_assert(kU1 * full_step_bytes(0) <= (kRingSlots - 1) * CH && kUdp * full_step_bytes(3) <= (kRingSlots - 1) * CH,
+              "steps decoded together must fit in the ring");
 
 struct ColInfo {
   int32_t sum_x;  // sum of the column's 64 fixed-point values
@@ -117,40 +127,92 @@ __device__ __forceinline__ int fixed_exponent(float max_row_l1, float max_abs_x)
 
 // ---- staging of x ------------------------------------------------------------
 
-// Stores a column into staging slot j: lane l gives x_{2l} and x_{2l+1} (bf16
-// values held in floats). Whole warp. F is the fixed-point exponent.
-__device__ __forceinline__ void put_column(const SmemLayout& L, int j, float x0, float x1, int F, int lane) {
-  float m = fmaxf(fabsf(x0), fabsf(x1));
+// 2^e as a float for -126 <= e <= 127 (exact).
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+// v * 2^e, exact unless the result leaves the float range (two steps when 2^e does).
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+  if (e >= -126 && e <= 127) return v * pow2f(e);
+  return scalbnf(v, e);
+}
+// The e with m < 2^e, for m > 0 (as frexpf gives it).
+__device__ __forceinline__ int exp_above(float m) {
+  const uint32_t b = __float_as_uint(m);
+  if ((b >> 23) != 0u) return static_cast<int>(b >> 23) - 126;
+  int e;
+  frexpf(m, &e);  // subnormal
+  return e;
+}
+
+// Stores NC columns into staging slots j0 + q * jstep (q < NC, only those
+// below ncols): lane l gives x_{2l} and x_{2l+1} of each (bf16 values held in
+// floats). Whole warp; the columns' reductions are interleaved. F is the
+// fixed-point exponent.
+template <int NC>
+__device__ __forceinline__ void put_columns(const SmemLayout& L, uint32_t j0, uint32_t jstep, uint32_t ncols,
+                                           const float (&x0)[NC], const float (&x1)[NC], int F, int lane) {
+  float m[NC];
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-  int s = 0;
-  if (m > 0.0f) {
-    int e;
-    frexpf(m, &e);  // m < 2^e, so |x| * 2^(14 - e) < 2^14
-    s = 14 - e;
-  }
-  const int X0 = __float2int_rn(scalbnf(x0, s)), X1 = __float2int_rn(scalbnf(x1, s));
-  int sx = X0 + X1;
+  for (int q = 0; q < NC; ++q) m[q] = fmaxf(fabsf(x0[q]), fabsf(x1[q]));
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, d);
-  sts<uint32_t>(L.X + j * 128 + 4 * lane, (static_cast<uint32_t>(X0) & 0xFFFFu) | (static_cast<uint32_t>(X1) << 16));
-  // Lookup order: float2 (x'_{10p+i}, x'_{10p+5+i}) at pair p*5 + i, p = 0..6, i = 0..4, x' = x * 2^F.
-  const uint32_t xb = L.xl + j * XL_FLOATS * 4;
+  for (int d = 16; d >= 1; d >>= 1)
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int jj = 2 * lane + h;
-    const int p = jj / 10, w = jj - 10 * p;
-    const int idx = (p * 5 + (w % 5)) * 2 + w / 5;
-    sts<float>(xb + idx * 4, scalbnf(h ? x1 : x0, F));
+    for (int q = 0; q < NC; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], d));
+  int s[NC], sx[NC], X0[NC], X1[NC];
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    s[q] = m[q] > 0.0f ? 14 - exp_above(m[q]) : 0;  // |x| * 2^s < 2^14
+    X0[q] = __float2int_rn(mul_pow2(x0[q], s[q]));
+    X1[q] = __float2int_rn(mul_pow2(x1[q], s[q]));
+    sx[q] = X0[q] + X1[q];
   }
-  // x_64 .. x_69 do not exist: zero their slots (indices 68 and 61, 63, 65, 67, 69).
-  if (lane < 6) sts<float>(xb + (lane == 0 ? 68 : 59 + 2 * lane) * 4, 0.0f);
-  if (lane == 0) {
-    ColInfo ci;
-    ci.sum_x = sx;
-    ci.u = scalbnf(1.0f, F - s - 1);
-    sts<ColInfo>(L.col + j * 8, ci);
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1)
+#pragma unroll
+    for (int q = 0; q < NC; ++q) sx[q] += __shfl_xor_sync(0xffffffffu, sx[q], d);
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    const uint32_t j = j0 + q * jstep;
+    if (j >= ncols) continue;
+    sts<uint32_t>(L.X + j * 128 + 4 * lane, (static_cast<uint32_t>(X0[q]) & 0xFFFFu) | (static_cast<uint32_t>(X1[q]) << 16));
+    // Lookup order: float2 (x'_{10p+i}, x'_{10p+5+i}) at pair p*5 + i, p = 0..6, i = 0..4, x' = x * 2^F.
+    const uint32_t xb = L.xl + j * XL_FLOATS * 4;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int jj = 2 * lane + h;
+      const int p = jj / 10, w = jj - 10 * p;
+      const int idx = (p * 5 + (w % 5)) * 2 + w / 5;
+      sts<float>(xb + idx * 4, mul_pow2(h ? x1[q] : x0[q], F));
+    }
+    // x_64 .. x_69 do not exist: zero their slots (indices 68 and 61, 63, 65, 67, 69).
+    if (lane < 6) sts<float>(xb + (lane == 0 ? 68 : 59 + 2 * lane) * 4, 0.0f);
+    if (lane == 0) {
+      ColInfo ci;
+      ci.sum_x = sx[q];
+      ci.u = mul_pow2(1.0f, F - s[q] - 1);
+      sts<ColInfo>(L.col + j * 8, ci);
+    }
   }
+}
+
+// Stages the warp's columns (slots warp, warp + KW, ...) from values given by get(j, &x0, &x1).
+template <typename Get>
+__device__ __forceinline__ void stage_columns(const SmemLayout& L, uint32_t ncols, int F, int lane, int warp, Get get) {
+  constexpr int CPW = (CCAP + KW - 1) / KW;
+  if (static_cast<uint32_t>(warp) >= ncols) return;
+  if (ncols <= static_cast<uint32_t>(KW)) {  // one column for this warp
+    float a[1], b[1];
+    get(static_cast<uint32_t>(warp), &a[0], &b[0]);
+    put_columns<1>(L, warp, KW, ncols, a, b, F, lane);
+    return;
+  }
+  float a[CPW], b[CPW];
+#pragma unroll
+  for (int q = 0; q < CPW; ++q) {
+    const uint32_t j = warp + q * KW;
+    a[q] = b[q] = 0.0f;
+    if (j < ncols) get(j, &a[q], &b[q]);
+  }
+  put_columns<CPW>(L, warp, KW, ncols, a, b, F, lane);
 }
 
 // ---- per-warp stream ---------------------------------------------------------
@@ -296,33 +358,34 @@ __device__ __forceinline__ float decode_plane(uint2 cw, const float (&lut)[NLUT]
   return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
-// sum q X over the lane's slice of a 2-, 4- or 8-bit entry (exact int32).
+// sum q X over the lane's 2-, 4- or 8-bit entry (exact int32): its 2b code
+// words w against the column's 32 X pairs, in four independent sums.
 template <int CLS>
-__device__ __forceinline__ int decode_dp(uint2 cw, const uint32_t (&xp)[16]) {
-  int s = 0;
+__device__ __forceinline__ int decode_dp(const uint32_t (&w)[16], const uint32_t (&xp)[32]) {
+  constexpr int NW = 2 << CLS;
+  int s[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t w = h ? cw.y : cw.x;
-    if constexpr (CLS == 1) {
+  for (int k = 0; k < NW; ++k) {
+    if constexpr (CLS == 1) {  // word k: codes 16k .. 16k+15
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t by = (w >> (2 * i)) & 0x03030303u;
-        s = dp2a_lo(xp[8 * h + 2 * i], by, s);
-        s = dp2a_hi(xp[8 * h + 2 * i + 1], by, s);
+        const uint32_t by = (w[k] >> (2 * i)) & 0x03030303u;
+        s[i & 3] = dp2a_lo(xp[8 * k + 2 * i], by, s[i & 3]);
+        s[i & 3] = dp2a_hi(xp[8 * k + 2 * i + 1], by, s[i & 3]);
       }
-    } else if constexpr (CLS == 2) {
+    } else if constexpr (CLS == 2) {  // word k: codes 8k .. 8k+7
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const uint32_t by = (w >> (4 * i)) & 0x0F0F0F0Fu;
-        s = dp2a_lo(xp[4 * h + 2 * i], by, s);
-        s = dp2a_hi(xp[4 * h + 2 * i + 1], by, s);
+        const uint32_t by = (w[k] >> (4 * i)) & 0x0F0F0F0Fu;
+        s[(2 * k + i) & 3] = dp2a_lo(xp[4 * k + 2 * i], by, s[(2 * k + i) & 3]);
+        s[(2 * k + i) & 3] = dp2a_hi(xp[4 * k + 2 * i + 1], by, s[(2 * k + i) & 3]);
       }
-    } else {
-      s = dp2a_lo(xp[2 * h], w, s);
-      s = dp2a_hi(xp[2 * h + 1], w, s);
+    } else {  // word k: codes 4k .. 4k+3
+      s[k & 3] = dp2a_lo(xp[2 * k], w[k], s[k & 3]);
+      s[k & 3] = dp2a_hi(xp[2 * k + 1], w[k], s[k & 3]);
     }
   }
-  return s;
+  return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 // Per-warp consumer state.
@@ -356,15 +419,12 @@ __device__ __forceinline__ void build_lut(const SmemLayout& L, int j, Worker& K)
   K.lut_col = j;
 }
 
-// Loads the lane's X pairs of staging slot j for class CLS (lane slice s = lane & (b - 1)).
-template <int CLS>
-__device__ __forceinline__ void load_xp(const SmemLayout& L, int j, int lane, uint32_t (&xp)[16]) {
-  constexpr int B = 1 << CLS;
-  constexpr int NP = 32 / B;  // int16 pairs in the slice
-  const uint32_t base = L.X + j * 128 + (lane & (B - 1)) * (128 / B);
+// Loads the 32 X pairs of staging slot j (the same in every lane).
+__device__ __forceinline__ void load_xp(const SmemLayout& L, int j, uint32_t (&xp)[32]) {
+  const uint32_t base = smem_u32(vbq_smem) + L.X + j * 128;
 #pragma unroll
-  for (int q = 0; q < NP / 4; ++q) {
-    const uint4 v = lds_v4(smem_u32(vbq_smem) + base + 16 * q);
+  for (int q = 0; q < 8; ++q) {
+    const uint4 v = lds_v4(base + 16 * q);
     xp[4 * q] = v.x;
     xp[4 * q + 1] = v.y;
     xp[4 * q + 2] = v.z;
@@ -374,49 +434,51 @@ __device__ __forceinline__ void load_xp(const SmemLayout& L, int j, int lane, ui
 
 // Decodes U consecutive steps of class CLS with e entries each, the first at
 // ring position pos, and adds the entries into the CTA's row accumulators at
-// acc_a (the run's super-tile slot). The first step's first entry is entry i0
-// of the run (its tile comes from the header's prefix counts).
+// acc_a (the run's super-tile slot). Lane l works on entry l of each step (lanes
+// past e of a partial step read entry 0 and add nothing). The first step's
+// first entry is entry i0 of the run (its tile comes from the header's prefix
+// counts).
 template <int CLS, int U>
 __device__ __forceinline__ void do_steps(const WarpStream& S, uint32_t pos, uint32_t e, uint32_t i0,
                                          const RunHeader& h, uint32_t acc_a, const Worker& K,
-                                         const uint32_t (&xp)[16], const ColInfo& ci, int lane) {
+                                         const uint32_t (&xp)[32], const ColInfo& ci, int lane) {
   constexpr uint32_t B = 1u << CLS;
-  constexpr uint32_t E = 32u >> CLS;
   constexpr uint32_t FULL = full_step_bytes(CLS);
-  const uint32_t j = static_cast<uint32_t>(lane) >> CLS;
-  const uint32_t sigma = static_cast<uint32_t>(lane) & (B - 1u);
-  const uint32_t me = CLS == 0 ? static_cast<uint32_t>(lane) : j;  // the entry whose scale and row this lane reads
-  const bool lead = (CLS == 0 ? static_cast<uint32_t>(lane) < e : (sigma == 0 && j < e));
-  uint2 cw[U];
-  uint32_t sb[U], row[U];
+  const uint32_t me = static_cast<uint32_t>(lane) < e ? static_cast<uint32_t>(lane) : 0u;
+  const bool lead = static_cast<uint32_t>(lane) < e;
+  int iv[U];
+  uint32_t row[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     uint32_t p = pos + u * FULL;
     if (p >= S.rbytes) p -= S.rbytes;
     const uint32_t rec = S.ring + p;
-    cw[u] = lds<uint2>(rec + 8u * lane);
-    sb[u] = lds<uint16_t>(rec + rec_scale_off(CLS, e) + 2u * me);
+    const uint32_t sb = lds<uint16_t>(rec + rec_scale_off(CLS, e) + 2u * me);
     row[u] = lds<uint8_t>(rec + rec_row_off(CLS, e) + me);
-  }
-  int iv[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
     float v;
     if constexpr (CLS == 0) {
-      v = half_bits_to_float(sb[u]) * decode_plane(cw[u], K.lut);
+      const uint2 cw = lds<uint2>(rec + 8u * me);
+      v = half_bits_to_float(sb) * decode_plane(cw, K.lut);
     } else {
-      int s = decode_dp<CLS>(cw[u], xp);
+      uint32_t w[16];
 #pragma unroll
-      for (uint32_t d = 1; d < B; d <<= 1) s += __shfl_xor_sync(0xffffffffu, s, static_cast<int>(d));
-      const int t2 = 2 * s - static_cast<int>((1u << B) - 1u) * ci.sum_x;
-      v = half_bits_to_float(sb[u]) * (static_cast<float>(t2) * ci.u);
+      for (uint32_t q = 0; q < B / 2; ++q) {
+        const uint4 c = lds_v4(smem_u32(vbq_smem) + rec + (q * e + me) * 16u);
+        w[4 * q] = c.x;
+        w[4 * q + 1] = c.y;
+        w[4 * q + 2] = c.z;
+        w[4 * q + 3] = c.w;
+      }
+      const int sum = decode_dp<CLS>(w, xp);
+      const int t2 = 2 * sum - static_cast<int>((1u << B) - 1u) * ci.sum_x;
+      v = half_bits_to_float(sb) * (static_cast<float>(t2) * ci.u);
     }
     iv[u] = __float2int_rn(v);
   }
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     if (lead) {
-      const uint32_t tile = entry_tile(h, i0 + u * E + me);
+      const uint32_t tile = entry_tile(h, i0 + u * 32u + static_cast<uint32_t>(lane));
       red_shared_add_s32(acc_a + (tile * TILE + row[u]) * 4u, iv[u]);
     }
   }
@@ -428,30 +490,32 @@ __device__ __forceinline__ void do_steps(const WarpStream& S, uint32_t pos, uint
 template <int CLS, int U>
 __device__ __forceinline__ void run_steps_cls(const SmemLayout& L, const RunHeader& h, int cj, uint32_t k,
                                               uint32_t kend, uint32_t acc_a, WarpStream& S, Worker& K, int lane) {
-  constexpr uint32_t E = 32u >> CLS;
+  constexpr uint32_t E = STEP_LANES;
   constexpr uint32_t FULL = full_step_bytes(CLS);
   const uint32_t n = h.n;
-  const uint32_t nfull = n >> (5 - CLS);
+  const uint32_t nfull = n >> 5;
   const uint32_t e_last = n - nfull * E;
-  uint32_t xp[16];
+  uint32_t xp[32];
   ColInfo ci{0, 0.0f};
   if constexpr (CLS == 0) {
     if (K.lut_col != cj) build_lut(L, cj, K);
   } else {
-    load_xp<CLS>(L, cj, lane, xp);
+    load_xp(L, cj, xp);
     ci = lds<ColInfo>(L.col + cj * 8);
   }
-  const uint32_t kf = min(kend, nfull);
-  while (k + U <= kf) {
-    const uint32_t need = K.o + U * FULL;
-    if (S.avail < need) {
-      S.wait_for(need);
-      if (!S.ok) return;
+  if constexpr (U > 1) {
+    const uint32_t kf = min(kend, nfull);
+    while (k + U <= kf) {
+      const uint32_t need = K.o + U * FULL;
+      if (S.avail < need) {
+        S.wait_for(need);
+        if (!S.ok) return;
+      }
+      do_steps<CLS, U>(S, K.opos, E, k * E, h, acc_a, K, xp, ci, lane);
+      K.advance(U * FULL, S.rbytes);
+      k += U;
+      S.refill(K.o, lane);
     }
-    do_steps<CLS, U>(S, K.opos, E, k * E, h, acc_a, K, xp, ci, lane);
-    K.advance(U * FULL, S.rbytes);
-    k += U;
-    S.refill(K.o, lane);
   }
   for (; k < kend; ++k) {
     const uint32_t e = k < nfull ? E : e_last;
@@ -476,22 +540,23 @@ __device__ __forceinline__ void run_steps_any(const SmemLayout& L, const RunHead
   }
 }
 
-// One warp's part of one item: its sub-ranges of the plan, accumulated into
-// the CTA's accumulators (slot = item super-tile - cp.st_base). seg_st_off[s]
-// is the first item super-tile of segment s (null: one segment at 0).
+// One warp's part of one item: its sub-ranges of the plan (in global or
+// shared memory), accumulated into the CTA's accumulators (slot = item
+// super-tile - cp.st_base). seg_st_off[s] is the first item super-tile of
+// segment s (null: one segment at 0).
 __device__ __forceinline__ void warp_item(const SmemLayout& L, const WarpPlan* wp_g, const uint32_t* seg_st_off,
                                           const CtaPlan& cp, WarpStream& S, Worker& K, int lane) {
-  const uint32_t nsub = __ldg(&wp_g->nsub);
+  const uint32_t nsub = wp_g->nsub;
   for (uint32_t si = 0; si < nsub && S.ok; ++si) {
     const SubRange* sp = &wp_g->sub[si];
     RunHeader h;
     {
-      const uint4 hv = __ldg(reinterpret_cast<const uint4*>(&sp->first));
+      const uint4 hv = *reinterpret_cast<const uint4*>(&sp->first);
       h = *reinterpret_cast<const RunHeader*>(&hv);
     }
-    uint32_t k = __ldg(&sp->k0);
-    uint32_t left = __ldg(&sp->nsteps);
-    const uint32_t soff = seg_st_off ? seg_st_off[__ldg(&sp->seg)] : 0u;
+    uint32_t k = sp->k0;
+    uint32_t left = sp->nsteps;
+    const uint32_t soff = seg_st_off ? seg_st_off[sp->seg] : 0u;
     if (left == 0) continue;
     if (k == 0) K.advance(HEADER_BYTES, S.rbytes);  // the range starts at the run's header, which the warp has
     while (true) {

@@ -102,19 +102,12 @@ __global__ void __launch_bounds__(KW * 32, 1) vbq_gemv1_kernel(const __grid_cons
   const uint32_t na = cp.a1 - cp.a0;
   const uint32_t ncols = na + (cp.b1 - cp.b0);
   {
-    constexpr int CPW = (CCAP + KW - 1) / KW;
-    uint32_t v[CPW];
-#pragma unroll
-    for (int q = 0; q < CPW; ++q) {
-      const uint32_t j = warp + q * KW;
+    stage_columns(L, ncols, F, lane, warp, [&](uint32_t j, float* x0, float* x1) {
       const uint32_t g = j < na ? cp.a0 + j : cp.b0 + (j - na);
-      v[q] = j < ncols ? ldg_nc_u32(a.x + static_cast<size_t>(g) * GROUP + 2 * lane) : 0u;
-    }
-#pragma unroll
-    for (int q = 0; q < CPW; ++q) {
-      const uint32_t j = warp + q * KW;
-      if (j < ncols) put_column(L, static_cast<int>(j), bf16_lo(v[q]), bf16_hi(v[q]), F, lane);
-    }
+      const uint32_t v = ldg_nc_u32(a.x + static_cast<size_t>(g) * GROUP + 2 * lane);
+      *x0 = bf16_lo(v);
+      *x1 = bf16_hi(v);
+    });
   }
   __syncthreads();
 
@@ -223,16 +216,9 @@ __global__ void __launch_bounds__(256) vbq_dequant_kernel(const uint8_t* __restr
       const uint8_t* rec = data + o;
       for (uint32_t i = threadIdx.x; i < e * GROUP; i += blockDim.x) {
         const uint32_t j = i / GROUP, m = i % GROUP;
-        const uint8_t* ent = rec + 8u * b * j;
-        uint32_t q;
-        if (b == 1) {
-          q = (ent[m >> 3] >> (m & 7)) & 1u;
-        } else {
-          const uint32_t per_slice = GROUP / b, per_word = per_slice / 2;
-          const uint32_t s = m / per_slice, within = m % per_slice, hw = within / per_word, r = within % per_word;
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(ent + 8 * s + 4 * hw);
-          q = (w >> code_bit(b, r)) & ((1u << b) - 1u);
-        }
+        const uint32_t per_word = 32u / b, r = m % per_word;
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + code_word_off(cls, e, j, m / per_word));
+        const uint32_t q = (w >> (b == 1 ? r : code_bit(b, r))) & ((1u << b) - 1u);
         const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rec + rec_scale_off(cls, e) + 2 * j));
         const uint32_t row = h.row0 + entry_tile(h, done + j) * TILE + rec[rec_row_off(cls, e) + j];
         W[static_cast<int64_t>(row) * K + static_cast<int64_t>(h.g) * GROUP + m] = __fmul_rn(sc, static_cast<float>(q) - c);

@@ -13,23 +13,23 @@
 //
 //     [16-byte RunHeader][step][step]...
 //
-// and a step holds up to 32/b groups ("entries"), so that each of the 32 lanes
-// of a warp reads exactly 8 code bytes of it: lane l works on entry l >> c of
-// the step (c = log2 b) and on slice s = l & (b - 1) of that entry. A step
-// record of class c with e entries is
+// and a step holds up to 32 groups ("entries"); lane l of a warp works on
+// entry l. A step record of class c (b = 2^c bits) with e entries is
 //
 //     [codes: e * 8 * b bytes][scales: e * fp16][rows: e * u8 row-in-tile][pad to 16 B]
 //
-// Every step of a run is full except possibly the last one. The tile of entry
-// i of a run (counted from the run's start) is the number of prefix counts
-// c1, c2, c3 of the header that are <= i.
+// Every step of a run is full (32 entries) except possibly the last one. The
+// tile of entry i of a run (counted from the run's start) is the number of
+// prefix counts c1, c2, c3 of the header that are <= i.
 //
-// Code order inside an entry (64 codes, 8*b bytes): lane slice s holds the
-// 64/b codes [s*64/b, (s+1)*64/b) in its 8 bytes, as two 32-bit words of 32/b
-// codes each (word h holds slice codes [h*32/b, (h+1)*32/b)).
-//  * b = 1: code m of the word at bit m (little-endian bits).
-//  * b = 2, 4, 8: code r of the word (0 <= r < 32/b) sits in byte (r & 3) at
-//    bit offset b * (r >> 2). Then (word >> (b*i)) & mask puts codes
+// Codes of an entry (64 codes, 8*b bytes) are 2*b 32-bit words; word w holds
+// codes [w*32/b, (w+1)*32/b).
+//  * b = 1: the entry's 8 bytes sit at 8*j in the record (entry j); code m of
+//    a word at bit m (little-endian bits).
+//  * b = 2, 4, 8: the words go in 16-byte chunks of four, chunk q of entry j at
+//    byte 16 * (q * e + j), so that the 32 lanes read one chunk each with no
+//    bank conflict. Code r of a word (0 <= r < 32/b) sits in byte (r & 3) at
+//    bit offset b * (r >> 2); then (word >> (b*i)) & mask puts codes
 //    4i .. 4i+3 into the four bytes of a word, ready for a byte dot product.
 #pragma once
 
@@ -48,13 +48,12 @@ constexpr int GROUP = 64;
 constexpr int TILE = 256;          // rows per tile; a row index in a tile fits one byte
 constexpr int SUPER = 4;           // tiles per super-tile
 constexpr int SROWS = TILE * SUPER;  // rows per super-tile
-constexpr int STEP_LANES = 32;
-constexpr int LANE_BYTES = 8;      // code bytes per lane per step
+constexpr int STEP_LANES = 32;     // entries per full step
 constexpr int MAX_G = 65535;       // group columns per matrix (g fits 16 bits)
 constexpr int HEADER_BYTES = 16;
 
 __host__ __device__ inline constexpr int cls_bits(int cls) { return 1 << cls; }
-__host__ __device__ inline constexpr uint32_t entries_per_step(uint32_t cls) { return STEP_LANES >> cls; }
+__host__ __device__ inline constexpr uint32_t entries_per_step(uint32_t) { return STEP_LANES; }
 
 // Byte layout of a step record with e entries of class cls.
 __host__ __device__ inline constexpr uint32_t rec_code_bytes(uint32_t cls, uint32_t e) { return e * 8u << cls; }
@@ -68,9 +67,7 @@ __host__ __device__ inline constexpr uint32_t rec_bytes(uint32_t cls, uint32_t e
 // Bytes of a full step of class cls.
 __host__ __device__ inline constexpr uint32_t full_step_bytes(uint32_t cls) { return rec_bytes(cls, entries_per_step(cls)); }
 // Steps of a run of n entries, and its bytes including the header.
-__host__ __device__ inline constexpr uint32_t run_steps(uint32_t cls, uint32_t n) {
-  return (n + entries_per_step(cls) - 1u) >> (5u - cls);
-}
+__host__ __device__ inline constexpr uint32_t run_steps(uint32_t, uint32_t n) { return (n + STEP_LANES - 1u) >> 5; }
 __host__ __device__ inline constexpr uint32_t run_bytes(uint32_t cls, uint32_t n) {
   return HEADER_BYTES + (n / entries_per_step(cls)) * full_step_bytes(cls) +
          ((n % entries_per_step(cls)) ? rec_bytes(cls, n % entries_per_step(cls)) : 0u);
@@ -89,6 +86,11 @@ static_assert(sizeof(RunHeader) == HEADER_BYTES, "run header is 16 bytes");
 // Tile (0 .. SUPER-1) inside the super-tile of entry i of a run.
 __host__ __device__ inline uint32_t entry_tile(const RunHeader& h, uint32_t i) {
   return static_cast<uint32_t>(i >= h.c1) + static_cast<uint32_t>(i >= h.c2) + static_cast<uint32_t>(i >= h.c3);
+}
+
+// Byte offset of code word w (0 <= w < 2b) of entry j in a step record of class cls with e entries.
+__host__ __device__ inline constexpr uint32_t code_word_off(uint32_t cls, uint32_t e, uint32_t j, uint32_t w) {
+  return cls == 0 ? 8u * j + 4u * w : ((w >> 2) * e + j) * 16u + 4u * (w & 3u);
 }
 
 // Bit offset of code r (0 <= r < 32/b) inside its 32-bit word, b >= 2.

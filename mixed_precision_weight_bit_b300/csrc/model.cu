@@ -7,13 +7,15 @@
 // group's v), SwiGLU, fp32 residual, and bf16 at every projection input.
 //
 // A step is one persistent cooperative launch (vbq_decode_kernel): per layer
-// the items [q;k;v], o, [gate;up], down, then the head, with a grid barrier
-// between items. Each warp streams its share of every item's packed weights
-// back to back, so the next item's weights arrive while the CTAs wait at a
-// barrier. Items, work plans and per-warp piece lists are built once, here.
+// the items [q;k;v], o, [gate;up], down, then the head, linked by per-super-tile
+// flags instead of grid barriers. Each warp streams its share of every item's
+// packed weights back to back, so the next item's weights arrive while a CTA
+// waits for its inputs. Items, work plans and per-warp piece lists are built
+// once, here.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -49,28 +51,52 @@ int64_t proj_k(const vbq_model_desc& d, int p) {
 }
 
 int64_t n_super_of(int64_t n) { return (n + SROWS - 1) / SROWS; }
-uint32_t decode_smem_bytes() { return smem_layout(kRingSlots).total + XT_MAX * 2; }
+uint32_t decode_smem_bytes() { return smem_layout(kRingSlots).total + 2 * kItemSmem; }
+static_assert(smem_layout(kRingSlots).total + 2 * kItemSmem <= 232448, "shared memory of the decode kernel");
 
-// Offsets (in 8-byte words) of one step's scratch inside a region. All of it
-// must be zero before the first step; every step leaves the fixed-point sums
-// and counters so, and writes h and the per-item exponents before reading them.
-struct Layout {
-  int64_t bar = 0, F = 0, maxx = 0, h = 0, qkv = 0, o = 0, gu = 0, dn = 0, logits = 0, total = 0;
+int64_t r8(int64_t n) { return (n + 7) & ~int64_t(7); }
+
+// Scratch of one item, in 8-byte words from the scratch base: 64-bit sums,
+// float outputs (none for the head, which writes the logits), and the
+// per-super-tile arrival counters, flags and statistics.
+struct ItemBuf {
+  int64_t acc = 0, out = -1, cnt = 0, flag = 0, stats = 0;
+  int64_t n_super = 0;
 };
 
-Layout layout_of(const vbq_model_desc& d, int32_t n_items) {
+// The step scratch. Sums and counters must be zero before the first step and
+// every step leaves them so; flags hold the epoch of the launch that set them.
+struct Layout {
+  int64_t h0 = 0, h0_flag = 0, h0_stats = 0, n_super_in = 0;
+  std::vector<ItemBuf> items;
+  int64_t total = 0;
+};
+
+// n_super per item, in step order.
+Layout layout_of(const vbq_model_desc& d, const std::vector<int64_t>& item_super) {
   Layout L;
-  auto r8 = [](int64_t n) { return (n + 7) & ~int64_t(7); };
-  L.bar = 0;
-  L.F = 8;                                   // int [n_items]
-  L.maxx = L.F + r8((n_items + 1) / 2);      // float [n_items]
-  L.h = L.maxx + r8((n_items + 1) / 2);      // float [2][d]
-  L.qkv = L.h + r8(d.d);                     // u64 [1024 * (st(q) + st(k) + st(v))]
-  L.o = L.qkv + SROWS * (n_super_of(proj_n(d, P_Q)) + 2 * n_super_of(proj_n(d, P_K)));
-  L.gu = L.o + SROWS * n_super_of(d.d);
-  L.dn = L.gu + SROWS * 2 * n_super_of(d.d_ff);
-  L.logits = L.dn + SROWS * n_super_of(d.d);
-  L.total = L.logits + SROWS * n_super_of(d.vocab);
+  int64_t w = 0;
+  auto take = [&](int64_t words) {  // 128-byte aligned, so counters, flags and statistics share no cache line
+    const int64_t o = w;
+    w += (words + 15) & ~int64_t(15);
+    return o;
+  };
+  L.n_super_in = n_super_of(d.d);
+  L.h0 = take(L.n_super_in * SROWS / 2);
+  L.h0_flag = take((L.n_super_in + 1) / 2);
+  L.h0_stats = take(L.n_super_in);
+  const size_t n = item_super.size();
+  for (size_t i = 0; i < n; ++i) {
+    ItemBuf b;
+    b.n_super = item_super[i];
+    b.acc = take(b.n_super * SROWS);
+    if (i + 1 < n) b.out = take(b.n_super * SROWS / 2);
+    b.cnt = take((b.n_super + 1) / 2);
+    b.flag = take((b.n_super + 1) / 2);
+    b.stats = take(b.n_super);
+    L.items.push_back(b);
+  }
+  L.total = w;
   return L;
 }
 
@@ -91,11 +117,11 @@ struct vbq_model {
   float* tr_out = nullptr;
   std::vector<int64_t> in_off, out_off;
   int64_t in_total = 0, out_total = 0;
-  std::vector<void*> plan_mem;       // per item: warp and CTA plans
-  std::vector<const WarpPlan*> item_warps;
-  std::vector<const CtaPlan*> item_ctas;
   std::vector<std::vector<uint32_t>> item_st_off;
-  void* prog_mem = nullptr;          // piece lists and the item arrays
+  std::vector<int64_t> item_super;
+  void* prog_mem = nullptr;          // plans, piece lists and the item arrays
+  const CtaPlan* ctas = nullptr;     // [n_items][sms]
+  const WarpPlan* warps = nullptr;   // [n_items][sms][KW]
   const uint64_t* pieces = nullptr;
   const uint32_t* pstart = nullptr;
   const uint32_t* pbytes = nullptr;
@@ -109,7 +135,7 @@ namespace {
 
 // The static scratch of vbq_decode_step_noalloc (defined at the bottom of this file).
 vbq_status step_scratch_address(int dev, uint64_t** out);
-constexpr int64_t kStepScratchWords = 262144;  // 2 MiB
+constexpr int64_t kStepScratchWords = int64_t(4) << 20;  // 32 MiB
 
 float l1_of(std::initializer_list<const vbq_matrix*> ms) {
   float v = 0.0f;
@@ -117,109 +143,123 @@ float l1_of(std::initializer_list<const vbq_matrix*> ms) {
   return v;
 }
 
+// Flag values: one per launch, unique across models and devices (0 is never used).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e;
+  do {
+    e = counter.fetch_add(1u) + 1u;
+  } while (e == 0u);
+  return e;
+}
+
 // The items of one step over the scratch at base.
 std::vector<DItem> make_items(const vbq_model* m, uint64_t* base, bool trace) {
   const vbq_model_desc& d = m->desc;
   const Layout& L = m->lay;
-  int* Fs = reinterpret_cast<int*>(base + L.F);
-  float* mx = reinterpret_cast<float*>(base + L.maxx);
-  float* hb[2] = {reinterpret_cast<float*>(base + L.h), reinterpret_cast<float*>(base + L.h) + d.d};
-  unsigned long long* qkv = reinterpret_cast<unsigned long long*>(base + L.qkv);
-  unsigned long long* yo = reinterpret_cast<unsigned long long*>(base + L.o);
-  unsigned long long* gu = reinterpret_cast<unsigned long long*>(base + L.gu);
-  unsigned long long* yd = reinterpret_cast<unsigned long long*>(base + L.dn);
-  unsigned long long* lg = reinterpret_cast<unsigned long long*>(base + L.logits);
-  const int64_t nq = proj_n(d, P_Q), nkv = proj_n(d, P_K);
-  const int64_t n_qkv = L.o - L.qkv, n_yo = L.gu - L.o, n_gu = L.dn - L.gu, n_yd = L.logits - L.dn;
+  auto words = [&](int64_t off) { return base + off; };
   auto tin = [&](int p) -> uint16_t* { return trace ? m->tr_in + m->in_off[p] : nullptr; };
   auto tout = [&](int p) -> float* { return trace ? m->tr_out + m->out_off[p] : nullptr; };
+  const int64_t nq = proj_n(d, P_Q);
+  // The residual read by the next RMSNorm: its vector and statistics.
+  const float* res_vec = reinterpret_cast<const float*>(words(L.h0));
+  ResStats res{reinterpret_cast<const float2*>(words(L.h0_stats)), reinterpret_cast<const uint32_t*>(words(L.h0_flag)),
+               static_cast<int32_t>(L.n_super_in), d.d};
   std::vector<DItem> items;
-  int cur = 0;  // h buffer holding the latest residual
-  auto base_item = [&](int idx, int mode, int K, float l1, unsigned long long* out) {
+  auto base_item = [&](int idx, int mode, int K, float l1) {
+    const ItemBuf& b = L.items[idx];
     DItem it{};
-    it.warps = m->item_warps[idx];
-    it.ctas = m->item_ctas[idx];
     for (size_t s = 0; s < m->item_st_off[idx].size() && s < static_cast<size_t>(MAX_SEG); ++s)
       it.seg_st_off[s] = m->item_st_off[idx][s];
     it.mode = mode;
     it.K = K;
     it.l1 = l1;
-    it.out = out;
-    it.F_out = Fs + idx;
-    it.maxx_out = mx + idx;
     it.eps = d.rms_eps;
+    it.n_super = static_cast<int32_t>(b.n_super);
+    it.acc = reinterpret_cast<unsigned long long*>(words(b.acc));
+    it.cnt = reinterpret_cast<uint32_t*>(words(b.cnt));
+    it.flag = reinterpret_cast<uint32_t*>(words(b.flag));
+    it.out = b.out >= 0 ? reinterpret_cast<float*>(words(b.out)) : nullptr;
+    it.out_n = b.n_super * SROWS;
     return it;
+  };
+  auto rms_input = [&](DItem& it) {
+    it.src = res_vec;
+    it.src_flag = res.flag;
+    it.src_nsuper = res.n_super;
+    it.rs = res;
+  };
+  auto residual_output = [&](DItem& it, int idx) {  // out = res_vec + y; the next RMSNorm reads it
+    it.res = res_vec;
+    it.out_n = d.d;
+    it.stats = reinterpret_cast<float2*>(words(L.items[idx].stats));
+    res_vec = it.out;
+    res = ResStats{it.stats, it.flag, it.n_super, d.d};
   };
   for (int l = 0; l < d.n_layers; ++l) {
     const vbq_matrix* const* W = &m->mats[static_cast<size_t>(l) * P_PER_LAYER];
     const int p0 = l * P_PER_LAYER, i0 = l * L_PER_LAYER;
-    {  // [q; k; v] = W bf16(rmsnorm(h)), h = h + y_down of the previous layer
-      DItem it = base_item(i0 + L_QKV, X_RMS, d.d, l1_of({W[P_Q], W[P_K], W[P_V]}), qkv);
-      it.h_prev = l == 0 ? nullptr : hb[cur];
-      it.y_add = l == 0 ? nullptr : yd;
-      it.F_add = l == 0 ? nullptr : Fs + (i0 - 1);
-      it.h_next = hb[1 - cur];
-      cur = 1 - cur;
-      it.zero[0] = ZeroSpec{gu, n_gu};
-      if (trace && l > 0) it.tcopy[0] = CopySpec{yd, Fs + (i0 - 1), tout(p0 - 1), d.d};
-      it.trace_x = tin(p0 + P_Q);
-      items.push_back(it);
+    const float l1_qkv = l1_of({W[P_Q], W[P_K], W[P_V]});
+    const ResStats rs_qkv = res;
+    DItem qkv = base_item(i0 + L_QKV, X_RMS, d.d, l1_qkv);  // [q; k; v] = W bf16(rmsnorm(h))
+    rms_input(qkv);
+    qkv.trace_x = tin(p0 + P_Q);
+    for (int s = 0; s < 3; ++s) {
+      qkv.trace_y[s] = tout(p0 + P_Q + s);
+      qkv.trace_n[s] = proj_n(d, P_Q + s);
     }
+    items.push_back(qkv);
     const std::vector<uint32_t>& so = m->item_st_off[i0 + L_QKV];
     {  // h += W_o bf16(v of each head's kv group)
-      DItem it = base_item(i0 + L_O, X_GQA, static_cast<int>(nq), l1_of({W[P_O]}), yo);
-      it.src = qkv;
-      it.F_src = Fs + i0 + L_QKV;
+      DItem it = base_item(i0 + L_O, X_GQA, static_cast<int>(nq), l1_of({W[P_O]}));
+      it.src = qkv.out;
+      it.src_flag = qkv.flag;
+      it.src_nsuper = qkv.n_super;
+      it.rs = rs_qkv;
+      it.l1_src = l1_qkv;
       it.v_off = int64_t(so[2]) * SROWS;
+      it.v_st0 = static_cast<int32_t>(so[2]);
+      it.v_st1 = static_cast<int32_t>(so[2] + n_super_of(proj_n(d, P_V)));
       it.head_dim = d.head_dim;
       it.group = d.n_heads / d.n_kv_heads;
-      it.zero[0] = ZeroSpec{yd, n_yd};
-      if (trace) {
-        it.tcopy[0] = CopySpec{qkv, Fs + i0, tout(p0 + P_Q), static_cast<int32_t>(nq)};
-        it.tcopy[1] = CopySpec{qkv + int64_t(so[1]) * SROWS, Fs + i0, tout(p0 + P_K), static_cast<int32_t>(nkv)};
-        it.tcopy[2] = CopySpec{qkv + int64_t(so[2]) * SROWS, Fs + i0, tout(p0 + P_V), static_cast<int32_t>(nkv)};
-      }
       it.trace_x = tin(p0 + P_O);
+      it.trace_y[0] = tout(p0 + P_O);
+      it.trace_n[0] = d.d;
+      residual_output(it, i0 + L_O);
       items.push_back(it);
     }
-    {  // [gate; up] = W bf16(rmsnorm(h)), h = h + y_o
-      DItem it = base_item(i0 + L_GU, X_RMS, d.d, l1_of({W[P_GATE], W[P_UP]}), gu);
-      it.h_prev = hb[cur];
-      it.y_add = yo;
-      it.F_add = Fs + i0 + L_O;
-      it.h_next = hb[1 - cur];
-      cur = 1 - cur;
-      it.zero[0] = ZeroSpec{qkv, n_qkv};
-      if (trace) it.tcopy[0] = CopySpec{yo, Fs + i0 + L_O, tout(p0 + P_O), d.d};
-      it.trace_x = tin(p0 + P_GATE);
-      items.push_back(it);
+    const ResStats rs_gu = res;
+    DItem gu = base_item(i0 + L_GU, X_RMS, d.d, l1_of({W[P_GATE], W[P_UP]}));  // [gate; up] = W bf16(rmsnorm(h))
+    rms_input(gu);
+    gu.trace_x = tin(p0 + P_GATE);
+    for (int s = 0; s < 2; ++s) {
+      gu.trace_y[s] = tout(p0 + P_GATE + s);
+      gu.trace_n[s] = d.d_ff;
     }
+    items.push_back(gu);
     const std::vector<uint32_t>& sg = m->item_st_off[i0 + L_GU];
     {  // h += W_down bf16(silu(gate) * up)
-      DItem it = base_item(i0 + L_DOWN, X_SWIGLU, d.d_ff, l1_of({W[P_DOWN]}), yd);
-      it.src = gu;
-      it.F_src = Fs + i0 + L_GU;
+      DItem it = base_item(i0 + L_DOWN, X_SWIGLU, d.d_ff, l1_of({W[P_DOWN]}));
+      it.src = gu.out;
+      it.src_flag = gu.flag;
+      it.src_nsuper = gu.n_super;
+      it.rs = rs_gu;
       it.up_off = int64_t(sg[1]) * SROWS;
-      it.maxx_src = mx + i0 + L_GU;
       it.l1_gate = W[P_GATE]->max_row_l1;
       it.l1_up = W[P_UP]->max_row_l1;
-      it.zero[0] = ZeroSpec{yo, n_yo};
-      if (trace) {
-        it.tcopy[0] = CopySpec{gu, Fs + i0 + L_GU, tout(p0 + P_GATE), d.d_ff};
-        it.tcopy[1] = CopySpec{gu + it.up_off, Fs + i0 + L_GU, tout(p0 + P_UP), d.d_ff};
-      }
       it.trace_x = tin(p0 + P_DOWN);
+      it.trace_y[0] = tout(p0 + P_DOWN);
+      it.trace_n[0] = d.d;
+      residual_output(it, i0 + L_DOWN);
       items.push_back(it);
     }
   }
-  {  // logits = W_head bf16(rmsnorm(h + y_down))
+  {  // logits = W_head bf16(rmsnorm(h)), written by the conversions into the launch's buffer
     const int ih = d.n_layers * L_PER_LAYER, ph = d.n_layers * P_PER_LAYER;
-    DItem it = base_item(ih, X_RMS, d.d, l1_of({m->mats[ph]}), lg);
-    it.h_prev = d.n_layers > 0 ? hb[cur] : nullptr;
-    it.y_add = d.n_layers > 0 ? yd : nullptr;
-    it.F_add = d.n_layers > 0 ? Fs + (ih - 1) : nullptr;
-    it.zero[0] = ZeroSpec{gu, n_gu};
-    if (trace && d.n_layers > 0) it.tcopy[0] = CopySpec{yd, Fs + (ih - 1), tout(ph - 1), d.d};
+    DItem it = base_item(ih, X_RMS, d.d, l1_of({m->mats[ph]}));
+    rms_input(it);
+    it.out = nullptr;
+    it.out_n = d.vocab;
     it.trace_x = tin(ph);
     items.push_back(it);
   }
@@ -230,23 +270,34 @@ cudaError_t upload_items(const std::vector<DItem>& items, DItem* dst) {
   return cudaMemcpy(dst, items.data(), sizeof(DItem) * items.size(), cudaMemcpyHostToDevice);
 }
 
+// Test hooks (vbq_debug_set): the cycles a flag wait may take before the
+// kernel records a timeout (default about a second), whether waits look for a
+// flag value that no launch writes, and how many words of the static scratch
+// vbq_decode_step_noalloc may use.
+std::atomic<long long> g_spin_limit{kSpinCycles};
+std::atomic<int> g_never_ready{0};
+std::atomic<int64_t> g_noalloc_words{0};
+
 cudaError_t launch_decode(const vbq_model* m, const DItem* items, uint64_t* base, const uint16_t* x, float* out,
                           cudaStream_t st, int* err) {
   const Layout& L = m->lay;
   DecodeArgs a{};
   a.items = items;
+  a.ctas = m->ctas;
+  a.warps = m->warps;
   a.n_items = m->n_items;
   a.pieces = m->pieces;
   a.pstart = m->pstart;
   a.pbytes = m->pbytes;
   a.x = x;
+  a.d = m->desc.d;
+  a.h0 = reinterpret_cast<float*>(base + L.h0);
+  a.h0_stats = reinterpret_cast<float2*>(base + L.h0_stats);
+  a.h0_flag = reinterpret_cast<uint32_t*>(base + L.h0_flag);
   a.logits = out;
-  a.logits_acc = reinterpret_cast<const unsigned long long*>(base + L.logits);
-  a.logits_acc_w = reinterpret_cast<unsigned long long*>(base + L.logits);
-  a.F_head = reinterpret_cast<const int*>(base + L.F) + (m->n_items - 1);
-  a.vocab = m->desc.vocab;
-  a.final_zero = ZeroSpec{reinterpret_cast<unsigned long long*>(base + L.dn), L.logits - L.dn};
-  a.grid_bar = reinterpret_cast<uint32_t*>(base + L.bar);
+  a.epoch = next_epoch();
+  a.wait_epoch = g_never_ready.load() ? (a.epoch | 0x80000000u) : a.epoch;
+  a.spin_limit = g_spin_limit.load();
   a.ns = kRingSlots;
   a.err = err;
   cudaLaunchConfig_t cfg{};
@@ -255,7 +306,7 @@ cudaError_t launch_decode(const vbq_model* m, const DItem* items, uint64_t* base
   cfg.dynamicSmemBytes = decode_smem_bytes();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA is resident: the grid barriers need it
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA is resident: the flag waits need it
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -339,6 +390,8 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
 
   // One plan per item, each over exactly one CTA per SM; the piece lists of all items in turn.
   std::vector<std::vector<uint64_t>> per_warp;
+  std::vector<WarpPlan> all_warps;
+  std::vector<CtaPlan> all_ctas;
   auto add_plan = [&](std::initializer_list<const vbq_matrix*> ms) -> vbq_status {
     std::vector<SegPlanInput> segs;
     for (const vbq_matrix* w : ms) {
@@ -356,20 +409,10 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
     if (!append_pieces(pl, segs, &per_warp))
       return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: weight address beyond 2^48");
     per_warp.resize(static_cast<size_t>(m->sms) * KW);
-    auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
-    const size_t bw = al(sizeof(WarpPlan) * pl.warps.size()), bc = al(sizeof(CtaPlan) * pl.ctas.size());
-    void* mem = nullptr;
-    cudaError_t e = cudaMalloc(&mem, bw + bc);
-    if (e == cudaSuccess)
-      e = cudaMemcpy(mem, pl.warps.data(), sizeof(WarpPlan) * pl.warps.size(), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess)
-      e = cudaMemcpy(static_cast<char*>(mem) + bw, pl.ctas.data(), sizeof(CtaPlan) * pl.ctas.size(),
-                     cudaMemcpyHostToDevice);
-    if (mem) m->plan_mem.push_back(mem);
-    if (e != cudaSuccess) return cuda_fail(e, "vbq_model_create: plan upload");
-    m->item_warps.push_back(static_cast<const WarpPlan*>(mem));
-    m->item_ctas.push_back(reinterpret_cast<const CtaPlan*>(static_cast<char*>(mem) + bw));
+    all_warps.insert(all_warps.end(), pl.warps.begin(), pl.warps.end());
+    all_ctas.insert(all_ctas.end(), pl.ctas.begin(), pl.ctas.end());
     m->item_st_off.push_back(pl.st_off);
+    m->item_super.push_back(pl.n_item_super);
     return VBQ_OK;
   };
   vbq_status s = VBQ_OK;
@@ -386,10 +429,10 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
     vbq_model_free(m);
     return s;
   }
-  m->n_items = static_cast<int32_t>(m->item_warps.size());
-  m->lay = layout_of(d, m->n_items);
+  m->n_items = static_cast<int32_t>(m->item_super.size());
+  m->lay = layout_of(d, m->item_super);
 
-  // Device memory: the step scratch, the host-step staging, the piece lists and both item arrays.
+  // Device memory: the step scratch, the host-step staging, then the plans, the piece lists and both item arrays.
   const PieceSet ps = finish_pieces(per_warp);
   auto al = [](int64_t b) { return (b + 255) & ~int64_t(255); };
   const int64_t b_ws = al(8 * m->lay.total), b_x = al(2 * int64_t(d.d)), b_lg = al(4 * int64_t(d.vocab));
@@ -401,13 +444,18 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   }
   m->x_stage = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(m->ws) + b_ws);
   m->logits_stage = reinterpret_cast<float*>(reinterpret_cast<char*>(m->ws) + b_ws + b_x);
-  const int64_t o_p = 0, o_s = al(8 * int64_t(std::max<size_t>(1, ps.pieces.size())));
+  const int64_t o_c = 0, o_w = al(int64_t(sizeof(CtaPlan) * all_ctas.size()));
+  const int64_t o_p = o_w + al(int64_t(sizeof(WarpPlan) * all_warps.size()));
+  const int64_t o_s = o_p + al(8 * int64_t(std::max<size_t>(1, ps.pieces.size())));
   const int64_t o_b = o_s + al(4 * int64_t(ps.start.size()));
   const int64_t o_i1 = o_b + al(4 * int64_t(std::max<size_t>(1, ps.bytes.size())));
   const int64_t o_i2 = o_i1 + al(int64_t(sizeof(DItem)) * m->n_items);
   const int64_t total = o_i2 + al(int64_t(sizeof(DItem)) * m->n_items);
   e = cudaMalloc(&m->prog_mem, total);
   char* pm = static_cast<char*>(m->prog_mem);
+  if (e == cudaSuccess) e = cudaMemcpy(pm + o_c, all_ctas.data(), sizeof(CtaPlan) * all_ctas.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(pm + o_w, all_warps.data(), sizeof(WarpPlan) * all_warps.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess && !ps.pieces.empty())
     e = cudaMemcpy(pm + o_p, ps.pieces.data(), 8 * ps.pieces.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(pm + o_s, ps.start.data(), 4 * ps.start.size(), cudaMemcpyHostToDevice);
@@ -417,6 +465,8 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
     vbq_model_free(m);
     return cuda_fail(e, "vbq_model_create: programs");
   }
+  m->ctas = reinterpret_cast<const CtaPlan*>(pm + o_c);
+  m->warps = reinterpret_cast<const WarpPlan*>(pm + o_w);
   m->pieces = reinterpret_cast<const uint64_t*>(pm + o_p);
   m->pstart = reinterpret_cast<const uint32_t*>(pm + o_s);
   m->pbytes = reinterpret_cast<const uint32_t*>(pm + o_b);
@@ -454,7 +504,6 @@ extern "C" void vbq_model_free(vbq_model* m) {
   cudaFree(m->prog_mem);
   cudaFree(m->tr_in);
   cudaFree(m->tr_out);
-  for (void* p : m->plan_mem) cudaFree(p);
   cudaSetDevice(cur);
   delete m;
 }
@@ -524,21 +573,19 @@ extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host
 
 // ---------------------------------------------------------------- allocation-free decode step
 //
-// vbq_decode_step keeps its step scratch (fixed-point sums, the residual,
-// per-item exponents and the grid-barrier counters) in memory that
+// vbq_decode_step keeps its step scratch (each item's fixed-point sums,
+// float outputs, arrival counters, flags and statistics) in memory that
 // vbq_model_create allocated for the model. Some callers cannot tie device
-// memory to a model they step: code that runs while another component is
-// capturing the stream into its own graph, real-time loops whose device memory
-// is fixed before the loop starts, or hosts that hand out device memory only
-// from their own pool. vbq_decode_step_noalloc serves them: it launches the
-// same kernel with the step's scratch in the file-scope array below, and
-// allocates nothing.
+// memory to a model they step: real-time loops whose device memory is fixed
+// before the loop starts, or hosts that hand out device memory only from their
+// own pool. vbq_decode_step_noalloc serves them: it launches the same kernel
+// with the step's scratch in the file-scope array below, and allocates nothing.
 
 namespace {
 
-// Step scratch of vbq_decode_step_noalloc, in the Layout of the model: 262,144
-// 8-byte words = 2 MiB on every device that loads this library, held until the
-// process exits.
+// Step scratch of vbq_decode_step_noalloc, in the Layout of the model:
+// 4,194,304 8-byte words = 32 MiB on every device that loads this library,
+// held until the process exits.
 static __device__ __align__(256) uint64_t g_step_scratch[kStepScratchWords];
 
 std::mutex g_step_scratch_mu;
@@ -573,11 +620,13 @@ extern "C" vbq_status vbq_decode_step_noalloc(vbq_model* m, const uint16_t* x_de
   if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 4)
     return fail(VBQ_ERR_INVALID_ARG,
                 "vbq_decode_step_noalloc: misaligned buffer (x and logits need 4-byte alignment)");
-  if (m->lay.total > kStepScratchWords)
+  const int64_t limit = g_noalloc_words.load() > 0 ? std::min(g_noalloc_words.load(), kStepScratchWords)
+                                                    : kStepScratchWords;
+  if (m->lay.total > limit)
     return fail(VBQ_ERR_SHAPE, "vbq_decode_step_noalloc: the step needs " + std::to_string(m->lay.total) +
-                                   " scratch words of 8 bytes (counters, exponents, h, and the fixed-point sums of "
-                                   "q/k/v, o, gate/up, down and the head); the static scratch holds " +
-                                   std::to_string(kStepScratchWords));
+                                   " scratch words of 8 bytes (per item: fixed-point sums, outputs, counters and "
+                                   "flags); the static scratch holds " +
+                                   std::to_string(limit));
   int dev = 0;
   VBQ_CUDA_TRY(cudaGetDevice(&dev));
   if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_noalloc: model is on another device");
@@ -586,4 +635,22 @@ extern "C" vbq_status vbq_decode_step_noalloc(vbq_model* m, const uint16_t* x_de
                                 static_cast<cudaStream_t>(stream), m->err);
   if (e != cudaSuccess) return cuda_fail(e, "vbq_decode_step_noalloc: launch");
   return VBQ_OK;
+}
+
+extern "C" vbq_status vbq_debug_set(int32_t key, int64_t value) {
+  switch (key) {
+    case VBQ_DEBUG_WAIT_LIMIT:
+      if (value < 0) return fail(VBQ_ERR_INVALID_ARG, "vbq_debug_set: negative wait limit");
+      g_spin_limit.store(value == 0 ? kSpinCycles : value);
+      return VBQ_OK;
+    case VBQ_DEBUG_NEVER_READY:
+      g_never_ready.store(value != 0);
+      return VBQ_OK;
+    case VBQ_DEBUG_NOALLOC_WORDS:
+      if (value < 0) return fail(VBQ_ERR_INVALID_ARG, "vbq_debug_set: negative word count");
+      g_noalloc_words.store(value);
+      return VBQ_OK;
+    default:
+      return fail(VBQ_ERR_INVALID_ARG, "vbq_debug_set: unknown key " + std::to_string(key));
+  }
 }

@@ -18,21 +18,15 @@ using namespace vbq;
 
 inline int bits_to_cls(uint8_t b) { return b == 1 ? 0 : b == 2 ? 1 : b == 4 ? 2 : 3; }
 
-// Packs the 64 codes q of one group of b bits into 8*b bytes (layout.h).
-inline void pack_entry(const uint8_t* q, int b, uint8_t* dst) {
-  const int nbytes = 8 * b;
-  std::memset(dst, 0, nbytes);
-  if (b == 1) {
-    for (int m = 0; m < GROUP; ++m) dst[m >> 3] |= static_cast<uint8_t>((q[m] & 1u) << (m & 7));
-    return;
-  }
-  const int per_slice = GROUP / b;     // codes in a lane slice
-  const int per_word = per_slice / 2;  // codes in a 32-bit word
-  for (int m = 0; m < GROUP; ++m) {
-    const int s = m / per_slice, within = m % per_slice;
-    const int h = within / per_word, r = within % per_word;
-    uint32_t* w = reinterpret_cast<uint32_t*>(dst + 8 * s + 4 * h);
-    *w |= static_cast<uint32_t>(q[m]) << code_bit(static_cast<uint32_t>(b), static_cast<uint32_t>(r));
+// Packs the 64 codes q of one group of class cls as entry j of a step record
+// with e entries (layout.h); the record's code bytes start zeroed.
+inline void pack_entry(const uint8_t* q, uint32_t cls, uint8_t* rec, uint32_t e, uint32_t j) {
+  const uint32_t b = 1u << cls, per_word = 32u / b;
+  for (uint32_t m = 0; m < GROUP; ++m) {
+    const uint32_t w = m / per_word, r = m % per_word;
+    uint32_t* word = reinterpret_cast<uint32_t*>(rec + code_word_off(cls, e, j, w));
+    const uint32_t bit = b == 1 ? r : code_bit(b, r);
+    *word |= static_cast<uint32_t>(q[m]) << bit;
   }
 }
 
@@ -212,9 +206,10 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
           uint8_t* rec = host.data() + o;
           uint16_t* sc = reinterpret_cast<uint16_t*>(rec + rec_scale_off(c, e));
           uint8_t* rw = rec + rec_row_off(c, e);
+          std::memset(rec, 0, rec_code_bytes(c, e));
           for (uint32_t j = 0; j < e; ++j) {
             const int64_t r = rows[c][done + j];
-            pack_entry(codes + r * K + static_cast<int64_t>(g) * GROUP, b, rec + j * 8u * b);
+            pack_entry(codes + r * K + static_cast<int64_t>(g) * GROUP, c, rec, e, j);
             sc[j] = scales_f16[r * G + g];
             rw[j] = static_cast<uint8_t>((r - r0) % TILE);
           }

@@ -213,6 +213,8 @@ bool make_item_plan(const std::vector<SegPlanInput>& segs, int32_t n_ctas, ItemP
       wa = wb;
     }
   }
+  for (CtaPlan& cp : P.ctas)
+    for (uint32_t t = 0; t < cp.n_slots; ++t) cp.expect[t] = P.arrivals[cp.st_base + t];
   return true;
 }
 

@@ -58,7 +58,7 @@ struct CtaPlan {           // 32 bytes
   uint32_t st_base;        // first item super-tile the CTA touches
   uint32_t n_slots;        // item super-tiles it touches (<= SLOTS_MAX; 0 for an idle CTA)
   uint32_t a0, a1, b0, b1;
-  uint32_t pad[2];
+  uint32_t expect[SLOTS_MAX];  // per slot: CTAs that touch that super-tile (its arrivals)
 };
 
 __host__ __device__ inline uint32_t col_slot(const CtaPlan& c, uint32_t g) {
@@ -67,8 +67,8 @@ __host__ __device__ inline uint32_t col_slot(const CtaPlan& c, uint32_t g) {
 
 // Cost model of a warp's work: per step of each class, per run and per group
 // column the warp prepares (lookup tables and fixed-point x).
-constexpr double kCostStep[4] = {45.0, 28.0, 18.0, 16.0};
-constexpr double kCostRun = 20.0;
+constexpr double kCostStep[4] = {64.0, 81.0, 78.0, 64.0};
+constexpr double kCostRun = 40.0;
 constexpr double kCostColumn = 60.0;
 
 struct SegPlanInput {

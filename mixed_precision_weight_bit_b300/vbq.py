@@ -69,6 +69,7 @@ _SIGNATURES = {
     "vbq_dense_gemv_bf16": (_ST, [_P, _P, _P, _I64, _I64, _P]),
     "vbq_device_check": (_ST, [ctypes.POINTER(_I32)]),
     "vbq_launch_count": (_I64, [_I32]),
+    "vbq_debug_set": (_ST, [_I32, _I64]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -240,6 +241,16 @@ def vbq_device_check() -> int:
 
 def vbq_launch_count(reset: bool = False) -> int:
     return int(_L().vbq_launch_count(1 if reset else 0))
+
+
+VBQ_DEBUG_WAIT_LIMIT = 1
+VBQ_DEBUG_NEVER_READY = 2
+VBQ_DEBUG_NOALLOC_WORDS = 3
+
+
+def vbq_debug_set(key: int, value: int) -> None:
+    """Test hooks of the decode step (see include/vbq.h); value 0 restores the default."""
+    _check("vbq_debug_set", _L().vbq_debug_set(int(key), int(value)))
 
 
 class Matrix:

@@ -104,15 +104,11 @@ static Logical make_matrix(int64_t N, int64_t K, const double p[4], uint32_t see
 }
 
 // Code m of entry j of a step record of class cls with e entries (layout.h).
-static uint32_t decode_code(const uint8_t* rec, uint32_t cls, uint32_t j, uint32_t m) {
-  const uint32_t b = 1u << cls;
-  const uint8_t* ent = rec + 8u * b * j;
-  if (b == 1) return (ent[m >> 3] >> (m & 7)) & 1u;
-  const uint32_t per_slice = 64 / b, per_word = per_slice / 2;
-  const uint32_t s = m / per_slice, within = m % per_slice, h = within / per_word, r = within % per_word;
+static uint32_t decode_code(const uint8_t* rec, uint32_t cls, uint32_t e, uint32_t j, uint32_t m) {
+  const uint32_t b = 1u << cls, per_word = 32u / b, r = m % per_word;
   uint32_t w;
-  std::memcpy(&w, ent + 8 * s + 4 * h, 4);
-  return (w >> code_bit(b, r)) & ((1u << b) - 1u);
+  std::memcpy(&w, rec + code_word_off(cls, e, j, m / per_word), 4);
+  return (w >> (b == 1 ? r : code_bit(b, r))) & ((1u << b) - 1u);
 }
 
 // Checks the entries of one step (entries i0 .. i0+e-1 of its run) against the
@@ -135,7 +131,7 @@ static void check_step(const Logical& L, const RunHeader& h, const uint8_t* rec,
     CHECK(L.bits[gi] == (1 << cls), "class of (%lld, %u)", (long long)r, h.g);
     CHECK(L.scales[gi] == sc, "scale of (%lld, %u)", (long long)r, h.g);
     for (uint32_t m = 0; m < 64; ++m)
-      CHECK(decode_code(rec, cls, j, m) == L.codes[r * L.K + int64_t(h.g) * 64 + m], "code %u of (%lld, %u)", m,
+      CHECK(decode_code(rec, cls, e, j, m) == L.codes[r * L.K + int64_t(h.g) * 64 + m], "code %u of (%lld, %u)", m,
             (long long)r, h.g);
     (*seen)[gi] += 1;
   }

@@ -124,10 +124,8 @@ def check_glue(b, per, x):
     total = 0
 
     def residual(h, err_h, v):
-        # The kernel adds each split of a tile's partial rows onto h with fp32
-        # atomic adds (up to 16 of them, in any order), while the trace holds the
-        # same partials summed on their own: allow one rounding of the partial
-        # sums and of h per add.
+        # The kernel adds each projection's fp32 output onto the fp32 h once:
+        # allow one rounding of the output and of h per add (generously).
         v = v.astype(np.float64)
         new = h + v
         return new, err_h + 2.0 ** -20 * (np.abs(new) + np.abs(h) + np.abs(v)) + 2.0 ** -24 * err_h
@@ -172,29 +170,22 @@ def test_tiny_decode_step_teacher_forced(V):
 
 
 def test_decode_step_repeatable_and_host_path(V):
-    """Steps on the same input agree within the parity bar: the partial rows of split tiles are added
-    with fp32 atomic adds in no fixed order, so the last bits can differ from one step to the next."""
+    """Steps on the same input give the same logits bit for bit: every sum of a step is an integer
+    add or a float reduction in a fixed order, whatever the timing of the CTAs."""
     import torch
     b = Built(V, model_tiny(), seed=1)
     x = gen_x(b.shape.d, seed=4)
-    hm = b.get(b.shape.n_layers, "head")
-    norms = O.row_norms(*hm)
-    ones = O.f64_to_bf16_bits(np.ones(b.shape.d))  # the head's input bf16(rmsnorm(h)) has 2-norm ~ sqrt(d)
-
-    def close(a, ref):
-        assert np.isfinite(a).all()
-        assert O.normalized_error(a, ref.astype(np.float64), norms, ones) <= TOL
-
     l1, _ = run_step(V, b, x)
+    assert np.isfinite(l1).all()
     l2, _ = run_step(V, b, x)          # new device buffers
-    close(l2, l1)
+    assert np.array_equal(l2, l1)
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
     lh = torch.empty(b.shape.vocab, dtype=torch.float32).pin_memory()
     V.vbq_decode_step_host(b.model.handle, xh, lh)
-    close(lh.numpy(), l1)
+    assert np.array_equal(lh.numpy(), l1)
     # trace off and on give the same logits
     l3, _ = run_step(V, b, x, trace=True)
-    close(l3, l1)
+    assert np.array_equal(l3, l1)
     b.close()
 
 

@@ -1,9 +1,8 @@
-"""The allocation-free decode step against vbq_decode_step, through the C ABI (GPU).
+"""The allocation-free decode step against vbq_decode_step and the oracle, through the C ABI (GPU).
 
-vbq_decode_step_noalloc is for callers that may not allocate device memory at
-step time (for example while another component captures the stream into a CUDA
-graph). It keeps its activations in a static device array instead of the model's
-workspace. This file is named so that pytest
+vbq_decode_step_noalloc is for callers that may not allocate device memory, or
+tie it to a model, at step time. It keeps the step's scratch in a static device
+array instead of the model's workspace. This file is named so that pytest
 collects it last: if it fails, a run that stops at the first failure has
 already run every other test.
 """
@@ -40,6 +39,7 @@ def test_noalloc_step_matches_decode_step_twice(V):
     mats, handles, model = _build(V, shape, seed=2)
     head = mats[(shape.n_layers, "head")]
     norms = O.row_norms(head.codes, head.bits, head.scales)
+    get = lambda layer, proj: (mats[(layer, proj)].codes, mats[(layer, proj)].bits, mats[(layer, proj)].scales)
     for call, seed in enumerate((31, 32)):          # two calls in a row, different inputs
         x = gen_x(shape.d, seed=seed)
         xd = dev_u16(x)
@@ -50,12 +50,13 @@ def test_noalloc_step_matches_decode_step_twice(V):
         torch.cuda.synchronize()
         r, o = ref.cpu().numpy(), out.cpu().numpy()
         assert np.isfinite(o).all(), call
-        # The parity bar of every GEMV test. The head's input is bf16(rmsnorm(h)), whose 2-norm is
-        # sqrt(d), so a vector of ones stands in for it in the denominator.
-        ones = O.f64_to_bf16_bits(np.ones(shape.d))
-        # The same kernel on the same inputs; split tiles add their partial rows with fp32 atomic adds
-        # in no fixed order, so the logits agree to the last bits only up to that order.
-        assert O.normalized_error(o, r.astype(np.float64), norms, ones) <= TOL
+        # The same kernel on the same inputs, and a step's sums do not depend on timing.
+        assert np.array_equal(o, r), call
+        # Against the oracle's fp64 chain from the same x (each bf16 rounding of a projection input
+        # may differ by one ulp between the chains, so the bar is the end-to-end drift of the
+        # decode tests, relative to the largest head row norm times sqrt(d)).
+        chain = O.decode_step(get, shape.n_layers, shape.n_heads, shape.n_kv_heads, shape.head_dim, x)
+        assert np.max(np.abs(o - chain)) / (np.max(norms) * np.sqrt(shape.d)) < 2e-2, call
     assert V.vbq_device_check() == 0
     model.close()
     for h in handles:
@@ -63,20 +64,25 @@ def test_noalloc_step_matches_decode_step_twice(V):
 
 
 def test_noalloc_step_rejects_models_over_the_scratch_limit(V):
-    import dataclasses
     import torch
-    # 64 + 64 + 3*16384 ([q;k;v]) + 2*16384 ([gate;up]) = 82,048 floats > 65,536, with every
-    # dimension within the decode kernel's limit of 16384 and every matrix small.
-    big = dataclasses.replace(model_tiny(), name="wide", n_layers=1, d=64, n_heads=128, n_kv_heads=128,
-                              head_dim=128, d_ff=16384, vocab=64)
-    mats, handles, model = _build(V, big, seed=3)
-    x = dev_u16(gen_x(big.d, seed=4))
-    out = torch.zeros(big.vocab, device="cuda")
-    with pytest.raises(V.VbqError) as e:
-        V.vbq_decode_step_noalloc(model.handle, x, out)
-    assert e.value.status == 2 and "scratch" in e.value.detail
+    # The size check: a model that needs more words than the usable part of the
+    # static array (lowered by a test hook) is refused and nothing is enqueued.
+    shape = model_tiny()
+    mats, handles, model = _build(V, shape, seed=3)
+    x = dev_u16(gen_x(shape.d, seed=4))
+    out = torch.zeros(shape.vocab, device="cuda")
+    try:
+        V.vbq_debug_set(V.VBQ_DEBUG_NOALLOC_WORDS, 1024)
+        with pytest.raises(V.VbqError) as e:
+            V.vbq_decode_step_noalloc(model.handle, x, out)
+        assert e.value.status == 2 and "scratch" in e.value.detail
+        torch.cuda.synchronize()
+        assert (out.cpu().numpy() == 0).all()           # nothing was enqueued
+    finally:
+        V.vbq_debug_set(V.VBQ_DEBUG_NOALLOC_WORDS, 0)
+    V.vbq_decode_step_noalloc(model.handle, x, out)   # the full array holds it
     torch.cuda.synchronize()
-    assert (out.cpu().numpy() == 0).all()           # nothing was enqueued
+    assert np.isfinite(out.cpu().numpy()).all()
     model.close()
     for h in handles:
         h.close()
