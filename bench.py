@@ -7,11 +7,13 @@ value    whole-job effective HBM GB/s of the decode step:
          exactly --steps steps. A barrier and a synchronize bracket the timed
          region on both sides, and the max over ranks is taken.
 extra    decode-step microseconds at the 9B and 1B shapes, the dominant kernel's
-         roofline, a dense bf16 GEMV on the same shapes, the CPU oracle timed on
-         host cores, and an end-to-end number through host buffers.
+         roofline, a dense bf16 GEMV over the same shapes (distinct weights per
+         layer), the 768x768 config-0 GEMV hot and cold, the batch sweep, the C++
+         CPU oracle timed on one host core, and an end-to-end number through
+         host buffers.
 
---impl reference times the CPU oracle (the only reference implementation)
-on a bounded sample of the same workload, with the same metric.
+--impl reference times the C++ CPU oracle (the only reference implementation,
+single-threaded) on a bounded sample of the same workload, with the same metric.
 
 Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
 torchrun, each rank runs an independent replica (the path has no data-path
@@ -23,6 +25,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import subprocess
 import sys
 import threading
 import time
@@ -273,13 +276,10 @@ def time_steps(fn, steps, warmup, stream, ws):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one decode-kernel
 # launch on the 9B-shaped step, from an ncu capture of the build whose kernel
-# sources hash to the key (the summary and command are in profiles/). Any other
-# build reports null.
+# sources hash to the key; any other build reports null.
 DECODE_TRAFFIC = {
-    # profiles/vbq_decode_kernel_9b_decode_step.md: 2,080,101,376 B read + 3,156,992 B written in one launch
-    "9393895caeb6df1e": 2083258368,
 }
-KERNEL_SOURCES = ("gemv.cuh", "ptx.cuh", "layout.h", "model.cu", "plan.cpp", "plan.h", "pack.cpp")
+KERNEL_SOURCES = ("decode.cuh", "gemv.cuh", "ptx.cuh", "layout.h", "model.cu", "plan.cpp", "plan.h", "pack.cpp")
 
 
 def kernel_source_hash() -> str:
@@ -311,7 +311,7 @@ def decode_kernel_roofline(V, pm, x, logits, stream, peak_gbs, ms_step, steps, w
     traffic = DECODE_TRAFFIC.get(key) if workload == "9b" else None
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
             "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
-            "kernel": "vbq_decode_kernel<16,2>", "launches_timed": steps,
+            "kernel": "vbq_decode_kernel", "launches_timed": steps,
             "avg_launch_us": round(ms_step * 1e3, 2),
             "bracketed_launch_us": {"min": round(min(ms) * 1e3, 2), "avg": round(sum(ms) / len(ms) * 1e3, 2)},
             "alg_bytes_per_launch": round(pm.alg_bytes), "kernel_source_hash": key,
@@ -348,40 +348,69 @@ def standalone_gemv(V, pm, stream, peak_gbs, reps=3):
     launches = len(ev)
     achieved = tot_b / (tot_ms * 1e-3) / 1e9
     return {"achieved": round(achieved, 1), "unit": "GB/s", "frac": round(achieved / peak_gbs, 4),
-            "kernel": "vbq_gemv_kernel<1,16,2>", "launches": launches,
+            "kernel": "vbq_gemv1_kernel", "launches": launches,
             "avg_launch_us": round(tot_ms * 1e3 / launches, 2),
             "alg_bytes_per_launch": round(tot_b / launches),
             "note": "each projection of the 9B stack launched alone through vbq_gemv"}
 
 
 def dense_baseline(V, shape, stream, steps=3):
-    """Dense bf16 GEMV (same codebase) over one layer's projections x n_layers + the head."""
+    """Dense bf16 GEMV (same codebase) over every projection of the stack, with distinct weights per layer
+    (n_layers x 7 matrices + the head, as the VBQ step streams them), on the launching stream."""
     import torch
     from synth import PROJS, model_matrix_shape
-    torch.manual_seed(0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
     mats = []
-    for p in PROJS:
-        n, k = model_matrix_shape(shape, p)
-        mats.append((torch.randn(n, k, device="cuda", dtype=torch.bfloat16), n, k))
+    for _ in range(shape.n_layers):
+        for p in PROJS:
+            n, k = model_matrix_shape(shape, p)
+            mats.append((torch.randn(n, k, device="cuda", dtype=torch.bfloat16, generator=g) * 0.02, n, k))
     n, k = model_matrix_shape(shape, "head")
-    head = (torch.randn(n, k, device="cuda", dtype=torch.bfloat16), n, k)
-    xs = {k: torch.randn(k, device="cuda", dtype=torch.bfloat16) for (_, _, k) in mats + [head]}
-    ys = {n: torch.empty(n, device="cuda") for (_, n, _) in mats + [head]}
+    mats.append((torch.randn(n, k, device="cuda", dtype=torch.bfloat16, generator=g) * 0.02, n, k))
+    xs = {k: torch.randn(k, device="cuda", dtype=torch.bfloat16, generator=g) for (_, _, k) in mats}
+    ys = {n: torch.empty(n, device="cuda") for (_, n, _) in mats}
 
     def step():
-        for _ in range(shape.n_layers):
-            for (W, n, k) in mats:
-                V.vbq_dense_gemv_bf16(W, xs[k], ys[n], n, k, stream)
-        W, n, k = head
-        V.vbq_dense_gemv_bf16(W, xs[k], ys[n], n, k, stream)
+        for (W, n, k) in mats:
+            V.vbq_dense_gemv_bf16(W, xs[k], ys[n], n, k, stream)
 
     with torch.cuda.stream(stream):
         ms = time_steps(step, steps, 1, stream, 1)
-    nbytes = shape.n_layers * sum(2.0 * n * k for (_, n, k) in mats) + 2.0 * head[1] * head[2]
-    del mats, head
+    nbytes = sum(2.0 * n * k + 2.0 * k + 4.0 * n for (_, n, k) in mats)
+    del mats
     torch.cuda.empty_cache()
     return {"us_per_step": round(ms * 1e3, 1), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
-            "weight_bytes": nbytes}
+            "weight_bytes": nbytes, "launches_per_step": shape.n_layers * len(PROJS) + 1,
+            "note": "bf16 W and x, fp32 accumulate; bytes = 2NK + 2K + 4N per matrix"}
+
+
+def config0_gemv(V, stream, peak_gbs):
+    """The 768x768 config-0 linear, batch 1: one vbq_gemv launch, hot (repeated, L2-resident) and cold
+    (512 MiB written between launches)."""
+    import torch
+    from synth import CONFIG0_PROBS, gen_matrix, gen_x
+    m = gen_matrix(768, 768, CONFIG0_PROBS, seed=0)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    info = mat.info()
+    x = torch.from_numpy(gen_x(768, seed=0).view(np.int16)).cuda()
+    y = torch.empty(768, device="cuda")
+    cold = time_cold(lambda: V.vbq_gemv(mat.handle, x, y, stream), stream)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            V.vbq_gemv(mat.handle, x, y, stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(100):
+            V.vbq_gemv(mat.handle, x, y, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    hot = a.elapsed_time(b) / 100 * 1e3
+    alg = algorithmic_bytes(768, 768, info["code_bytes"])
+    mat.close()
+    return {"cold_us": round(cold, 2), "hot_us": round(hot, 2), "alg_bytes": round(alg),
+            "GB/s_cold": round(alg / cold / 1e3, 1), "frac_cold": round(alg / cold / 1e3 / peak_gbs, 5),
+            "note": "one launch per call; at 211 KB the call is bound by launch and synchronization latency"}
 
 
 def time_cold(fn, stream, reps=10):
@@ -405,7 +434,7 @@ def time_cold(fn, stream, reps=10):
 
 
 def batch_sweep(V, stream):
-    """14336x4096 at the config-0 allocation, batch 1..64, cold L2 (CUDA-core path to 8, tensor cores from 16)."""
+    """14336x4096 at the config-0 allocation, batch 1..64, cold L2 (CUDA cores at 1, tensor cores from 2)."""
     import torch
     from synth import CONFIG0_PROBS, gen_matrix, gen_x
     m = gen_matrix(14336, 4096, CONFIG0_PROBS, seed=0)
@@ -443,34 +472,78 @@ def stress_8192(V, stream):
 
 # --------------------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_sample(shape, budget_s: float):
-    """The oracle's GEMV over the first layers' projections, until the time budget is spent."""
-    from oracle import vbq_oracle as O
-    from synth import gen_model_matrix, gen_x, model_matrix_list, model_matrix_shape
+def host_cpu():
+    """Logical CPUs of the host (nproc) and the CPU model (lscpu, else /proc/cpuinfo)."""
+    cores = os.cpu_count()
+    model = None
     try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
     except Exception:
-        threads = 1
-    done_bytes = 0.0
-    spent = 0.0
-    n_mats = 0
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return cores, model
+
+
+def step_weights(shape) -> int:
+    from synth import model_matrix_list, model_matrix_shape
+    return sum(int(np.prod(model_matrix_shape(shape, p))) for (_, p) in model_matrix_list(shape))
+
+
+def cpu_oracle_sample(shape, budget_s: float):
+    """The C++ oracle's GEMV (one core: fp32 dequant, fp64 sums) over the stack's projections in step
+    order, until the time budget is spent. The per-weight rate of the sample gives the seconds of a
+    whole decode step."""
+    from oracle import vbq_oracle_cpp as C
+    from synth import gen_model_matrix, gen_x, model_matrix_list
+    C.build()
+    done_bytes, spent, n_mats, weights = 0.0, 0.0, 0, 0
     for (layer, proj) in model_matrix_list(shape):
         m = gen_model_matrix(shape, layer, proj, seed=0)
         x = gen_x(m.K, seed=9)
-        code_bytes = O.storage_bytes(m.bits)["code_bytes"]
+        code_bytes = int((8 * m.bits.astype(np.int64)).sum())
         t0 = time.perf_counter()
-        O.gemv(m.codes, m.bits, m.scales, x)
+        C.gemv(m.codes, m.bits, m.scales, x)
         spent += time.perf_counter() - t0
         done_bytes += algorithmic_bytes(m.N, m.K, code_bytes)
+        weights += m.N * m.K
         n_mats += 1
         if spent >= budget_s:
             break
-    gbs = done_bytes / spent / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"oracle gemv (fp32 dequant, fp64 dot) over the first {n_mats} projections of the "
-                      f"{shape.name} stack ({done_bytes / 1e6:.0f} MB algorithmic, {spent:.1f} s)",
-            "seconds": round(spent, 2)}
+    per_step = step_weights(shape) * spent / weights
+    return {"value": round(done_bytes / spent / 1e9, 4), "unit": "GB/s", "seconds": round(spent, 2),
+            "seconds_per_step": round(per_step, 2), "weights": weights, "n_mats": n_mats,
+            "sample": f"C++ oracle gemv over the first {n_mats} projections of the {shape.name} stack "
+                      f"({weights / 1e6:.0f}M weights, {done_bytes / 1e6:.0f} MB algorithmic, {spent:.1f} s)"}
+
+
+def cpu_baseline(shape, budget_s: float):
+    """The cpu_baseline object: the oracle on one core, with the host described and the seconds of one
+    decode step at both model shapes (from each shape's sample rate)."""
+    from synth import model_1b, model_9b
+    cores_total, cpu_model = host_cpu()
+    main = cpu_oracle_sample(shape, budget_s)
+    other = model_1b() if shape.name == "vbq-9b" else model_9b()
+    side = cpu_oracle_sample(other, budget_s / 3.0)
+    per = {shape.name: main, other.name: side}
+    return {"value": main["value"], "unit": "GB/s", "cores": 1, "cores_total": cores_total,
+            "cpu_model": cpu_model, "kind": "oracle",
+            "threads": "1 core used: the C++ oracle is single-threaded (no BLAS)",
+            "sample": main["sample"],
+            "seconds_per_step_9b": per["vbq-9b"]["seconds_per_step"],
+            "seconds_per_step_1b": per["vbq-1b"]["seconds_per_step"],
+            "seconds_per_step_note": "sample seconds x (weights of one step / weights sampled)"}
 
 
 # --------------------------------------------------------------------------- main arms
@@ -493,24 +566,46 @@ def workload_text(shape):
 
 
 def run_reference(args, ws, rank):
+    """The C++ oracle arm: the first projections of the stack (about one second of oracle work) are drawn
+    once; each step times the oracle's GEMV over all of them."""
     if rank != 0:
         return
-    from synth import model_1b, model_9b
+    from oracle import vbq_oracle_cpp as C
+    from synth import gen_model_matrix, gen_x, model_1b, model_9b, model_matrix_list
     shape = model_9b() if args.workload == "9b" else model_1b()
-    vals = []
-    last = None
+    cores_total, cpu_model = host_cpu()
+    C.build()
+    per_step_s = max(0.5, min(2.0, args.cpu_seconds / max(1, args.steps + args.warmup)))
+    target = per_step_s / 3e-9  # weights, at about 3 ns per weight on one core
+    mats, weights = [], 0
+    for (layer, proj) in model_matrix_list(shape):
+        m = gen_model_matrix(shape, layer, proj, seed=0)
+        mats.append((m, gen_x(m.K, seed=9), algorithmic_bytes(m.N, m.K, int((8 * m.bits.astype(np.int64)).sum()))))
+        weights += m.N * m.K
+        if weights >= target:
+            break
+
+    def step():
+        t0 = time.perf_counter()
+        for m, x, _ in mats:
+            C.gemv(m.codes, m.bits, m.scales, x)
+        return time.perf_counter() - t0
+
     for _ in range(args.warmup):
-        cpu_oracle_sample(shape, budget_s=min(2.0, args.cpu_seconds))
-    for _ in range(args.steps):
-        last = cpu_oracle_sample(shape, budget_s=max(1.0, args.cpu_seconds / max(1, args.steps)))
-        vals.append(last["value"])
-    v = float(np.median(vals))
+        step()
+    secs = [step() for _ in range(args.steps)]
+    t = float(np.median(secs))
+    v = sum(ab for _, _, ab in mats) / t / 1e9
+    per_step = step_weights(shape) * t / weights
+    sample = (f"C++ oracle gemv over the first {len(mats)} projections of the {shape.name} stack "
+              f"({weights / 1e6:.0f}M weights), median of {args.steps} timed passes")
     line = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload_text(shape)},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
-                             "sample": last["sample"]},
+            "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": {"workload": workload_text(shape)},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "cores_total": cores_total,
+                             "cpu_model": cpu_model, "kind": "oracle", "sample": sample,
+                             "seconds_per_step": round(per_step, 2)},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -586,6 +681,7 @@ def run_vbq(args, ws, rank, local):
         extra["GB/s_1b"] = round(pm1.alg_bytes / (ms1 * 1e-3) / 1e9, 1)
         pm1.close()
         torch.cuda.empty_cache()
+    extra["config0_768x768"] = config0_gemv(V, stream, peak)
     if not args.no_sweep:
         extra["batch_sweep_14336x4096"] = batch_sweep(V, stream)
         extra["stress_8192"] = stress_8192(V, stream)
@@ -595,7 +691,7 @@ def run_vbq(args, ws, rank, local):
 
     cpu = None
     if rank == 0:
-        cpu = cpu_oracle_sample(shape, args.cpu_seconds)
+        cpu = cpu_baseline(shape, args.cpu_seconds)
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,

@@ -231,16 +231,30 @@ __global__ void __launch_bounds__(256) vbq_dequant_kernel(const uint8_t* __restr
 // ---------------------------------------------------------------- dense bf16 baseline
 
 // y = W x for a dense bf16 W [N][K]; one warp per row, x staged in shared memory.
+// Launched with programmatic dependent launch: a CTA first issues the loads of
+// its first row's weights, which do not depend on earlier kernels, then waits
+// for the preceding grid's memory before it reads x; the next launch may start
+// as soon as every CTA of this one has started.
 __global__ void __launch_bounds__(256) vbq_dense_gemv_kernel(const uint16_t* __restrict__ W,
                                                              const uint16_t* __restrict__ x, float* __restrict__ y,
                                                              int32_t N, int32_t K) {
   extern __shared__ __align__(16) uint8_t xs_raw[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(xs_raw);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  grid_dep_launch();
+  int64_t r = static_cast<int64_t>(blockIdx.x) * nw + warp;
+  uint4 pre[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int k = lane * 8 + u * 256;
+    pre[u] = (r < N && k < K) ? ldg_stream_v4(W + r * K + k) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  grid_dep_wait();
   for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8)
     *reinterpret_cast<uint4*>(xs + k) = *reinterpret_cast<const uint4*>(x + k);
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * nw + warp; r < N; r += static_cast<int64_t>(gridDim.x) * nw) {
+  bool first = true;
+  for (; r < N; r += static_cast<int64_t>(gridDim.x) * nw) {
     const uint16_t* wr = W + r * K;
     float acc0 = 0.f, acc1 = 0.f;
     int k = lane * 8;
@@ -248,7 +262,8 @@ __global__ void __launch_bounds__(256) vbq_dense_gemv_kernel(const uint16_t* __r
     for (; k + 3 * 256 < K; k += 4 * 256) {
       uint4 wv[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) wv[u] = ldg_stream_v4(wr + k + u * 256);
+      for (int u = 0; u < 4; ++u) wv[u] = first ? pre[u] : ldg_stream_v4(wr + k + u * 256);
+      first = false;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xs + k + u * 256);
@@ -261,6 +276,7 @@ __global__ void __launch_bounds__(256) vbq_dense_gemv_kernel(const uint16_t* __r
         }
       }
     }
+    first = false;
     for (; k < K; k += 256) {
       const uint4 wv = ldg_stream_v4(wr + k);
       const uint4 xv = *reinterpret_cast<const uint4*>(xs + k);
@@ -406,8 +422,17 @@ extern "C" vbq_status vbq_dense_gemv_bf16(const uint16_t* W_dev, const uint16_t*
   const int64_t cap = static_cast<int64_t>(gpu_info().sms) * 16;
   if (grid > cap) grid = cap;
   note_launches(1);
-  vbq_dense_gemv_kernel<<<static_cast<unsigned>(grid), 256, smem, st>>>(W_dev, x_dev, y_dev, static_cast<int32_t>(N),
-                                                                        static_cast<int32_t>(K));
-  VBQ_CUDA_TRY(cudaGetLastError());
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  VBQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, vbq_dense_gemv_kernel, W_dev, x_dev, y_dev, static_cast<int32_t>(N),
+                                  static_cast<int32_t>(K)));
   return VBQ_OK;
 }

@@ -149,3 +149,37 @@ def check_storage(storage_bytes, seed: int = 5) -> None:
     assert st["code_bytes"] == want
     assert st["weights"] == bits.size * 64
     assert abs(st["mean_bits"] - want * 8 / (bits.size * 64)) < 1e-15
+
+
+def check_row_norms_bruteforce(row_norms, seed: int = 0) -> None:
+    """||W_r||_2^2 against the exact rational sum of squares of the grid values."""
+    codes, bits, scales, _ = tiny_case(seed)
+    got = row_norms(codes, bits, scales)
+    n, k = codes.shape
+    for r in range(n):
+        ss = sum((exact_weight(int(codes[r, c]), int(bits[r, c // GROUP]), int(scales[r, c // GROUP])) ** 2
+                  for c in range(k)), Fraction(0))
+        assert abs(float(got[r]) ** 2 - float(ss)) <= 1e-13 * float(ss) + 1e-300, (r, float(got[r]), float(ss))
+
+
+def row_norms_hand_case():
+    """Three 64-wide rows whose norms are known by hand.
+
+    row 0: b = 2, s = 1, sixteen each of q = 0, 1, 2, 3: w = -1.5, -0.5, 0.5, 1.5,
+           sum w^2 = 16 * (2.25 + 0.25 + 0.25 + 2.25) = 80.
+    row 1: b = 1, s = 2: every w = +-1, sum w^2 = 64.
+    row 2: b = 8, s = 0: every w = 0.
+    """
+    codes = np.zeros((3, GROUP), np.uint8)
+    codes[0] = np.tile(np.arange(4, dtype=np.uint8), 16)
+    codes[1] = np.arange(GROUP, dtype=np.uint8) % 2
+    codes[2] = np.arange(GROUP, dtype=np.uint8)
+    bits = np.array([[2], [1], [8]], np.uint8)
+    scales = np.array([[0x3C00], [0x4000], [0x0000]], np.uint16)   # fp16 1.0, 2.0, 0.0
+    return codes, bits, scales, np.array([np.sqrt(80.0), 8.0, 0.0])
+
+
+def check_row_norms_hand(row_norms) -> None:
+    codes, bits, scales, want = row_norms_hand_case()
+    got = row_norms(codes, bits, scales)
+    np.testing.assert_allclose(got, want, rtol=1e-15, atol=0.0)

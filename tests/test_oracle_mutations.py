@@ -94,3 +94,37 @@ def test_mutant_is_caught(name):
 
 def test_real_oracle_passes_all():
     assert _caught(O.dequant, O.gemv) == 0
+
+
+# ---- row norms: the denominator of every parity bar ----
+
+def _norms_from(kind):
+    def rn(codes, bits, scales):
+        W = O.dequant(codes, bits, scales).astype(np.float64)
+        if kind == "squared_norm":
+            return (W * W).sum(axis=1)
+        if kind == "l1_norm":
+            return np.abs(W).sum(axis=1)
+        if kind == "mean_square_root":
+            return np.sqrt((W * W).mean(axis=1))
+        raise ValueError(kind)
+    return rn
+
+
+def _norms_caught(rn):
+    failures = 0
+    for c in (lambda: P.check_row_norms_bruteforce(rn), lambda: P.check_row_norms_hand(rn)):
+        try:
+            c()
+        except AssertionError:
+            failures += 1
+    return failures
+
+
+@pytest.mark.parametrize("kind", ["squared_norm", "l1_norm", "mean_square_root"])
+def test_row_norm_mutant_is_caught(kind):
+    assert _norms_caught(_norms_from(kind)) >= 1, kind
+
+
+def test_real_row_norms_pass():
+    assert _norms_caught(O.row_norms) == 0

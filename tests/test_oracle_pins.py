@@ -44,6 +44,44 @@ def test_storage_invariants():
     P.check_storage(O.storage_bytes)
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_row_norms_bruteforce_exact(seed):
+    P.check_row_norms_bruteforce(O.row_norms, seed)
+
+
+def test_row_norms_hand_matrix():
+    P.check_row_norms_hand(O.row_norms)
+
+
+def test_row_chunks_cover_rows_in_order():
+    # rows per chunk = budget // (8 K), at least 1; the chunks tile [0, n) in order
+    for n, k, budget in [(10, 64, 8 * 64 * 3), (7, 128, 1), (5, 64, 1 << 30), (0, 64, 100)]:
+        chunks = list(O._row_chunks(n, k, budget))
+        rows = max(1, budget // (8 * k))
+        assert [r0 for r0, _ in chunks] == list(range(0, n, rows))
+        assert all(r1 - r0 == min(rows, n - r0) for r0, r1 in chunks)
+
+
+def test_gemm_and_row_norms_over_several_chunks(monkeypatch):
+    # The same rows through at least three chunks give the same values: rows are independent.
+    m = gen_matrix(37, 256, CONFIG0_PROBS, seed=8)
+    X = gen_x(256, seed=8, batch=2)
+    Y1, n1 = O.gemm(m.codes, m.bits, m.scales, X), O.row_norms(m.codes, m.bits, m.scales)
+    real = O._row_chunks
+    seen = []
+
+    def small(n, k, budget_bytes=0):
+        out = list(real(n, k, 8 * k * 10))   # 10 rows per chunk
+        seen.append(len(out))
+        return iter(out)
+
+    monkeypatch.setattr(O, "_row_chunks", small)
+    Y2, n2 = O.gemm(m.codes, m.bits, m.scales, X), O.row_norms(m.codes, m.bits, m.scales)
+    assert min(seen) >= 3
+    np.testing.assert_allclose(Y2, Y1, rtol=1e-15, atol=0.0)
+    assert np.array_equal(n2, n1)
+
+
 def test_gemm_columns_are_gemvs():
     m = gen_matrix(40, 256, CONFIG0_PROBS, seed=7)
     X = gen_x(256, seed=7, batch=3)
