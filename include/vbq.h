@@ -273,12 +273,16 @@ VBQ_API vbq_status vbq_decode_step_noalloc(vbq_model* model, const uint16_t* x_d
  *                           completes with wrong logits and check code 3.
  *  VBQ_DEBUG_NOALLOC_WORDS  words of vbq_decode_step_noalloc's static array
  *                           that it may use (to test its size check).
+ *  VBQ_DEBUG_ALLOC_CAP      bytes: a device allocation of this library above
+ *                           the cap fails as if the device were out of memory
+ *                           (VBQ_ERR_OOM), without reaching the driver.
  * Errors: VBQ_ERR_INVALID_ARG (unknown key, negative value).
  */
 enum {
   VBQ_DEBUG_WAIT_LIMIT = 1,
   VBQ_DEBUG_NEVER_READY = 2,
-  VBQ_DEBUG_NOALLOC_WORDS = 3
+  VBQ_DEBUG_NOALLOC_WORDS = 3,
+  VBQ_DEBUG_ALLOC_CAP = 4
 };
 VBQ_API vbq_status vbq_debug_set(int32_t key, int64_t value);
 

@@ -665,7 +665,7 @@ bool tc_state(const vbq_matrix* m, TcState** out, vbq_status* err) {
   const size_t o_bt = o_sx + al(4 * TC_NMAX);
   const size_t o_part = o_bt + al(static_cast<size_t>(m->G) * TC_BTILE);
   const size_t total = o_part + size_t(H.n_blocks) * TC_NMAX * 256 * 4;
-  cudaError_t e = cudaMalloc(&s.mem, total);
+  cudaError_t e = dev_alloc(&s.mem, total);
   char* b = static_cast<char*>(s.mem);
   if (e == cudaSuccess) e = cudaMemcpy(b + o_c, H.ctas.data(), sizeof(TcCta) * H.ctas.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)

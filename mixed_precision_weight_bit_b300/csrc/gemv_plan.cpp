@@ -48,7 +48,7 @@ vbq_status build_gemv_plan(vbq_matrix* m, cudaStream_t st) {
   std::memcpy(host.data() + o_ps, ps.start.data(), 4 * ps.start.size());
   if (!ps.bytes.empty()) std::memcpy(host.data() + o_pb, ps.bytes.data(), 4 * ps.bytes.size());
   void* base = nullptr;
-  cudaError_t e = cudaMalloc(&base, total);
+  cudaError_t e = dev_alloc(reinterpret_cast<void**>(&base), total);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "vbq_pack: plan allocation");

@@ -64,7 +64,13 @@ struct GpuInfo {
 };
 const GpuInfo& gpu_info();
 
-// Tensor-core dequant-MMA for 2..256 batch columns (gemm_tc.cu).
+// Device allocation of the library's buffers. Under the test hook
+// VBQ_DEBUG_ALLOC_CAP a request above the cap fails with
+// cudaErrorMemoryAllocation without reaching the driver.
+cudaError_t dev_alloc(void** p, size_t bytes);
+void set_alloc_cap(int64_t bytes);
+
+// Tensor-core dequant-MMA for 2..64 batch columns (gemm_tc.cu).
 bool tc_eligible(const vbq_matrix* m);
 vbq_status launch_gemm_tc(const vbq_matrix* m, const uint16_t* X, int32_t B, float* Y, cudaStream_t st);
 void tc_forget(const vbq_matrix* m);

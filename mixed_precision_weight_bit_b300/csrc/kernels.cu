@@ -24,6 +24,19 @@ vbq_status fail(vbq_status s, const std::string& detail) {
   return s;
 }
 
+static std::atomic<int64_t> g_alloc_cap{0};
+
+void set_alloc_cap(int64_t bytes) { g_alloc_cap.store(bytes); }
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  const int64_t cap = g_alloc_cap.load();
+  if (cap > 0 && bytes > static_cast<size_t>(cap)) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
+}
+
 vbq_status cuda_fail(cudaError_t e, const char* what) {
   g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
   if (e == cudaErrorMemoryAllocation) return VBQ_ERR_OOM;

@@ -436,7 +436,7 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   const PieceSet ps = finish_pieces(per_warp);
   auto al = [](int64_t b) { return (b + 255) & ~int64_t(255); };
   const int64_t b_ws = al(8 * m->lay.total), b_x = al(2 * int64_t(d.d)), b_lg = al(4 * int64_t(d.vocab));
-  cudaError_t e = cudaMalloc(&m->ws, b_ws + b_x + b_lg);
+  cudaError_t e = dev_alloc(reinterpret_cast<void**>(&m->ws), b_ws + b_x + b_lg);
   if (e == cudaSuccess) e = cudaMemset(m->ws, 0, b_ws);
   if (e != cudaSuccess) {
     vbq_model_free(m);
@@ -451,7 +451,7 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
   const int64_t o_i1 = o_b + al(4 * int64_t(std::max<size_t>(1, ps.bytes.size())));
   const int64_t o_i2 = o_i1 + al(int64_t(sizeof(DItem)) * m->n_items);
   const int64_t total = o_i2 + al(int64_t(sizeof(DItem)) * m->n_items);
-  e = cudaMalloc(&m->prog_mem, total);
+  e = dev_alloc(&m->prog_mem, total);
   char* pm = static_cast<char*>(m->prog_mem);
   if (e == cudaSuccess) e = cudaMemcpy(pm + o_c, all_ctas.data(), sizeof(CtaPlan) * all_ctas.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
@@ -645,6 +645,10 @@ extern "C" vbq_status vbq_debug_set(int32_t key, int64_t value) {
       return VBQ_OK;
     case VBQ_DEBUG_NEVER_READY:
       g_never_ready.store(value != 0);
+      return VBQ_OK;
+    case VBQ_DEBUG_ALLOC_CAP:
+      if (value < 0) return fail(VBQ_ERR_INVALID_ARG, "vbq_debug_set: negative byte count");
+      set_alloc_cap(value);
       return VBQ_OK;
     case VBQ_DEBUG_NOALLOC_WORDS:
       if (value < 0) return fail(VBQ_ERR_INVALID_ARG, "vbq_debug_set: negative word count");

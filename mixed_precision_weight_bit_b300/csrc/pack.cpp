@@ -251,7 +251,7 @@ extern "C" vbq_status vbq_pack(const uint8_t* codes, const uint8_t* bits, const 
   }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMalloc(&m->dev_base, total);
+  cudaError_t e = dev_alloc(reinterpret_cast<void**>(&m->dev_base), total);
   if (e != cudaSuccess) {
     delete m;
     cudaGetLastError();

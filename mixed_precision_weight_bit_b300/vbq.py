@@ -246,6 +246,7 @@ def vbq_launch_count(reset: bool = False) -> int:
 VBQ_DEBUG_WAIT_LIMIT = 1
 VBQ_DEBUG_NEVER_READY = 2
 VBQ_DEBUG_NOALLOC_WORDS = 3
+VBQ_DEBUG_ALLOC_CAP = 4
 
 
 def vbq_debug_set(key: int, value: int) -> None:

@@ -48,6 +48,7 @@ vbq_status fail(vbq_status s, const std::string& d) { g_err = d; return s; }
 vbq_status cuda_fail(cudaError_t, const char* w) { g_err = w; return VBQ_ERR_CUDA; }
 void note_launches(int64_t) {}
 void tc_forget(const vbq_matrix*) {}
+cudaError_t dev_alloc(void** p, size_t n) { return cudaMalloc(p, n); }
 static int g_sms = 148;
 const GpuInfo& gpu_info() {
   static GpuInfo gi;

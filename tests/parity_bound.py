@@ -1,0 +1,156 @@
+"""Per-element error bounds of the library's GEMV arithmetic, and an emulation of it.
+
+The parity bar of every GEMV test is a normalized error of 2e-3. Beside it the
+tests check each output element against a bound derived from the arithmetic
+the kernels do, which is far tighter where that arithmetic is exact:
+
+CUDA-core path (vbq_gemv, and every projection of vbq_decode_step):
+  * a row's partial sums are integers in units of 2^-F, F = 30 - (e(L1) + e(max|x|)),
+    e(v) the exponent with v < 2^e, L1 the largest row sum of |w| rounded up to
+    fp32; each (row, group) entry adds round(v) for its real contribution v,
+    an error of at most half a unit;
+  * 1-bit groups: v = s * sum of 13 table values, each a 5-term fp32 sum of
+    +-x * 2^F / 2: fp32 rounding of at most 24 * 2^-24 * |s| * sum|x| / 2;
+  * 2-, 4- and 8-bit groups: x is rounded to X = rint(x * 2^s_g), s_g = 14 -
+    e(max over the group of |x|), so the dot product is exact in integers but
+    off by |s| * sum|q - c| * 2^-(s_g + 1); three fp32 roundings follow;
+  * the 64-bit sum is rounded once to fp32.
+In the decode step each CTA's F is at least the F of the whole input, and its
+64-bit sums carry 32 more bits, so the same bound holds with a small slack.
+
+Tensor-core path (vbq_gemm_smallbatch, B >= 2): each weight and each scaled x
+is rounded once to fp16 (relative 2^-11) and the products are summed in fp32.
+
+emulate_gemv follows the CUDA-core arithmetic in numpy (fp32 where the kernel
+uses fp32). It is test infrastructure: tests check the emulation against the
+oracle within the bound, which pins the bound on the CPU.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import vbq_oracle as O
+
+GROUP = 64
+U = 2.0 ** -24
+
+
+def exp_above(v: np.ndarray) -> np.ndarray:
+    """e with |v| < 2^e (frexp's exponent); 0 where v == 0."""
+    _, e = np.frexp(np.asarray(v, dtype=np.float64))
+    return e.astype(np.int64)
+
+
+def max_row_l1(codes, bits, scales) -> float:
+    """The packer's L1 bound: max over rows of sum |w|, rounded up to the next fp32."""
+    W = np.abs(O.dequant(codes, bits, scales).astype(np.float64))
+    l1 = float(W.sum(axis=1).max()) if W.size else 0.0
+    return float(np.nextafter(np.float32(l1), np.float32(3e38)))
+
+
+def fixed_exponent(l1: float, maxx: float) -> int:
+    if not (maxx > 0.0) or not (l1 > 0.0):
+        return 0
+    return int(30 - (exp_above(np.float32(l1)) + exp_above(np.float32(maxx))))
+
+
+def group_shift(x: np.ndarray) -> np.ndarray:
+    """s_g per group of 64: 14 - e(max|x_g|), 0 for an all-zero group."""
+    m = np.abs(x).reshape(-1, GROUP).max(axis=1)
+    return np.where(m > 0.0, 14 - exp_above(m), 0)
+
+
+def cuda_core_bound(codes, bits, scales, x_bits, F: int, slack_units: float = 0.0) -> np.ndarray:
+    """Bound on |y - y_exact| per row for the CUDA-core arithmetic with unit 2^-F."""
+    n, k = codes.shape
+    g = k // GROUP
+    x = O.bf16_bits_to_f64(x_bits)
+    ax = np.abs(x).reshape(g, GROUP)
+    s = np.abs(O.f16_bits_to_f64(scales))                       # [n, g]
+    cq = np.abs(O.dequant(codes, bits, np.full_like(scales, 0x3C00)).astype(np.float64)).reshape(n, g, GROUP)
+    unit = 2.0 ** -F
+    sumx = ax.sum(axis=1)                                       # [g]
+    sg = group_shift(x)                                         # [g]
+    one = (bits == 1)
+    b1 = 24.0 * U * s * 0.5 * sumx[None, :]
+    qx = (cq * ax[None]).sum(axis=2)                            # sum |q - c| |x| per entry
+    q1 = cq.sum(axis=2)                                         # sum |q - c| per entry
+    bdp = s * q1 * np.ldexp(0.5, -sg)[None, :] + 4.0 * U * s * (qx + q1 * np.ldexp(0.5, -sg)[None, :])
+    per_entry = np.where(one, b1, bdp) + (0.5 + slack_units) * unit
+    total = per_entry.sum(axis=1)
+    W = O.dequant(codes, bits, scales).astype(np.float64)
+    mag = np.abs(W) @ np.abs(x)
+    return total + 2.0 * U * (mag + total)
+
+
+def gemv_bound(codes, bits, scales, x_bits) -> np.ndarray:
+    """The bound for vbq_gemv (F from the matrix's L1 bound and max|x|)."""
+    x = O.bf16_bits_to_f64(x_bits)
+    F = fixed_exponent(max_row_l1(codes, bits, scales), float(np.abs(x).max()) if x.size else 0.0)
+    return cuda_core_bound(codes, bits, scales, x_bits, F)
+
+
+def tc_bound(codes, bits, scales, X_bits) -> np.ndarray:
+    """Bound [B, N] for the tensor-core path: fp16 rounding of w and of x * 2^p, fp32 sums."""
+    X = O.bf16_bits_to_f64(X_bits)
+    W = np.abs(O.dequant(codes, bits, scales).astype(np.float64))
+    k = codes.shape[1]
+    mag = np.abs(X) @ W.T                                       # [B, N]
+    rel = 2.0 * 2.0 ** -11 + 2.0 ** -22 + (k / 16.0 + 4.0) * 2.0 ** -23
+    # fp16 subnormals: absolute error 2^-25 for a weight, 2^-25 / 2^p for an x (max|x| 2^p in [2^13, 2^14))
+    mx = np.abs(X).max(axis=1)
+    p = np.where(mx > 0.0, 14 - exp_above(mx), 0)
+    sub = 2.0 ** -25 * (np.abs(X).sum(axis=1)[:, None] + W.sum(axis=1)[None, :] * np.ldexp(1.0, -p)[:, None])
+    return rel * mag + 2.0 * sub + 1e-300
+
+
+def check_within(y, y_ref, bound) -> float:
+    """Largest |y - y_ref| / bound; asserts it is at most 1."""
+    d = np.abs(np.asarray(y, np.float64) - np.asarray(y_ref, np.float64))
+    r = d / np.maximum(bound, 1e-300)
+    worst = float(r.max()) if r.size else 0.0
+    assert worst <= 1.0, (worst, np.unravel_index(int(np.argmax(r)), r.shape))
+    return worst
+
+
+# ---- emulation of the CUDA-core arithmetic ----
+
+def _f32(v):
+    return np.float32(v)
+
+
+def emulate_gemv(codes, bits, scales, x_bits) -> np.ndarray:
+    """The CUDA-core GEMV's arithmetic, entry by entry, in numpy (fp32 where the kernel is fp32)."""
+    n, k = codes.shape
+    g = k // GROUP
+    x = O.bf16_bits_to_f64(x_bits).astype(np.float32)
+    F = fixed_exponent(max_row_l1(codes, bits, scales), float(np.abs(x).max()) if x.size else 0.0)
+    xp = (x.astype(np.float64) * 2.0 ** F).astype(np.float32)   # exact while in range
+    sg = group_shift(x.astype(np.float64))
+    s16 = O.f16_bits_to_f64(scales).astype(np.float32)
+    acc = np.zeros(n, dtype=np.int64)
+    for j in range(g):
+        xs = xp[j * GROUP:(j + 1) * GROUP]
+        xe = np.concatenate([xs, np.zeros(6, np.float32)])
+        X = np.rint(x[j * GROUP:(j + 1) * GROUP].astype(np.float64) * 2.0 ** int(sg[j])).astype(np.int64)
+        u = np.float32(2.0 ** (F - int(sg[j]) - 1))
+        for r in range(n):
+            b = int(bits[r, j])
+            q = codes[r, j * GROUP:(j + 1) * GROUP].astype(np.int64)
+            if b == 1:
+                a = [np.float32(0.0)] * 4
+                for kk in range(13):
+                    t = np.float32(0.0)
+                    for i in range(5):
+                        m = 5 * kk + i
+                        qm = int(q[m]) if m < GROUP else 0
+                        t = _f32(t + _f32((0.5 if qm else -0.5) * xe[m]))
+                    a[kk & 3] = _f32(a[kk & 3] + t)
+                v = _f32(s16[r, j] * _f32(_f32(a[0] + a[1]) + _f32(a[2] + a[3])))
+            else:
+                t2 = 2 * int((q * X).sum()) - ((1 << b) - 1) * int(X.sum())
+                v = _f32(s16[r, j] * _f32(_f32(t2) * u))
+            acc[r] += int(np.rint(np.float64(v)))
+    return np.array([np.float32(np.float32(a) * np.float32(2.0 ** -F)) if abs(F) < 100 else
+                     np.float32(np.ldexp(np.float64(np.float32(a)), -F)) for a in acc], dtype=np.float32)

@@ -5,6 +5,7 @@ import pytest
 
 from oracle import vbq_oracle as O
 from synth import PROJS, gen_model_matrix, gen_x, model_1b, model_9b, model_matrix_list, model_matrix_shape, model_tiny
+from tests import parity_bound as PB
 from tests.gpu_util import TOL, bf16_ulp_diff, dev_u16, lib
 
 pytestmark = pytest.mark.gpu
@@ -75,6 +76,30 @@ def check_projections(b, per, rows_per_proj=None, seed=0):
         err = O.normalized_error(yout, ref, O.row_norms(codes, bits, scales), xin)
         assert err <= TOL, (key, err)
         worst = max(worst, err)
+    return worst
+
+
+ITEMS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
+def check_bounds(b, per, layers, head=True):
+    """Every output row of the given layers' projections (and the head) within the per-element bound of
+    the CUDA-core arithmetic, for the GPU's own traced input. Each CTA's fixed-point unit is at most the
+    one from the whole input's max |x| and the item's L1 bound, and its 64-bit sums carry 32 more bits."""
+    groups = [(layer, g) for layer in layers for g in ITEMS]
+    if head:
+        groups.append((b.shape.n_layers, ("head",)))
+    worst = 0.0
+    for layer, group in groups:
+        mats = {p: b.get(layer, p) for p in group}
+        l1 = max(PB.max_row_l1(*mats[p]) for p in group)
+        x = per[(layer, group[0])][0]
+        F = PB.fixed_exponent(l1, float(np.abs(O.bf16_bits_to_f64(x)).max()))
+        for p in group:
+            y = per[(layer, p)][1]
+            ref = O.gemv(*mats[p], x)
+            bound = PB.cuda_core_bound(*mats[p], x, F, slack_units=2.0 ** -8)
+            worst = max(worst, PB.check_within(y, ref, bound))
     return worst
 
 
@@ -160,6 +185,7 @@ def test_tiny_decode_step_teacher_forced(V):
     assert np.isfinite(logits).all()
     assert np.array_equal(per[(b.shape.n_layers, "head")][1], logits)
     check_projections(b, per)
+    check_bounds(b, per, range(b.shape.n_layers))
     check_glue(b, per, x)
     # end to end (information): the fp64 chain from the same x
     ref = O.decode_step(b.get, b.shape.n_layers, b.shape.n_heads, b.shape.n_kv_heads, b.shape.head_dim, x)
@@ -210,6 +236,7 @@ def test_1b_decode_step_sampled(V):
     logits, per = run_step(V, b, x, trace=True)
     assert np.isfinite(logits).all()
     check_projections(b, per, rows_per_proj=24)
+    check_bounds(b, per, [0, b.shape.n_layers - 1])
     check_glue(b, per, x)
     b.close()
     assert V.vbq_device_check() == 0
@@ -223,6 +250,17 @@ def test_9b_decode_step_sampled(V):
     logits, per = run_step(V, b, x, trace=True)
     assert np.isfinite(logits).all()
     check_projections(b, per, rows_per_proj=6)
+    check_bounds(b, per, [0])        # a full layer (every row of its seven projections) and the head
     check_glue(b, per, x)
     b.close()
     assert V.vbq_device_check() == 0
+
+
+def test_decode_step_zero_input(V):
+    """x = 0: every RMSNorm input is 0, so every projection input and output and the logits are 0."""
+    b = Built(V, model_tiny(), seed=2)
+    logits, per = run_step(V, b, np.zeros(b.shape.d, np.uint16), trace=True)
+    assert np.array_equal(logits, np.zeros_like(logits))
+    for key, (xin, yout) in per.items():
+        assert not xin.any() and not yout.any(), key
+    b.close()
