@@ -68,8 +68,8 @@ typedef struct {
   int64_t meta_bytes;    /* scales, row indices, step descriptors and offsets, tile table */
   int64_t total_bytes;   /* device bytes of the packed matrix */
   double mean_bits;      /* 8*code_bytes/(N*K): mean code bits per weight */
-  int32_t n_tiles;       /* row tiles of the layout */
-  int32_t n_steps;       /* 256-byte code steps of the layout */
+  int32_t n_tiles;       /* 256-row tiles of the layout */
+  int32_t n_steps;       /* 32-entry steps of the layout (layout.h) */
   int64_t groups_by_bits[4]; /* groups at 1, 2, 4 and 8 bits */
 } vbq_info;
 
@@ -120,42 +120,66 @@ VBQ_API vbq_status vbq_matrix_info(const vbq_matrix* m, vbq_info* info);
 
 /*
  * vbq_dequant: packed -> fp32 W (for checking). W[r][k] = s * (q - c_b),
- * computed exactly in fp32.
+ * computed exactly in fp32 (an fp16 scale has 11 significant bits and q - c_b
+ * at most 9), so it equals the oracle bit for bit.
+ * Source: the VBQ abstract (per-group bit-widths from {1,2,4,8}, stored as
+ * packed low-bit codes); the grid w = s * (q - c_b) is this library's, as
+ * stated at the top of this file.
+ *  m      from vbq_pack, on the current device
  *  W_dev  device, float [N][K] row-major, caller-owned; every element is written.
+ * One CTA per 1024-row super-tile; enqueued on stream.
+ * Errors: VBQ_ERR_INVALID_ARG (NULL, misaligned or other-device arguments), VBQ_ERR_CUDA.
  */
 VBQ_API vbq_status vbq_dequant(const vbq_matrix* m, float* W_dev, void* stream);
 
 /*
- * vbq_gemv: y = W x for one bf16 activation vector, fp32 accumulation.
+ * vbq_gemv: y = W x for one bf16 activation vector.
  * Source: the VBQ abstract (dequantization fused with the multiply, for
  * batch-1 autoregressive decode).
- *  x_dev  device, bf16 [K] (uint16 bit patterns)
- *  y_dev  device, float [N]; every element is written (zeros when K == 0)
+ *  x_dev  device, bf16 [K] (uint16 bit patterns), 4-byte aligned
+ *  y_dev  device, float [N], 4-byte aligned; every element is written (zeros when K == 0)
+ * Arithmetic: each (row, group) contribution is rounded to an integer in units
+ * of 2^-F, F = 30 - (e(L1) + e(max|x|)) (e(v): v < 2^e; L1 the largest row sum
+ * of |w|), and summed in 32- then 64-bit integers: results do not depend on
+ * timing, and the error per element is within the bound of the parity tests
+ * (far below the normalized 2e-3 bar). One launch. K <= 16384 (larger K takes
+ * the tensor-core path when the matrix is eligible, else VBQ_ERR_UNSUPPORTED).
+ * Errors: VBQ_ERR_INVALID_ARG, VBQ_ERR_UNSUPPORTED, VBQ_ERR_CUDA.
  */
 VBQ_API vbq_status vbq_gemv(const vbq_matrix* m, const uint16_t* x_dev, float* y_dev, void* stream);
 
 /*
- * vbq_gemm_smallbatch: Y[j] = W X[j] for a batch of 1..64 bf16 vectors, fp32 accumulation.
- *  X_dev  device, bf16 [B][K] row-major
- *  B      1 <= B <= 64
- *  Y_dev  device, float [B][N] row-major; every element is written
- * Batches up to 8 use the CUDA-core decode (each code is decoded once and
- * reused across the batch). Larger batches use the tensor-core dequant-MMA
- * path when this build has it.
+ * vbq_gemm_smallbatch: Y[j] = W X[j] for a batch of 1..64 bf16 vectors.
+ * Source: the VBQ abstract (fused dequantize-and-multiply); with several
+ * activation columns the product is a dense contraction, which this library
+ * runs on the tensor cores.
+ *  X_dev  device, bf16 [B][K] row-major, 4-byte aligned
+ *  B      1 <= B <= 64 (else VBQ_ERR_INVALID_ARG, nothing written)
+ *  Y_dev  device, float [B][N] row-major, 4-byte aligned; every element is written
+ * B <= 3: one vbq_gemv launch per column. B >= 4: three launches (per-column
+ * powers of two that keep x inside fp16's range, the fp16 activation tiles,
+ * and one tcgen05 dequant-MMA launch for all columns), with weights rounded
+ * once to fp16 and fp32 accumulation. Matrices whose scales exceed 512 (their
+ * fp16 weights would overflow) take the per-column path at every B.
+ * Errors: VBQ_ERR_INVALID_ARG, VBQ_ERR_OOM (first tensor-core call: its plan), VBQ_ERR_CUDA.
  */
 VBQ_API vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X_dev, int32_t B, float* Y_dev,
                                void* stream);
 
 /*
  * vbq_model_create: bind the packed projections of a decoder stack for vbq_decode_step.
+ * Source: the VBQ abstract (token-by-token decode through VBQ projections);
+ * the stack's shape and glue are this library's reading (see vbq_decode_step).
  *  desc  host; the shapes. Each matrix must match its projection's (N, K).
  *  mats  host array of n_layers*7 + 1 handles: per layer q, k, v, o, gate, up,
  *        down (in that order), then the LM head. The handles must stay alive
  *        while the model exists. The model does not own them.
- *  out   receives the model. It owns a device workspace for the activations
- *        and one work plan per GEMV of the step, built here once.
- * Limits: d, d_ff and n_heads*head_dim at most 16384 (the decode kernel keeps
- * each projection's input in shared memory); VBQ_ERR_UNSUPPORTED otherwise.
+ *  out   receives the model. It owns a device workspace (per projection group:
+ *        64-bit sums, float outputs, arrival counters, flags) and the work
+ *        plans of every GEMV of the step, built here once.
+ * Limits: d and n_heads*head_dim at most 8192, d_ff at most 16384, all
+ * multiples of 64 (VBQ_ERR_UNSUPPORTED / VBQ_ERR_SHAPE otherwise).
+ * Errors: VBQ_ERR_INVALID_ARG, VBQ_ERR_SHAPE, VBQ_ERR_UNSUPPORTED, VBQ_ERR_OOM, VBQ_ERR_CUDA.
  */
 VBQ_API vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_matrix* const* mats, vbq_model** out);
 
@@ -171,12 +195,20 @@ VBQ_API void vbq_model_free(vbq_model* model);
  *                       h += Wo a;  u = bf16(rmsnorm(h));
  *                       h += Wdown bf16(silu(Wgate u) * Wup u)
  *   logits = Whead bf16(rmsnorm(h))
- * The residual h is fp32. Every projection accumulates in fp32.
- * The step is one cooperative launch of a persistent kernel (one CTA per SM)
- * with a grid barrier between dependent projections; its activations live in
- * the model's workspace, so steps on the same model must not overlap.
- *  x_dev       device, bf16 [d]
- *  logits_dev  device, float [vocab]
+ * The residual h is fp32; every projection sums in fixed point as vbq_gemv
+ * does, so a step's logits do not depend on timing (two steps on the same
+ * input agree bit for bit).
+ * The step is one cooperative launch of a persistent kernel (one CTA per SM).
+ * Dependent projections are linked by per-super-tile flags, not grid barriers:
+ * the CTA that adds last into 1024 output rows converts them and sets their
+ * flag; a CTA starts a projection once the rows it reads are flagged. Its
+ * activations live in the model's workspace, so steps on the same model must
+ * not overlap. Residual values must stay below 2^57 in magnitude (the RMSNorm
+ * sums of squares are fp32).
+ *  x_dev       device, bf16 [d], 4-byte aligned
+ *  logits_dev  device, float [vocab], 4-byte aligned
+ * Errors: VBQ_ERR_INVALID_ARG (NULL, misaligned, model on another device),
+ * VBQ_ERR_CUDA; a bounded wait that ran out is reported by vbq_device_check (code 3).
  */
 VBQ_API vbq_status vbq_decode_step(vbq_model* model, const uint16_t* x_dev, float* logits_dev, void* stream);
 
@@ -221,36 +253,35 @@ VBQ_API int64_t vbq_launch_count(int32_t reset);
 
 /*
  * vbq_decode_step_noalloc: the step of vbq_decode_step for callers that may not
- * tie step memory to the model they step. Examples are code running while
- * another component captures the stream into its own CUDA graph, loops whose
- * device memory is fixed before they start, and hosts that hand out device
- * memory only from their own pool. The pages have no counterpart: this is an
- * interface of this library.
+ * allocate device memory, or tie it to the model they step, at step time: for
+ * example loops whose device memory is fixed before they start, or hosts that
+ * hand out device memory only from their own pool. The pages have no
+ * counterpart: this is an interface of this library.
  *
- * It launches the same kernel as vbq_decode_step, with the step's activations
- * in one static device array instead of the model's workspace, and gives the
- * same logits bit for bit. The array has 65,536 floats (256 KiB) on every GPU
- * that loads this library and lives until the process exits. In 64-float
- * blocks it holds the grid-barrier counters, h [d], [q;k;v] and [gate;up]. The
- * call allocates nothing: no cudaMalloc, no cudaFree. Split-tile partial rows
- * and their counters stay in the model's own work plans.
+ * It launches the same kernel as vbq_decode_step with the step's scratch (per
+ * projection group: 64-bit sums, float outputs, arrival counters, flags and
+ * statistics) in one static device array instead of the model's workspace,
+ * and gives the same logits bit for bit. The array has 4,194,304 8-byte words
+ * (32 MiB) on every GPU that loads this library and lives until the process
+ * exits. The call allocates nothing: no cudaMalloc, no cudaFree. It records no
+ * trace, whether or not vbq_model_set_trace enabled one.
  *
  *  model       from vbq_model_create, on the current device
- *  x_dev       device, bf16 [d]
- *  logits_dev  device, float [vocab]
+ *  x_dev       device, bf16 [d], 4-byte aligned
+ *  logits_dev  device, float [vocab], 4-byte aligned
  *
- * Size limit: 64 + r(d) + r(n_heads*head_dim + 2*n_kv_heads*head_dim)
- * + r(2*d_ff) <= 65,536 floats, where r() rounds up to a multiple of 64.
- * Larger models get VBQ_ERR_SHAPE, the detail text gives the count, and
- * nothing is enqueued.
+ * Size limit: the model's scratch must fit the array (the 9B-shaped stack of
+ * the tests needs about 2.2 million words). Larger models get VBQ_ERR_SHAPE,
+ * the detail text gives the count, and nothing is enqueued.
  * Set-up: vbq_model_create looks up the array's device address with
  * cudaGetSymbolAddress on the model's device (once per device, with that
  * device current) and clears it, so the calls themselves do neither.
- * Sharing: every call on a device uses the same array. The counters must be
- * zero when a step starts; every step leaves them at zero, and every other
- * value is written before it is read. Calls that overlap on the GPU (two
- * streams, or two host threads), with each other or with vbq_decode_step on
- * the same model, race and give undefined results; serialize them.
+ * Sharing: every call on a device uses the same array. The sums and counters
+ * must be zero when a step starts, and every step leaves them at zero; flags
+ * hold a per-launch value, and every other value is written before it is read.
+ * Calls that overlap on the GPU (two streams, or two host threads), with each
+ * other or with vbq_decode_step on the same model, race and give undefined
+ * results; serialize them.
  * Errors: VBQ_ERR_INVALID_ARG (NULL or misaligned pointers, model on another
  * device), VBQ_ERR_SHAPE (over the limit), VBQ_ERR_CUDA (the launch failed). A
  * bounded wait that runs out is recorded in the device check word; read it

@@ -58,7 +58,7 @@ constexpr uint32_t kNoRefill = 0xFFFFFFFFu;
 #define VBQ_NS 2
 #endif
 #ifndef VBQ_U1
-#define VBQ_U1 1
+#define VBQ_U1 2
 #endif
 #ifndef VBQ_UDP
 #define VBQ_UDP 1

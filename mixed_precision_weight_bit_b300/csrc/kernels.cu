@@ -360,6 +360,8 @@ extern "C" vbq_status vbq_dequant(const vbq_matrix* m, float* W_dev, void* strea
 }
 
 // Batch columns one at a time through the batch-1 kernel (each call streams the matrix once).
+static constexpr int32_t kTcMinBatch = 4;
+
 static vbq_status gemv_columns(const vbq_matrix* m, const uint16_t* X, int32_t B, float* Y, cudaStream_t st) {
   if (m->N == 0) return VBQ_OK;
   if (m->K == 0) {
@@ -403,7 +405,9 @@ extern "C" vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X
   if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm_smallbatch: matrix is on another device");
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   // Two or more columns form a dense contraction: the tensor-core dequant-MMA decodes each code once.
-  if (B >= 2 && m->N > 0 && m->K > 0 && tc_eligible(m)) return launch_gemm_tc(m, X_dev, B, Y_dev, st);
+  // Batches of 4 and more take the tensor cores: their cost hardly depends on B, and on 14336x4096 at
+  // the config-0 allocation it is below four batch-1 GEMVs (measured crossover between 3 and 4).
+  if (B >= kTcMinBatch && m->N > 0 && m->K > 0 && tc_eligible(m)) return launch_gemm_tc(m, X_dev, B, Y_dev, st);
   if (B == 1 && m->K > XCAP && m->N > 0 && tc_eligible(m)) return launch_gemm_tc(m, X_dev, 1, Y_dev, st);
   return gemv_columns(m, X_dev, B, Y_dev, st);
 }
