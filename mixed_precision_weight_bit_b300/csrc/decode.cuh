@@ -510,11 +510,14 @@ __global__ void __launch_bounds__(KW * 32, 1) vbq_decode_kernel(const __grid_con
       if (threadIdx.x == 0) {
         // Release: this CTA's adds (ordered before by the barrier) before its
         // arrival. Acquire: the last arriver sees every other CTA's adds.
+        // Both arrivals in flight at once (a CTA touches at most two super-tiles).
+        static_assert(SLOTS_MAX == 2, "two arrivals");
+        const uint32_t st0 = cp.st_base, st1 = cp.st_base + 1;
+        const uint32_t c0 = atom_add_acq_rel_u32(it.cnt + st0, 1u);
+        const uint32_t c1 = cp.n_slots > 1 ? atom_add_acq_rel_u32(it.cnt + st1, 1u) : 0u;
         uint32_t nf = 0;
-        for (uint32_t s = 0; s < cp.n_slots; ++s) {
-          const uint32_t st = cp.st_base + s;
-          if (atom_add_acq_rel_u32(it.cnt + st, 1u) + 1u == cp.expect[s]) fin[1 + nf++] = st;
-        }
+        if (c0 + 1u == cp.expect[0]) fin[1 + nf++] = st0;
+        if (cp.n_slots > 1 && c1 + 1u == cp.expect[1]) fin[1 + nf++] = st1;
         fin[0] = nf;
       }
       __syncthreads();
