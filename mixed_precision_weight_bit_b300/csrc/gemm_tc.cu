@@ -8,19 +8,25 @@
 // time, and feeds it to tcgen05.mma. The design is this library's own:
 //
 //  * Work: the (tile, group column) pairs in tile-major order are cut into
-//    contiguous ranges of about equal cost, one range per CTA (one CTA per SM,
-//    8 warps). A tile whose columns span several CTAs adds their partial sums
-//    in CTA order (fixed, so results do not depend on timing).
+//    contiguous ranges of about equal cost, one range per CTA (one CTA per
+//    SM). A tile whose columns span several CTAs adds their partial sums in
+//    CTA order (fixed, so results do not depend on timing); the last of its
+//    CTAs to finish does the sum, with many loads in flight per thread.
 //  * Stream: a pair's data are, for each bit class, the steps of the class's
 //    run (layout.h) that hold the tile's entries: at most four pieces, copied
-//    with cp.async.bulk into one of three shared-memory stages. Every wait is
-//    bounded.
-//  * Dequant: a warp takes one 32-entry step at a time, lane l entry l, and
-//    writes the entry's row of A = s_g * (q - c_b), rounded once to fp16, into
-//    a 256 x 64 K-major tile with the 128-byte swizzle (two 128-row halves).
-//    Inside each 32-code block of a group, K position 2s + h holds code
-//    s + 16h (s < 16): a 1-bit word yields the pair with one shift and one
-//    mask, a 2-, 4- or 8-bit entry with a mask per word and one byte permute.
+//    with cp.async.bulk into one of four shared-memory stages. Every wait is
+//    bounded. The column scales, the B tiles and this kernel are three
+//    launches chained as programmatic dependents, so each starts while the one
+//    before finishes.
+//  * Dequant: a warp takes one 32-code block of a 32-entry step at a time,
+//    lane l entry l, and writes that part of the entry's row of
+//    A = s_g * (q - c_b), rounded once to fp16, into a 256 x 64 K-major tile
+//    with the 128-byte swizzle (two 128-row halves). Inside each 32-code
+//    block of a group, K position 2s + h holds code s + 16h (s < 16): a 1-bit
+//    word yields the pair as the pattern of -s/2 with one shift and one
+//    sign flip, a 2-, 4- or 8-bit entry with a mask per word and one byte
+//    permute. The blocks of a pair are dealt to the warps in turn, continuing
+//    from pair to pair, so that no warp always gets a pair's leftovers.
 //    B is the same group of each batch column, times a per-column power of two
 //    that keeps it inside fp16's range, in the same order; the product does
 //    not depend on the order of K.
@@ -52,7 +58,11 @@ extern __shared__ __align__(1024) uint8_t tc_smem[];
 
 namespace {
 
-constexpr int TC_DEQ = 16;               // dequant warps
+#ifndef VBQ_TC_DEQ
+#define VBQ_TC_DEQ 16
+#endif
+constexpr int TC_DEQ = VBQ_TC_DEQ;       // dequant warps (a multiple of 8: the epilogue's quadrants)
+static_assert(TC_DEQ % 8 == 0 && TC_DEQ >= 8, "dequant warps");
 constexpr int TC_WARPS = TC_DEQ + 2;     // and a copy warp and an MMA warp
 constexpr int TC_THREADS = TC_WARPS * 32;
 constexpr int TC_NMAX = 64;              // batch columns per launch
@@ -139,76 +149,84 @@ __device__ __forceinline__ void put16(uint32_t a_base, uint32_t row, uint32_t ch
   *reinterpret_cast<uint4*>(tc_smem + a_base + (row >> 7) * (TC_ATILE / 2) + sw128(row & 127u, chunk)) = v;
 }
 
-// Dequantizes entry `lane` of a step of class CLS (e entries) at shared offset
-// rec into its row of A, if the entry is one of the tile's.
+// Dequantizes block blk (codes 32 blk .. 32 blk + 31) of entry `lane` of a
+// step of class CLS (e entries) at shared offset rec into its row of A, if the
+// entry is one of the tile's. Inside the block, K position 2s + h holds code
+// s + 16h (s < 16), four pairs per 16-byte chunk.
 template <int CLS>
-__device__ __forceinline__ void tc_entry(uint32_t rec, uint32_t e, bool mine, uint32_t a_base, int lane) {
+__device__ __forceinline__ void tc_entry(uint32_t rec, uint32_t e, bool mine, uint32_t blk, uint32_t a_base, int lane) {
   constexpr uint32_t B = 1u << CLS;
-  const uint32_t j = mine ? static_cast<uint32_t>(lane) : 0u;
+  if (!mine) return;
+  const uint32_t j = static_cast<uint32_t>(lane);
   const uint16_t sb = *reinterpret_cast<const uint16_t*>(tc_smem + rec + rec_scale_off(CLS, e) + 2u * j);
   const uint32_t row = tc_smem[rec + rec_row_off(CLS, e) + j];
-  const __half2 sc = __half2half2(__ushort_as_half(sb));
-  const __half2 nhs = __hmul2(sc, __float2half2_rn(-0.5f));
-  const __half2 base = __float2half2_rn(static_cast<float>(1024u + (1u << (B - 1u)) - 1u));
-  if (!mine) return;
   if constexpr (CLS == 0) {
-    const uint2 cw = *reinterpret_cast<const uint2*>(tc_smem + rec + 8u * j);
+    // w = s (q - 1/2) = -+s/2: the fp16 pattern of -s/2, its sign flipped where
+    // q = 1 (the same two values the fma form gives when s/2 is exact).
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(tc_smem + rec + 8u * j + 4u * blk);
+    const __half hs = __hmul(__ushort_as_half(sb), __float2half_rn(0.5f));
+    const uint32_t neg = static_cast<uint32_t>(__half_as_ushort(hs)) ^ 0x8000u;
+    const uint32_t pat = neg | (neg << 16);
 #pragma unroll
-    for (uint32_t blk = 0; blk < 2; ++blk) {
-      const uint32_t w = blk ? cw.y : cw.x;
+    for (uint32_t c = 0; c < 4; ++c) {  // chunk 4 blk + c: pairs s = 4c .. 4c + 3
+      uint32_t o[4];
 #pragma unroll
-      for (uint32_t c = 0; c < 4; ++c) {  // chunk 4 blk + c: pairs s = 4c .. 4c + 3, (code s, code s + 16)
-        uint32_t o[4];
-#pragma unroll
-        for (uint32_t t = 0; t < 4; ++t)
-          o[t] = deq_pair(((w >> (4u * c + t)) & 0x00010001u) | 0x64006400u, base, sc, nhs);
-        put16(a_base, row, 4u * blk + c, make_uint4(o[0], o[1], o[2], o[3]));
+      for (uint32_t t = 0; t < 4; ++t) {
+        const uint32_t sh = 4u * c + t;                       // code sh at bit 15, code sh + 16 at bit 31
+        o[t] = pat ^ ((w << (15u - sh)) & 0x80008000u);
       }
+      put16(a_base, row, 4u * blk + c, make_uint4(o[0], o[1], o[2], o[3]));
     }
   } else {
-    // The entry's 2b words, 16-byte chunk q of entry j at 16 (q e + j).
-    uint32_t w[2 * B];
+    const __half2 sc = __half2half2(__ushort_as_half(sb));
+    const __half2 nhs = __hmul2(sc, __float2half2_rn(-0.5f));
+    const __half2 base = __float2half2_rn(static_cast<float>(1024u + (1u << (B - 1u)) - 1u));
+    // The block's B words (blk*B .. blk*B + B - 1), 16-byte chunk q of entry j at 16 (q e + j).
+    uint32_t w[B];
+    if constexpr (B == 2) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tc_smem + rec + j * 16u);
+      w[0] = blk ? v.z : v.x;
+      w[1] = blk ? v.w : v.y;
+    } else {
 #pragma unroll
-    for (uint32_t q = 0; q < B / 2; ++q) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tc_smem + rec + (q * e + j) * 16u);
-      w[4 * q] = v.x;
-      w[4 * q + 1] = v.y;
-      w[4 * q + 2] = v.z;
-      w[4 * q + 3] = v.w;
+      for (uint32_t q = 0; q < B / 4; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tc_smem + rec + ((blk * B / 4 + q) * e + j) * 16u);
+        w[4 * q] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
+      }
     }
     constexpr uint32_t CPW = 32u / B;              // codes per word
     constexpr uint32_t MASK = B == 8 ? 0xFFFFFFFFu : (B == 4 ? 0x0F0F0F0Fu : 0x03030303u);
+    // Code s (< 16) of the block is code s % CPW of word s / CPW, and code s + 16
+    // the same code of the word B/2 further on.
 #pragma unroll
-    for (uint32_t blk = 0; blk < 2; ++blk) {
-      // Code s (< 16) of the block is code s % CPW of word blk*B + s/CPW, and code
-      // s + 16 the same code of the word B/2 further on.
+    for (uint32_t u = 0; u < B / 2; ++u) {
+      const uint32_t wa = w[u], wb = w[u + B / 2];
 #pragma unroll
-      for (uint32_t u = 0; u < B / 2; ++u) {
-        const uint32_t wa = w[blk * B + u], wb = w[blk * B + u + B / 2];
+      for (uint32_t i = 0; i < CPW / 4; ++i) {
+        const uint32_t va = (wa >> (B * i)) & MASK, vb = (wb >> (B * i)) & MASK;
+        uint32_t o[4];
 #pragma unroll
-        for (uint32_t i = 0; i < CPW / 4; ++i) {
-          const uint32_t va = (wa >> (B * i)) & MASK, vb = (wb >> (B * i)) & MASK;
-          uint32_t o[4];
-#pragma unroll
-          for (uint32_t t = 0; t < 4; ++t) {
-            const uint32_t pr = __byte_perm(va, vb, t | (t << 4) | ((4u + t) << 8) | ((4u + t) << 12));
-            o[t] = deq_pair((pr & 0x00FF00FFu) | 0x64006400u, base, sc, nhs);
-          }
-          // pairs s = u * CPW + 4i .. + 3: chunk (u * CPW + 4i) / 4 of the block
-          put16(a_base, row, 4u * blk + u * (CPW / 4) + i, make_uint4(o[0], o[1], o[2], o[3]));
+        for (uint32_t t = 0; t < 4; ++t) {
+          const uint32_t pr = __byte_perm(va, vb, t | (t << 4) | ((4u + t) << 8) | ((4u + t) << 12));
+          o[t] = deq_pair((pr & 0x00FF00FFu) | 0x64006400u, base, sc, nhs);
         }
+        // pairs s = u * CPW + 4i .. + 3: chunk (u * CPW + 4i) / 4 of the block
+        put16(a_base, row, 4u * blk + u * (CPW / 4) + i, make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
   }
 }
 
-__device__ __forceinline__ void tc_step(uint32_t rec, uint32_t cls, uint32_t e, bool mine, uint32_t a_base,
-                                        int lane) {
+__device__ __forceinline__ void tc_step(uint32_t rec, uint32_t cls, uint32_t e, bool mine, uint32_t blk,
+                                        uint32_t a_base, int lane) {
   switch (cls) {
-    case 0: tc_entry<0>(rec, e, mine, a_base, lane); break;
-    case 1: tc_entry<1>(rec, e, mine, a_base, lane); break;
-    case 2: tc_entry<2>(rec, e, mine, a_base, lane); break;
-    default: tc_entry<3>(rec, e, mine, a_base, lane); break;
+    case 0: tc_entry<0>(rec, e, mine, blk, a_base, lane); break;
+    case 1: tc_entry<1>(rec, e, mine, blk, a_base, lane); break;
+    case 2: tc_entry<2>(rec, e, mine, blk, a_base, lane); break;
+    default: tc_entry<3>(rec, e, mine, blk, a_base, lane); break;
   }
 }
 
@@ -253,6 +271,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) vbq_gemm_tc_kernel(const __grid
   for (uint32_t i = tid; i < cta.q1 - cta.q0; i += TC_THREADS) pcs[i] = a.pieces[cta.q0 + i];
   const uint32_t pa = a.units[cta.u0].p0, pb = a.units[cta.u1 - 1].p1;  // the CTA's pairs
   for (uint32_t i = tid; i <= pb - pa; i += TC_THREADS) pfirst[i] = a.pair_piece[pa + i] - cta.q0;
+  grid_dep_wait();  // the B tiles and column scales of the kernels before are complete
   for (int i = tid; i < TC_NMAX; i += TC_THREADS) sxs[i] = i < a.B ? a.sx[i] : 0.0f;
   if (tid == 0) {
     for (int i = 0; i < TC_NST; ++i) {
@@ -355,7 +374,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) vbq_gemm_tc_kernel(const __grid
     }
   } else {
     // ---- dequant warps, then the epilogue of each unit ----
-    uint32_t gi = 0, su = 0;  // pairs, and split units, of this CTA so far
+    uint32_t gi = 0, su = 0, ibase = 0;  // pairs, split units and work items of this CTA so far
     bool ok = true;
     for (uint32_t u = 0; u < nu && ok; ++u) {
       const TcUnit un = units[u];
@@ -371,18 +390,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) vbq_gemm_tc_kernel(const __grid
           break;
         }
         const uint32_t a_base = L::kA + buf * TC_ATILE + pad;
-        uint32_t o = L::kStage + s * TC_STAGE + pad + TC_BTILE, sidx = 0;
+        // Work items: two per step (its two 32-code blocks), numbered in piece order
+        // across the CTA's pairs; warp w takes the items numbered w mod TC_DEQ, so
+        // a pair's leftover items fall to different warps from pair to pair.
+        uint32_t o = L::kStage + s * TC_STAGE + pad + TC_BTILE;
         for (uint32_t q = pfirst[gi]; q < pfirst[gi + 1]; ++q) {
           const TcPiece pc = pcs[q];
           const uint32_t fb = full_step_bytes(pc.cls);
-          for (uint32_t k = 0; k < pc.nst; ++k, ++sidx) {
-            if (static_cast<int>(sidx % TC_DEQ) != warp) continue;
+          const uint32_t nit = 2u * pc.nst;
+          uint32_t it = (static_cast<uint32_t>(warp) + TC_DEQ - ibase % TC_DEQ) % TC_DEQ;
+          for (; it < nit; it += TC_DEQ) {
+            const uint32_t k = it >> 1, blk = it & 1u;
             const uint32_t k0 = 32u * (pc.ks + k);
             const uint32_t e = min(32u, static_cast<uint32_t>(pc.n) - k0);
             const uint32_t i = k0 + static_cast<uint32_t>(lane);
             const bool mine = static_cast<uint32_t>(lane) < e && i >= pc.lo && i < pc.hi;
-            tc_step(o + k * fb, pc.cls, e, mine, a_base, lane);
+            tc_step(o + k * fb, pc.cls, e, mine, blk, a_base, lane);
           }
+          ibase += nit;
           o += 16u * pc.bytes16;
         }
         fence_proxy_async_smem();  // this warp's rows of A, for the tensor cores
@@ -442,12 +467,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1) vbq_gemm_tc_kernel(const __grid
           break;
         }
         if (misc[2]) {
-          const float* pb0 = a.partial + static_cast<size_t>(un.pbase) * (TC_NMAX * 256);
-          for (uint32_t i = tid; i < rows * static_cast<uint32_t>(a.B); i += TC_DEQ * 32) {
-            const uint32_t bc = i / rows, rr = i % rows;
-            float y = 0.0f;
-            for (uint32_t sp = 0; sp < un.nsplit; ++sp) y += __ldcg(pb0 + (sp * TC_NMAX + bc) * 256u + rr);
-            a.Y[static_cast<int64_t>(bc) * a.N + r0 + rr] = y;
+          // y = ((0 + part_0) + part_1) + ...: four float4 of each split in flight per thread.
+          const float4* pb0 = reinterpret_cast<const float4*>(a.partial + static_cast<size_t>(un.pbase) * (TC_NMAX * 256));
+          const uint32_t nv = static_cast<uint32_t>(a.B) * 64u;   // float4 of the B columns' 256 rows
+          constexpr uint32_t kT = TC_DEQ * 32;
+          for (uint32_t v0 = static_cast<uint32_t>(tid); v0 < nv; v0 += 4u * kT) {
+            float4 y[4];
+#pragma unroll
+            for (uint32_t k = 0; k < 4; ++k) y[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (uint32_t sp = 0; sp < un.nsplit; ++sp) {
+              float4 t[4];
+#pragma unroll
+              for (uint32_t k = 0; k < 4; ++k) {
+                const uint32_t v = v0 + k * kT;
+                t[k] = v < nv ? __ldcg(pb0 + sp * (TC_NMAX * 64u) + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              }
+#pragma unroll
+              for (uint32_t k = 0; k < 4; ++k) {
+                y[k].x += t[k].x;
+                y[k].y += t[k].y;
+                y[k].z += t[k].z;
+                y[k].w += t[k].w;
+              }
+            }
+#pragma unroll
+            for (uint32_t k = 0; k < 4; ++k) {
+              const uint32_t v = v0 + k * kT;
+              if (v >= nv) break;
+              const uint32_t bc = v >> 6, rr = 4u * (v & 63u);
+              float* yr = a.Y + static_cast<int64_t>(bc) * a.N + r0 + rr;
+              const float yv[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
+#pragma unroll
+              for (uint32_t c = 0; c < 4; ++c)
+                if (rr + c < rows) yr[c] = yv[c];
+            }
           }
           if (tid == 0) a.counters[un.tile] = 0u;
         }
@@ -469,6 +522,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) vbq_gemm_tc_kernel(const __grid
 __global__ void vbq_xprep_kernel(const uint16_t* __restrict__ X, int32_t K, int32_t B, int32_t Npad,
                                  const float* __restrict__ sx, uint8_t* __restrict__ bt) {
   const uint32_t g = blockIdx.x;
+  grid_dep_launch();  // the dequant-MMA kernel may start its set-up
+  grid_dep_wait();    // sx is complete
   for (uint32_t i = threadIdx.x; i < static_cast<uint32_t>(Npad) * 8u; i += blockDim.x) {
     const uint32_t bc = i >> 3, ch = i & 7u;
     uint4 pk = make_uint4(0u, 0u, 0u, 0u);
@@ -495,6 +550,7 @@ __global__ void vbq_xprep_kernel(const uint16_t* __restrict__ X, int32_t K, int3
 // (p limited to the float range).
 __global__ void vbq_xscale_kernel(const uint16_t* __restrict__ X, int32_t K, float* __restrict__ sx) {
   __shared__ float red[32];
+  grid_dep_launch();  // the B-tile kernel may start; it waits for this grid before reading sx
   const uint16_t* x = X + static_cast<int64_t>(blockIdx.x) * K;
   float m = 0.0f;
   for (int k = threadIdx.x; k < K; k += blockDim.x)
@@ -723,8 +779,21 @@ vbq_status launch_gemm_tc(const vbq_matrix* m, const uint16_t* X, int32_t B, flo
   note_launches(2);
   vbq_xscale_kernel<<<B, 256, 0, st>>>(X, static_cast<int32_t>(m->K), s->sx);
   VBQ_CUDA_TRY(cudaGetLastError());
-  vbq_xprep_kernel<<<m->G, 256, 0, st>>>(X, static_cast<int32_t>(m->K), B, npad, s->sx, s->bt);
-  VBQ_CUDA_TRY(cudaGetLastError());
+  // The two kernels after the first are programmatic dependents: each starts
+  // while the one before runs and waits for it (griddepcontrol.wait) before
+  // reading its output.
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(m->G));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  VBQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, vbq_xprep_kernel, X, static_cast<int32_t>(m->K), B, npad,
+                                  static_cast<const float*>(s->sx), s->bt));
   TcArgs a{};
   a.data = m->data;
   a.ctas = s->ctas;
@@ -743,8 +812,10 @@ vbq_status launch_gemm_tc(const vbq_matrix* m, const uint16_t* X, int32_t B, flo
   a.N = m->N;
   a.err = chk;
   note_launches(1);
-  vbq_gemm_tc_kernel<<<s->n_ctas, TC_THREADS, TcSmem::kBytes, st>>>(a);
-  VBQ_CUDA_TRY(cudaGetLastError());
+  cfg.gridDim = dim3(static_cast<unsigned>(s->n_ctas));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = TcSmem::kBytes;
+  VBQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, vbq_gemm_tc_kernel, a));
   return VBQ_OK;
 }
 

@@ -359,8 +359,12 @@ extern "C" vbq_status vbq_dequant(const vbq_matrix* m, float* W_dev, void* strea
   return VBQ_OK;
 }
 
-// Batch columns one at a time through the batch-1 kernel (each call streams the matrix once).
-static constexpr int32_t kTcMinBatch = 4;
+// Batch columns one at a time through the batch-1 kernel (each call streams the
+// matrix once); from VBQ_TC_MIN_BATCH columns on, the tensor-core path.
+#ifndef VBQ_TC_MIN_BATCH
+#define VBQ_TC_MIN_BATCH 4
+#endif
+static constexpr int32_t kTcMinBatch = VBQ_TC_MIN_BATCH;
 
 static vbq_status gemv_columns(const vbq_matrix* m, const uint16_t* X, int32_t B, float* Y, cudaStream_t st) {
   if (m->N == 0) return VBQ_OK;
