@@ -372,18 +372,28 @@ def dense_baseline(V, shape, stream, steps=3):
     xs = {k: torch.randn(k, device="cuda", dtype=torch.bfloat16, generator=g) for (_, _, k) in mats}
     ys = {n: torch.empty(n, device="cuda") for (_, n, _) in mats}
 
-    def step():
+    jobs = [(W, xs[k], ys[n], n, k) for (W, n, k) in mats]
+
+    def step_many():
+        V.vbq_dense_gemv_bf16_many(jobs, stream)
+
+    def step_each():
         for (W, n, k) in mats:
             V.vbq_dense_gemv_bf16(W, xs[k], ys[n], n, k, stream)
 
     with torch.cuda.stream(stream):
-        ms = time_steps(step, steps, 1, stream, 1)
+        ms = time_steps(step_many, steps, 1, stream, 1)
+        ms_each = time_steps(step_each, steps, 1, stream, 1)
     nbytes = sum(2.0 * n * k + 2.0 * k + 4.0 * n for (_, n, k) in mats)
-    del mats
+    del mats, jobs
     torch.cuda.empty_cache()
     return {"us_per_step": round(ms * 1e3, 1), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
-            "weight_bytes": nbytes, "launches_per_step": shape.n_layers * len(PROJS) + 1,
-            "note": "bf16 W and x, fp32 accumulate; bytes = 2NK + 2K + 4N per matrix"}
+            "weight_bytes": nbytes, "launches_per_step": 1,
+            "one_launch_per_matrix": {"us_per_step": round(ms_each * 1e3, 1),
+                                      "GB/s": round(nbytes / (ms_each * 1e-3) / 1e9, 1),
+                                      "launches_per_step": shape.n_layers * len(PROJS) + 1},
+            "note": "bf16 W and x, fp32 accumulate; bytes = 2NK + 2K + 4N per matrix; "
+                    "every matrix of the step in one launch (vbq_dense_gemv_bf16_many)"}
 
 
 def config0_gemv(V, stream, peak_gbs):

@@ -242,6 +242,27 @@ VBQ_API vbq_status vbq_dense_gemv_bf16(const uint16_t* W_dev, const uint16_t* x_
                                int64_t K, void* stream);
 
 /*
+ * Many dense bf16 GEMVs in one launch (the dense baseline of a whole decode
+ * step, without a launch per matrix): for each job j, y_j = W_j x_j with the
+ * layout and arithmetic of vbq_dense_gemv_bf16. Rows of all jobs are dealt to
+ * the warps of one persistent grid in job order. jobs: host array of n_jobs
+ * (at most VBQ_DENSE_MAX_JOBS) descriptors of device buffers, read before the
+ * call returns. Every K % 8 == 0, 0 <= N, K < 2^31, W and x 16-byte aligned;
+ * jobs with N == 0 are skipped, jobs with K == 0 get y = 0. An invalid job
+ * fails the whole call before anything is launched. There is no counterpart
+ * on the source pages: the pages compare against dense weights, and this is
+ * the dense side of that comparison.
+ */
+#define VBQ_DENSE_MAX_JOBS 256
+typedef struct {
+  const uint16_t* W; /* bf16 [N][K], device */
+  const uint16_t* x; /* bf16 [K], device */
+  float* y;          /* float [N], device */
+  int64_t N, K;
+} vbq_dense_job;
+VBQ_API vbq_status vbq_dense_gemv_bf16_many(const vbq_dense_job* jobs, int32_t n_jobs, void* stream);
+
+/*
  * Reads and clears the device-side check word of the current device. Kernels
  * set it when a bounded wait runs out. Synchronizes the device. Returns
  * VBQ_OK, or VBQ_ERR_DEVICE_CHECK with *code set (code may be NULL).

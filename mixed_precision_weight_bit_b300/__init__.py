@@ -2,7 +2,8 @@
 with fused dequantize-and-multiply kernels behind a C ABI (include/vbq.h).
 
 Importing this package loads libvbq.so and fails if it is missing: there is no
-CPU or PyTorch fallback. Build it with ``python -m mixed_precision_weight_bit_b300.build``.
+CPU or PyTorch fallback. Build it with ``python mixed_precision_weight_bit_b300/build.py``
+(by path: importing the package needs a library that is already built).
 """
 
 from .vbq import *  # noqa: F401,F403

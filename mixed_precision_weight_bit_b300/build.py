@@ -1,6 +1,7 @@
 """Builds libvbq.so in-tree for sm_103a with nvcc (no JIT cache, no torch extension).
 
-Usage: python -m mixed_precision_weight_bit_b300.build [--force]
+Usage: python mixed_precision_weight_bit_b300/build.py [--force]
+(run it by path: importing the package loads the library this script builds)
 """
 
 from __future__ import annotations

@@ -416,6 +416,123 @@ extern "C" vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X
   return gemv_columns(m, X_dev, B, Y_dev, st);
 }
 
+// Many dense GEMVs, one persistent launch: global row r (rows of all jobs in
+// job order) goes to warp r mod (warps of the grid); x is read through L1,
+// where the rows of one job that a CTA's warps take in turn find it.
+struct DenseManyArgs {
+  const uint16_t* W[VBQ_DENSE_MAX_JOBS];
+  const uint16_t* x[VBQ_DENSE_MAX_JOBS];
+  float* y[VBQ_DENSE_MAX_JOBS];
+  int32_t K[VBQ_DENSE_MAX_JOBS];
+  int64_t row0[VBQ_DENSE_MAX_JOBS + 1];  // first global row of each job; row0[n] = all rows
+  int32_t n;
+};
+static_assert(sizeof(DenseManyArgs) < 32000, "kernel parameter space");
+
+constexpr int kDenseWarps = 8;  // per CTA
+constexpr int kDenseUnroll = 8;  // 16-byte loads in flight per lane
+
+__global__ void __launch_bounds__(kDenseWarps * 32, 3) vbq_dense_many_kernel(const __grid_constant__ DenseManyArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kDenseWarps, total = a.row0[a.n];
+  grid_dep_wait();
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kDenseWarps + warp; r < total; r += stride) {
+    int lo = 0, hi = a.n - 1;  // the job: the last with row0 <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.row0[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const int K = a.K[lo];
+    const uint16_t* wr = a.W[lo] + (r - a.row0[lo]) * K;
+    const uint16_t* x = a.x[lo];
+    float acc0 = 0.f, acc1 = 0.f;
+    int k = lane * 8;
+    for (; k + (kDenseUnroll - 1) * 256 < K; k += kDenseUnroll * 256) {
+      uint4 wv[kDenseUnroll], xv[kDenseUnroll];
+#pragma unroll
+      for (int u = 0; u < kDenseUnroll; ++u) wv[u] = ldg_stream_v4(wr + k + u * 256);
+#pragma unroll
+      for (int u = 0; u < kDenseUnroll; ++u) xv[u] = __ldg(reinterpret_cast<const uint4*>(x + k + u * 256));
+#pragma unroll
+      for (int u = 0; u < kDenseUnroll; ++u) {
+        const uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+        const uint32_t xx[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc0 = fmaf(bf16_lo(ww[q]), bf16_lo(xx[q]), acc0);
+          acc1 = fmaf(bf16_hi(ww[q]), bf16_hi(xx[q]), acc1);
+        }
+      }
+    }
+    for (; k < K; k += 256) {
+      const uint4 wv = ldg_stream_v4(wr + k);
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + k));
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+      const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc0 = fmaf(bf16_lo(ww[q]), bf16_lo(xx[q]), acc0);
+        acc1 = fmaf(bf16_hi(ww[q]), bf16_hi(xx[q]), acc1);
+      }
+    }
+    float v = acc0 + acc1;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    if (lane == 0) a.y[lo][r - a.row0[lo]] = v;
+  }
+}
+
+extern "C" vbq_status vbq_dense_gemv_bf16_many(const vbq_dense_job* jobs, int32_t n_jobs, void* stream) {
+  if (n_jobs < 0 || n_jobs > VBQ_DENSE_MAX_JOBS)
+    return fail(VBQ_ERR_INVALID_ARG, "vbq_dense_gemv_bf16_many: n_jobs out of range");
+  if (n_jobs > 0 && !jobs) return fail(VBQ_ERR_INVALID_ARG, "vbq_dense_gemv_bf16_many: NULL jobs");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const vbq_dense_job& d = jobs[j];
+    if (d.N < 0 || d.K < 0 || d.K % 8 || d.N >= (int64_t(1) << 31) || d.K >= (int64_t(1) << 31))
+      return fail(VBQ_ERR_SHAPE, "vbq_dense_gemv_bf16_many: need K % 8 == 0 and N, K < 2^31");
+    if (d.N > 0 && !d.y) return fail(VBQ_ERR_INVALID_ARG, "vbq_dense_gemv_bf16_many: NULL y");
+    if (d.N > 0 && d.K > 0 && (!d.W || !d.x || !aligned(d.W, 16) || !aligned(d.x, 16)))
+      return fail(VBQ_ERR_INVALID_ARG, "vbq_dense_gemv_bf16_many: W and x must be 16-byte aligned device buffers");
+  }
+  DenseManyArgs a{};
+  int64_t rows = 0;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const vbq_dense_job& d = jobs[j];
+    if (d.N == 0) continue;
+    if (d.K == 0) {
+      VBQ_CUDA_TRY(cudaMemsetAsync(d.y, 0, sizeof(float) * d.N, st));
+      continue;
+    }
+    a.W[a.n] = d.W;
+    a.x[a.n] = d.x;
+    a.y[a.n] = d.y;
+    a.K[a.n] = static_cast<int32_t>(d.K);
+    a.row0[a.n] = rows;
+    rows += d.N;
+    ++a.n;
+  }
+  a.row0[a.n] = rows;
+  if (a.n == 0) return VBQ_OK;
+  int64_t grid = (rows + kDenseWarps - 1) / kDenseWarps;
+  const int64_t cap = static_cast<int64_t>(gpu_info().sms) * 3;
+  if (grid > cap) grid = cap;
+  note_launches(1);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kDenseWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  VBQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, vbq_dense_many_kernel, a));
+  return VBQ_OK;
+}
+
 extern "C" vbq_status vbq_dense_gemv_bf16(const uint16_t* W_dev, const uint16_t* x_dev, float* y_dev, int64_t N,
                                           int64_t K, void* stream) {
   if (N < 0 || K < 0 || K % 8 || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))

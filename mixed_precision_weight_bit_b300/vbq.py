@@ -49,6 +49,15 @@ _I64 = ctypes.c_int64
 _I32 = ctypes.c_int32
 _ST = ctypes.c_int
 
+
+class VbqDenseJob(ctypes.Structure):
+    """vbq_dense_job: device pointers and the shape of one dense GEMV."""
+    _fields_ = [("W", _P), ("x", _P), ("y", _P), ("N", _I64), ("K", _I64)]
+
+
+VBQ_DENSE_MAX_JOBS = 256
+
+
 _SIGNATURES = {
     "vbq_status_str": (ctypes.c_char_p, [_ST]),
     "vbq_last_error": (ctypes.c_char_p, []),
@@ -67,6 +76,7 @@ _SIGNATURES = {
     "vbq_model_trace_info": (_ST, [_P, _P, _P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "vbq_model_read_trace": (_ST, [_P, _P, _P]),
     "vbq_dense_gemv_bf16": (_ST, [_P, _P, _P, _I64, _I64, _P]),
+    "vbq_dense_gemv_bf16_many": (_ST, [_P, _I32, _P]),
     "vbq_device_check": (_ST, [ctypes.POINTER(_I32)]),
     "vbq_launch_count": (_I64, [_I32]),
     "vbq_debug_set": (_ST, [_I32, _I64]),
@@ -81,7 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     if _lib is not None and path == LIB_PATH:
         return _lib
     if not os.path.exists(path):
-        raise ImportError(f"libvbq.so is not built ({path}); run: python -m mixed_precision_weight_bit_b300.build")
+        raise ImportError(f"libvbq.so is not built ({path}); run: python mixed_precision_weight_bit_b300/build.py")
     lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGNATURES.items():
         fn = getattr(lib, name)
@@ -230,6 +240,15 @@ def vbq_model_read_trace(model: int, in_total: int, out_total: int):
 def vbq_dense_gemv_bf16(W, x, y, N: int, K: int, stream=None) -> None:
     _check("vbq_dense_gemv_bf16", _L().vbq_dense_gemv_bf16(_dptr(W), _dptr(x), _dptr(y), int(N), int(K),
                                                            _stream(stream)))
+
+
+def vbq_dense_gemv_bf16_many(jobs, stream=None) -> None:
+    """jobs: sequence of (W, x, y, N, K) with device tensors or pointers; one launch for all."""
+    arr = (VbqDenseJob * max(1, len(jobs)))()
+    for i, (W, x, y, N, K) in enumerate(jobs):
+        arr[i] = VbqDenseJob(_dptr(W), _dptr(x), _dptr(y), int(N), int(K))
+    _check("vbq_dense_gemv_bf16_many", _L().vbq_dense_gemv_bf16_many(ctypes.cast(arr, _P), len(jobs),
+                                                                     _stream(stream)))
 
 
 def vbq_device_check() -> int:

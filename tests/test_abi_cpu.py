@@ -85,3 +85,21 @@ def test_null_handles_rejected(lib):
     assert lib.vbq_model_create(None, None, None) == 1
     info = V.VbqInfo()
     assert lib.vbq_matrix_info(None, ctypes.byref(info)) == 1
+
+
+def test_dense_many_validation_without_gpu(lib):
+    """The batched dense baseline checks every job before it launches anything."""
+    from mixed_precision_weight_bit_b300 import vbq as V
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_dense_gemv_bf16_many([(None, None, None, 4, 8)] * (V.VBQ_DENSE_MAX_JOBS + 1))
+    assert e.value.status == 1
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_dense_gemv_bf16_many([(16, 16, 16, 4, 12)])   # K % 8
+    assert e.value.status == 2
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_dense_gemv_bf16_many([(16, 16, None, 4, 8)])  # NULL y
+    assert e.value.status == 1
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_dense_gemv_bf16_many([(16, 16, 16, 4, 8), (18, 16, 16, 4, 8)])  # W not 16-byte aligned
+    assert e.value.status == 1
+    assert lib.vbq_dense_gemv_bf16_many(None, 1, None) == 1

@@ -244,3 +244,31 @@ def test_dense_bf16_gemv(V, N, K):
     norms = np.linalg.norm(w, axis=1) * np.linalg.norm(x)
     assert np.isfinite(got).all()
     assert np.max(np.abs(got - ref) / norms) <= TOL
+
+
+def test_dense_bf16_gemv_many(V):
+    """One launch for several dense GEMVs of different shapes (and an empty and a K = 0 job)."""
+    import torch
+    shapes = [(300, 1024), (0, 64), (7, 0), (4099, 4096), (1, 8), (1024, 14336), (65, 72)]
+    jobs, refs = [], []
+    for i, (N, K) in enumerate(shapes):
+        rng = np.random.default_rng(1000 + i)
+        w_bits = O.f64_to_bf16_bits(rng.standard_normal((N, K)) * 0.05)
+        x_bits = gen_x(K, seed=2000 + i) if K else np.zeros(0, np.uint16)
+        W = dev_u16(w_bits) if N * K else torch.empty(8, dtype=torch.int16, device="cuda")
+        x = dev_u16(x_bits) if K else torch.empty(8, dtype=torch.int16, device="cuda")
+        y = torch.full((max(N, 1),), float("nan"), device="cuda")
+        jobs.append((W, x, y, N, K))
+        w = O.bf16_bits_to_f64(w_bits).reshape(N, K)
+        xf = O.bf16_bits_to_f64(x_bits)
+        refs.append((w @ xf if N else np.zeros(0), np.linalg.norm(w, axis=1) * np.linalg.norm(xf)))
+    V.vbq_dense_gemv_bf16_many(jobs)
+    torch.cuda.synchronize()
+    for (W, x, y, N, K), (ref, norms) in zip(jobs, refs):
+        got = y.cpu().numpy()[:N].astype(np.float64)
+        assert np.isfinite(got).all(), (N, K)
+        if K == 0:
+            assert np.array_equal(got, np.zeros(N))
+        elif N:
+            assert np.max(np.abs(got - ref) / norms) <= TOL, (N, K)
+
