@@ -352,7 +352,7 @@ def standalone_gemv(V, pm, stream, peak_gbs, reps=3):
             "kernel": "vbq_gemv1_kernel", "launches": launches,
             "avg_launch_us": round(tot_ms * 1e3 / launches, 2),
             "alg_bytes_per_launch": round(tot_b / launches),
-            "note": "each projection of the 9B stack launched alone through vbq_gemv"}
+            "note": "each projection of the step's stack launched alone through vbq_gemv"}
 
 
 def dense_baseline(V, shape, stream, steps=3):
