@@ -463,6 +463,35 @@ def batch_sweep(V, stream):
     return out
 
 
+def attention_decode_sweep(V, stream, peak_gbs):
+    """Decode attention of one token over a bf16 KV cache at the 9B shape (32 query heads, 8 kv heads,
+    head_dim 128), cold L2: the cache bytes read per call over the call's time."""
+    import torch
+    H, Hkv, d = 32, 8, 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    out = {}
+    for T in (1024, 4096, 16384, 65536):
+        q = (torch.randn(H, d, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+        kc = (torch.randn(Hkv, T, d, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+        vc = torch.randn(Hkv, T, d, device="cuda", generator=g).to(torch.bfloat16)
+        o = torch.empty(H, d, device="cuda")
+        us = time_cold(lambda: V.vbq_attention_decode(q, kc, vc, H, Hkv, d, T, T, o, stream), stream)
+        nbytes = 2.0 * Hkv * T * d * 2 + H * d * 2 + H * d * 4
+        out[str(T)] = {"us": round(us, 2), "GB/s": round(nbytes / us / 1e3, 1),
+                       "frac": round(nbytes / us / 1e3 / peak_gbs, 4)}
+        del kc, vc
+    kn = torch.zeros(Hkv, d, device="cuda", dtype=torch.bfloat16)
+    kc = torch.zeros(Hkv, 4096, d, device="cuda", dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    q = torch.zeros(H, d, device="cuda", dtype=torch.bfloat16)
+    us = time_cold(lambda: V.vbq_rope_append(q, kn, kn, kc, vc, H, Hkv, d, 4096, 1000, 10000.0, stream), stream)
+    out["rope_append_us"] = round(us, 2)
+    out["note"] = ("vbq_attention_decode, 32 q heads over 8 kv heads, head_dim 128, T positions, up to 64 spans per kv head; "
+                   "bytes = K and V of the T positions + q + out")
+    return out
+
+
 def stress_8192(V, stream):
     """The 8192x8192 allocation-stress matrices (a)-(e), batch 1, cold L2."""
     import torch
@@ -696,6 +725,7 @@ def run_vbq(args, ws, rank, local):
     if not args.no_sweep:
         extra["batch_sweep_14336x4096"] = batch_sweep(V, stream)
         extra["stress_8192"] = stress_8192(V, stream)
+        extra["attention_decode_9b_heads"] = attention_decode_sweep(V, stream, peak)
     if not args.no_dense:
         extra["dense_bf16" + w] = dense_baseline(V, shape, stream)
         extra["dense_bf16" + w]["speedup_vbq"] = round(extra["dense_bf16" + w]["us_per_step"] / (ms * 1e3), 2)

@@ -263,6 +263,43 @@ typedef struct {
 VBQ_API vbq_status vbq_dense_gemv_bf16_many(const vbq_dense_job* jobs, int32_t n_jobs, void* stream);
 
 /*
+ * Decode attention for one new token over a bf16 KV cache (the other half of
+ * a decode step beside the projections; the source pages name only
+ * "autoregressive decode" in the VBQ abstract, so the operations below are the
+ * standard definitions, read as stated).
+ *
+ * vbq_rope_append: rotary position embedding at position pos, rotate-half
+ * pairing (for i < d/2 the pair (x_i, x_{i+d/2}) turns by the angle
+ * pos * theta^(-2i/d)), computed in fp64, rounded to fp32 and then to bf16
+ * (nearest even). q (bf16 [n_heads][head_dim], device) is turned in place;
+ * k_new (bf16 [n_kv_heads][head_dim]) is turned into k_cache at position pos
+ * and v_new copied into v_cache there. Caches: bf16
+ * [n_kv_heads][kv_stride][head_dim], device. One launch.
+ *
+ * vbq_attention_decode: for each query head h (kv head g = h / (n_heads /
+ * n_kv_heads)), out[h] = sum_j p_j v_g[j] with p = softmax_j(q_h . k_g[j] /
+ * sqrt(head_dim)) over positions j < T. q bf16 [n_heads][head_dim], out float
+ * [n_heads][head_dim], device. fp32 dot products and sums; each kv head's
+ * positions are split into at most 64 spans (one CTA each, a running softmax
+ * over sub-chunks of 32 positions) that the last CTA of the kv head merges in
+ * span order, so results are deterministic. The library keeps a
+ * per-device scratch for the merge (grown on demand; calls that overlap on
+ * the GPU must not share a device).
+ *
+ * Both: head_dim 64 or 128, n_heads a multiple of n_kv_heads with at most 8
+ * query heads per kv head; 1 <= T <= min(kv_stride, 65536); 0 <= pos <
+ * kv_stride; theta > 1; q (for attention) and the caches 16-byte aligned.
+ * A bad argument returns an
+ * error with nothing launched. Device check code 5: a chunk copy never landed.
+ */
+VBQ_API vbq_status vbq_rope_append(uint16_t* q, const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache,
+                           uint16_t* v_cache, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                           int64_t kv_stride, int32_t pos, double theta, void* stream);
+VBQ_API vbq_status vbq_attention_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int64_t kv_stride,
+                                int32_t T, float* out, void* stream);
+
+/*
  * Reads and clears the device-side check word of the current device. Kernels
  * set it when a bounded wait runs out. Synchronizes the device. Returns
  * VBQ_OK, or VBQ_ERR_DEVICE_CHECK with *code set (code may be NULL).

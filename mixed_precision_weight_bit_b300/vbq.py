@@ -77,6 +77,8 @@ _SIGNATURES = {
     "vbq_model_read_trace": (_ST, [_P, _P, _P]),
     "vbq_dense_gemv_bf16": (_ST, [_P, _P, _P, _I64, _I64, _P]),
     "vbq_dense_gemv_bf16_many": (_ST, [_P, _I32, _P]),
+    "vbq_rope_append": (_ST, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I64, _I32, ctypes.c_double, _P]),
+    "vbq_attention_decode": (_ST, [_P, _P, _P, _I32, _I32, _I32, _I64, _I32, _P, _P]),
     "vbq_device_check": (_ST, [ctypes.POINTER(_I32)]),
     "vbq_launch_count": (_I64, [_I32]),
     "vbq_debug_set": (_ST, [_I32, _I64]),
@@ -249,6 +251,20 @@ def vbq_dense_gemv_bf16_many(jobs, stream=None) -> None:
         arr[i] = VbqDenseJob(_dptr(W), _dptr(x), _dptr(y), int(N), int(K))
     _check("vbq_dense_gemv_bf16_many", _L().vbq_dense_gemv_bf16_many(ctypes.cast(arr, _P), len(jobs),
                                                                      _stream(stream)))
+
+
+def vbq_rope_append(q, k_new, v_new, k_cache, v_cache, n_heads: int, n_kv_heads: int, head_dim: int,
+                    kv_stride: int, pos: int, theta: float = 10000.0, stream=None) -> None:
+    _check("vbq_rope_append", _L().vbq_rope_append(_dptr(q), _dptr(k_new), _dptr(v_new), _dptr(k_cache),
+                                                   _dptr(v_cache), int(n_heads), int(n_kv_heads), int(head_dim),
+                                                   int(kv_stride), int(pos), float(theta), _stream(stream)))
+
+
+def vbq_attention_decode(q, k_cache, v_cache, n_heads: int, n_kv_heads: int, head_dim: int, kv_stride: int,
+                         T: int, out, stream=None) -> None:
+    _check("vbq_attention_decode", _L().vbq_attention_decode(_dptr(q), _dptr(k_cache), _dptr(v_cache), int(n_heads),
+                                                             int(n_kv_heads), int(head_dim), int(kv_stride), int(T),
+                                                             _dptr(out), _stream(stream)))
 
 
 def vbq_device_check() -> int:

@@ -103,3 +103,37 @@ def test_dense_many_validation_without_gpu(lib):
         V.vbq_dense_gemv_bf16_many([(16, 16, 16, 4, 8), (18, 16, 16, 4, 8)])  # W not 16-byte aligned
     assert e.value.status == 1
     assert lib.vbq_dense_gemv_bf16_many(None, 1, None) == 1
+
+
+def test_attention_validation_without_gpu(lib):
+    """Shape and argument checks of the attention calls come before any CUDA call."""
+    from mixed_precision_weight_bit_b300 import vbq as V
+    p = 1 << 20  # a 16-byte aligned stand-in address; nothing is launched
+    bad = [
+        dict(n_heads=32, n_kv_heads=8, head_dim=96, kv_stride=16, T=4),     # head_dim
+        dict(n_heads=30, n_kv_heads=8, head_dim=128, kv_stride=16, T=4),    # H % H_kv
+        dict(n_heads=72, n_kv_heads=8, head_dim=128, kv_stride=16, T=4),    # 9 query heads per kv head
+        dict(n_heads=32, n_kv_heads=8, head_dim=128, kv_stride=16, T=0),    # T
+        dict(n_heads=32, n_kv_heads=8, head_dim=128, kv_stride=16, T=17),   # T > kv_stride
+        dict(n_heads=32, n_kv_heads=8, head_dim=128, kv_stride=70000, T=65537),
+    ]
+    for kw in bad:
+        with pytest.raises(V.VbqError) as e:
+            V.vbq_attention_decode(p, p, p, kw["n_heads"], kw["n_kv_heads"], kw["head_dim"], kw["kv_stride"],
+                                   kw["T"], p)
+        assert e.value.status == 2, kw
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_attention_decode(p, None, p, 32, 8, 128, 16, 4, p)
+    assert e.value.status == 1
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_attention_decode(p, p + 2, p, 32, 8, 128, 16, 4, p)   # cache not 16-byte aligned
+    assert e.value.status == 1
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_rope_append(p, p, p, p, p, 32, 8, 128, 16, 16)         # pos >= kv_stride
+    assert e.value.status == 2
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_rope_append(p, p, p, p, p, 32, 8, 128, 16, 3, theta=1.0)
+    assert e.value.status == 1
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_rope_append(p, p, None, p, p, 32, 8, 128, 16, 3)
+    assert e.value.status == 1
