@@ -59,10 +59,9 @@ struct AttnSmem {
   static constexpr int kS = kAttnBufs * kBuf;                   // float [G][kAttnSub]: scores, then exp
   static constexpr int kW = 0;                                  // the merge's float [G][kAttnMaxParts], over buffer 0
   static_assert(kAttnMaxGroup * kAttnMaxParts * 4 <= kBuf, "merge weights fit over a buffer");
-  static constexpr int kRed = kS + kAttnMaxGroup * kAttnSub * 4;  // float2 [kAttnThreads]: replica sums
-  static constexpr int kStat = kRed + kAttnThreads * 2 * 4;     // float [G][4]: max, sum, rescale, -
-  static constexpr int kQ = kStat + kAttnMaxGroup * 4 * 4;      // bf16 [G][HD]: the group's queries
-  static constexpr int kBar = kQ + kAttnMaxGroup * HD * 2;      // an mbarrier per buffer
+  static constexpr int kRed = kS + kAttnMaxGroup * kAttnSub * 4;  // float2 [G][HD/2]: the replicas' sum
+  static constexpr int kStat = kRed + kAttnMaxGroup * HD * 4;   // float [G][4]: max, sum, rescale, -
+  static constexpr int kBar = kStat + kAttnMaxGroup * 4 * 4;    // an mbarrier per buffer
   static constexpr int kFlag = kBar + 8 * kAttnBufs;
   static constexpr int kBytes = kFlag + 16;
 };
@@ -85,9 +84,9 @@ template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 3) vbq_attn_decode_kernel(const __grid_constant__ AttnArgs a) {
   using L = AttnSmem<HD>;
   constexpr int NQ = HD / 64;             // 16-byte pieces of a row per lane in the score phase
-  constexpr int HP = HD == 128 ? 2 : 4;   // heads per score pass (their queries held in registers)
-  constexpr int UMAX = kAttnMaxGroup * HD / 2 / kAttnThreads;  // units per thread at most
-  static_assert(UMAX <= 2, "two units per thread at most");
+  constexpr int NU = HD / 2;              // output threads per replica: one pair of dims each
+  constexpr int R = kAttnThreads / NU;    // replicas: they split a sub-chunk's positions
+  static_assert(kAttnThreads % NU == 0, "whole replicas");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, sub = lane >> 3, li = lane & 7;
   const int c = blockIdx.x, g = blockIdx.y, G = a.G;
   const int p0 = c * a.span, p1 = min(a.T, p0 + a.span);
@@ -119,15 +118,30 @@ __global__ void __launch_bounds__(kAttnThreads, 3) vbq_attn_decode_kernel(const 
     stat[4 * tid] = -INFINITY;
     stat[4 * tid + 1] = 0.0f;
   }
-  for (int i = tid; i < G * HD / 8; i += kAttnThreads)  // the group's queries, 16 bytes at a time
-    reinterpret_cast<uint4*>(attn_smem + L::kQ)[i] = reinterpret_cast<const uint4*>(a.q + g * G * HD)[i];
-  // Output units u = (head, pair of dims); R replicas split the positions when
-  // there are fewer units than threads.
-  const int units = G * (HD / 2);
-  const int R = units >= kAttnThreads ? 1 : kAttnThreads / units;
-  float2 acc[UMAX];
+  // Score work: warp w takes head hw = w / wph of the group (wph = 8 / G warps
+  // per head) and positions wi * 4 + sub, + 4 wph, ... (wi = w % wph), 8 lanes
+  // per position. Its head's query stays in registers, as fp32: lane li holds
+  // dims [8 li, 8 li + 8) and, for d = 128, [64 + 8 li, ...).
+  const int wph = (kAttnThreads / 32) / G, hw = warp / wph, wi = warp - hw * wph;
+  const bool scorer = hw < G;
+  float qv[NQ * 8];
 #pragma unroll
-  for (int k = 0; k < UMAX; ++k) acc[k] = make_float2(0.0f, 0.0f);
+  for (int n = 0; n < NQ; ++n) {
+    const uint4 w = scorer ? *reinterpret_cast<const uint4*>(a.q + (g * G + hw) * HD + 64 * n + 8 * li)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qv[8 * n + 2 * e] = __uint_as_float(ww[e] << 16);
+      qv[8 * n + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+    }
+  }
+  // Output: thread (r, dp) keeps, for every head of the group, the running
+  // p-weighted sum of v's dims 2 dp, 2 dp + 1 over positions r, r + R, ...
+  const int dp = tid % NU, rr = tid / NU;
+  float2 acc[kAttnMaxGroup];
+#pragma unroll
+  for (int h = 0; h < kAttnMaxGroup; ++h) acc[h] = make_float2(0.0f, 0.0f);
   __syncthreads();  // the barriers and the running statistics
 
   bool ok = true;
@@ -144,51 +158,29 @@ __global__ void __launch_bounds__(kAttnThreads, 3) vbq_attn_decode_kernel(const 
     const uint8_t* Kb = attn_smem + (t % kAttnBufs) * L::kBuf;
     const uint32_t* V32 = reinterpret_cast<const uint32_t*>(Kb + kAttnSub * HD * 2);
     const int np = min(kAttnSub, p1 - (p0 + t * kAttnSub));
-    // Scores: 8 lanes per position, 4 positions per warp at a time. Lane li of
-    // a position holds dims [8 li, 8 li + 8) and, for d = 128, [64 + 8 li, ...),
-    // so each 16-byte shared load of a row is conflict-free; a 3-step
-    // butterfly sums a position's 8 lanes.
-    for (int h0 = 0; h0 < G; h0 += HP) {
-      float qv[HP][NQ * 8];
-#pragma unroll
-      for (int hh = 0; hh < HP; ++hh)
-#pragma unroll
-        for (int n = 0; n < NQ; ++n) {
-          const int h = h0 + hh;
-          const uint4 w = h < G ? *reinterpret_cast<const uint4*>(attn_smem + L::kQ + (h * HD + 64 * n + 8 * li) * 2)
-                                : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            qv[hh][8 * n + 2 * e] = __uint_as_float(ww[e] << 16);
-            qv[hh][8 * n + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
-          }
-        }
-      for (int base = warp * 4; base < np; base += kAttnThreads / 8) {
+    // Scores: 8 lanes per position; each 16-byte shared load of a row is
+    // conflict-free; two FMA chains, then a 3-step butterfly over the 8 lanes.
+    if (scorer) {
+      for (int base = wi * 4; base < np; base += 4 * wph) {
         const int j = base + sub;
         const bool valid = j < np;
         const uint8_t* row = Kb + (valid ? j : 0) * HD * 2;
-        float kx[NQ * 8];
+        float d0 = 0.0f, d1 = 0.0f;
 #pragma unroll
         for (int n = 0; n < NQ; ++n) {
           const uint4 w = *reinterpret_cast<const uint4*>(row + 128 * n + 16 * li);
           const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            kx[8 * n + 2 * e] = __uint_as_float(ww[e] << 16);
-            kx[8 * n + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+            d0 = fmaf(qv[8 * n + 2 * e], __uint_as_float(ww[e] << 16), d0);
+            d1 = fmaf(qv[8 * n + 2 * e + 1], __uint_as_float(ww[e] & 0xFFFF0000u), d1);
           }
         }
-#pragma unroll
-        for (int hh = 0; hh < HP; ++hh) {
-          float d = 0.0f;
-#pragma unroll
-          for (int i = 0; i < NQ * 8; ++i) d = fmaf(qv[hh][i], kx[i], d);
-          d += __shfl_xor_sync(0xffffffffu, d, 4);
-          d += __shfl_xor_sync(0xffffffffu, d, 2);
-          d += __shfl_xor_sync(0xffffffffu, d, 1);
-          if (li == 0 && valid && h0 + hh < G) S[(h0 + hh) * kAttnSub + j] = d * a.scale;
-        }
+        float d = d0 + d1;
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        if (li == 0 && valid) S[hw * kAttnSub + j] = d * a.scale;
       }
     }
     __syncthreads();
@@ -213,21 +205,27 @@ __global__ void __launch_bounds__(kAttnThreads, 3) vbq_attn_decode_kernel(const 
       }
     }
     __syncthreads();
-    // p-weighted sums of v, the old ones rescaled.
+    // p-weighted sums of v, the old ones rescaled; v converted once for all heads.
+    {
+      float al[kAttnMaxGroup];
 #pragma unroll
-    for (int k = 0; k < UMAX; ++k) {
-      const int w = tid + k * kAttnThreads;
-      if (w >= units * R) continue;
-      const int r = w / units, u = w - r * units, h = u / (HD / 2), dp = u - h * (HD / 2);
-      const float alpha = stat[4 * h + 2];
-      float2 s2 = make_float2(acc[k].x * alpha, acc[k].y * alpha);
-      for (int j = r; j < np; j += R) {
-        const float p = S[h * kAttnSub + j];
-        const uint32_t vv = V32[j * (HD / 2) + dp];
-        s2.x = fmaf(p, __uint_as_float(vv << 16), s2.x);
-        s2.y = fmaf(p, __uint_as_float(vv & 0xFFFF0000u), s2.y);
+      for (int h = 0; h < kAttnMaxGroup; ++h) al[h] = h < G ? stat[4 * h + 2] : 0.0f;
+#pragma unroll
+      for (int h = 0; h < kAttnMaxGroup; ++h) {
+        acc[h].x *= al[h];
+        acc[h].y *= al[h];
       }
-      acc[k] = s2;
+      for (int j = rr; j < np; j += R) {
+        const uint32_t vv = V32[j * (HD / 2) + dp];
+        const float vx = __uint_as_float(vv << 16), vy = __uint_as_float(vv & 0xFFFF0000u);
+#pragma unroll
+        for (int h = 0; h < kAttnMaxGroup; ++h) {
+          if (h >= G) break;
+          const float p = S[h * kAttnSub + j];
+          acc[h].x = fmaf(p, vx, acc[h].x);
+          acc[h].y = fmaf(p, vy, acc[h].y);
+        }
+      }
     }
     __syncthreads();  // buffer t % kAttnBufs is free for sub-chunk t + kAttnBufs; S and the rescales for the next step
   }
@@ -235,36 +233,36 @@ __global__ void __launch_bounds__(kAttnThreads, 3) vbq_attn_decode_kernel(const 
     if (tid == 0) atomicExch(a.err, kErrAttnCopyTimeout);
     return;  // the barrier wait gave up everywhere at once (__syncthreads_and)
   }
-  if (R > 1) {
-    red[tid] = acc[0];
+  // The replicas' sums, added in replica order into red[h][dp].
+  for (int r = 0; r < R; ++r) {
+    if (rr == r)
+#pragma unroll
+      for (int h = 0; h < kAttnMaxGroup; ++h) {
+        if (h >= G) break;
+        float2 o = acc[h];
+        if (r > 0) {
+          const float2 t2 = red[h * NU + dp];
+          o = make_float2(t2.x + o.x, t2.y + o.y);
+        }
+        red[h * NU + dp] = o;
+      }
     __syncthreads();
   }
-  // This CTA's span result for (h, pair dp), by the threads tid < units.
+  // This CTA's span result for (h, pair dp).
   float* part = a.part + (static_cast<size_t>(g) * a.nparts + c) * kAttnMaxGroup * part_stride(HD);
   const bool single = a.nparts == 1;
-#pragma unroll
-  for (int k = 0; k < UMAX; ++k) {
-    const int u = tid + k * kAttnThreads;
-    if (u >= units) continue;
-    float2 o = acc[k];
-    if (R > 1) {
-      o = make_float2(0.0f, 0.0f);
-      for (int r = 0; r < R; ++r) {
-        const float2 t2 = red[r * units + u];
-        o.x += t2.x;
-        o.y += t2.y;
-      }
-    }
-    const int h = u / (HD / 2), dp = u - h * (HD / 2);
+  for (int u = tid; u < G * NU; u += kAttnThreads) {
+    const int h = u / NU, d2 = u - h * NU;
+    const float2 o = red[u];
     if (single) {
       const float inv = 1.0f / stat[4 * h + 1];
-      a.out[(g * G + h) * HD + 2 * dp] = o.x * inv;
-      a.out[(g * G + h) * HD + 2 * dp + 1] = o.y * inv;
+      a.out[(g * G + h) * HD + 2 * d2] = o.x * inv;
+      a.out[(g * G + h) * HD + 2 * d2 + 1] = o.y * inv;
     } else {
       float* ph = part + h * part_stride(HD);
-      ph[4 + 2 * dp] = o.x;
-      ph[4 + 2 * dp + 1] = o.y;
-      if (dp == 0) {
+      ph[4 + 2 * d2] = o.x;
+      ph[4 + 2 * d2 + 1] = o.y;
+      if (d2 == 0) {
         ph[0] = stat[4 * h];
         ph[1] = stat[4 * h + 1];
       }
