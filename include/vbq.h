@@ -281,7 +281,7 @@ VBQ_API vbq_status vbq_dense_gemv_bf16_many(const vbq_dense_job* jobs, int32_t n
  * sqrt(head_dim)) over positions j < T. q bf16 [n_heads][head_dim], out float
  * [n_heads][head_dim], device. fp32 dot products and sums; each kv head's
  * positions are split into at most 64 spans (one CTA each, a running softmax
- * over sub-chunks of 32 positions) that the last CTA of the kv head merges in
+ * over sub-chunks of 64 positions) that the last CTA of the kv head merges in
  * span order, so results are deterministic. The library keeps a
  * per-device scratch for the merge (grown on demand; calls that overlap on
  * the GPU must not share a device).

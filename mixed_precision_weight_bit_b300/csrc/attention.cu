@@ -13,13 +13,15 @@
 //
 // Work split (split-KV decoding): each kv head's positions are cut into at
 // most kAttnMaxParts contiguous spans, one CTA per (span, kv head), about three
-// CTAs per SM in all. A CTA streams its span through kAttnBufs shared-memory
-// buffers of kAttnSub positions (bulk copies of K and V, up to three
-// sub-chunks in flight while one is used) and keeps, for each head of the
-// group, a running softmax: the max score so far, the sum of exp, and the
+// CTAs per SM in all (what their shared memory allows; more CTAs per SM, with
+// smaller or more buffers, measured slower). A CTA streams its span through
+// kAttnBufs shared-memory buffers of kAttnSub positions (bulk copies of K and
+// V, the next sub-chunk landing while one is used) and keeps, for each head of
+// the group, a running softmax: the max score so far, the sum of exp, and the
 // p-weighted sum of v, rescaled when the max grows. The last CTA of a kv head
 // to finish (an atomic counter) merges the spans in span order, so results do
-// not depend on timing. The cache is read once: the kernel is bound by HBM.
+// not depend on timing. The cache is read from HBM once; what paces a CTA is
+// its per-sub-chunk work (scores, softmax, weighted sums) between barriers.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -33,8 +35,8 @@ namespace vbq {
 namespace {
 
 constexpr int kAttnThreads = 256;
-constexpr int kAttnSub = 32;            // positions per sub-chunk (one buffer)
-constexpr int kAttnBufs = 4;            // buffers: up to three sub-chunks in flight while one is used
+constexpr int kAttnSub = 64;            // positions per sub-chunk (one buffer)
+constexpr int kAttnBufs = 2;            // buffers: the next sub-chunk lands while one is used
 constexpr int kAttnMaxGroup = 8;        // query heads per kv head
 constexpr int kAttnMaxT = 65536;        // positions
 constexpr int kAttnMaxParts = 64;       // spans per kv head

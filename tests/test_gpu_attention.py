@@ -33,7 +33,7 @@ def _u16(t):
 
 def attention_bound(q_bits, k_bits, v_bits, T, p):
     """Per-element bound for fp32 scores (d-term sums), expf, the running sums over
-    sub-chunks of 32 positions (a rescale per sub-chunk) and the merge of at most
+    sub-chunks of 64 positions (a rescale per sub-chunk) and the merge of at most
     64 spans: twice the largest score error, plus the rounding of the weighted
     sums, times sum_j p_j |v_j|."""
     q = bf16_bits_to_f64(q_bits)
@@ -41,7 +41,7 @@ def attention_bound(q_bits, k_bits, v_bits, T, p):
     Vv = np.abs(bf16_bits_to_f64(v_bits)[:, :T, :])
     H, d = q.shape
     group = H // K.shape[0]
-    steps = (T + 31) // 32 + 64
+    steps = (T + 63) // 64 + 64
     out = np.zeros((H, d))
     for h in range(H):
         g = h // group
