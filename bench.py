@@ -321,6 +321,39 @@ def decode_kernel_roofline(V, pm, x, logits, stream, peak_gbs, ms_step, steps, w
                     "unless captured on this build)"}
 
 
+def context_step(V, pm, shape, x, logits, stream, peak_gbs, ctx, steps=10):
+    """The decode step at position ctx - 1 (vbq_decode_step_at): every layer's rotary append and
+    attention over ctx cached positions (seeded bf16 keys and values) between the projections."""
+    import torch
+    from cuda.bindings import runtime as rt
+    V.vbq_model_set_context(pm.model.handle, ctx)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    for layer in range(shape.n_layers):
+        kp, vp, stride = V.vbq_model_kv_cache(pm.model.handle, layer)
+        for ptr in (kp, vp):
+            t = torch.randn(shape.n_kv_heads, stride, shape.head_dim, device="cuda", generator=g).to(torch.bfloat16)
+            (err,) = rt.cudaMemcpy(ptr, t.data_ptr(), t.numel() * 2, rt.cudaMemcpyKind.cudaMemcpyDeviceToDevice)
+            assert int(err) == 0
+    torch.cuda.synchronize()
+
+    def step():
+        V.vbq_decode_step_at(pm.model.handle, x, ctx - 1, logits, stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_steps(step, steps, 3, stream, 1)
+    assert V.vbq_device_check() == 0
+    kv_bytes = 2.0 * shape.n_layers * shape.n_kv_heads * ctx * shape.head_dim * 2
+    V.vbq_model_set_context(pm.model.handle, 0)
+    return {"us": round(ms * 1e3, 1), "context": ctx, "kv_bytes": kv_bytes,
+            "GB/s": round((pm.alg_bytes + kv_bytes) / (ms * 1e-3) / 1e9, 1),
+            "frac": round((pm.alg_bytes + kv_bytes) / (ms * 1e-3) / 1e9 / peak_gbs, 4),
+            "launches_per_step": 3 * shape.n_layers + 1,
+            "note": "vbq_decode_step_at at position ctx - 1: n_layers + 1 decode-kernel launches with each "
+                    "layer's rotary append and attention between them; bytes = the step's algorithmic bytes + "
+                    "the K and V caches read"}
+
+
 def standalone_gemv(V, pm, stream, peak_gbs, reps=3):
     """Each projection as its own vbq_gemv launch, bracketed by events on the launching stream."""
     import torch
@@ -704,7 +737,8 @@ def run_vbq(args, ws, rank, local):
     extra = {"decode_step_us" + w: round(ms * 1e3, 1), "pack_seconds" + w: round(pack_s, 1),
              "weights" + w: pm.weights, "alg_bytes_per_step" + w: round(pm.alg_bytes),
              "device_bytes" + w: pm.total_bytes, "code_bytes" + w: pm.code_bytes,
-             "standalone_gemv" + w: standalone}
+             "standalone_gemv" + w: standalone,
+             "decode_step_ctx4096" + w: context_step(V, pm, shape, x, logits, stream, peak, 4096)}
     pm.close()
     torch.cuda.empty_cache()
 

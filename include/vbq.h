@@ -220,6 +220,40 @@ VBQ_API vbq_status vbq_decode_step(vbq_model* model, const uint16_t* x_dev, floa
 VBQ_API vbq_status vbq_decode_step_host(vbq_model* model, const uint16_t* x_host, float* logits_host, void* stream);
 
 /*
+ * The decode step at a position above 0 ("autoregressive decode", VBQ
+ * abstract): the same projections and glue as vbq_decode_step, with each
+ * layer's attention over a bf16 KV cache in place of the position-0 shortcut.
+ * Per layer, q, k and v (the [q;k;v] projection's outputs, rounded to bf16)
+ * are turned by the rotary embedding at pos (as vbq_rope_append: rotate-half
+ * pairing, theta^(-2i/d), fp64 rounded to fp32 then bf16); k and v are written
+ * to the layer's cache at pos; each query head attends over positions
+ * 0 .. pos of its kv head (as vbq_attention_decode); and o reads the result,
+ * rounded to bf16. At pos = 0 the logits equal vbq_decode_step's bit for bit.
+ *
+ * vbq_model_set_context: allocates the caches of every layer for max_context
+ * positions (bf16 [n_kv_heads][max_context][head_dim] per layer for K and for
+ * V, zeroed) and the programs of the segmented step; 0 frees them. theta is
+ * the rotary base (10000 in the usual models). Needs head_dim 64 or 128 and at
+ * most 8 query heads per kv head; max_context <= 65536. Synchronizes the
+ * device.
+ * vbq_model_kv_cache: the device addresses of layer's K and V caches (owned by
+ * the model) and their position stride (max_context), for a caller that fills
+ * or reads them.
+ * vbq_decode_step_at: x_dev bf16 [d] and logits_dev float [vocab] as in
+ * vbq_decode_step; 0 <= pos < max_context; positions below pos must already
+ * hold the caller's keys and values. The step runs as n_layers + 1 launches of
+ * the decode kernel (cut after each layer's [q;k;v]) with each layer's
+ * attention between them; the trace, when enabled, covers it as it covers
+ * vbq_decode_step. Errors as vbq_decode_step, and VBQ_ERR_INVALID_ARG without
+ * a context.
+ */
+VBQ_API vbq_status vbq_model_set_context(vbq_model* model, int32_t max_context, double rope_theta);
+VBQ_API vbq_status vbq_model_kv_cache(const vbq_model* model, int32_t layer, uint16_t** k_cache, uint16_t** v_cache,
+                              int64_t* stride);
+VBQ_API vbq_status vbq_decode_step_at(vbq_model* model, const uint16_t* x_dev, int32_t pos, float* logits_dev,
+                              void* stream);
+
+/*
  * Teacher-forcing trace. When enabled, each step also records, for every
  * projection p (layer-major, q..down per layer, then the head), the bf16
  * input it consumed and its fp32 output. vbq_model_trace_info gives the

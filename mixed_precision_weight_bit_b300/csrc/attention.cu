@@ -340,6 +340,37 @@ __global__ void vbq_rope_append_kernel(uint16_t* __restrict__ q, const uint16_t*
   }
 }
 
+// The decode step's attention input (vbq_decode_step_at): q, k and v from a
+// [q;k;v] item's float output (rows q_off.., k_off.., v_off..), each rounded to
+// bf16 (nearest even) as the cache stores them; then block b < H turns q head
+// b into q_rot, and block H + g turns k head g into the cache at pos and
+// stores v head g there (the rotation of vbq_rope_append).
+__global__ void vbq_attn_prep_kernel(const float* __restrict__ qkv, int64_t q_off, int64_t k_off, int64_t v_off,
+                                     uint16_t* __restrict__ q_rot, uint16_t* __restrict__ k_cache,
+                                     uint16_t* __restrict__ v_cache, int32_t H, int32_t d, int64_t stride, int32_t pos,
+                                     double theta) {
+  const int b = blockIdx.x, i = threadIdx.x, half = d / 2;
+  if (i >= half) return;
+  const double inv_freq = pow(theta, -2.0 * i / d);
+  double s, c;
+  sincos(static_cast<double>(pos) * inv_freq, &s, &c);
+  auto bf = [](float v) { return __float2bfloat16_rn(v); };
+  auto turn = [&](const float* src, uint16_t* dst) {
+    const double x0 = __bfloat162float(bf(src[i])), x1 = __bfloat162float(bf(src[i + half]));
+    dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(__double2float_rn(x0 * c - x1 * s)));
+    dst[i + half] = __bfloat16_as_ushort(__float2bfloat16_rn(__double2float_rn(x0 * s + x1 * c)));
+  };
+  if (b < H) {
+    turn(qkv + q_off + static_cast<int64_t>(b) * d, q_rot + static_cast<size_t>(b) * d);
+  } else {
+    const int g = b - H;
+    const size_t at = (static_cast<size_t>(g) * stride + pos) * d;
+    turn(qkv + k_off + static_cast<int64_t>(g) * d, k_cache + at);
+    v_cache[at + i] = __bfloat16_as_ushort(bf(qkv[v_off + static_cast<int64_t>(g) * d + i]));
+    v_cache[at + i + half] = __bfloat16_as_ushort(bf(qkv[v_off + static_cast<int64_t>(g) * d + i + half]));
+  }
+}
+
 // Per-device scratch of the attention merge: partial results and counters.
 struct AttnScratch {
   float* part = nullptr;
@@ -414,6 +445,16 @@ vbq_status launch_attn(const AttnArgs& a, int32_t Hkv, cudaStream_t st) {
 }
 
 }  // namespace
+
+vbq_status launch_attn_prep(const float* qkv, int64_t q_off, int64_t k_off, int64_t v_off, uint16_t* q_rot,
+                            uint16_t* k_cache, uint16_t* v_cache, int32_t H, int32_t Hkv, int32_t d, int64_t stride,
+                            int32_t pos, double theta, cudaStream_t st) {
+  note_launches(1);
+  vbq_attn_prep_kernel<<<H + Hkv, d / 2, 0, st>>>(qkv, q_off, k_off, v_off, q_rot, k_cache, v_cache, H, d, stride,
+                                                  pos, theta);
+  VBQ_CUDA_TRY(cudaGetLastError());
+  return VBQ_OK;
+}
 
 }  // namespace vbq
 

@@ -70,6 +70,13 @@ const GpuInfo& gpu_info();
 cudaError_t dev_alloc(void** p, size_t bytes);
 void set_alloc_cap(int64_t bytes);
 
+// The decode step's attention input: rounds q, k, v of a [q;k;v] item's float
+// output to bf16, turns q (into q_rot) and k (into the cache at pos) by the
+// rotary embedding, and stores v at pos (attention.cu).
+vbq_status launch_attn_prep(const float* qkv, int64_t q_off, int64_t k_off, int64_t v_off, uint16_t* q_rot,
+                            uint16_t* k_cache, uint16_t* v_cache, int32_t H, int32_t Hkv, int32_t d, int64_t stride,
+                            int32_t pos, double theta, cudaStream_t st);
+
 // Tensor-core dequant-MMA for 2..64 batch columns (gemm_tc.cu).
 bool tc_eligible(const vbq_matrix* m);
 vbq_status launch_gemm_tc(const vbq_matrix* m, const uint16_t* X, int32_t B, float* Y, cudaStream_t st);

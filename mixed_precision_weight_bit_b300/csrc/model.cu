@@ -54,7 +54,6 @@ int64_t n_super_of(int64_t n) { return (n + SROWS - 1) / SROWS; }
 uint32_t decode_smem_bytes() { return smem_layout(kRingSlots).total + 2 * kItemSmem; }
 static_assert(smem_layout(kRingSlots).total + 2 * kItemSmem <= 232448, "shared memory of the decode kernel");
 
-int64_t r8(int64_t n) { return (n + 7) & ~int64_t(7); }
 
 // Scratch of one item, in 8-byte words from the scratch base: 64-bit sums,
 // float outputs (none for the head, which writes the logits), and the
@@ -129,6 +128,23 @@ struct vbq_model {
   DItem* items_static = nullptr;     // items over the static scratch (null if the model does not fit it)
   uint64_t* static_base = nullptr;
   int* err = nullptr;
+  // Host copies kept for the context step: each warp's pieces of every item in
+  // step order, and per item each warp's piece count once that item is in.
+  std::vector<std::vector<uint64_t>> per_warp;
+  std::vector<std::vector<uint32_t>> marks;
+  // Context steps (vbq_model_set_context): the KV caches, the rotated query,
+  // the attention output, and the programs of the segmented launches.
+  int32_t max_ctx = 0;
+  double rope_theta = 10000.0;
+  uint16_t* kv = nullptr;            // bf16 [n_layers][2][n_kv_heads][max_ctx][head_dim]
+  uint16_t* q_rot = nullptr;         // bf16 [n_heads * head_dim]
+  float* attn_out = nullptr;         // [n_heads * head_dim]
+  void* ctx_mem = nullptr;
+  DItem* items_ctx = nullptr;        // items over ws, the o items reading attn_out
+  const uint64_t* seg_pieces = nullptr;
+  const uint32_t* seg_start = nullptr;  // [n_seg][n_warps + 1]
+  const uint32_t* seg_bytes = nullptr;  // [n_seg][n_warps]
+  std::vector<int32_t> seg_item0;    // first item of each segment, then n_items
 };
 
 namespace {
@@ -154,7 +170,7 @@ uint32_t next_epoch() {
 }
 
 // The items of one step over the scratch at base.
-std::vector<DItem> make_items(const vbq_model* m, uint64_t* base, bool trace) {
+std::vector<DItem> make_items(const vbq_model* m, uint64_t* base, bool trace, bool ctx = false) {
   const vbq_model_desc& d = m->desc;
   const Layout& L = m->lay;
   auto words = [&](int64_t off) { return base + off; };
@@ -222,6 +238,16 @@ std::vector<DItem> make_items(const vbq_model* m, uint64_t* base, bool trace) {
       it.v_st1 = static_cast<int32_t>(so[2] + n_super_of(proj_n(d, P_V)));
       it.head_dim = d.head_dim;
       it.group = d.n_heads / d.n_kv_heads;
+      if (ctx) {
+        // The context step: o reads the attention output, [n_heads][head_dim] in
+        // order, which a launch before this one completed (no flags to wait on).
+        // Each element is a convex combination of v's, so the bound through v
+        // (rs, l1_src) still holds.
+        it.src = m->attn_out;
+        it.v_off = 0;
+        it.v_st0 = it.v_st1 = 0;
+        it.group = 1;
+      }
       it.trace_x = tin(p0 + P_O);
       it.trace_y[0] = tout(p0 + P_O);
       it.trace_n[0] = d.d;
@@ -278,24 +304,28 @@ std::atomic<long long> g_spin_limit{kSpinCycles};
 std::atomic<int> g_never_ready{0};
 std::atomic<int64_t> g_noalloc_words{0};
 
-cudaError_t launch_decode(const vbq_model* m, const DItem* items, uint64_t* base, const uint16_t* x, float* out,
-                          cudaStream_t st, int* err) {
+// Items [i0, i1) of a step in one launch. pieces/pstart/pbytes: the warps'
+// piece lists of exactly those items; the step input is converted only by the
+// launch that starts at item 0; every launch of a step shares its epoch.
+cudaError_t launch_decode_range(const vbq_model* m, const DItem* items, int32_t i0, int32_t i1, const uint64_t* pieces,
+                                const uint32_t* pstart, const uint32_t* pbytes, uint32_t epoch, uint64_t* base,
+                                const uint16_t* x, float* out, cudaStream_t st, int* err) {
   const Layout& L = m->lay;
   DecodeArgs a{};
-  a.items = items;
-  a.ctas = m->ctas;
-  a.warps = m->warps;
-  a.n_items = m->n_items;
-  a.pieces = m->pieces;
-  a.pstart = m->pstart;
-  a.pbytes = m->pbytes;
+  a.items = items + i0;
+  a.ctas = m->ctas + static_cast<size_t>(i0) * m->sms;
+  a.warps = m->warps + static_cast<size_t>(i0) * m->sms * KW;
+  a.n_items = i1 - i0;
+  a.pieces = pieces;
+  a.pstart = pstart;
+  a.pbytes = pbytes;
   a.x = x;
-  a.d = m->desc.d;
+  a.d = i0 == 0 ? m->desc.d : 0;
   a.h0 = reinterpret_cast<float*>(base + L.h0);
   a.h0_stats = reinterpret_cast<float2*>(base + L.h0_stats);
   a.h0_flag = reinterpret_cast<uint32_t*>(base + L.h0_flag);
   a.logits = out;
-  a.epoch = next_epoch();
+  a.epoch = epoch;
   a.wait_epoch = g_never_ready.load() ? (a.epoch | 0x80000000u) : a.epoch;
   a.spin_limit = g_spin_limit.load();
   a.ns = kRingSlots;
@@ -312,6 +342,12 @@ cudaError_t launch_decode(const vbq_model* m, const DItem* items, uint64_t* base
   cfg.numAttrs = 1;
   note_launches(1);
   return cudaLaunchKernelEx(&cfg, vbq_decode_kernel, a);
+}
+
+cudaError_t launch_decode(const vbq_model* m, const DItem* items, uint64_t* base, const uint16_t* x, float* out,
+                          cudaStream_t st, int* err) {
+  return launch_decode_range(m, items, 0, m->n_items, m->pieces, m->pstart, m->pbytes, next_epoch(), base, x, out, st,
+                             err);
 }
 
 void prepare_decode_kernel() {
@@ -409,6 +445,9 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
     if (!append_pieces(pl, segs, &per_warp))
       return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_create: weight address beyond 2^48");
     per_warp.resize(static_cast<size_t>(m->sms) * KW);
+    std::vector<uint32_t> mk(per_warp.size());
+    for (size_t w = 0; w < per_warp.size(); ++w) mk[w] = static_cast<uint32_t>(per_warp[w].size());
+    m->marks.push_back(std::move(mk));
     all_warps.insert(all_warps.end(), pl.warps.begin(), pl.warps.end());
     all_ctas.insert(all_ctas.end(), pl.ctas.begin(), pl.ctas.end());
     m->item_st_off.push_back(pl.st_off);
@@ -490,6 +529,7 @@ extern "C" vbq_status vbq_model_create(const vbq_model_desc* desc, const vbq_mat
     return cuda_fail(e, "vbq_model_create: items");
   }
   prepare_decode_kernel();
+  m->per_warp = std::move(per_warp);
   *out = m;
   return VBQ_OK;
 }
@@ -504,6 +544,8 @@ extern "C" void vbq_model_free(vbq_model* m) {
   cudaFree(m->prog_mem);
   cudaFree(m->tr_in);
   cudaFree(m->tr_out);
+  cudaFree(m->kv);
+  cudaFree(m->ctx_mem);
   cudaSetDevice(cur);
   delete m;
 }
@@ -546,6 +588,7 @@ extern "C" vbq_status vbq_model_set_trace(vbq_model* m, int32_t enable) {
   m->trace = enable != 0;
   VBQ_CUDA_TRY(cudaDeviceSynchronize());  // no step may be reading the items
   VBQ_CUDA_TRY(upload_items(make_items(m, m->ws, m->trace), m->items_ws));
+  if (m->items_ctx) VBQ_CUDA_TRY(upload_items(make_items(m, m->ws, m->trace, true), m->items_ctx));
   return VBQ_OK;
 }
 
@@ -573,6 +616,156 @@ extern "C" vbq_status vbq_model_read_trace(const vbq_model* m, uint16_t* in_host
 
 // ---------------------------------------------------------------- allocation-free decode step
 //
+// ---- context steps -----------------------------------------------------------
+//
+// vbq_decode_step_at runs the same items as vbq_decode_step, cut after each
+// layer's [q;k;v] item into n_layers + 1 launches; between them, one layer's
+// attention: its q and new k turned by the rotary embedding at pos and k, v
+// appended to the layer's cache (vbq_attn_prep_kernel), then attention of the
+// query heads over positions 0 .. pos (vbq_attention_decode) into attn_out,
+// which the layer's o item reads. Every launch of a step shares its epoch; a
+// launch's flags are all set when the next launch starts.
+
+extern "C" vbq_status vbq_model_set_context(vbq_model* m, int32_t max_context, double rope_theta) {
+  if (!m) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_set_context: NULL model");
+  const vbq_model_desc& d = m->desc;
+  if (max_context < 0 || max_context > 65536)
+    return fail(VBQ_ERR_SHAPE, "vbq_model_set_context: max_context must be in [0, 65536]");
+  if (max_context > 0 && (d.head_dim != 64 && d.head_dim != 128))
+    return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_set_context: head_dim must be 64 or 128");
+  if (max_context > 0 && d.n_heads / d.n_kv_heads > 8)
+    return fail(VBQ_ERR_UNSUPPORTED, "vbq_model_set_context: at most 8 query heads per kv head");
+  if (max_context > 0 && !(rope_theta > 1.0)) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_set_context: theta must be > 1");
+  int cur = 0;
+  VBQ_CUDA_TRY(cudaGetDevice(&cur));
+  if (cur != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_set_context: model is on another device");
+  VBQ_CUDA_TRY(cudaDeviceSynchronize());  // no step may be using what is freed
+  cudaFree(m->kv);
+  cudaFree(m->ctx_mem);
+  m->kv = nullptr;
+  m->ctx_mem = nullptr;
+  m->q_rot = nullptr;
+  m->attn_out = nullptr;
+  m->items_ctx = nullptr;
+  m->max_ctx = 0;
+  m->seg_item0.clear();
+  if (max_context == 0) return VBQ_OK;
+
+  // Segments: items [seg_item0[s], seg_item0[s + 1]), cut after every [q;k;v] item.
+  std::vector<int32_t> b{0};
+  for (int l = 0; l < d.n_layers; ++l) b.push_back(l * L_PER_LAYER + L_QKV + 1);
+  b.push_back(m->n_items);
+  const size_t n_seg = b.size() - 1, nw = m->per_warp.size();
+  // Each segment's piece lists, warp after warp.
+  std::vector<uint64_t> pieces;
+  std::vector<uint32_t> start, bytes;
+  for (size_t sg = 0; sg < n_seg; ++sg) {
+    for (size_t w = 0; w < nw; ++w) {
+      const uint32_t p0 = b[sg] == 0 ? 0u : m->marks[b[sg] - 1][w];
+      const uint32_t p1 = m->marks[b[sg + 1] - 1][w];
+      start.push_back(static_cast<uint32_t>(pieces.size()));
+      uint64_t by = 0;
+      for (uint32_t p = p0; p < p1; ++p) {
+        pieces.push_back(m->per_warp[w][p]);
+        by += (m->per_warp[w][p] & 0xFFFFFu) << 4;
+      }
+      bytes.push_back(static_cast<uint32_t>(by));
+    }
+    start.push_back(static_cast<uint32_t>(pieces.size()));
+  }
+  const int64_t hd = int64_t(d.n_heads) * d.head_dim;
+  const size_t kv_elems = size_t(d.n_layers) * 2 * d.n_kv_heads * size_t(max_context) * d.head_dim;
+  auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
+  const size_t o_q = 0, o_a = o_q + al(2 * hd), o_i = o_a + al(4 * hd);
+  const size_t o_p = o_i + al(sizeof(DItem) * m->n_items);
+  const size_t o_s = o_p + al(8 * std::max<size_t>(1, pieces.size()));
+  const size_t o_b = o_s + al(4 * start.size());
+  const size_t total = o_b + al(4 * bytes.size());
+  cudaError_t e = dev_alloc(reinterpret_cast<void**>(&m->kv), std::max<size_t>(2, 2 * kv_elems));
+  if (e == cudaSuccess) e = cudaMemset(m->kv, 0, std::max<size_t>(2, 2 * kv_elems));
+  if (e == cudaSuccess) e = dev_alloc(&m->ctx_mem, total);
+  char* cm = static_cast<char*>(m->ctx_mem);
+  if (e == cudaSuccess && !pieces.empty()) e = cudaMemcpy(cm + o_p, pieces.data(), 8 * pieces.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(cm + o_s, start.data(), 4 * start.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !bytes.empty()) e = cudaMemcpy(cm + o_b, bytes.data(), 4 * bytes.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) {
+    m->q_rot = reinterpret_cast<uint16_t*>(cm + o_q);
+    m->attn_out = reinterpret_cast<float*>(cm + o_a);
+    m->items_ctx = reinterpret_cast<DItem*>(cm + o_i);
+    m->seg_pieces = reinterpret_cast<const uint64_t*>(cm + o_p);
+    m->seg_start = reinterpret_cast<const uint32_t*>(cm + o_s);
+    m->seg_bytes = reinterpret_cast<const uint32_t*>(cm + o_b);
+    e = upload_items(make_items(m, m->ws, m->trace, true), m->items_ctx);
+  }
+  if (e != cudaSuccess) {
+    cudaFree(m->kv);
+    cudaFree(m->ctx_mem);
+    m->kv = nullptr;
+    m->ctx_mem = nullptr;
+    m->items_ctx = nullptr;
+    return cuda_fail(e, "vbq_model_set_context");
+  }
+  m->max_ctx = max_context;
+  m->rope_theta = rope_theta;
+  m->seg_item0 = b;
+  return VBQ_OK;
+}
+
+extern "C" vbq_status vbq_model_kv_cache(const vbq_model* m, int32_t layer, uint16_t** k, uint16_t** v,
+                                         int64_t* stride) {
+  if (!m || !k || !v || !stride) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_kv_cache: NULL argument");
+  if (!m->kv) return fail(VBQ_ERR_INVALID_ARG, "vbq_model_kv_cache: no context set (vbq_model_set_context)");
+  if (layer < 0 || layer >= m->desc.n_layers) return fail(VBQ_ERR_SHAPE, "vbq_model_kv_cache: layer out of range");
+  const size_t per = size_t(m->desc.n_kv_heads) * size_t(m->max_ctx) * m->desc.head_dim;
+  *k = m->kv + size_t(layer) * 2 * per;
+  *v = *k + per;
+  *stride = m->max_ctx;
+  return VBQ_OK;
+}
+
+extern "C" vbq_status vbq_decode_step_at(vbq_model* m, const uint16_t* x_dev, int32_t pos, float* logits_dev,
+                                         void* stream) {
+  if (!m || !x_dev || !logits_dev) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_at: NULL argument");
+  if (reinterpret_cast<uintptr_t>(logits_dev) % 4 || reinterpret_cast<uintptr_t>(x_dev) % 4)
+    return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_at: misaligned buffer (x and logits need 4-byte alignment)");
+  if (!m->items_ctx) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_at: no context set (vbq_model_set_context)");
+  if (pos < 0 || pos >= m->max_ctx) return fail(VBQ_ERR_SHAPE, "vbq_decode_step_at: need 0 <= pos < max_context");
+  int dev = 0;
+  VBQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != m->device) return fail(VBQ_ERR_INVALID_ARG, "vbq_decode_step_at: model is on another device");
+  const vbq_model_desc& d = m->desc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint32_t epoch = next_epoch();
+  const size_t nw = m->per_warp.size(), n_seg = m->seg_item0.size() - 1;
+  for (size_t sg = 0; sg < n_seg; ++sg) {
+    VBQ_CUDA_TRY(launch_decode_range(m, m->items_ctx, m->seg_item0[sg], m->seg_item0[sg + 1], m->seg_pieces,
+                                     m->seg_start + sg * (nw + 1), m->seg_bytes + sg * nw, epoch, m->ws, x_dev,
+                                     logits_dev, st, m->err));
+    if (sg + 1 == n_seg) break;
+    const int l = static_cast<int>(sg);  // the segment ended with layer l's [q;k;v]
+    const Layout& L = m->lay;
+    const int iq = l * L_PER_LAYER + L_QKV;
+    const float* qkv = reinterpret_cast<const float*>(m->ws + L.items[iq].out);
+    const std::vector<uint32_t>& so = m->item_st_off[iq];
+    uint16_t *kc = nullptr, *vc = nullptr;
+    int64_t stride = 0;
+    vbq_status s = vbq_model_kv_cache(m, l, &kc, &vc, &stride);
+    if (s != VBQ_OK) return s;
+    s = launch_attn_prep(qkv, int64_t(so[0]) * SROWS, int64_t(so[1]) * SROWS, int64_t(so[2]) * SROWS, m->q_rot, kc,
+                         vc, d.n_heads, d.n_kv_heads, d.head_dim, stride, pos, m->rope_theta, st);
+    if (s != VBQ_OK) return s;
+    s = vbq_attention_decode(m->q_rot, kc, vc, d.n_heads, d.n_kv_heads, d.head_dim, stride, pos + 1, m->attn_out,
+                             stream);
+    if (s != VBQ_OK) return s;
+  }
+  if (m->trace) {
+    const int64_t ph = int64_t(d.n_layers) * P_PER_LAYER;
+    VBQ_CUDA_TRY(cudaMemcpyAsync(m->tr_out + m->out_off[ph], logits_dev, 4 * static_cast<size_t>(d.vocab),
+                                 cudaMemcpyDeviceToDevice, st));
+  }
+  return VBQ_OK;
+}
+
 // vbq_decode_step keeps its step scratch (each item's fixed-point sums,
 // float outputs, arrival counters, flags and statistics) in memory that
 // vbq_model_create allocated for the model. Some callers cannot tie device

@@ -73,6 +73,9 @@ _SIGNATURES = {
     "vbq_decode_step_host": (_ST, [_P, _P, _P, _P]),
     "vbq_decode_step_noalloc": (_ST, [_P, _P, _P, _P]),
     "vbq_model_set_trace": (_ST, [_P, _I32]),
+    "vbq_model_set_context": (_ST, [_P, _I32, ctypes.c_double]),
+    "vbq_model_kv_cache": (_ST, [_P, _I32, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_I64)]),
+    "vbq_decode_step_at": (_ST, [_P, _P, _I32, _P, _P]),
     "vbq_model_trace_info": (_ST, [_P, _P, _P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "vbq_model_read_trace": (_ST, [_P, _P, _P]),
     "vbq_dense_gemv_bf16": (_ST, [_P, _P, _P, _I64, _I64, _P]),
@@ -237,6 +240,22 @@ def vbq_model_read_trace(model: int, in_total: int, out_total: int):
     tout = np.zeros(out_total, np.float32)
     _check("vbq_model_read_trace", _L().vbq_model_read_trace(model, tin.ctypes.data, tout.ctypes.data))
     return tin, tout
+
+
+def vbq_model_set_context(model: int, max_context: int, rope_theta: float = 10000.0) -> None:
+    _check("vbq_model_set_context", _L().vbq_model_set_context(model, int(max_context), float(rope_theta)))
+
+
+def vbq_model_kv_cache(model: int, layer: int):
+    """(k_ptr, v_ptr, stride): device addresses of the layer's bf16 caches [n_kv_heads][stride][head_dim]."""
+    k, v, st = _P(), _P(), _I64()
+    _check("vbq_model_kv_cache", _L().vbq_model_kv_cache(model, int(layer), ctypes.byref(k), ctypes.byref(v),
+                                                         ctypes.byref(st)))
+    return int(k.value), int(v.value), int(st.value)
+
+
+def vbq_decode_step_at(model: int, x, pos: int, logits, stream=None) -> None:
+    _check("vbq_decode_step_at", _L().vbq_decode_step_at(model, _dptr(x), int(pos), _dptr(logits), _stream(stream)))
 
 
 def vbq_dense_gemv_bf16(W, x, y, N: int, K: int, stream=None) -> None:

@@ -74,3 +74,27 @@ def attention_decode(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
         p_all[h] = p
         out[h] = p @ V[g]
     return out, p_all
+
+
+def step_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, k_cache_bits: np.ndarray, v_cache_bits: np.ndarray,
+                   pos: int, theta: float = 10000.0) -> Tuple[np.ndarray, np.ndarray]:
+    """One layer's attention in a decode step at position pos.
+
+    q [H*d], k and v [H_kv*d]: the projection outputs, rounded to bf16 as the
+    cache stores them; q and k turned by rope_bf16 at pos; k and v written into
+    copies of the caches (bf16 [H_kv, >= pos + 1, d]) at pos; then
+    attention_decode over positions 0 .. pos. Returns (out [H*d] fp64, the
+    updated (k, v) cache rows at pos as bf16 [H_kv, d] each, stacked).
+    """
+    Hkv, _, d = k_cache_bits.shape
+    H = q.size // d
+    qb = rope_bf16(f64_to_bf16_bits(np.asarray(q, np.float64)).reshape(H, d), pos, theta)
+    kb = rope_bf16(f64_to_bf16_bits(np.asarray(k, np.float64)).reshape(Hkv, d), pos, theta)
+    vb = f64_to_bf16_bits(np.asarray(v, np.float64)).reshape(Hkv, d)
+    kc = k_cache_bits.copy()
+    vc = v_cache_bits.copy()
+    kc[:, pos, :] = kb
+    vc[:, pos, :] = vb
+    out, _ = attention_decode(qb, kc, vc, pos + 1)
+    return out.reshape(-1), np.stack([kb, vb])
+

@@ -204,9 +204,12 @@ def attention_pos0(v: np.ndarray, n_heads: int, n_kv_heads: int, head_dim: int) 
 MatrixGetter = Callable[[int, str], Tuple[np.ndarray, np.ndarray, np.ndarray]]
 
 
+AttendFn = Callable[[int, np.ndarray, np.ndarray, np.ndarray], np.ndarray]
+
+
 def decode_step(get_matrix: MatrixGetter, n_layers: int, n_heads: int, n_kv_heads: int,
                 head_dim: int, x_bits: np.ndarray, eps: float = RMS_EPS,
-                trace: Optional[list] = None) -> np.ndarray:
+                trace: Optional[list] = None, attend: Optional[AttendFn] = None) -> np.ndarray:
     """Logits of one decode step, fp64 throughout, bf16 at every projection input.
 
     get_matrix(layer, proj) returns (codes, bits, scales). proj is one of
@@ -219,6 +222,9 @@ def decode_step(get_matrix: MatrixGetter, n_layers: int, n_heads: int, n_kv_head
     logits = Whead bf16(rmsnorm(h))
 
     If trace is a list, one (layer, proj, input_bits, output) tuple is appended per projection.
+    attend(layer, q, k, v), if given, replaces attention_pos0 (a step at a later
+    position: see oracle/attention_oracle.py); it returns the fp64 attention
+    output [n_heads * head_dim], which is rounded to bf16 like every projection input.
     """
     def proj(layer: int, name: str, inp_bits: np.ndarray) -> np.ndarray:
         y = gemv(*get_matrix(layer, name), inp_bits)
@@ -229,10 +235,11 @@ def decode_step(get_matrix: MatrixGetter, n_layers: int, n_heads: int, n_kv_head
     h = bf16_bits_to_f64(x_bits)
     for layer in range(n_layers):
         u = f64_to_bf16_bits(rmsnorm(h, eps))
-        proj(layer, "q", u)
-        proj(layer, "k", u)
+        q = proj(layer, "q", u)
+        k = proj(layer, "k", u)
         v = proj(layer, "v", u)
-        a = f64_to_bf16_bits(attention_pos0(v, n_heads, n_kv_heads, head_dim))
+        att = attention_pos0(v, n_heads, n_kv_heads, head_dim) if attend is None else attend(layer, q, k, v)
+        a = f64_to_bf16_bits(att)
         h = h + proj(layer, "o", a)
         u = f64_to_bf16_bits(rmsnorm(h, eps))
         g = proj(layer, "gate", u)

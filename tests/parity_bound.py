@@ -154,3 +154,25 @@ def emulate_gemv(codes, bits, scales, x_bits) -> np.ndarray:
             acc[r] += int(np.rint(np.float64(v)))
     return np.array([np.float32(np.float32(a) * np.float32(2.0 ** -F)) if abs(F) < 100 else
                      np.float32(np.ldexp(np.float64(np.float32(a)), -F)) for a in acc], dtype=np.float32)
+
+
+# ---- decode attention ----
+
+def attention_bound(q_bits, k_bits, v_bits, T, p):
+    """Per-element bound for fp32 scores (d-term sums), expf, the running sums over
+    sub-chunks of 64 positions (a rescale per sub-chunk) and the merge of at most
+    64 spans: twice the largest score error, plus the rounding of the weighted
+    sums, times sum_j p_j |v_j|."""
+    q = O.bf16_bits_to_f64(q_bits)
+    K = O.bf16_bits_to_f64(k_bits)[:, :T, :]
+    Vv = np.abs(O.bf16_bits_to_f64(v_bits)[:, :T, :])
+    H, d = q.shape
+    group = H // K.shape[0]
+    steps = (T + 63) // 64 + 64
+    out = np.zeros((H, d))
+    for h in range(H):
+        g = h // group
+        ds = (d + 2) * 2.0 ** -24 * (np.abs(K[g]) @ np.abs(q[h])) / np.sqrt(d)
+        rel = 4.0 * ds.max() + (steps + 140) * 2.0 ** -22
+        out[h] = rel * (p[h] @ Vv[g]) + 1e-30
+    return out

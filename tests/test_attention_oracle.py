@@ -203,3 +203,17 @@ def test_planted_mistakes_fail_a_pin(name):
         except AssertionError:
             failed.append(check.__name__)
     assert failed, f"no pin caught the mutant {name}"
+
+
+def test_step_attention_at_position_zero_is_the_position_zero_rule():
+    """At pos 0 the rotation is the identity and the softmax is over one key: each query head returns
+    its kv head's v, rounded to bf16, whatever the cache held."""
+    from oracle import vbq_oracle as O
+    rng = np.random.default_rng(9)
+    H, Hkv, d = 8, 2, 64
+    q, k, v = rng.standard_normal(H * d), rng.standard_normal(Hkv * d), rng.standard_normal(Hkv * d)
+    kc, vc = _bf16(rng, (Hkv, 5, d)), _bf16(rng, (Hkv, 5, d))
+    out, rows = A.step_attention(q, k, v, kc, vc, 0)
+    vb = bf16_bits_to_f64(f64_to_bf16_bits(v))
+    assert np.array_equal(out, O.attention_pos0(vb, H, Hkv, d))
+    assert np.array_equal(rows[0], f64_to_bf16_bits(k).reshape(Hkv, d))

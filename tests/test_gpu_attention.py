@@ -14,6 +14,7 @@ import pytest
 from oracle import attention_oracle as A
 from oracle.vbq_oracle import bf16_bits_to_f64, f64_to_bf16_bits
 from tests.gpu_util import dev_u16, lib
+from tests.parity_bound import attention_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -29,26 +30,6 @@ def _bf16(rng, shape, scale=1.0):
 
 def _u16(t):
     return t.cpu().numpy().view(np.uint16)
-
-
-def attention_bound(q_bits, k_bits, v_bits, T, p):
-    """Per-element bound for fp32 scores (d-term sums), expf, the running sums over
-    sub-chunks of 64 positions (a rescale per sub-chunk) and the merge of at most
-    64 spans: twice the largest score error, plus the rounding of the weighted
-    sums, times sum_j p_j |v_j|."""
-    q = bf16_bits_to_f64(q_bits)
-    K = bf16_bits_to_f64(k_bits)[:, :T, :]
-    Vv = np.abs(bf16_bits_to_f64(v_bits)[:, :T, :])
-    H, d = q.shape
-    group = H // K.shape[0]
-    steps = (T + 63) // 64 + 64
-    out = np.zeros((H, d))
-    for h in range(H):
-        g = h // group
-        ds = (d + 2) * 2.0 ** -24 * (np.abs(K[g]) @ np.abs(q[h])) / np.sqrt(d)
-        rel = 4.0 * ds.max() + (steps + 140) * 2.0 ** -22
-        out[h] = rel * (p[h] @ Vv[g]) + 1e-30
-    return out
 
 
 @pytest.mark.parametrize("H,Hkv,d,pos", [(32, 8, 128, 0), (32, 8, 128, 1), (16, 16, 64, 37), (8, 1, 128, 4095)])
