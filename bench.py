@@ -479,7 +479,8 @@ def time_cold(fn, stream, reps=10):
 
 
 def batch_sweep(V, stream):
-    """14336x4096 at the config-0 allocation, batch 1..64, cold L2 (CUDA cores at 1, tensor cores from 2)."""
+    """14336x4096 at the config-0 allocation, batch 1..64 and 128, 256, cold L2 (CUDA cores up to 3 columns,
+    tensor cores from 4)."""
     import torch
     from synth import CONFIG0_PROBS, gen_matrix, gen_x
     m = gen_matrix(14336, 4096, CONFIG0_PROBS, seed=0)
@@ -493,6 +494,12 @@ def batch_sweep(V, stream):
         alg = algorithmic_bytes(14336, 4096, info["code_bytes"]) + 2.0 * 4096 * (B - 1) + 4.0 * 14336 * (B - 1)
         out[str(B)] = {"us": round(us, 1), "GB/s": round(alg / us / 1e3, 1),
                        "TFLOP/s": round(2.0 * 14336 * 4096 * B / us / 1e6, 2)}
+    for B in (128, 256):  # prefill-sized batches through vbq_gemm (blocks of 64 columns)
+        X = torch.from_numpy(gen_x(4096, seed=100 + B, batch=B).view(np.int16)).cuda()
+        Y = torch.empty(B, 14336, device="cuda")
+        us = time_cold(lambda: V.vbq_gemm(mat.handle, X, B, Y, stream), stream)
+        out[str(B)] = {"us": round(us, 1), "TFLOP/s": round(2.0 * 14336 * 4096 * B / us / 1e6, 2),
+                       "note": "vbq_gemm: one tensor-core call per 64 columns"}
     mat.close()
     return out
 

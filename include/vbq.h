@@ -167,6 +167,14 @@ VBQ_API vbq_status vbq_gemm_smallbatch(const vbq_matrix* m, const uint16_t* X_de
                                void* stream);
 
 /*
+ * vbq_gemm: Y[j] = W X[j] for any batch (prefill-sized included), in blocks of
+ * 64 columns, each a vbq_gemm_smallbatch call on the same stream (so the
+ * weights stream once per block of 64). Layouts and errors as
+ * vbq_gemm_smallbatch; 1 <= B <= 2^24.
+ */
+VBQ_API vbq_status vbq_gemm(const vbq_matrix* m, const uint16_t* X_dev, int64_t B, float* Y_dev, void* stream);
+
+/*
  * vbq_model_create: bind the packed projections of a decoder stack for vbq_decode_step.
  * Source: the VBQ abstract (token-by-token decode through VBQ projections);
  * the stack's shape and glue are this library's reading (see vbq_decode_step).

@@ -483,6 +483,19 @@ __global__ void __launch_bounds__(kDenseWarps * 32, 3) vbq_dense_many_kernel(con
   }
 }
 
+extern "C" vbq_status vbq_gemm(const vbq_matrix* m, const uint16_t* X_dev, int64_t B, float* Y_dev, void* stream) {
+  if (!m) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm: NULL matrix");
+  if (B < 1 || B > (int64_t(1) << 24)) return fail(VBQ_ERR_INVALID_ARG, "vbq_gemm: B must be in [1, 2^24]");
+  // Blocks of 64 columns, each one vbq_gemm_smallbatch call (the tensor cores from 4 columns on).
+  for (int64_t b0 = 0; b0 < B; b0 += 64) {
+    const int32_t nb = static_cast<int32_t>(B - b0 < 64 ? B - b0 : 64);
+    const vbq_status s = vbq_gemm_smallbatch(m, X_dev ? X_dev + b0 * m->K : nullptr, nb,
+                                             Y_dev ? Y_dev + b0 * m->N : nullptr, stream);
+    if (s != VBQ_OK) return s;
+  }
+  return VBQ_OK;
+}
+
 extern "C" vbq_status vbq_dense_gemv_bf16_many(const vbq_dense_job* jobs, int32_t n_jobs, void* stream) {
   if (n_jobs < 0 || n_jobs > VBQ_DENSE_MAX_JOBS)
     return fail(VBQ_ERR_INVALID_ARG, "vbq_dense_gemv_bf16_many: n_jobs out of range");

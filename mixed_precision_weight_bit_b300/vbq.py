@@ -67,6 +67,7 @@ _SIGNATURES = {
     "vbq_dequant": (_ST, [_P, _P, _P]),
     "vbq_gemv": (_ST, [_P, _P, _P, _P]),
     "vbq_gemm_smallbatch": (_ST, [_P, _P, _I32, _P, _P]),
+    "vbq_gemm": (_ST, [_P, _P, _I64, _P, _P]),
     "vbq_model_create": (_ST, [ctypes.POINTER(VbqModelDesc), ctypes.POINTER(_P), ctypes.POINTER(_P)]),
     "vbq_model_free": (None, [_P]),
     "vbq_decode_step": (_ST, [_P, _P, _P, _P]),
@@ -183,6 +184,10 @@ def vbq_gemv(handle: int, x, y, stream=None) -> None:
 
 def vbq_gemm_smallbatch(handle: int, X, B: int, Y, stream=None) -> None:
     _check("vbq_gemm_smallbatch", _L().vbq_gemm_smallbatch(handle, _dptr(X), int(B), _dptr(Y), _stream(stream)))
+
+
+def vbq_gemm(handle: int, X, B: int, Y, stream=None) -> None:
+    _check("vbq_gemm", _L().vbq_gemm(handle, _dptr(X), int(B), _dptr(Y), _stream(stream)))
 
 
 def make_model_desc(n_layers, d, n_heads, n_kv_heads, head_dim, d_ff, vocab, rms_eps=1e-5) -> VbqModelDesc:

@@ -137,3 +137,12 @@ def test_attention_validation_without_gpu(lib):
     with pytest.raises(V.VbqError) as e:
         V.vbq_rope_append(p, p, None, p, p, 32, 8, 128, 16, 3)
     assert e.value.status == 1
+
+
+def test_gemm_validation_without_gpu(lib):
+    assert lib.vbq_gemm(None, None, 65, None, None) == 1
+    from mixed_precision_weight_bit_b300 import vbq as V
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_gemm(0, 0, 128, 0)
+    assert e.value.status == 1
+

@@ -7,7 +7,7 @@ import pytest
 from oracle import vbq_oracle as O
 from synth import CONFIG0_PROBS, f32_to_bf16_bits, gen_matrix, gen_stress, gen_x
 from tests import parity_bound as PB
-from tests.gpu_util import TOL, gemv_err, gpu_gemm, gpu_gemv, lib
+from tests.gpu_util import TOL, dev_u16, gemv_err, gpu_gemm, gpu_gemv, lib
 
 pytestmark = pytest.mark.gpu
 
@@ -86,3 +86,22 @@ def test_smallbatch_all_rows_14336x4096_every_batch(V):
         PB.check_within(Y, ref, PB.tc_bound(m.codes, m.bits, m.scales, X))
         assert gemv_err(m, X, Y) <= TOL, B
     mat.close()
+
+
+@pytest.mark.parametrize("B", [65, 130, 200])
+def test_gemm_prefill_batches(V, B):
+    """vbq_gemm above 64 columns (blocks of 64 on the tensor cores, a short last block on the CUDA
+    cores): every element within the tensor-core bound, which also covers the CUDA-core columns."""
+    import torch
+    m = gen_matrix(1500, 2048, CONFIG0_PROBS, seed=40)
+    mat = V.Matrix(m.codes, m.bits, m.scales)
+    X = gen_x(m.K, seed=41 + B, batch=B)
+    Y = torch.full((B, m.N), float("nan"), device="cuda")
+    V.vbq_gemm(mat.handle, dev_u16(X), B, Y)
+    torch.cuda.synchronize()
+    got = Y.cpu().numpy()
+    mat.close()
+    assert np.isfinite(got).all()
+    ref = O.gemm(m.codes, m.bits, m.scales, X)
+    PB.check_within(got, ref, PB.tc_bound(m.codes, m.bits, m.scales, X))
+    assert gemv_err(m, X, got) <= TOL
