@@ -533,6 +533,83 @@ def attention_decode_sweep(V, stream, peak_gbs):
     return out
 
 
+def dense_chain(W, shape, x_bits, eps=1e-5):
+    """Logits of the dense model over the same glue as the decode step (unit-gain RMSNorm, attention at
+    position 0, SwiGLU, bf16 at every projection input), in fp64 torch on the host: the dense side of the
+    divergence measurement."""
+    import torch
+    def bf16(t):
+        return t.to(torch.bfloat16).to(torch.float64)
+    def rms(h):
+        return h / torch.sqrt((h * h).mean() + eps)
+    def mm(layer, proj, u):
+        return torch.from_numpy(W[(layer, proj)]).to(torch.float64) @ u
+    h = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    group = shape.n_heads // shape.n_kv_heads
+    for layer in range(shape.n_layers):
+        u = bf16(rms(h))
+        v = mm(layer, "v", u).view(shape.n_kv_heads, shape.head_dim)
+        a = bf16(torch.cat([v[i // group] for i in range(shape.n_heads)]))
+        h = h + mm(layer, "o", a)
+        u = bf16(rms(h))
+        g, up = mm(layer, "gate", u), mm(layer, "up", u)
+        h = h + mm(layer, "down", bf16(g / (1.0 + torch.exp(-g)) * up))
+    return mm(shape.n_layers, "head", bf16(rms(h))).numpy()
+
+
+def divergence_tiny(V, n_inputs=16):
+    """KL divergence and argmax flips between a dense synthetic model (the tiny shape, Gaussian weights
+    of variance 1/K) and its VBQ encodings (vbq_quantize_rtn) at three allocations, over seeded inputs."""
+    import torch
+    from synth import CONFIG0_PROBS, gen_x, model_matrix_list, model_matrix_shape, model_tiny
+    shape = model_tiny()
+    rng = np.random.default_rng(11)
+    W = {}
+    for (layer, proj) in model_matrix_list(shape):
+        n, k = model_matrix_shape(shape, proj)
+        W[(layer, proj)] = (rng.standard_normal((n, k)) / np.sqrt(k)).astype(np.float32)
+    xs = [gen_x(shape.d, seed=100 + i) for i in range(n_inputs)]
+    ref = np.array([dense_chain(W, shape, x) for x in xs])
+
+    def log_softmax(z):
+        m = z.max(axis=-1, keepdims=True)
+        return z - m - np.log(np.exp(z - m).sum(axis=-1, keepdims=True))
+    out = {}
+    for name, probs in [("all_8bit", {8: 1.0}), ("config0_mix", CONFIG0_PROBS), ("all_1bit", {1: 1.0})]:
+        brng = np.random.default_rng(12)
+        handles = []
+        bits_total = 0
+        n_groups = 0
+        for (layer, proj) in model_matrix_list(shape):
+            w = W[(layer, proj)]
+            bits = brng.choice(list(probs.keys()), size=(w.shape[0], w.shape[1] // 64),
+                               p=list(probs.values())).astype(np.uint8)
+            bits_total += int(bits.astype(np.int64).sum())
+            n_groups += bits.size
+            codes, scales = V.vbq_quantize_rtn(w, bits)
+            handles.append(V.Matrix(codes, bits, scales))
+        desc = V.make_model_desc(shape.n_layers, shape.d, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                                 shape.d_ff, shape.vocab, 1e-5)
+        model = V.Model(desc, handles)
+        got = []
+        for x in xs:
+            lg = torch.empty(shape.vocab, device="cuda")
+            V.vbq_decode_step(model.handle, torch.from_numpy(x.view(np.int16)).cuda(), lg)
+            torch.cuda.synchronize()
+            got.append(lg.cpu().numpy().astype(np.float64))
+        model.close()
+        for h in handles:
+            h.close()
+        lp, lq = log_softmax(ref), log_softmax(np.array(got))
+        kl = (np.exp(lp) * (lp - lq)).sum(axis=-1)
+        flips = np.argmax(ref, axis=-1) != np.argmax(np.array(got), axis=-1)
+        out[name] = {"mean_bits": round(bits_total / n_groups, 3), "kl_mean": float(kl.mean()),
+                     "kl_max": float(kl.max()), "argmax_flip_rate": float(flips.mean())}
+    out["note"] = (f"tiny shape, {n_inputs} seeded inputs; the dense model's fp64 chain (same glue) vs the VBQ "
+                   "decode step on its round-to-nearest encodings; KL(dense || VBQ) of the next-token distributions")
+    return out
+
+
 def stress_8192(V, stream):
     """The 8192x8192 allocation-stress matrices (a)-(e), batch 1, cold L2."""
     import torch
@@ -768,6 +845,7 @@ def run_vbq(args, ws, rank, local):
         extra["batch_sweep_14336x4096"] = batch_sweep(V, stream)
         extra["stress_8192"] = stress_8192(V, stream)
         extra["attention_decode_9b_heads"] = attention_decode_sweep(V, stream, peak)
+        extra["divergence_tiny"] = divergence_tiny(V)
     if not args.no_dense:
         extra["dense_bf16" + w] = dense_baseline(V, shape, stream)
         extra["dense_bf16" + w]["speedup_vbq"] = round(extra["dense_bf16" + w]["us_per_step"] / (ms * 1e3), 2)

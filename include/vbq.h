@@ -92,6 +92,25 @@ VBQ_API const char* vbq_status_str(vbq_status s);
 VBQ_API const char* vbq_last_error(void);
 
 /*
+ * vbq_quantize_rtn: dense weights onto the VBQ grid at a given bit map, by
+ * absmax round-to-nearest per group (host; tooling for measuring how far a
+ * quantized model's logits move from the dense ones, VBQ abstract's
+ * distributional analysis). For each group: s = max|w| / c_b rounded to fp16
+ * (nearest, ties to even), c_b = (2^b - 1)/2; q = the nearest integer (ties to
+ * even) to w / s + c_b, clipped to [0, 2^b - 1]; q = 0 where s = 0. The pages
+ * learn the allocation and the weights; this encoding is the plainest one for
+ * a given allocation.
+ *  W           host, float [N][K] row-major, finite
+ *  bits        host, uint8 [N][K/64], each in {1,2,4,8}
+ *  codes       host, uint8 [N][K] (out), ready for vbq_pack
+ *  scales_f16  host, uint16 [N][K/64] (out), fp16 bit patterns
+ * Errors: VBQ_ERR_SHAPE (K % 64), VBQ_ERR_BITS, VBQ_ERR_INVALID_ARG (NULL,
+ * non-finite weight, a scale above fp16's range).
+ */
+VBQ_API vbq_status vbq_quantize_rtn(const float* W, int64_t N, int64_t K, const uint8_t* bits, uint8_t* codes,
+                            uint16_t* scales_f16);
+
+/*
  * vbq_pack: logical codes + per-group bit map + scales -> device layout.
  * Source: the VBQ abstract (a fixed per-group allocation is stored as packed
  * low-bit codes). The layout is this library's own design.

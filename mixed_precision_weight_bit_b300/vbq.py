@@ -62,6 +62,7 @@ _SIGNATURES = {
     "vbq_status_str": (ctypes.c_char_p, [_ST]),
     "vbq_last_error": (ctypes.c_char_p, []),
     "vbq_pack": (_ST, [_P, _P, _P, _I64, _I64, _P, ctypes.POINTER(_P)]),
+    "vbq_quantize_rtn": (_ST, [_P, _I64, _I64, _P, _P, _P]),
     "vbq_matrix_free": (None, [_P]),
     "vbq_matrix_info": (_ST, [_P, ctypes.POINTER(VbqInfo)]),
     "vbq_dequant": (_ST, [_P, _P, _P]),
@@ -176,6 +177,18 @@ def vbq_matrix_info(handle: int) -> dict:
 
 def vbq_dequant(handle: int, W, stream=None) -> None:
     _check("vbq_dequant", _L().vbq_dequant(handle, _dptr(W), _stream(stream)))
+
+
+def vbq_quantize_rtn(W: np.ndarray, bits: np.ndarray):
+    """Dense float [N][K] weights at a bit map [N][K/64] -> (codes uint8 [N][K], scales fp16 bits [N][K/64])."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    n, k = W.shape
+    codes = np.zeros((n, k), np.uint8)
+    scales = np.zeros((n, k // 64 if k % 64 == 0 else 0), np.uint16)
+    _check("vbq_quantize_rtn", _L().vbq_quantize_rtn(W.ctypes.data, n, k, bits.ctypes.data, codes.ctypes.data,
+                                                     scales.ctypes.data))
+    return codes, scales
 
 
 def vbq_gemv(handle: int, x, y, stream=None) -> None:

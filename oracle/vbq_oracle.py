@@ -209,7 +209,8 @@ AttendFn = Callable[[int, np.ndarray, np.ndarray, np.ndarray], np.ndarray]
 
 def decode_step(get_matrix: MatrixGetter, n_layers: int, n_heads: int, n_kv_heads: int,
                 head_dim: int, x_bits: np.ndarray, eps: float = RMS_EPS,
-                trace: Optional[list] = None, attend: Optional[AttendFn] = None) -> np.ndarray:
+                trace: Optional[list] = None, attend: Optional[AttendFn] = None,
+                dense: Optional[Callable[[int, str], np.ndarray]] = None) -> np.ndarray:
     """Logits of one decode step, fp64 throughout, bf16 at every projection input.
 
     get_matrix(layer, proj) returns (codes, bits, scales). proj is one of
@@ -225,9 +226,14 @@ def decode_step(get_matrix: MatrixGetter, n_layers: int, n_heads: int, n_kv_head
     attend(layer, q, k, v), if given, replaces attention_pos0 (a step at a later
     position: see oracle/attention_oracle.py); it returns the fp64 attention
     output [n_heads * head_dim], which is rounded to bf16 like every projection input.
+    dense(layer, proj), if given, returns a dense weight matrix [N][K] used in
+    place of get_matrix's packed one (the same chain over dense weights).
     """
     def proj(layer: int, name: str, inp_bits: np.ndarray) -> np.ndarray:
-        y = gemv(*get_matrix(layer, name), inp_bits)
+        if dense is not None:
+            y = np.asarray(dense(layer, name), dtype=np.float64) @ bf16_bits_to_f64(inp_bits)
+        else:
+            y = gemv(*get_matrix(layer, name), inp_bits)
         if trace is not None:
             trace.append((layer, name, inp_bits.copy(), y))
         return y
