@@ -610,6 +610,27 @@ def divergence_tiny(V, n_inputs=16):
     return out
 
 
+def fakequant_bench(V, stream, peak_gbs, n=8192, k=8192):
+    """The training-side fake quantization on an fp32 [n][k] weight (Gumbel-Softmax mixture over
+    {1,2,4,8} bits per group, straight-through backward), cold L2: bytes streamed over the call's time."""
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    W = torch.randn(n, k, device="cuda", generator=g) * 0.1
+    alpha = torch.randn(n, k // 64, 4, device="cuda", generator=g)
+    u = torch.rand(n, k // 64, 4, device="cuda", generator=g) * 0.98 + 0.01
+    G = torch.randn(n, k, device="cuda", generator=g)
+    out, dW, da = torch.empty_like(W), torch.empty_like(W), torch.empty_like(alpha)
+    fwd = time_cold(lambda: V.vbq_fakequant_forward(W, alpha, u, 0.7, n, k, out, stream), stream)
+    bwd = time_cold(lambda: V.vbq_fakequant_backward(W, alpha, u, 0.7, G, n, k, dW, da, stream), stream)
+    groups = n * (k // 64)
+    fb = 8.0 * n * k + 32.0 * groups          # W in, W_mix out; alpha and u
+    bb = 12.0 * n * k + 48.0 * groups         # W and G in, dW out; alpha, u in, dalpha out
+    return {"shape": [n, k], "forward_us": round(fwd, 1), "forward_GB/s": round(fb / fwd / 1e3, 1),
+            "forward_frac": round(fb / fwd / 1e3 / peak_gbs, 4), "backward_us": round(bwd, 1),
+            "backward_GB/s": round(bb / bwd / 1e3, 1), "backward_frac": round(bb / bwd / 1e3 / peak_gbs, 4)}
+
+
 def stress_8192(V, stream):
     """The 8192x8192 allocation-stress matrices (a)-(e), batch 1, cold L2."""
     import torch
@@ -846,6 +867,7 @@ def run_vbq(args, ws, rank, local):
         extra["stress_8192"] = stress_8192(V, stream)
         extra["attention_decode_9b_heads"] = attention_decode_sweep(V, stream, peak)
         extra["divergence_tiny"] = divergence_tiny(V)
+        extra["fakequant_8192x8192"] = fakequant_bench(V, stream, peak)
     if not args.no_dense:
         extra["dense_bf16" + w] = dense_baseline(V, shape, stream)
         extra["dense_bf16" + w]["speedup_vbq"] = round(extra["dense_bf16" + w]["us_per_step"] / (ms * 1e3), 2)

@@ -18,7 +18,7 @@ LIB = os.path.join(OUT_DIR, "libvbq.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 CUDA_LIB = "/usr/local/cuda/lib64"
 
-SOURCES = ["pack.cpp", "plan.cpp", "gemv_plan.cpp", "kernels.cu", "gemm_tc.cu", "model.cu", "attention.cu", "quantize.cpp"]
+SOURCES = ["pack.cpp", "plan.cpp", "gemv_plan.cpp", "kernels.cu", "gemm_tc.cu", "model.cu", "attention.cu", "quantize.cpp", "fakequant.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr"]
 

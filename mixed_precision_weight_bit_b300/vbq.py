@@ -63,6 +63,8 @@ _SIGNATURES = {
     "vbq_last_error": (ctypes.c_char_p, []),
     "vbq_pack": (_ST, [_P, _P, _P, _I64, _I64, _P, ctypes.POINTER(_P)]),
     "vbq_quantize_rtn": (_ST, [_P, _I64, _I64, _P, _P, _P]),
+    "vbq_fakequant_forward": (_ST, [_P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P]),
+    "vbq_fakequant_backward": (_ST, [_P, _P, _P, ctypes.c_float, _P, _I64, _I64, _P, _P, _P]),
     "vbq_matrix_free": (None, [_P]),
     "vbq_matrix_info": (_ST, [_P, ctypes.POINTER(VbqInfo)]),
     "vbq_dequant": (_ST, [_P, _P, _P]),
@@ -177,6 +179,17 @@ def vbq_matrix_info(handle: int) -> dict:
 
 def vbq_dequant(handle: int, W, stream=None) -> None:
     _check("vbq_dequant", _L().vbq_dequant(handle, _dptr(W), _stream(stream)))
+
+
+def vbq_fakequant_forward(W, alpha, u, tau: float, N: int, K: int, W_mix, stream=None) -> None:
+    _check("vbq_fakequant_forward", _L().vbq_fakequant_forward(_dptr(W), _dptr(alpha), _dptr(u), float(tau), int(N),
+                                                               int(K), _dptr(W_mix), _stream(stream)))
+
+
+def vbq_fakequant_backward(W, alpha, u, tau: float, G, N: int, K: int, dW, dalpha, stream=None) -> None:
+    _check("vbq_fakequant_backward", _L().vbq_fakequant_backward(_dptr(W), _dptr(alpha), _dptr(u), float(tau),
+                                                                 _dptr(G), int(N), int(K), _dptr(dW), _dptr(dalpha),
+                                                                 _stream(stream)))
 
 
 def vbq_quantize_rtn(W: np.ndarray, bits: np.ndarray):

@@ -146,3 +146,17 @@ def test_gemm_validation_without_gpu(lib):
         V.vbq_gemm(0, 0, 128, 0)
     assert e.value.status == 1
 
+
+def test_fakequant_validation_without_gpu(lib):
+    from mixed_precision_weight_bit_b300 import vbq as V
+    p = 1 << 20
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_fakequant_forward(p, p, p, 1.0, 4, 100, p)      # K % 64
+    assert e.value.status == 2
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_fakequant_forward(p, p, p, 0.0, 4, 64, p)       # tau
+    assert e.value.status == 1
+    with pytest.raises(V.VbqError) as e:
+        V.vbq_fakequant_backward(p, p, p, 1.0, None, 4, 64, p, p)
+    assert e.value.status == 1
+
