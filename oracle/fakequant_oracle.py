@@ -18,8 +18,10 @@ them in) and everything else in fp64:
 * backward for G = dL/dW_mix: dW = G; dalpha_b = (pi_b / tau) (D_b - sum_b' pi_b' D_b'),
   D_b = sum over the group of G Q_b(W).
 
-Parity pins: tests/test_fakequant_oracle.py (one-hot mixtures, on-grid weights, the closed-form
-gradient against finite differences of the forward, the straight-through identity).
+Parity pins: tests/test_fakequant_oracle.py (one-hot mixtures, on-grid weights, the Gumbel
+transform's closed form, softmax(alpha / tau) under equal noise, a two-width split, the closed-form
+gradient against finite differences of the forward, the straight-through identity), each checked to
+catch planted mistakes in a copy of this module.
 """
 
 from __future__ import annotations

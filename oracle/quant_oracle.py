@@ -18,7 +18,8 @@ KL(P || Q) = sum_i P_i (log P_i - log Q_i) for P = softmax(dense logits), Q = so
 logits); a flip is argmax P != argmax Q.
 
 Parity pins: tests/test_quant_oracle.py (grid round trip, the error bound, zero and 1-bit groups,
-the library's encoder against this one bit for bit, KL closed forms).
+brute-force nearest codes on the stored grid, the nearest fp16 scale, KL and log-softmax closed
+forms, the flip rule), each checked to catch planted mistakes in a copy of this module.
 """
 
 from __future__ import annotations
