@@ -117,14 +117,15 @@ VBQ_API vbq_status vbq_quantize_rtn(const float* W, int64_t N, int64_t K, const 
  * the formulas are this library's plainest reading). Per group g of 64
  * weights along K and bit-width b in {1,2,4,8} (index 0..3):
  *   Q_b(w) = s_b (q - c_b), c_b = (2^b - 1)/2, s_b = max|w_g| / c_b,
- *   q = rint(w / s_b + c_b) clipped to [0, 2^b - 1] (fp32; Q_b = 0 for an all-zero group),
+ *   q = rint(w r_b + c_b), r_b = c_b / max|w_g|, clipped to [0, 2^b - 1] (fp32, each operation
+ *   rounded once; Q_b = 0 for an all-zero group),
  *   pi_b = softmax_b((alpha_gb - log(-log u_gb)) / tau),   W_mix = sum_b pi_b Q_b(W).
  * Backward for G = dL/dW_mix: dW = G (straight through, sum_b pi_b = 1), and
  * dalpha_b = (pi_b / tau) (D_b - sum_b' pi_b' D_b'), D_b = sum over the group of G Q_b(W).
- *  W, G, W_mix, dW  device, float [N][K] row-major, 8-byte aligned; K % 64 == 0
+ *  W, G, W_mix, dW  device, float [N][K] row-major, 16-byte aligned; K % 64 == 0
  *  alpha, u, dalpha device, float [N][K/64][4]; u in (0, 1), drawn by the caller
  *  tau              > 0
- * One launch each, one warp per group. Errors: VBQ_ERR_SHAPE, VBQ_ERR_INVALID_ARG, VBQ_ERR_CUDA.
+ * One launch each, eight lanes per group. Errors: VBQ_ERR_SHAPE, VBQ_ERR_INVALID_ARG, VBQ_ERR_CUDA.
  */
 VBQ_API vbq_status vbq_fakequant_forward(const float* W, const float* alpha, const float* u, float tau, int64_t N,
                                  int64_t K, float* W_mix, void* stream);

@@ -18,9 +18,13 @@
 // dL/dw = G sum_b pi_b = G; and dL/dalpha_b = (pi_b / tau) (D_b - sum_b' pi_b'
 // D_b') with D_b = sum_i G_i Q_b(w_i) over the group's weights.
 //
-// One warp per group, two weights per lane. Lane b < 4 computes bit-width
-// b's scale, reciprocal and mixture weight once for the group; the other
-// lanes read them by shuffles. Weights, gradients and outputs stream once.
+// Four groups per warp, eight lanes per group ("octet"), eight weights per
+// lane in two 16-byte pieces: lane j of an octet holds weights 4j..4j+3 and
+// 32+4j..32+4j+3 of its group, so each of a warp's two loads (and stores)
+// covers four whole 128-byte lines. Lane b < 4 of an octet computes
+// bit-width b's scale, reciprocal and mixture weight once for the group; the
+// other lanes read them by shuffles. An octet past the last group computes on
+// zeros (every lane takes part in the shuffles) and stores nothing.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -31,29 +35,32 @@ namespace vbq {
 namespace {
 
 constexpr int kFqWarps = 8;
+constexpr int kFqGroupsPerWarp = 4;
+constexpr int kFqGroupsPerCta = kFqWarps * kFqGroupsPerWarp;
 
-__device__ __forceinline__ float fq_warp_sum(float v) {
+// Reductions over the 8 lanes of an octet.
+__device__ __forceinline__ float fq_octet_sum(float v) {
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  for (int d = 4; d >= 1; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
   return v;
 }
-__device__ __forceinline__ float fq_warp_max(float v) {
+__device__ __forceinline__ float fq_octet_max(float v) {
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
+  for (int d = 4; d >= 1; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
   return v;
 }
 
-// The group's per-width constants, in every lane: pi_b (mixture weight), s_b
-// (step) and r_b (c_b / max|w|); lane b < 4 computes width b's, then shuffles.
+// The group's per-width constants, in every lane of its octet: pi_b (mixture
+// weight), s_b (step) and r_b (c_b / max|w|). Octet lane b < 4 computes width
+// b's from a = alpha_gb and uu = u_gb, then shuffles.
 struct FqGroup {
   float pi[4], s[4], r[4];
 };
 
-__device__ __forceinline__ FqGroup fq_group(const float* alpha, const float* u, int64_t g, float inv_tau, float mx,
-                                           int lane) {
+__device__ __forceinline__ FqGroup fq_group(float a, float uu, float inv_tau, float mx, int lane) {
   const int k = lane & 3;
   const float qmax = static_cast<float>((1 << (1 << k)) - 1), c = 0.5f * qmax;
-  const float z = (alpha[g * 4 + k] - logf(-logf(u[g * 4 + k]))) * inv_tau;
+  const float z = (a - logf(-logf(uu))) * inv_tau;
   float m = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 1));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   const float e = expf(z - m);
@@ -61,26 +68,66 @@ __device__ __forceinline__ FqGroup fq_group(const float* alpha, const float* u, 
   t = t + __shfl_xor_sync(0xffffffffu, t, 2);
   const float pi = e / t;
   const float sk = mx > 0.0f ? mx / c : 0.0f, rk = mx > 0.0f ? c / mx : 0.0f;
+  const int base = lane & ~7;
   FqGroup G;
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    G.pi[b] = __shfl_sync(0xffffffffu, pi, b);
-    G.s[b] = __shfl_sync(0xffffffffu, sk, b);
-    G.r[b] = __shfl_sync(0xffffffffu, rk, b);
+    G.pi[b] = __shfl_sync(0xffffffffu, pi, base + b);
+    G.s[b] = __shfl_sync(0xffffffffu, sk, base + b);
+    G.r[b] = __shfl_sync(0xffffffffu, rk, base + b);
   }
   return G;
 }
 
-// Q_b of the lane's two weights for b = 1, 2, 4, 8 (index 0..3); all zero for an all-zero group.
-__device__ __forceinline__ void fq_levels(float w0, float w1, const FqGroup& G, float (&q0)[4], float (&q1)[4]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float qmax = static_cast<float>((1 << (1 << k)) - 1), c = 0.5f * qmax;
-    const float a = fminf(fmaxf(rintf(__fadd_rn(__fmul_rn(w0, G.r[k]), c)), 0.0f), qmax);
-    const float b = fminf(fmaxf(rintf(__fadd_rn(__fmul_rn(w1, G.r[k]), c)), 0.0f), qmax);
-    q0[k] = __fmul_rn(G.s[k], a - c);
-    q1[k] = __fmul_rn(G.s[k], b - c);
+// Q_b(w) for b = 1, 2, 4, 8 (index k = 0..3); zero for an all-zero group (r = s = 0).
+__device__ __forceinline__ float fq_level(float w, const FqGroup& G, int k) {
+  const float qmax = static_cast<float>((1 << (1 << k)) - 1), c = 0.5f * qmax;
+  const float q = fminf(fmaxf(rintf(__fadd_rn(__fmul_rn(w, G.r[k]), c)), 0.0f), qmax);
+  return __fmul_rn(G.s[k], q - c);
+}
+
+// The lane's place: its group, whether that group exists, and the element offsets of its two pieces.
+struct FqLane {
+  int64_t g;
+  bool ok;
+  int64_t off0, off1;
+};
+
+__device__ __forceinline__ FqLane fq_lane(int64_t n_groups) {
+  const int lane = threadIdx.x & 31;
+  FqLane L;
+  L.g = (static_cast<int64_t>(blockIdx.x) * kFqWarps + (threadIdx.x >> 5)) * kFqGroupsPerWarp + (lane >> 3);
+  L.ok = L.g < n_groups;
+  L.off0 = L.g * 64 + 4 * (lane & 7);
+  L.off1 = L.off0 + 32;
+  return L;
+}
+
+__device__ __forceinline__ void fq_load8(const float* __restrict__ p, const FqLane& L, float (&v)[8]) {
+  float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
+  if (L.ok) {
+    a = __ldcs(reinterpret_cast<const float4*>(p + L.off0));
+    b = __ldcs(reinterpret_cast<const float4*>(p + L.off1));
   }
+  v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w;
+  v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
+
+__device__ __forceinline__ void fq_store8(float* __restrict__ p, const FqLane& L, const float (&v)[8]) {
+  if (!L.ok) return;
+  __stcs(reinterpret_cast<float4*>(p + L.off0), make_float4(v[0], v[1], v[2], v[3]));
+  __stcs(reinterpret_cast<float4*>(p + L.off1), make_float4(v[4], v[5], v[6], v[7]));
+}
+
+__device__ __forceinline__ FqGroup fq_group_of(const float* __restrict__ alpha, const float* __restrict__ u,
+                                               const FqLane& L, float inv_tau, const float (&w)[8], int lane) {
+  const int k = lane & 3;
+  const float a = L.ok ? alpha[L.g * 4 + k] : 0.0f;
+  const float uu = L.ok ? u[L.g * 4 + k] : 0.5f;
+  float mx = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(w[i]));
+  return fq_group(a, uu, inv_tau, fq_octet_max(mx), lane);
 }
 
 __global__ void __launch_bounds__(kFqWarps * 32) vbq_fq_forward_kernel(const float* __restrict__ W,
@@ -88,20 +135,19 @@ __global__ void __launch_bounds__(kFqWarps * 32) vbq_fq_forward_kernel(const flo
                                                                       const float* __restrict__ u, float inv_tau,
                                                                       int64_t n_groups, float* __restrict__ Wmix) {
   const int lane = threadIdx.x & 31;
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * kFqWarps + (threadIdx.x >> 5);
-  if (g >= n_groups) return;
-  const float2 w = __ldcs(reinterpret_cast<const float2*>(W + g * 64) + lane);
-  const float mx = fq_warp_max(fmaxf(fabsf(w.x), fabsf(w.y)));
-  const FqGroup P = fq_group(alpha, u, g, inv_tau, mx, lane);
-  float q0[4], q1[4];
-  fq_levels(w.x, w.y, P, q0, q1);
-  float2 o = make_float2(0.0f, 0.0f);
+  const FqLane L = fq_lane(n_groups);
+  float w[8];
+  fq_load8(W, L, w);
+  const FqGroup P = fq_group_of(alpha, u, L, inv_tau, w, lane);
+  float o[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    o.x = fmaf(P.pi[k], q0[k], o.x);
-    o.y = fmaf(P.pi[k], q1[k], o.y);
+  for (int i = 0; i < 8; ++i) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc = fmaf(P.pi[k], fq_level(w[i], P, k), acc);
+    o[i] = acc;
   }
-  __stcs(reinterpret_cast<float2*>(Wmix + g * 64) + lane, o);
+  fq_store8(Wmix, L, o);
 }
 
 __global__ void __launch_bounds__(kFqWarps * 32) vbq_fq_backward_kernel(const float* __restrict__ W,
@@ -111,42 +157,45 @@ __global__ void __launch_bounds__(kFqWarps * 32) vbq_fq_backward_kernel(const fl
                                                                        float* __restrict__ dW,
                                                                        float* __restrict__ dalpha) {
   const int lane = threadIdx.x & 31;
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * kFqWarps + (threadIdx.x >> 5);
-  if (g >= n_groups) return;
-  const float2 w = __ldcs(reinterpret_cast<const float2*>(W + g * 64) + lane);
-  const float2 gr = __ldcs(reinterpret_cast<const float2*>(G + g * 64) + lane);
-  __stcs(reinterpret_cast<float2*>(dW + g * 64) + lane, gr);  // straight through: sum_b pi_b = 1
-  const float mx = fq_warp_max(fmaxf(fabsf(w.x), fabsf(w.y)));
-  const FqGroup P = fq_group(alpha, u, g, inv_tau, mx, lane);
-  float q0[4], q1[4];
-  fq_levels(w.x, w.y, P, q0, q1);
+  const FqLane L = fq_lane(n_groups);
+  float w[8], gr[8];
+  fq_load8(W, L, w);
+  fq_load8(G, L, gr);
+  fq_store8(dW, L, gr);  // straight through: sum_b pi_b = 1
+  const FqGroup P = fq_group_of(alpha, u, L, inv_tau, w, lane);
   float D[4], mean = 0.0f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    D[k] = fq_warp_sum(fmaf(gr.x, q0[k], gr.y * q1[k]));
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(gr[i], fq_level(w[i], P, k), acc);
+    D[k] = fq_octet_sum(acc);
     mean = fmaf(P.pi[k], D[k], mean);
   }
-  if (lane < 4) {
+  const int sl = lane & 7;
+  if (L.ok && sl < 4) {
     float d = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      if (k == lane) d = P.pi[k] * inv_tau * (D[k] - mean);
-    dalpha[g * 4 + lane] = d;
+      if (k == sl) d = P.pi[k] * inv_tau * (D[k] - mean);
+    dalpha[L.g * 4 + sl] = d;
   }
 }
 
-bool fq_aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+bool fq_aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 vbq_status fq_check(const char* fn, const float* W, const float* alpha, const float* u, float tau, int64_t N,
                     int64_t K) {
   if (N < 0 || K < 0 || K % GROUP) return fail(VBQ_ERR_SHAPE, std::string(fn) + ": need N, K >= 0 and K % 64 == 0");
   if (N * K > 0 && (!W || !alpha || !u)) return fail(VBQ_ERR_INVALID_ARG, std::string(fn) + ": NULL buffer");
   if (!(tau > 0.0f)) return fail(VBQ_ERR_INVALID_ARG, std::string(fn) + ": tau must be > 0");
-  if (!fq_aligned(W)) return fail(VBQ_ERR_INVALID_ARG, std::string(fn) + ": W must be 8-byte aligned");
+  if (!fq_aligned(W)) return fail(VBQ_ERR_INVALID_ARG, std::string(fn) + ": W must be 16-byte aligned");
   return VBQ_OK;
 }
 
-unsigned fq_grid(int64_t n_groups) { return static_cast<unsigned>((n_groups + kFqWarps - 1) / kFqWarps); }
+unsigned fq_grid(int64_t n_groups) {
+  return static_cast<unsigned>((n_groups + kFqGroupsPerCta - 1) / kFqGroupsPerCta);
+}
 
 }  // namespace
 
@@ -161,7 +210,7 @@ extern "C" vbq_status vbq_fakequant_forward(const float* W, const float* alpha, 
   if (N * K == 0) return VBQ_OK;
   if (!W_mix || !fq_aligned(W_mix)) return fail(VBQ_ERR_INVALID_ARG, "vbq_fakequant_forward: W_mix NULL or misaligned");
   const int64_t ng = N * (K / GROUP);
-  if (ng > (int64_t(1) << 40)) return fail(VBQ_ERR_SHAPE, "vbq_fakequant_forward: too many groups");
+  if (ng > int64_t(0x7fffffff) * kFqGroupsPerCta) return fail(VBQ_ERR_SHAPE, "vbq_fakequant_forward: too many groups");
   note_launches(1);
   vbq_fq_forward_kernel<<<fq_grid(ng), kFqWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(W, alpha, u, 1.0f / tau,
                                                                                               ng, W_mix);
@@ -178,7 +227,7 @@ extern "C" vbq_status vbq_fakequant_backward(const float* W, const float* alpha,
   if (!G || !dW || !dalpha || !fq_aligned(G) || !fq_aligned(dW))
     return fail(VBQ_ERR_INVALID_ARG, "vbq_fakequant_backward: G, dW or dalpha NULL or misaligned");
   const int64_t ng = N * (K / GROUP);
-  if (ng > (int64_t(1) << 40)) return fail(VBQ_ERR_SHAPE, "vbq_fakequant_backward: too many groups");
+  if (ng > int64_t(0x7fffffff) * kFqGroupsPerCta) return fail(VBQ_ERR_SHAPE, "vbq_fakequant_backward: too many groups");
   note_launches(1);
   vbq_fq_backward_kernel<<<fq_grid(ng), kFqWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
       W, alpha, u, 1.0f / tau, G, ng, dW, dalpha);
