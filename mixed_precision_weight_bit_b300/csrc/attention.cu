@@ -315,12 +315,12 @@ __global__ void vbq_rope_append_kernel(uint16_t* __restrict__ q, const uint16_t*
                                        const uint16_t* __restrict__ v_new, uint16_t* __restrict__ k_cache,
                                        uint16_t* __restrict__ v_cache, int32_t H, int32_t d, int64_t stride,
                                        int32_t pos, double theta) {
-  grid_dep_wait();
   const int b = blockIdx.x, i = threadIdx.x, half = d / 2;
   if (i >= half) return;
   const double inv_freq = pow(theta, -2.0 * i / d);
   double s, c;
   sincos(static_cast<double>(pos) * inv_freq, &s, &c);
+  grid_dep_wait();  // the angles above need nothing from the kernel before; q, k and v do
   auto turn = [&](const uint16_t* src, uint16_t* dst) {
     const double x0 = __uint_as_float(static_cast<uint32_t>(src[i]) << 16);
     const double x1 = __uint_as_float(static_cast<uint32_t>(src[i + half]) << 16);
@@ -354,6 +354,7 @@ __global__ void vbq_attn_prep_kernel(const float* __restrict__ qkv, int64_t q_of
   const double inv_freq = pow(theta, -2.0 * i / d);
   double s, c;
   sincos(static_cast<double>(pos) * inv_freq, &s, &c);
+  grid_dep_wait();  // the angles above need nothing from the kernel before; q, k and v do
   auto bf = [](float v) { return __float2bfloat16_rn(v); };
   auto turn = [&](const float* src, uint16_t* dst) {
     const double x0 = __bfloat162float(bf(src[i])), x1 = __bfloat162float(bf(src[i + half]));
@@ -450,9 +451,19 @@ vbq_status launch_attn_prep(const float* qkv, int64_t q_off, int64_t k_off, int6
                             uint16_t* k_cache, uint16_t* v_cache, int32_t H, int32_t Hkv, int32_t d, int64_t stride,
                             int32_t pos, double theta, cudaStream_t st) {
   note_launches(1);
-  vbq_attn_prep_kernel<<<H + Hkv, d / 2, 0, st>>>(qkv, q_off, k_off, v_off, q_rot, k_cache, v_cache, H, d, stride,
-                                                  pos, theta);
-  VBQ_CUDA_TRY(cudaGetLastError());
+  // Programmatic dependent launch: the CTAs start, and compute their angles,
+  // as the decode kernel before them drains; they wait for it before reading q, k and v.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(H + Hkv), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(d / 2), 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  VBQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, vbq_attn_prep_kernel, qkv, q_off, k_off, v_off, q_rot, k_cache, v_cache, H, d,
+                                  stride, pos, theta));
   return VBQ_OK;
 }
 
