@@ -159,4 +159,13 @@ def test_fakequant_validation_without_gpu(lib):
     with pytest.raises(V.VbqError) as e:
         V.vbq_fakequant_backward(p, p, p, 1.0, None, 4, 64, p, p)
     assert e.value.status == 1
+    # 16-byte pieces: W, W_mix, G and dW must be 16-byte aligned; 8 is not enough
+    for args in [(p + 8, p, p, 1.0, 4, 64, p), (p, p, p, 1.0, 4, 64, p + 8)]:
+        with pytest.raises(V.VbqError) as e:
+            V.vbq_fakequant_forward(*args)
+        assert e.value.status == 1 and "align" in str(e.value)
+    for args in [(p, p, p, 1.0, p + 8, 4, 64, p, p), (p, p, p, 1.0, p, 4, 64, p + 8, p)]:
+        with pytest.raises(V.VbqError) as e:
+            V.vbq_fakequant_backward(*args)
+        assert e.value.status == 1 and "align" in str(e.value)
 
