@@ -176,3 +176,52 @@ def attention_bound(q_bits, k_bits, v_bits, T, p):
         rel = 4.0 * ds.max() + (steps + 140) * 2.0 ** -22
         out[h] = rel * (p[h] @ Vv[g]) + 1e-30
     return out
+
+
+def emulate_attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, T: int, nparts: int,
+                      sub: int = 64, drop_last: bool = False, scale_by_d: bool = False) -> np.ndarray:
+    """The split-KV decode attention's arithmetic in numpy fp32: fp32 scores times an fp32 1/sqrt(d);
+    per span of whole 64-position sub-chunks a running max, exp(s - m), a rescale by exp(m_old - m) of
+    the running sum and of the p-weighted sums of v; then the spans merged with weights exp(m_c - M)
+    and one division. The dot products and sums run in numpy's order, not the kernel's, which the
+    bound allows. drop_last and scale_by_d plant mistakes (the last position left out; 1/d for
+    1/sqrt(d)) for the self-test of the bound. Returns [H, d] fp64 of fp32 values."""
+    f32 = np.float32
+    q = O.bf16_bits_to_f64(q_bits).astype(f32)
+    K = O.bf16_bits_to_f64(k_bits)[:, :T, :].astype(f32)
+    Vv = O.bf16_bits_to_f64(v_bits)[:, :T, :].astype(f32)
+    H, d = q.shape
+    group = H // K.shape[0]
+    scale = f32(1.0) / (f32(d) if scale_by_d else np.sqrt(f32(d)))
+    Tn = T - 1 if drop_last else T
+    nsub = (Tn + sub - 1) // sub
+    span_sub = (nsub + nparts - 1) // nparts
+    nparts = (nsub + span_sub - 1) // span_sub
+    out = np.zeros((H, d), f32)
+    with np.errstate(over="ignore", under="ignore"):
+        for h in range(H):
+            g = h // group
+            S = (K[g, :Tn] @ q[h]).astype(f32) * scale
+            ms, ls, accs = [], [], []
+            for c in range(nparts):
+                p0, p1 = c * span_sub * sub, min(Tn, (c + 1) * span_sub * sub)
+                m, l, acc = f32(-np.inf), f32(0.0), np.zeros(d, f32)
+                for j0 in range(p0, p1, sub):
+                    s = S[j0:min(p1, j0 + sub)]
+                    mn = max(m, s.max())
+                    p = np.exp(s - mn).astype(f32)
+                    alpha = np.exp(f32(m - mn)).astype(f32)
+                    l = f32(l * alpha + p.sum(dtype=f32))
+                    acc = (acc * alpha + p @ Vv[g, j0:j0 + p.size]).astype(f32)
+                    m = mn
+                ms.append(m)
+                ls.append(l)
+                accs.append(acc)
+            if nparts == 1:
+                out[h] = accs[0] * (f32(1.0) / ls[0])
+                continue
+            M = max(ms)
+            w = np.exp(np.array(ms, f32) - M).astype(f32)
+            L = f32((w * np.array(ls, f32)).sum(dtype=f32))
+            out[h] = (w @ np.array(accs, f32)).astype(f32) / L
+    return out.astype(np.float64)
