@@ -225,3 +225,76 @@ def emulate_attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray
             L = f32((w * np.array(ls, f32)).sum(dtype=f32))
             out[h] = (w @ np.array(accs, f32)).astype(f32) / L
     return out.astype(np.float64)
+
+
+def fakequant_tolerances(W, tau: float, G, Q=None):
+    """Per-element tolerances of vbq_fakequant_forward and vbq_fakequant_backward against the fp64
+    oracle. Forward: 2e-6 * sum_b |Q_b| / min(tau, 1), for the fp32 log, exp and division of the
+    mixture weights (their error grows as tau shrinks) and four fp32 products. dalpha: (70 * 2^-24 +
+    2e-6 / min(tau, 1)) * 4 * max_b D'_b / tau per group, D'_b = sum over the group of |G| |Q_b|, for
+    the fp32 sums of 64 products and the fp32 weights. Q: the oracle's levels, if already computed."""
+    from oracle import fakequant_oracle as F
+    if Q is None:
+        Q = F.levels(W).astype(np.float64)
+    n, k = np.asarray(W).shape
+    tol = 2e-6 * np.abs(Q).sum(axis=0) / min(tau, 1.0) + 1e-30
+    Dabs = (np.abs(np.asarray(G, np.float64))[None] * np.abs(Q)).reshape(4, n, k // 64, 64).sum(axis=3)
+    scale = np.moveaxis(Dabs, 0, -1).max(axis=-1, keepdims=True) / tau
+    tol_a = (70 * 2.0 ** -24 + 2e-6 / min(tau, 1.0)) * 4 * scale + 1e-30
+    return tol, tol_a
+
+
+def _fma32(a, b, c):
+    """fp32 fma: the fp64 product of two fp32 values is exact; one rounding of the fp64 sum to fp32
+    (a double rounding, at most an ulp of fp32 off a true fma, which the tolerances absorb)."""
+    return (np.asarray(a, np.float64) * np.asarray(b, np.float64) + np.asarray(c, np.float64)).astype(np.float32)
+
+
+def emulate_fakequant(W, alpha, u, tau: float, G, tau_multiplies: bool = False, offset_half_range: bool = False,
+                      D_without_G: bool = False):
+    """The fake-quantization kernels' arithmetic in numpy fp32, with their order: mixture weights from
+    fp32 log, exp and a 4-lane butterfly; levels rint(w r_b + c_b) with r_b = c_b / max|w|, each op
+    rounded once; the forward an fma chain over b; D_b as 8 lanes of 8-term fma chains (weights 4j..4j+3
+    and 32+4j..32+4j+3 of lane j) and a 3-step butterfly; dalpha = (pi_b / tau) (D_b - sum pi D). The
+    keyword flags plant mistakes for the self-test. Returns (W_mix [N, K], dalpha [N, K/64, 4]) in fp64."""
+    f32 = np.float32
+    W = np.asarray(W, f32)
+    n, k = W.shape
+    g = k // 64
+    Wg = W.reshape(n, g, 64)
+    inv_tau = f32(tau) if tau_multiplies else f32(1.0) / f32(tau)
+    z = ((np.asarray(alpha, f32) - np.log(-np.log(np.asarray(u, f32)))) * inv_tau).astype(f32)  # [n, g, 4]
+    m = np.maximum(np.maximum(z[..., 0], z[..., 1]), np.maximum(z[..., 2], z[..., 3]))[..., None]
+    e = np.exp((z - m).astype(f32)).astype(f32)
+    t = ((e[..., 0] + e[..., 1]).astype(f32) + (e[..., 2] + e[..., 3]).astype(f32)).astype(f32)[..., None]
+    pi = (e / t).astype(f32)
+    mx = np.abs(Wg).max(axis=2)  # [n, g]
+    Q = np.zeros((4, n, g, 64), f32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        for i, b in enumerate((1, 2, 4, 8)):
+            qmax = f32((1 << b) - 1)
+            c = f32(1 << (b - 1)) if offset_half_range else f32(0.5) * qmax
+            s = np.where(mx > 0, mx / c, f32(0)).astype(f32)[..., None]
+            r = np.where(mx > 0, c / mx, f32(0)).astype(f32)[..., None]
+            q = np.clip(np.rint(((Wg * r).astype(f32) + c).astype(f32)), f32(0), qmax)
+            Q[i] = (s * (q - c).astype(f32)).astype(f32)
+    out = np.zeros((n, g, 64), f32)
+    for i in range(4):
+        out = _fma32(pi[..., i][..., None], Q[i], out)
+    Gg = np.asarray(G, f32).reshape(n, g, 64)
+    lanes = np.array([[4 * j + t for t in range(4)] + [32 + 4 * j + t for t in range(4)] for j in range(8)])
+    D = np.zeros((n, g, 4), f32)
+    for i in range(4):
+        prod_g = np.ones_like(Gg) if D_without_G else Gg
+        acc = np.zeros((n, g, 8), f32)
+        for t in range(8):
+            idx = lanes[:, t]
+            acc = _fma32(prod_g[..., idx], Q[i][..., idx], acc)
+        for dlt in (4, 2, 1):
+            acc = (acc + acc[..., np.arange(8) ^ dlt]).astype(f32)
+        D[..., i] = acc[..., 0]
+    mean = np.zeros((n, g), f32)
+    for i in range(4):
+        mean = _fma32(pi[..., i], D[..., i], mean)
+    da = ((pi * inv_tau).astype(f32) * (D - mean[..., None]).astype(f32)).astype(f32)
+    return out.reshape(n, k).astype(np.float64), da.astype(np.float64)

@@ -6,6 +6,7 @@ import pytest
 
 from oracle import fakequant_oracle as F
 from tests.gpu_util import lib
+from tests.parity_bound import fakequant_tolerances
 
 pytestmark = pytest.mark.gpu
 
@@ -39,16 +40,11 @@ def test_fakequant_forward_backward(V, n, k, tau, zero_group):
     V.vbq_fakequant_backward(Wd, ad, ud, tau, Gd, n, k, dW, da)
     torch.cuda.synchronize()
     ref = F.forward(W, alpha.astype(np.float64), u.astype(np.float64), tau)
-    Q = F.levels(W).astype(np.float64)
-    # fp32 mixture weights (log, exp, a division) and four fp32 products: a few ulps of sum_b |Q_b|
-    tol = 2e-6 * np.abs(Q).sum(axis=0) / min(tau, 1.0) + 1e-30
+    # the tolerances of the kernels' fp32 arithmetic (pinned on the CPU by test_fakequant_bound_cpu.py)
+    tol, tol_a = fakequant_tolerances(W, tau, G)
     got = out.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got - ref) <= tol), float((np.abs(got - ref) / tol).max())
     dW_ref, da_ref = F.backward(W, alpha.astype(np.float64), u.astype(np.float64), tau, G)
     assert np.array_equal(dW.cpu().numpy(), G)
-    # D_b: fp32 sums of 64 products; pi: fp32
-    Dabs = (np.abs(G)[None] * np.abs(Q)).reshape(4, n, k // 64, 64).sum(axis=3)
-    scale = np.moveaxis(Dabs, 0, -1).max(axis=-1, keepdims=True) / tau
-    tol_a = (70 * 2.0 ** -24 + 2e-6 / min(tau, 1.0)) * 4 * scale + 1e-30
     da_got = da.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(da_got - da_ref) <= tol_a), float((np.abs(da_got - da_ref) / tol_a).max())
