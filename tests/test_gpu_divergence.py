@@ -27,15 +27,17 @@ def dense_weights(shape, seed):
     return W
 
 
-def divergence(V, shape, W, probs, xs, seed):
+def divergence(V, shape, W, probs, xs, seed, with_oracle=False):
     import torch
     rng = np.random.default_rng(seed)
     handles = []
+    packed = {}
     for (layer, proj) in model_matrix_list(shape):
         w = W[(layer, proj)]
         bits = rng.choice(list(probs.keys()), size=(w.shape[0], w.shape[1] // 64),
                           p=list(probs.values())).astype(np.uint8)
         codes, scales = V.vbq_quantize_rtn(w, bits)
+        packed[(layer, proj)] = (codes, bits, scales)
         handles.append(V.Matrix(codes, bits, scales))
     desc = V.make_model_desc(shape.n_layers, shape.d, shape.n_heads, shape.n_kv_heads, shape.head_dim,
                              shape.d_ff, shape.vocab, O.RMS_EPS)
@@ -51,7 +53,13 @@ def divergence(V, shape, W, probs, xs, seed):
         h.close()
     ref = [O.decode_step(None, shape.n_layers, shape.n_heads, shape.n_kv_heads, shape.head_dim, x,
                          dense=lambda layer, proj: W[(layer, proj)]) for x in xs]
-    return Q.kl_and_flips(np.array(ref), np.array(got))
+    if not with_oracle:
+        return Q.kl_and_flips(np.array(ref), np.array(got))
+    # the oracle's fp64 chain over the same codes and scales: the VBQ side of the measurement without the GPU
+    orc = [O.decode_step(lambda layer, proj: packed[(layer, proj)], shape.n_layers, shape.n_heads,
+                         shape.n_kv_heads, shape.head_dim, x) for x in xs]
+    return (Q.kl_and_flips(np.array(ref), np.array(got)), Q.kl_and_flips(np.array(ref), np.array(orc)),
+            Q.kl_and_flips(np.array(orc), np.array(got)))
 
 
 def test_divergence_grows_as_bits_shrink(V):
@@ -65,3 +73,17 @@ def test_divergence_grows_as_bits_shrink(V):
         res[name] = (float(kl.mean()), float(flips.mean()))
     assert res["8bit"][0] < res["config0"][0] < res["1bit"][0], res
     assert res["8bit"][0] < 1e-3 and res["8bit"][1] == 0.0, res
+
+
+def test_measured_divergence_is_the_oracles(V):
+    """The KL and flips measured through the GPU step equal, within the step's own error, those of the
+    oracle's fp64 chain over the same encodings; the GPU and oracle distributions are near-identical."""
+    shape = model_tiny()
+    W = dense_weights(shape, seed=11)
+    xs = [gen_x(shape.d, seed=100 + i) for i in range(8)]
+    for name, probs in [("8bit", {8: 1.0}), ("config0", CONFIG0_PROBS), ("1bit", {1: 1.0})]:
+        (kl_g, fl_g), (kl_o, fl_o), (kl_og, _) = divergence(V, shape, W, probs, xs, seed=12, with_oracle=True)
+        info = (name, kl_g.tolist(), kl_o.tolist(), kl_og.tolist(), fl_g.tolist(), fl_o.tolist())
+        assert kl_og.max() <= 1e-3, info
+        assert np.all(np.abs(kl_g - kl_o) <= 0.1 * kl_o + 1e-4), info
+        assert int((fl_g != fl_o).sum()) <= 1, info
